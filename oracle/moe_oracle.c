@@ -1,0 +1,389 @@
+/*
+ * CPU ORACLE for the routed 4-bit MoE layer -- TEST INFRASTRUCTURE ONLY.
+ *
+ * Plain, slow, obviously correct C. Only the tests, the smoke check and the
+ * benchmark's CPU-baseline leg may load it. It shares no code, header,
+ * table or helper with the CUDA library; neither includes the other.
+ *
+ * Source: the DiffusionGemma language-model page ("diffusion-gemma/model.ts"),
+ * classes DiffRouter (router forward) and DiffExperts (experts forward), and
+ * the vision page ("diffusion-gemma/vision.ts", manualRms) for the fp32
+ * semantics of the no-scale RMS norm.
+ *
+ * Precision rules used here:
+ *  - Every tensor the pages hold in the model dtype is rounded to bf16
+ *    (round to nearest even) exactly where the pages produce it.
+ *  - Where the pages fix the arithmetic precision it is followed: the RMS
+ *    norm is fp32 (manualRms: x_f32 * rsqrt(mean(x^2) + eps), cast back) and
+ *    the routing softmax is fp32 ("precise" softmax).
+ *  - Where the pages are silent (matmul accumulation, GeGLU internals, the
+ *    k-way sum of the combine) the oracle computes in double and rounds once.
+ *  - A 4-bit weight dequantises to the model dtype: w = bf16(S*q + B), as the
+ *    pages' `dequantize` of a quantized table yields a bf16 matmul operand
+ *    (DiffusionGemmaModel.dequantEmbedWeight, used by softEmbeddings).
+ *
+ * Every function is pinned by the CPU tests in tests/test_oracle_pins.py.
+ *
+ * Build: gcc -O2 -std=c11 -fopenmp -ffp-contract=off -shared -fPIC
+ * (no contraction: each fp32 operation rounds exactly once).
+ *
+ * ORACLE_MUTANT (compile-time, tests only): plants one known mistake so the
+ * tests can show that the pins catch it. 0 (default) is the oracle proper.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#ifndef ORACLE_MUTANT
+#define ORACLE_MUTANT 0
+#endif
+
+typedef struct {
+    int32_t T, H, E, k, inter, group, bits;
+    float eps;
+} oracle_dims;
+
+/* ---------------------------------------------------------------- bf16 --- */
+
+/* bf16 bits -> float: exact widening (bf16 is the top half of an fp32). */
+static float bf(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* float -> bf16 bits, round to nearest, ties to even. */
+static uint16_t bf16_from_float(float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu))
+        return (uint16_t)((u >> 16) | 0x0040u); /* quiet NaN */
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+/* double -> bf16 bits with ONE rounding (nearest, ties to even).
+ * bf16 keeps 8 significant bits; normal exponents down to 2^-126 and
+ * subnormals on the fixed grid 2^-133. */
+static uint16_t bf16_from_double(double d) {
+    if (isnan(d)) return 0x7FC0u;
+    uint16_t sign = signbit(d) ? 0x8000u : 0u;
+    double a = fabs(d);
+    if (a == 0.0) return sign;
+    int e;
+    frexp(a, &e);                 /* a = m * 2^e, m in [0.5, 1) */
+    int q = e - 8;                /* weight of the last kept bit */
+    if (q < -133) q = -133;
+    double r = nearbyint(ldexp(a, -q)); /* default mode: nearest-even */
+    double v = ldexp(r, q);
+    if (v >= 0x1p128) return (uint16_t)(sign | 0x7F80u); /* overflow -> inf */
+    float f = (float)v;           /* exact: v has <= 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    return (uint16_t)(sign | (u >> 16));
+}
+
+/* Exported so the tests can pin the rounding helpers themselves. */
+uint16_t oracle_bf16_from_float(float f) { return bf16_from_float(f); }
+uint16_t oracle_bf16_from_double(double d) { return bf16_from_double(d); }
+
+static void set_threads(int nthreads) {
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* ------------------------------------------------------------- router --- */
+
+/*
+ * DiffRouter.forward: x [T,H] -> indices [T,k], weights [T,k].
+ *   normed = rms_norm(x, no weight, eps)        (fp32 inside, bf16 out)
+ *   normed = normed * scale                      (bf16 op)
+ *   normed = normed * hidden^-0.5                (bf16 op; scalar in bf16)
+ *   scores = proj(normed)                        (bf16 out)
+ *   indices = top-k of scores (argpartition, unordered on the page;
+ *             emitted here as value descending, ties to the lower expert id)
+ *   weights = softmax_precise(scores[indices]) * per_expert_scale[indices]
+ *
+ * Optional taps (NULL to skip): normed [T,H] bf16 after both scale ops,
+ * logits_exact [T,E] double (before rounding), scores [T,E] bf16.
+ * Returns 0, or -1 on bad sizes.
+ */
+int oracle_route(const oracle_dims* d, const uint16_t* x, const uint16_t* router_w,
+                 const uint16_t* router_scale, const uint16_t* per_expert_scale,
+                 int32_t* idx_out, uint16_t* w_out, uint16_t* normed_tap,
+                 double* logits_exact_tap, uint16_t* scores_tap, int nthreads) {
+    const int T = d->T, H = d->H, E = d->E, k = d->k;
+    if (T < 0 || H <= 0 || E <= 0 || k <= 0 || k > E || k > 64) return -1;
+    set_threads(nthreads);
+    /* hidden^-0.5 enters as a scalar in the array dtype (bf16). */
+    const float root = bf(bf16_from_double(pow((double)H, -0.5)));
+
+#pragma omp parallel
+    {
+        uint16_t* n3 = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)H);
+        double* lex = (double*)malloc(sizeof(double) * (size_t)E);
+        uint16_t* s = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)E);
+        int* taken = (int*)malloc(sizeof(int) * (size_t)E);
+#pragma omp for schedule(static)
+        for (int t = 0; t < T; ++t) {
+            const uint16_t* xt = x + (size_t)t * H;
+            /* RMSNormNoScale in fp32: mean of squares, + eps, rsqrt. */
+            float ss = 0.0f;
+            for (int h = 0; h < H; ++h) {
+                float v = bf(xt[h]);
+                ss += v * v;
+            }
+#if ORACLE_MUTANT == 1
+            float mean = ss / (float)(H - 1); /* planted: wrong divisor */
+#else
+            float mean = ss / (float)H;
+#endif
+            float denom = mean + d->eps;
+            float r = (float)(1.0 / sqrt((double)denom)); /* rsqrt, rounded to fp32 */
+            for (int h = 0; h < H; ++h) {
+                float nv = bf(bf16_from_float(bf(xt[h]) * r));             /* cast to bf16 */
+                float n2 = bf(bf16_from_float(nv * bf(router_scale[h])));  /* * scale */
+                n3[h] = bf16_from_float(n2 * root);                         /* * H^-0.5 */
+            }
+            if (normed_tap) memcpy(normed_tap + (size_t)t * H, n3, sizeof(uint16_t) * H);
+            /* Projection to E logits (dense bf16 weight [E,H], out = n W^T). */
+            for (int e = 0; e < E; ++e) {
+                const uint16_t* we = router_w + (size_t)e * H;
+                double acc = 0.0;
+                for (int h = 0; h < H; ++h) acc += (double)bf(n3[h]) * (double)bf(we[h]);
+                lex[e] = acc;
+                s[e] = bf16_from_double(acc);
+            }
+            if (logits_exact_tap) memcpy(logits_exact_tap + (size_t)t * E, lex, sizeof(double) * E);
+            if (scores_tap) memcpy(scores_tap + (size_t)t * E, s, sizeof(uint16_t) * E);
+            /* Top-k: k passes of "largest remaining score, lowest id on ties". */
+            for (int e = 0; e < E; ++e) taken[e] = 0;
+            int32_t* it = idx_out + (size_t)t * k;
+            for (int j = 0; j < k; ++j) {
+                int best = -1;
+                for (int e = 0; e < E; ++e) {
+                    if (taken[e]) continue;
+#if ORACLE_MUTANT == 2
+                    if (best < 0 || bf(s[e]) >= bf(s[best])) best = e; /* planted: ties to higher id */
+#else
+                    if (best < 0 || bf(s[e]) > bf(s[best])) best = e;
+#endif
+                }
+                taken[best] = 1;
+                it[j] = best;
+            }
+            /* Precise softmax over the k gathered scores, fp32. */
+            float mx = bf(s[it[0]]);
+            for (int j = 1; j < k; ++j)
+                if (bf(s[it[j]]) > mx) mx = bf(s[it[j]]);
+            float ex[64];
+            float sum = 0.0f;
+            for (int j = 0; j < k; ++j) {
+                ex[j] = (float)exp((double)(bf(s[it[j]]) - mx)); /* exp rounded to fp32 */
+                sum += ex[j];
+            }
+            uint16_t* wt = w_out + (size_t)t * k;
+            for (int j = 0; j < k; ++j) {
+                float p = bf(bf16_from_float(ex[j] / sum)); /* softmax output, bf16 */
+#if ORACLE_MUTANT == 3
+                wt[j] = bf16_from_float(p * bf(per_expert_scale[j])); /* planted: wrong gather */
+#else
+                wt[j] = bf16_from_float(p * bf(per_expert_scale[it[j]])); /* * pes[idx] */
+#endif
+            }
+        }
+        free(n3);
+        free(lex);
+        free(s);
+        free(taken);
+    }
+    return 0;
+}
+
+/* ----------------------------------------------------------- dispatch --- */
+
+/*
+ * The sorted path of DiffExperts.forward: order = argsort(idx.flat),
+ * invOrder = argsort(order), rowIdx = order // k. Read as a stable sort of
+ * the flat slots f = t*k + j by expert id (counting sort), so the result is
+ * unique: perm[p] = f (p-th slot in expert order), inv[f] = p, and
+ * offsets[e]..offsets[e+1] is expert e's slot range.
+ * Returns 0, or -1 on an expert id out of range.
+ */
+int oracle_dispatch(int32_t T, int32_t k, int32_t E, const int32_t* idx, int32_t* perm,
+                    int32_t* offsets, int32_t* inv) {
+    const int64_t S = (int64_t)T * k;
+    for (int e = 0; e <= E; ++e) offsets[e] = 0;
+    for (int64_t f = 0; f < S; ++f) {
+        if (idx[f] < 0 || idx[f] >= E) return -1;
+        offsets[idx[f] + 1] += 1;
+    }
+    for (int e = 0; e < E; ++e) offsets[e + 1] += offsets[e];
+    int32_t* next = (int32_t*)malloc(sizeof(int32_t) * (size_t)(E > 0 ? E : 1));
+    for (int e = 0; e < E; ++e) next[e] = offsets[e];
+#if ORACLE_MUTANT == 4
+    for (int64_t f = S - 1; f >= 0; --f) { /* planted: unstable (reverse) order */
+#else
+    for (int64_t f = 0; f < S; ++f) {
+#endif
+        int32_t p = next[idx[f]]++;
+        perm[p] = (int32_t)f;
+        inv[f] = p;
+    }
+    free(next);
+    return 0;
+}
+
+/* ------------------------------------------------------------ experts --- */
+
+/* Dequantise one expert's N x K block of a 4-bit affine weight:
+ * q = nibble (K mod 8) of word [n, K/8] (low nibble first),
+ * w = bf16(S[n, K/g] * q + B[n, K/g]) with one rounding. */
+static void dequant_expert(const uint32_t* w, const uint16_t* sc, const uint16_t* bi, int N, int K,
+                           int g, float* out) {
+    for (int n = 0; n < N; ++n) {
+        for (int kk = 0; kk < K; ++kk) {
+            uint32_t word = w[(size_t)n * (K / 8) + kk / 8];
+#if ORACLE_MUTANT == 5
+            int q = (int)((word >> (4 * (7 - kk % 8))) & 0xFu); /* planted: high nibble first */
+#else
+            int q = (int)((word >> (4 * (kk % 8))) & 0xFu);
+#endif
+            double S = bf(sc[(size_t)n * (K / g) + kk / g]);
+            double B = bf(bi[(size_t)n * (K / g) + kk / g]);
+            out[(size_t)n * K + kk] = bf(bf16_from_double(S * q + B));
+        }
+    }
+}
+
+/* gelu_approx(u) = 0.5 u (1 + tanh(sqrt(2/pi) (u + 0.044715 u^3))) */
+static double gelu_tanh(double u) {
+    const double c = sqrt(2.0 / 3.14159265358979323846);
+    return 0.5 * u * (1.0 + tanh(c * (u + 0.044715 * u * u * u)));
+}
+
+/*
+ * DiffExperts.forward: x [T,H], indices [T,k], weights [T,k] -> [T,H].
+ * For every slot f = t*k + j with expert e = idx[f]:
+ *   z = bf16(x[t] . W_gu[e]^T)           gate_up SwitchLinear, [2I]
+ *   gate = z[0:I], up = z[I:2I]          split at moe_intermediate
+ *   m = bf16(gelu_approx(gate) * up)     compiled geglu: one rounding
+ *   y = bf16(m . W_dn[e]^T)              down SwitchLinear, [H]
+ * and out[t] = bf16( sum_j bf16(y_{t,j} * w[t,j]) )   (mul, then sum over k).
+ * The sorted/unsorted choice on the page changes no value, so the oracle
+ * has one path. Optional taps (NULL to skip), per flat slot f:
+ * z_tap [T*k, 2I], m_tap [T*k, I], y_tap [T*k, H].
+ * Returns 0, or -1 on bad sizes / ids.
+ */
+int oracle_experts(const oracle_dims* d, const uint16_t* x, const int32_t* idx, const uint16_t* w,
+                   const uint32_t* gu_w, const uint16_t* gu_s, const uint16_t* gu_b,
+                   const uint32_t* dn_w, const uint16_t* dn_s, const uint16_t* dn_b, uint16_t* out,
+                   uint16_t* z_tap, uint16_t* m_tap, uint16_t* y_tap, int nthreads) {
+    const int T = d->T, H = d->H, E = d->E, k = d->k, I = d->inter, g = d->group;
+    if (T < 0 || H <= 0 || E <= 0 || k <= 0 || I <= 0 || g <= 0) return -1;
+    if (H % 8 || I % 8 || H % g || I % g || d->bits != 4) return -1;
+    const int64_t S = (int64_t)T * k;
+    for (int64_t f = 0; f < S; ++f)
+        if (idx[f] < 0 || idx[f] >= E) return -1;
+    set_threads(nthreads);
+    uint16_t* y_all = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(S > 0 ? S : 1) * H);
+    const size_t gu_words = (size_t)2 * I * (H / 8), gu_groups = (size_t)2 * I * (H / g);
+    const size_t dn_words = (size_t)H * (I / 8), dn_groups = (size_t)H * (I / g);
+
+#pragma omp parallel
+    {
+        float* wgu = (float*)malloc(sizeof(float) * (size_t)2 * I * H);
+        float* wdn = (float*)malloc(sizeof(float) * (size_t)H * I);
+        uint16_t* z = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)2 * I);
+        uint16_t* m = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)I);
+#pragma omp for schedule(dynamic, 1)
+        for (int e = 0; e < E; ++e) {
+            int used = 0;
+            for (int64_t f = 0; f < S && !used; ++f) used = (idx[f] == e);
+            if (!used) continue; /* an expert with no slots reads no weights */
+            dequant_expert(gu_w + e * gu_words, gu_s + e * gu_groups, gu_b + e * gu_groups, 2 * I, H,
+                           g, wgu);
+            dequant_expert(dn_w + e * dn_words, dn_s + e * dn_groups, dn_b + e * dn_groups, H, I, g,
+                           wdn);
+            for (int64_t f = 0; f < S; ++f) {
+                if (idx[f] != e) continue;
+                const uint16_t* xt = x + (size_t)(f / k) * H;
+                for (int n = 0; n < 2 * I; ++n) {
+                    const float* wr = wgu + (size_t)n * H;
+                    double acc = 0.0;
+                    for (int h = 0; h < H; ++h) acc += (double)bf(xt[h]) * (double)wr[h];
+                    z[n] = bf16_from_double(acc);
+                }
+                for (int n = 0; n < I; ++n) {
+#if ORACLE_MUTANT == 6
+                    m[n] = bf16_from_double(gelu_tanh(bf(z[n + I])) * (double)bf(z[n])); /* planted: halves swapped */
+#else
+                    m[n] = bf16_from_double(gelu_tanh(bf(z[n])) * (double)bf(z[n + I]));
+#endif
+                }
+                uint16_t* yf = y_all + (size_t)f * H;
+                for (int h = 0; h < H; ++h) {
+                    const float* wr = wdn + (size_t)h * I;
+                    double acc = 0.0;
+                    for (int n = 0; n < I; ++n) acc += (double)bf(m[n]) * (double)wr[n];
+                    yf[h] = bf16_from_double(acc);
+                }
+                if (z_tap) memcpy(z_tap + (size_t)f * 2 * I, z, sizeof(uint16_t) * 2 * I);
+                if (m_tap) memcpy(m_tap + (size_t)f * I, m, sizeof(uint16_t) * I);
+                if (y_tap) memcpy(y_tap + (size_t)f * H, yf, sizeof(uint16_t) * H);
+            }
+        }
+        free(wgu);
+        free(wdn);
+        free(z);
+        free(m);
+    }
+
+    /* (y * weights[..., None]).sum(-2): product in bf16, sum over k. */
+#pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; ++t) {
+        for (int h = 0; h < H; ++h) {
+            double acc = 0.0;
+            for (int j = 0; j < k; ++j) {
+                int64_t f = (int64_t)t * k + j;
+#if ORACLE_MUTANT == 7
+                acc += bf(y_all[(size_t)f * H + h]) * bf(w[f]) ; /* planted: product not rounded */
+#else
+                acc += bf(bf16_from_float(bf(y_all[(size_t)f * H + h]) * bf(w[f])));
+#endif
+            }
+            out[(size_t)t * H + h] = bf16_from_double(acc);
+        }
+    }
+    free(y_all);
+    return 0;
+}
+
+/* Router then experts on the same x: the layer as one call. */
+int oracle_forward(const oracle_dims* d, const uint16_t* x, const uint16_t* router_w,
+                   const uint16_t* router_scale, const uint16_t* per_expert_scale,
+                   const uint32_t* gu_w, const uint16_t* gu_s, const uint16_t* gu_b,
+                   const uint32_t* dn_w, const uint16_t* dn_s, const uint16_t* dn_b, uint16_t* out,
+                   int32_t* idx_out, uint16_t* w_out, int nthreads) {
+    int rc = oracle_route(d, x, router_w, router_scale, per_expert_scale, idx_out, w_out, NULL, NULL,
+                          NULL, nthreads);
+    if (rc) return rc;
+    return oracle_experts(d, x, idx_out, w_out, gu_w, gu_s, gu_b, dn_w, dn_s, dn_b, out, NULL, NULL,
+                          NULL, nthreads);
+}

@@ -1,0 +1,348 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle.
+
+Each check takes a loaded oracle library, so the same checks run against the
+oracle proper (tests/test_oracle_pins.py) and against builds of it with one
+planted mistake (tests/test_oracle_mutants.py), which they must catch.
+
+The references used here are independent of the oracle's code: closed forms,
+invariants, brute force over tiny inputs, numpy/torch library routines
+(float64 matmul, stable argsort, topk, gelu(approximate='tanh'), torch's
+float32 -> bf16 rounding), and a "nearest bf16" property that checks a
+rounded value against the exact one without re-implementing the rounding.
+"""
+from __future__ import annotations
+
+import dataclasses
+import json
+import math
+import os
+
+import numpy as np
+import torch
+
+import moe_synth as ms
+import oracle
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+# ----------------------------------------------------------------- helpers --
+def f64(bits) -> np.ndarray:
+    return ms.bits_to_f32(bits).astype(np.float64)
+
+
+def torch_bf16_bits(x_f32) -> np.ndarray:
+    """float32 -> bf16 bits via torch's own conversion (round to nearest even)."""
+    t = torch.from_numpy(np.ascontiguousarray(x_f32, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def neighbours(bits):
+    """The two bf16 values adjacent to each given bf16 value (as float64)."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.int32)
+    sign = b & 0x8000
+    mag = b & 0x7FFF
+    away = sign | np.minimum(mag + 1, 0x7F80)
+    toward = np.where(mag == 0, (sign ^ 0x8000) | 1, sign | (mag - 1))
+    return f64(away.astype(np.uint16)), f64(toward.astype(np.uint16))
+
+
+def assert_nearest_bf16(bits, exact, what: str, rel_slack: float = 0.0):
+    """Every bf16 value in `bits` is a nearest bf16 to the float64 `exact`."""
+    c = f64(bits)
+    exact = np.asarray(exact, dtype=np.float64)
+    a, t = neighbours(bits)
+    d0 = np.abs(c - exact)
+    slack = rel_slack * np.abs(exact)
+    ok = (d0 <= np.abs(a - exact) + slack) & (d0 <= np.abs(t - exact) + slack)
+    bad = np.flatnonzero(~ok.ravel())
+    assert bad.size == 0, (f"{what}: {bad.size} of {ok.size} values are not the nearest bf16; "
+                           f"first at {bad[0]}: got {c.ravel()[bad[0]]!r} for exact {exact.ravel()[bad[0]]!r}")
+
+
+def unpack_codes(w_words: np.ndarray, K: int) -> np.ndarray:
+    """[.., N, K/8] uint32 -> [.., N, K] codes, nibble j of word i is element 8i+j."""
+    shifts = (4 * np.arange(8, dtype=np.uint32))
+    q = (w_words[..., :, None] >> shifts) & np.uint32(0xF)
+    return q.reshape(*w_words.shape[:-1], K).astype(np.float64)
+
+
+def dense_dequant(w_words, s_bits, b_bits, K: int, g: int) -> np.ndarray:
+    """Dense dequantised weight bf16(S q + B) as float64, via float32 (where
+    S q + B is exact for these inputs) and torch's bf16 rounding."""
+    q = unpack_codes(w_words, K)
+    S = np.repeat(f64(s_bits), g, axis=-1)
+    B = np.repeat(f64(b_bits), g, axis=-1)
+    v = S * q + B
+    v32 = v.astype(np.float32)
+    assert np.array_equal(v32.astype(np.float64), v), "test input not exact in float32"
+    return f64(torch_bf16_bits(v32))
+
+
+def small_dims(**kw) -> ms.Dims:
+    base = dict(T=16, H=256, E=8, k=2, inter=128, group=64)
+    base.update(kw)
+    return ms.Dims(**base)
+
+
+def load_golden(name: str) -> dict:
+    with open(os.path.join(HERE, "golden", name)) as fh:
+        return json.load(fh)
+
+
+# --------------------------------------------------------- rounding pins --
+def check_bf16_from_float(lib):
+    rng = np.random.default_rng(1)
+    vals = np.concatenate([
+        rng.standard_normal(2000).astype(np.float32),
+        (rng.standard_normal(500) * 1e30).astype(np.float32),
+        (rng.standard_normal(500) * 1e-38).astype(np.float32),   # subnormal range
+        np.array([0.0, -0.0, 1.0, -1.0, 3.4e38, -3.4e38, 1.00390625, 1.01171875], np.float32),
+    ])
+    got = np.array([oracle.bf16_from_float(float(v), lib) for v in vals], np.uint16)
+    want = torch_bf16_bits(vals)
+    assert np.array_equal(got, want), "bf16_from_float disagrees with torch's RNE conversion"
+
+
+def check_bf16_from_double(lib):
+    rng = np.random.default_rng(2)
+    # float32-exact doubles: one rounding must equal torch's float32 -> bf16.
+    v32 = rng.standard_normal(1000).astype(np.float32)
+    got = np.array([oracle.bf16_from_double(float(v), lib) for v in v32], np.uint16)
+    assert np.array_equal(got, torch_bf16_bits(v32)), "bf16_from_double on float32-exact values"
+    # general doubles: nearest property.
+    vd = rng.standard_normal(1000) * np.exp(rng.uniform(-20, 20, 1000))
+    got = np.array([oracle.bf16_from_double(float(v), lib) for v in vd], np.uint16)
+    assert_nearest_bf16(got, vd, "bf16_from_double")
+    # exact ties go to even; a tie nudged by 2^-40 goes up (no double rounding).
+    one_plus = 1.0 + 2.0 ** -8            # halfway between 1 and 1+2^-7
+    assert oracle.bf16_from_double(one_plus, lib) == 0x3F80
+    assert oracle.bf16_from_double(one_plus + 2.0 ** -40, lib) == 0x3F81
+    three_half = 1.0 + 3 * 2.0 ** -8      # halfway between 1+2^-7 and 1+2^-6 -> even (1+2^-6)
+    assert oracle.bf16_from_double(three_half, lib) == 0x3F82
+    assert oracle.bf16_from_double(-one_plus - 2.0 ** -40, lib) == 0xBF81
+
+
+# ------------------------------------------------------------ router pins --
+def _route(lib, d, x, wr, sc, pes):
+    return oracle.route(d, x, wr, sc, pes, taps=True, lib=lib)
+
+
+def check_router_constant_row(lib):
+    """x = 1 everywhere, scale = 1: the norm gives 1 and the output is the
+    hidden**-0.5 scalar itself (H=256: 1/16 exactly; H=2816: golden)."""
+    golden = load_golden("router_root_bf16.json")
+    for H, want in ((256, 0x3D80), (golden["H"], int(golden["root_bits"], 16))):
+        d = small_dims(T=2, H=H, E=4, k=2)
+        x = np.full((d.T, H), 0x3F80, np.uint16)
+        _, sc, pes = ms.make_router(d)
+        sc = np.full(H, 0x3F80, np.uint16)
+        wr = ms.make_router(d)[0]
+        r = _route(lib, d, x, wr, sc, pes)
+        assert np.all(r["normed"] == want), f"constant row, H={H}: normed != {want:#06x}"
+
+
+def check_router_zero_row(lib):
+    """x = 0: every score is 0, the tie goes to the lowest ids and the
+    softmax is uniform: w_j = bf16(bf16(1/k) * pes[j])."""
+    d = small_dims(T=3, E=8, k=3)
+    inp = ms.make_custom(d)
+    x = np.zeros((d.T, d.H), np.uint16)
+    r = _route(lib, d, x, inp.router_w, inp.router_scale, inp.pes)
+    assert np.all(r["normed"] == 0)
+    assert np.array_equal(r["idx"], np.tile(np.arange(d.k, dtype=np.int32), (d.T, 1)))
+    p = torch.tensor(1.0 / d.k, dtype=torch.float32).to(torch.bfloat16)
+    pes = torch.from_numpy(ms.bits_to_f32(inp.pes[: d.k])).to(torch.bfloat16)
+    want = (p * pes).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(r["w"], np.tile(want, (d.T, 1))), "zero row: weights"
+
+
+def check_router_scale_invariance(lib):
+    """With eps = 0 the layer's router is invariant under x -> 2x, bit for bit."""
+    d = dataclasses.replace(small_dims(T=32, E=16, k=4), eps=0.0)
+    inp = ms.make_custom(d, seed=3)
+    x2 = ms.bf16_bits(ms.bits_to_f32(inp.x) * 2.0)
+    a = _route(lib, d, inp.x, inp.router_w, inp.router_scale, inp.pes)
+    b = _route(lib, d, x2, inp.router_w, inp.router_scale, inp.pes)
+    for key in ("normed", "idx", "w"):
+        assert np.array_equal(a[key], b[key]), f"x -> 2x changed {key}"
+
+
+def check_router_exact_math(lib):
+    """normed ~ x / sqrt(mean(x^2) + eps) * scale * H^-0.5 within the error of
+    its four roundings; mean(normed^2 / (scale H^-0.5)^2) ~ 1."""
+    d = small_dims(T=32, E=16, k=4)
+    inp = ms.make_custom(d, seed=4)
+    r = _route(lib, d, inp.x, inp.router_w, inp.router_scale, inp.pes)
+    x = f64(inp.x)
+    exact = x / np.sqrt(np.mean(x * x, axis=1, keepdims=True) + d.eps) * f64(inp.router_scale) * d.H ** -0.5
+    n = f64(r["normed"])
+    tol = 5 * 2.0 ** -8 * np.abs(exact) + 1e-30
+    assert np.all(np.abs(n - exact) <= tol), "normed far from the exact RMS-norm * scale * H^-0.5"
+
+
+def check_router_logits_topk(lib):
+    """scores = nearest bf16 of normed . W_r^T (float64 library matmul);
+    idx = first k of sorted by (score desc, id asc); torch.topk agrees
+    wherever the k-th and (k+1)-th scores differ."""
+    d = small_dims(T=64, E=16, k=4)
+    inp = ms.make_custom(d, seed=5)
+    r = _route(lib, d, inp.x, inp.router_w, inp.router_scale, inp.pes)
+    lg = f64(r["normed"]) @ f64(inp.router_w).T
+    assert np.allclose(r["logits"], lg, rtol=1e-12, atol=1e-15), "exact logits != library matmul"
+    assert_nearest_bf16(r["scores"], lg, "router scores")
+    s = f64(r["scores"])
+    for t in range(d.T):
+        want = sorted(range(d.E), key=lambda e: (-s[t, e], e))[: d.k]
+        assert list(r["idx"][t]) == want, f"top-k order, token {t}"
+        srt = np.sort(s[t])[::-1]
+        if srt[d.k - 1] != srt[d.k]:
+            tk = torch.topk(torch.from_numpy(s[t]), d.k).indices.numpy()
+            assert set(tk.tolist()) == set(want), f"torch.topk disagrees, token {t}"
+
+
+def check_router_weights(lib):
+    """w ~ softmax(scores[idx]) * pes[idx] (exact math, two bf16 roundings);
+    pes = 1 sums to 1 within k bf16 ulps; doubling pes doubles w exactly."""
+    d = small_dims(T=64, E=16, k=4)
+    inp = ms.make_custom(d, seed=6)
+    r = _route(lib, d, inp.x, inp.router_w, inp.router_scale, inp.pes)
+    s = np.take_along_axis(f64(r["scores"]), r["idx"].astype(np.int64), 1)
+    p = np.exp(s - s.max(1, keepdims=True))
+    p /= p.sum(1, keepdims=True)
+    exact = p * f64(inp.pes)[r["idx"]]
+    assert np.all(np.abs(f64(r["w"]) - exact) <= 2 * 2.0 ** -8 * exact), "routing weights"
+    ones = np.full_like(inp.pes, 0x3F80)
+    r1 = _route(lib, d, inp.x, inp.router_w, inp.router_scale, ones)
+    assert np.all(np.abs(f64(r1["w"]).sum(1) - 1.0) <= d.k * 2.0 ** -8), "pes=1: sum of w"
+    pes2 = ms.bf16_bits(ms.bits_to_f32(inp.pes) * 2.0)
+    r2 = _route(lib, d, inp.x, inp.router_w, inp.router_scale, pes2)
+    assert np.array_equal(r2["idx"], r["idx"])
+    assert np.array_equal(f64(r2["w"]), 2.0 * f64(r["w"])), "pes*2 must give w*2 exactly"
+
+
+# ---------------------------------------------------------- dispatch pins --
+def check_dispatch(lib):
+    rng = np.random.default_rng(7)
+    for T, k, E in ((1, 1, 1), (16, 2, 8), (100, 8, 128), (37, 3, 11)):
+        idx = rng.integers(0, max(1, E // 2 + 1), size=(T, k)).astype(np.int32)  # leaves experts empty
+        idx[0, 0] = E - 1
+        perm, off, inv = oracle.dispatch(T, k, E, idx, lib=lib)
+        flat = idx.ravel()
+        assert np.array_equal(perm, np.argsort(flat, kind="stable")), "perm != stable argsort"
+        assert np.array_equal(off, np.concatenate([[0], np.cumsum(np.bincount(flat, minlength=E))]))
+        assert np.array_equal(np.sort(perm), np.arange(T * k)), "perm is not a bijection"
+        assert np.array_equal(inv[perm], np.arange(T * k)), "inv is not perm's inverse"
+        assert np.all(flat[perm][:-1] <= flat[perm][1:])
+
+
+# ----------------------------------------------------------- expert pins --
+def check_experts_brute_force(lib):
+    """z, m, y and out of every slot against a dense float64 computation of
+    the same layer (library matmul, torch gelu tanh, torch bf16 rounding)."""
+    d = small_dims(T=8, E=4, k=2)
+    inp = ms.make_custom(d, seed=8)
+    rt = oracle.route(d, inp.x, inp.router_w, inp.router_scale, inp.pes, lib=lib)
+    out, z, m, y = oracle.experts(d, inp.x, rt["idx"], rt["w"], (inp.gu_w, inp.gu_s, inp.gu_b),
+                                  (inp.dn_w, inp.dn_s, inp.dn_b), taps=True, lib=lib)
+    I, H = d.inter, d.H
+    x = f64(inp.x)
+    for f in range(d.T * d.k):
+        t, e = f // d.k, int(rt["idx"].ravel()[f])
+        wgu = dense_dequant(inp.gu_w[e], inp.gu_s[e], inp.gu_b[e], H, d.group)
+        wdn = dense_dequant(inp.dn_w[e], inp.dn_s[e], inp.dn_b[e], I, d.group)
+        assert_nearest_bf16(z[f], wgu @ x[t], f"gate_up output, slot {f}")
+        zz = torch.from_numpy(f64(z[f]))
+        mm = torch.nn.functional.gelu(zz[:I], approximate="tanh") * zz[I:]
+        assert_nearest_bf16(m[f], mm.numpy(), f"GeGLU output, slot {f}", rel_slack=1e-12)
+        assert_nearest_bf16(y[f], wdn @ f64(m[f]), f"down output, slot {f}")
+    prods = f64(torch_bf16_bits(ms.bits_to_f32(y) * ms.bits_to_f32(rt["w"]).reshape(-1, 1)))
+    assert_nearest_bf16(out, prods.reshape(d.T, d.k, H).sum(1), "combine")
+
+
+def check_experts_one_hot(lib):
+    """Closed form. All codes 8 with S = 1, B = -8 make every weight 0, except
+    gate (n0, K0) = +1, up (I+n0, K1) = +2 and down (h0, n0) = +3. With k = 1
+    and pes = 1 the weight is 1, so out[t, h0] = bf16(3 m), with
+    m = bf16(gelu_tanh(x[t,K0]) * 2 x[t,K1]), and out is 0 elsewhere."""
+    d = small_dims(T=4, E=2, k=1)
+    inp = ms.make_custom(d, seed=9)
+    I, H, g = d.inter, d.H, d.group
+    n0, K0, K1, h0 = 37, 70, 201, 133
+    gu_w = np.full((d.E, 2 * I, H // 8), 0x88888888, np.uint32)
+    dn_w = np.full((d.E, H, I // 8), 0x88888888, np.uint32)
+    for e in range(d.E):
+        gu_w[e, n0, K0 // 8] = np.uint32(0x88888888 ^ (0x1 << (4 * (K0 % 8))))   # 8 -> 9
+        gu_w[e, I + n0, K1 // 8] = np.uint32(0x88888888 ^ (0x2 << (4 * (K1 % 8))))  # 8 -> 10
+        dn_w[e, h0, n0 // 8] = np.uint32(0x88888888 ^ (0x3 << (4 * (n0 % 8))))   # 8 -> 11
+    ones_g = lambda n, kk: np.full((d.E, n, kk // g), 0x3F80, np.uint16)
+    m8_g = lambda n, kk: np.full((d.E, n, kk // g), 0xC100, np.uint16)          # -8.0
+    idx = np.zeros((d.T, 1), np.int32)
+    idx[1::2] = 1
+    w = np.full((d.T, 1), 0x3F80, np.uint16)
+    out = oracle.experts(d, inp.x, idx, w, (gu_w, ones_g(2 * I, H), m8_g(2 * I, H)),
+                         (dn_w, ones_g(H, I), m8_g(H, I)), lib=lib)
+    x = f64(inp.x)
+    for t in range(d.T):
+        gate = torch.tensor(x[t, K0], dtype=torch.float64)
+        mval = (torch.nn.functional.gelu(gate, approximate="tanh") * 2.0 * x[t, K1]).item()
+        mbits = np.array([oracle.bf16_from_double(mval, lib)], np.uint16)  # helper pinned above
+        assert_nearest_bf16(mbits, [mval], "m")
+        mb = f64(mbits)[0]
+        want = np.zeros(H)
+        want[h0] = f64(torch_bf16_bits(np.float32(3.0 * mb)))[0]
+        assert np.array_equal(f64(out[t]), want), f"one-hot layer, token {t}"
+
+
+def check_single_expert_identity(lib):
+    """E = 1, k = 1, pes = 1: softmax of one score is 1, so w = 1 exactly and
+    the layer is the dense 4-bit GeGLU MLP: out = y."""
+    d = small_dims(T=8, E=1, k=1)
+    inp = ms.make_custom(d, seed=10)
+    pes = np.full(1, 0x3F80, np.uint16)
+    rt = oracle.route(d, inp.x, inp.router_w, inp.router_scale, pes, lib=lib)
+    assert np.all(rt["idx"] == 0) and np.all(rt["w"] == 0x3F80)
+    out, z, m, y = oracle.experts(d, inp.x, rt["idx"], rt["w"], (inp.gu_w, inp.gu_s, inp.gu_b),
+                                  (inp.dn_w, inp.dn_s, inp.dn_b), taps=True, lib=lib)
+    assert np.array_equal(out, y), "single expert: out != y"
+
+
+def check_expert_relabel(lib):
+    """Renaming the experts (router rows, pes, weights permuted together)
+    leaves the layer output unchanged on tokens without a score tie at the
+    top-k boundary."""
+    d = small_dims(T=32, E=8, k=2)
+    inp = ms.make_custom(d, seed=11)
+    out_a, idx_a, _ = oracle.forward(inp, lib=lib)
+    pi = np.random.default_rng(12).permutation(d.E)
+    perm_inp = dataclasses.replace(
+        inp, router_w=inp.router_w[pi], pes=inp.pes[pi], gu_w=inp.gu_w[pi], gu_s=inp.gu_s[pi],
+        gu_b=inp.gu_b[pi], dn_w=inp.dn_w[pi], dn_s=inp.dn_s[pi], dn_b=inp.dn_b[pi])
+    out_b, idx_b, _ = oracle.forward(perm_inp, lib=lib)
+    sc = f64(oracle.route(d, inp.x, inp.router_w, inp.router_scale, inp.pes, taps=True, lib=lib)["scores"])
+    srt = -np.sort(-sc, 1)
+    clean = srt[:, d.k - 1] != srt[:, d.k]
+    assert clean.sum() > d.T // 2
+    for t in np.flatnonzero(clean):
+        assert set(pi[idx_b[t]].tolist()) == set(idx_a[t].tolist()), f"relabelled routing, token {t}"
+    assert np.array_equal(out_a[clean], out_b[clean]), "relabelling experts changed the output"
+
+
+def check_token_permutation(lib):
+    """Tokens are independent: permuting them permutes the output rows."""
+    d = small_dims(T=24, E=8, k=2)
+    inp = ms.make_custom(d, seed=13)
+    out_a, _, _ = oracle.forward(inp, lib=lib)
+    pi = np.random.default_rng(14).permutation(d.T)
+    out_b, _, _ = oracle.forward(dataclasses.replace(inp, x=inp.x[pi]), lib=lib)
+    assert np.array_equal(out_b, out_a[pi]), "token permutation"
+
+
+ALL_CHECKS = [
+    check_bf16_from_float, check_bf16_from_double,
+    check_router_constant_row, check_router_zero_row, check_router_scale_invariance,
+    check_router_exact_math, check_router_logits_topk, check_router_weights,
+    check_dispatch,
+    check_experts_brute_force, check_experts_one_hot, check_single_expert_identity,
+    check_expert_relabel, check_token_permutation,
+]
