@@ -1,0 +1,343 @@
+"""Throughput of the routed 4-bit MoE layer on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload canvas] [--impl ours|reference]
+
+One step = one whole layer call (router, dispatch, gather, gate_up + GeGLU,
+down, combine) on one batch of synthetic tokens of the named workload
+(default: the decoder canvas pass, T=256, H=2816, E=128, k=8, inter=704,
+4-bit g64 weights). With N > 1 (torchrun) every rank runs its own replica on
+its own batch (weak scaling, no collective on the data path).
+
+Prints ONE JSON line (rank 0). `value` is tokens/s with the inputs resident
+in HBM, timed with CUDA events around each layer call on its stream; L2 is
+flushed (256 MB memset) between steps, outside the timed events. `e2e` is the
+same metric through moe_forward_hostio (pinned host x in, host out, copies
+inside the timed call). `roofline` is for the dominant kernel (gate_up),
+timed with the library's own CUDA events on the launching stream.
+`cpu_baseline` times the CPU oracle on a bounded sample of the workload.
+`--impl reference` times the CPU oracle alone (the only reference there is).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import moe_synth as ms  # noqa: E402
+
+METRIC = "MoE-layer tokens/s at T=256 canvas (H=2816,E=128,k=8); % of HBM/TC roofline"
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            j = json.load(fh)
+        return dict(hbm=j["hbm_gbs"], tc=j["bf16_tflops"], tc_sustained=j.get("bf16_tflops_sustained"),
+                    source="measured")
+    return dict(hbm=6800.0, tc=1900.0, tc_sustained=1700.0, source="fallback")
+
+
+def layer_bytes(d: ms.Dims):
+    """Algorithmic bytes of one expert's weights: (gate_up, down)."""
+    g = d.group
+    gu = 2 * d.inter * d.H // 2 + 2 * (2 * d.inter * d.H // g) * 2
+    dn = d.H * d.inter // 2 + 2 * (d.H * d.inter // g) * 2
+    return gu, dn
+
+
+def roofline_model(d: ms.Dims, touched: int, peaks):
+    gu, dn = layer_bytes(d)
+    S = d.T * d.k
+    bytes_alg = touched * (gu + dn) + d.E * d.H * 2 + d.H * 2 + d.E * 2 + 2 * d.T * d.H * 2
+    flops = 2 * d.T * d.H * d.E + S * (2 * d.H * 2 * d.inter + 2 * d.inter * d.H)
+    t_hbm = bytes_alg / (peaks["hbm"] * 1e9)
+    t_tc = flops / (peaks["tc"] * 1e12)
+    return dict(bytes=bytes_alg, flops=flops, t_roof_s=max(t_hbm, t_tc), bound="hbm" if t_hbm >= t_tc else "tensor")
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        rows = []
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            try:
+                rows.append(dict(sm=float(f[1]), smmax=float(f[2]), power=float(f[3]),
+                                 hw=f[5], hwt=f[6], swt=f[7], pcap=f[8]))
+            except (ValueError, IndexError):
+                continue
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return dict(sm_mhz=statistics.median(r["sm"] for r in rows), sm_max_mhz=max(r["smmax"] for r in rows),
+                    power_w_max=max(r["power"] for r in rows), samples=len(rows), reasons=sorted(reasons))
+
+
+def cores_available() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_sample(wl: ms.Workload, target_s: float = 8.0, max_tokens: int | None = None):
+    """Time the CPU oracle on a growing prefix of the workload's tokens until a
+    call takes target_s (bounded). Returns (tokens/s, tokens, seconds, threads)."""
+    import oracle
+    oracle.build()
+    full = ms.make_layer(wl)
+    n = 8
+    limit = max_tokens or full.dims.T
+    while True:
+        d = ms.Dims(**{**full.dims.__dict__, "T": n})
+        inp = ms.LayerInputs(d, full.x[:n], full.router_w, full.router_scale, full.pes, full.gu_w, full.gu_s,
+                             full.gu_b, full.dn_w, full.dn_s, full.dn_b)
+        t0 = time.perf_counter()
+        oracle.forward(inp)
+        dt = time.perf_counter() - t0
+        if dt >= target_s or n >= limit:
+            return n / dt, n, dt, oracle.max_threads()
+        n = min(limit, n * 2 if dt < target_s / 3 else int(n * target_s / dt) + 1)
+
+
+def run_reference(args, wl):
+    """--impl reference: the CPU oracle on the host cores (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    tps, n, dt, threads = oracle_sample(wl, target_s=min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    full = ms.make_layer(wl)
+    d = ms.Dims(**{**full.dims.__dict__, "T": n})
+    inp = ms.LayerInputs(d, full.x[:n], full.router_w, full.router_scale, full.pes, full.gu_w, full.gu_s,
+                         full.gu_b, full.dn_w, full.dn_s, full.dn_b)
+    for _ in range(args.warmup):
+        oracle.forward(inp)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.forward(inp)
+        times.append(time.perf_counter() - t0)
+    value = n / statistics.mean(times)
+    line = dict(metric=METRIC, value=value, unit="tokens/s", impl="reference", n_gpus=args.gpus,
+                steps=args.steps, warmup=args.warmup, ms_per_step=1e3 * statistics.mean(times),
+                higher_is_better=True, scaling="weak", vs_baseline=None, dtype="bf16", data="synthetic",
+                config=dict(workload=wl_desc(wl), sample_tokens=n),
+                cpu_baseline=dict(value=value, unit="tokens/s", cores=threads, kind="oracle",
+                                  sample=f"first {n} of {full.dims.T} tokens of the {wl.name} workload, "
+                                         f"per step"),
+                e2e=dict(value=value, unit="tokens/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    print(json.dumps(line), flush=True)
+
+
+def wl_desc(wl):
+    d = wl.dims
+    return (f"{wl.name}: T={d.T} H={d.H} E={d.E} k={d.k} inter={d.inter} group={d.group} 4-bit affine, "
+            f"bf16 activations" + (f", Zipf({wl.zipf_s}) skew" if wl.skew_kappa else ""))
+
+
+def traffic_from_profile(name: str, src_hash: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as fh:
+        j = json.load(fh)
+    e = j.get(name)
+    if not e or e.get("source_sha1") != src_hash:
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def run_ours(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    import bit_quantized_moe_layer_gb300 as moe
+    from bit_quantized_moe_layer_gb300 import build as lib_build
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    torch.cuda.set_device(local)
+    lib_build.build()
+    moe.load()
+    peaks = load_peaks()
+
+    inp = ms.make_layer(wl, seed=wl.seed + rank)  # each replica its own batch
+    d = moe.dims_of(inp.dims)
+    layer = moe.to_device_layer(inp)
+    x = torch.from_numpy(inp.x.view(np.int16).copy()).cuda()
+    out = torch.empty((d.T, d.H), dtype=torch.int16, device="cuda")
+    idx = torch.empty((d.T, d.k), dtype=torch.int32, device="cuda")
+    wts = torch.empty((d.T, d.k), dtype=torch.int16, device="cuda")
+    ws = torch.empty(moe.workspace_bytes(d), dtype=torch.uint8, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        moe.moe_forward(d, x, layer.router_w, layer.router_scale, layer.pes, layer.gate_up, layer.down, out,
+                        idx, wts, ws, ws.numel(), stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    touched = int(np.unique(idx.cpu().numpy()).size)
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    moe.timing_enable(True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    stage_ms, calls = moe.timing_read()
+    moe.timing_enable(False)
+    err = moe.device_error()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms_step = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([ms_step], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+
+    # end to end through the host-buffer call (x in, out back, copies inside)
+    x_host = torch.from_numpy(inp.x.view(np.int16).copy()).pin_memory()
+    out_host = torch.empty((d.T, d.H), dtype=torch.int16).pin_memory()
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        moe.moe_forward_hostio(d, x_host, layer.router_w, layer.router_scale, layer.pes, layer.gate_up,
+                               layer.down, out_host, ws, ws.numel(), stream)
+        if i >= args.warmup:
+            e2e_ms.append(1e3 * (time.perf_counter() - t0))
+    e2e_step = statistics.mean(e2e_ms)
+    if world > 1:
+        t = torch.tensor([e2e_step], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_step = float(t.item())
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    gu_bytes, dn_bytes = layer_bytes(inp.dims)
+    gu_ms = stage_ms["gate_up"] / max(1, calls)
+    achieved = touched * gu_bytes / (gu_ms * 1e-3) / 1e9
+    with open(os.path.join(ROOT, "bit_quantized_moe_layer_gb300", "csrc", "grouped_gemm.cu"), "rb") as fh:
+        src_hash = hashlib.sha1(fh.read()).hexdigest()
+    model = roofline_model(inp.dims, touched, peaks)
+    value = world * d.T / (ms_step * 1e-3)
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        tps, n, dt, threads = oracle_sample(wl, target_s=args.cpu_seconds)
+        cpu = dict(value=tps, unit="tokens/s", cores=threads, kind="oracle",
+                   sample=f"first {n} of {d.T} tokens of the {wl.name} workload, one oracle call ({dt:.1f} s)")
+    line = dict(
+        metric=METRIC, value=value, unit="tokens/s", n_gpus=world, steps=args.steps, warmup=args.warmup,
+        ms_per_step=ms_step, higher_is_better=True, scaling="weak", vs_baseline=None, dtype="bf16",
+        data="synthetic (seeded; no checkpoint on the pages)",
+        config=dict(workload=wl_desc(wl), global_batch=world * d.T, tokens_per_gpu=d.T, parallelism=f"replicas x{world}",
+                    l2="flushed between steps: 256 MB memset outside the timed events",
+                    experts_touched=touched),
+        roofline=dict(bound="hbm", achieved=achieved, peak=peaks["hbm"], unit="GB/s", frac=achieved / peaks["hbm"],
+                      traffic=traffic_from_profile(f"gate_up:{wl.name}", src_hash), kernel="grouped_gemm gate_up",
+                      bytes_per_launch=touched * gu_bytes, ms_per_launch=gu_ms,
+                      peak_source=f"{peaks['source']} hbm_gbs (copy)"),
+        layer_roofline=dict(bound=model["bound"], t_roof_us=model["t_roof_s"] * 1e6, t_step_us=ms_step * 1e3,
+                            frac=model["t_roof_s"] / (ms_step * 1e-3), bytes=model["bytes"], flops=model["flops"]),
+        stages_ms_per_call={k: v / max(1, calls) for k, v in stage_ms.items()},
+        cpu_baseline=cpu,
+        e2e=dict(value=world * d.T / (e2e_step * 1e-3), unit="tokens/s", h2d_bytes_per_step=d.T * d.H * 2,
+                 d2h_bytes_per_step=d.T * d.H * 2, ms_per_step=e2e_step),
+        gpu_launches=moe.launches_per_forward() * args.steps,
+        clocks=clk.summary(),
+        device_error=err,
+    )
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="canvas", choices=sorted(ms.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=8.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    wl = ms.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

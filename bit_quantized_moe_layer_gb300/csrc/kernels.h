@@ -1,0 +1,80 @@
+// Internal interface between the C-ABI host code (moe_api.cu) and the
+// kernels. Not installed; the public interface is include/moe.h.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// Router: x [T,H] -> idx [T,k], w [T,k].
+struct RouterArgs {
+    const uint16_t* x;
+    const uint16_t* router_w;
+    const uint16_t* router_scale;
+    const uint16_t* per_expert_scale;
+    int32_t* idx;
+    uint16_t* w;
+    int T, H, E, k;
+    float eps;
+    float root;  // bf16(H^-0.5) as a float
+};
+size_t router_smem_bytes(int H, int E);
+cudaError_t launch_router(const RouterArgs& a, cudaStream_t stream);
+int router_error_word();
+
+// A token tile of one expert: rows [p0, p0 + rows) of the expert-sorted slots.
+struct Tile {
+    int e, p0, rows, pad;
+};
+
+// Dispatch: stable counting sort of the flat slots by expert + tile list.
+struct DispatchArgs {
+    const int32_t* idx;  // [S]
+    int32_t* perm;       // [S]
+    int32_t* offsets;    // [E+1]
+    int32_t* inv;        // [S]
+    Tile* tiles;         // [max_tiles] (may be null)
+    int32_t* num_tiles;  // [1] (may be null)
+    int S, E, nmax;      // nmax: rows per token tile
+};
+cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream);
+
+// Gather: xs[p] = x[perm[p] / k] with each 8-element block of K stored in
+// the order (0,4,1,5,2,6,3,7), the order the grouped GEMM's dequantised
+// weights come out in.
+cudaError_t launch_gather(const uint16_t* x, const int32_t* perm, const int32_t* offsets, uint16_t* xs,
+                          int S, int k, int H, int E, cudaStream_t stream);
+
+// Combine: out[t] = bf16(sum_j bf16(y[t*k+j] * w[t*k+j])), fp32 sum in j order.
+cudaError_t launch_combine(const uint16_t* y, const uint16_t* w, uint16_t* out, int T, int k, int H,
+                           cudaStream_t stream);
+int dispatch_error_word();
+
+// Grouped dequant-GEMM on tcgen05 (one expert per token tile).
+enum GemmMode { kGateUp = 0, kDown = 1 };
+struct GemmArgs {
+    const uint16_t* scales;   // [E, N, K/64]
+    const uint16_t* biases;   // [E, N, K/64]
+    const Tile* tiles;
+    const int32_t* num_tiles;
+    const int32_t* perm;      // down: flat slot of each sorted row
+    uint16_t* out;            // gate_up: mid [S, inter]; down: y [S, H] by flat slot
+    int K;                    // reduction length (H or inter)
+    int N;                    // rows of the weight (2*inter or H)
+    int inter;                // gate_up: split point
+    int out_ld;               // row length of out (inter or H)
+    int nmax;                 // rows per token tile (64 or 128)
+    int n_tiles;              // weight-row tiles per token tile
+    int stages;               // smem pipeline depth
+};
+// wmap: packed weights as uint32 [E*N rows, K/8], box {32, 64 or 128}, 128B swizzle.
+// bmap: B operand (xs or mid) as bf16 [S rows, K], box {64, 16}, 128B swizzle.
+size_t gemm_smem_bytes(int mode, int K, int nmax, int stages);
+int gemm_max_stages(int mode, int K, int nmax);
+cudaError_t launch_gemm(int mode, const CUtensorMap& wmap, const CUtensorMap& bmap, const GemmArgs& a,
+                        int grid, cudaStream_t stream);
+int gemm_error_word();
+
+}  // namespace moe

@@ -1,0 +1,452 @@
+// C ABI of libmoe (declared in include/moe.h): argument checks, workspace
+// layout, TMA descriptors and the launch sequence of the routed 4-bit MoE
+// layer (DiffRouter + DiffExperts of "diffusion-gemma/model.ts").
+//
+// All checks happen on the host before anything is enqueued; the CUDA
+// runtime is touched only after the arguments passed, so the checks work on
+// a machine without a GPU.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+#include <vector>
+
+#include "../../include/moe.h"
+#include "kernels.h"
+
+using namespace moe;
+
+namespace {
+
+constexpr int kStages = 6;  // route, dispatch, gather, gate_up, down, combine
+constexpr int kMaxTimedCalls = 1024;
+
+// --------------------------------------------------------------- checks --
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_dims(const moe_dims* d) {
+    if (!d) return MOE_ERR_NULL;
+    if (d->T < 0 || d->H <= 0 || d->E <= 0 || d->k <= 0 || d->inter <= 0) return MOE_ERR_SHAPE;
+    if (d->bits != 4 || d->group != 64) return MOE_ERR_UNSUPPORTED;
+    if (d->H % 128 != 0 || d->inter % 64 != 0 || d->H > 6144) return MOE_ERR_UNSUPPORTED;
+    if (d->k > 32 || d->k > d->E || d->E > 256) return MOE_ERR_UNSUPPORTED;
+    if ((int64_t)d->T * d->k > (int64_t)1 << 28) return MOE_ERR_SHAPE;
+    if (!(d->eps >= 0.0f) || isinf(d->eps)) return MOE_ERR_SHAPE;
+    return MOE_OK;
+}
+
+int check_ptrs(std::initializer_list<const void*> ps) {
+    for (const void* p : ps)
+        if (!p) return MOE_ERR_NULL;
+    for (const void* p : ps)
+        if (!aligned16(p)) return MOE_ERR_ALIGN;
+    return MOE_OK;
+}
+
+int check_qweight(const moe_qweight* q) {
+    if (!q) return MOE_ERR_NULL;
+    return check_ptrs({q->w, q->scales, q->biases});
+}
+
+// --------------------------------------------------------------- device --
+struct DeviceInfo {
+    int sms = 0;
+    bool ok = false;
+};
+
+int device_info(DeviceInfo* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_DEVICE;
+    static std::mutex mu;
+    static std::vector<DeviceInfo> cache;
+    std::lock_guard<std::mutex> lock(mu);
+    if ((int)cache.size() <= dev) cache.resize(dev + 1);
+    if (!cache[dev].ok) {
+        int major = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+            return MOE_ERR_DEVICE;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ERR_DEVICE;
+        if (major != 10) return MOE_ERR_DEVICE;  // tcgen05 needs the sm_100 family
+        cache[dev].sms = sms;
+        cache[dev].ok = true;
+    }
+    *out = cache[dev];
+    return MOE_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void* ptr, uint64_t inner,
+                 uint64_t rows, uint32_t box_inner, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {inner * esize};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// bf16(x) of a double, one rounding to nearest even (x > 0, normal range).
+float bf16_round(double x) {
+    int e;
+    frexp(x, &e);
+    const double q = ldexp(1.0, e - 8);
+    return (float)(nearbyint(x / q) * q);
+}
+
+// ------------------------------------------------------------ workspace --
+struct Layout {
+    size_t idx, w, perm, inv, offsets, tiles, ntiles, xs, mid, y, xdev, outdev, total;
+    int max_tiles;
+};
+
+size_t up256(size_t v) { return (v + 255) & ~size_t(255); }
+
+Layout layout(const moe_dims* d) {
+    Layout L;
+    const size_t S = (size_t)d->T * d->k;
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = o;
+        o = up256(o + (bytes ? bytes : 1));
+        return at;
+    };
+    L.max_tiles = d->E + (int)((S + 15) / 16);
+    L.idx = take(S * 4);
+    L.w = take(S * 2);
+    L.perm = take(S * 4);
+    L.inv = take(S * 4);
+    L.offsets = take((size_t)(d->E + 1) * 4);
+    L.tiles = take((size_t)L.max_tiles * sizeof(Tile));
+    L.ntiles = take(4);
+    L.xs = take(S * d->H * 2);
+    L.mid = take(S * d->inter * 2);
+    L.y = take(S * d->H * 2);
+    L.xdev = take((size_t)d->T * d->H * 2);
+    L.outdev = take((size_t)d->T * d->H * 2);
+    L.total = o;
+    return L;
+}
+
+// Library-owned grow-only workspace, one per device.
+int owned_workspace(size_t bytes, void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_DEVICE;
+    static std::mutex mu;
+    static std::vector<std::pair<void*, size_t>> bufs;
+    std::lock_guard<std::mutex> lock(mu);
+    if ((int)bufs.size() <= dev) bufs.resize(dev + 1, {nullptr, 0});
+    if (bufs[dev].second < bytes) {
+        if (bufs[dev].first) {
+            cudaDeviceSynchronize();
+            cudaFree(bufs[dev].first);
+        }
+        bufs[dev] = {nullptr, 0};
+        void* p = nullptr;
+        if (cudaMalloc(&p, bytes) != cudaSuccess) return MOE_ERR_CUDA;
+        bufs[dev] = {p, bytes};
+    }
+    *out = bufs[dev].first;
+    return MOE_OK;
+}
+
+// --------------------------------------------------------------- timing --
+struct Timing {
+    bool enabled = false;
+    std::vector<cudaEvent_t> ev;  // kMaxTimedCalls * (kStages + 1)
+    int calls = 0;
+    std::mutex mu;
+};
+Timing& timing() {
+    static Timing t;
+    return t;
+}
+
+// Records boundary b (0..kStages) of the current timed call, if any.
+struct CallTimer {
+    cudaEvent_t* ev = nullptr;
+    cudaStream_t s;
+    explicit CallTimer(cudaStream_t st) : s(st) {
+        Timing& t = timing();
+        std::lock_guard<std::mutex> lock(t.mu);
+        if (t.enabled && t.calls < kMaxTimedCalls) {
+            ev = &t.ev[(size_t)t.calls * (kStages + 1)];
+            ++t.calls;
+        }
+    }
+    void mark(int b) {
+        if (ev) cudaEventRecord(ev[b], s);
+    }
+};
+
+int fail(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// ------------------------------------------------------------- pipeline --
+int run_experts(const moe_dims* d, const uint16_t* x, const int32_t* idx, const uint16_t* w,
+                const moe_qweight* gu, const moe_qweight* dn, uint16_t* out, uint8_t* ws, const Layout& L,
+                const DeviceInfo& di, cudaStream_t s, CallTimer& tm) {
+    const int S = d->T * d->k;
+    const int E = d->E, H = d->H, I = d->inter;
+    int32_t* perm = reinterpret_cast<int32_t*>(ws + L.perm);
+    int32_t* inv = reinterpret_cast<int32_t*>(ws + L.inv);
+    int32_t* offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
+    Tile* tiles = reinterpret_cast<Tile*>(ws + L.tiles);
+    int32_t* ntiles = reinterpret_cast<int32_t*>(ws + L.ntiles);
+    uint16_t* xs = reinterpret_cast<uint16_t*>(ws + L.xs);
+    uint16_t* mid = reinterpret_cast<uint16_t*>(ws + L.mid);
+    uint16_t* y = reinterpret_cast<uint16_t*>(ws + L.y);
+    const int nmax = (S / E > 40) ? 128 : 64;
+
+    CUtensorMap m_gu, m_dn, m_xs, m_mid;
+    if (!make_map_2d(&m_gu, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, gu->w, H / 8, (uint64_t)E * 2 * I, 32, 64) ||
+        !make_map_2d(&m_dn, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, dn->w, I / 8, (uint64_t)E * H, 32, 128) ||
+        !make_map_2d(&m_xs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, xs, H, S, 64, 16) ||
+        !make_map_2d(&m_mid, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, mid, I, S, 64, 16))
+        return MOE_ERR_CUDA;
+
+    DispatchArgs da{idx, perm, offsets, inv, tiles, ntiles, S, E, nmax};
+    int rc = fail(launch_dispatch(da, s));
+    if (rc) return rc;
+    tm.mark(2);
+    rc = fail(launch_gather(x, perm, offsets, xs, S, d->k, H, E, s));
+    if (rc) return rc;
+    tm.mark(3);
+
+    GemmArgs ga{};
+    ga.scales = gu->scales;
+    ga.biases = gu->biases;
+    ga.tiles = tiles;
+    ga.num_tiles = ntiles;
+    ga.perm = perm;
+    ga.out = mid;
+    ga.K = H;
+    ga.N = 2 * I;
+    ga.inter = I;
+    ga.out_ld = I;
+    ga.nmax = nmax;
+    ga.n_tiles = I / 64;
+    ga.stages = gemm_max_stages(kGateUp, H, nmax);
+    int grid = di.sms;
+    if ((long)L.max_tiles * ga.n_tiles < grid) grid = L.max_tiles * ga.n_tiles;
+    rc = fail(launch_gemm(kGateUp, m_gu, m_xs, ga, grid, s));
+    if (rc) return rc;
+    tm.mark(4);
+
+    GemmArgs gd = ga;
+    gd.scales = dn->scales;
+    gd.biases = dn->biases;
+    gd.out = y;
+    gd.K = I;
+    gd.N = H;
+    gd.inter = I;
+    gd.out_ld = H;
+    gd.n_tiles = H / 128;
+    gd.stages = gemm_max_stages(kDown, I, nmax);
+    grid = di.sms;
+    if ((long)L.max_tiles * gd.n_tiles < grid) grid = L.max_tiles * gd.n_tiles;
+    rc = fail(launch_gemm(kDown, m_dn, m_mid, gd, grid, s));
+    if (rc) return rc;
+    tm.mark(5);
+
+    rc = fail(launch_combine(y, w, out, d->T, d->k, H, s));
+    if (rc) return rc;
+    tm.mark(6);
+    return MOE_OK;
+}
+
+int route_impl(const moe_dims* d, const uint16_t* x, const uint16_t* rw, const uint16_t* rs, const uint16_t* pes,
+               int32_t* idx, uint16_t* w, cudaStream_t s) {
+    RouterArgs ra{x, rw, rs, pes, idx, w, d->T, d->H, d->E, d->k, d->eps, bf16_round(pow((double)d->H, -0.5))};
+    return fail(launch_router(ra, s));
+}
+
+int get_workspace(const moe_dims* d, void* workspace, size_t ws_bytes, const Layout& L, uint8_t** out) {
+    if (workspace) {
+        if (!aligned16(workspace)) return MOE_ERR_ALIGN;
+        if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+        *out = static_cast<uint8_t*>(workspace);
+        return MOE_OK;
+    }
+    void* p = nullptr;
+    int rc = owned_workspace(L.total, &p);
+    *out = static_cast<uint8_t*>(p);
+    return rc;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_str(int status) {
+    switch (status) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_NULL: return "null pointer";
+        case MOE_ERR_SHAPE: return "bad shape";
+        case MOE_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+        case MOE_ERR_WORKSPACE: return "workspace too small";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_TIMEOUT: return "kernel wait timed out";
+        case MOE_ERR_DEVICE: return "no usable sm_100-family GPU";
+        default: return "unknown status";
+    }
+}
+
+size_t moe_workspace_bytes(const moe_dims* d) {
+    if (check_dims(d) != MOE_OK) return 0;
+    return layout(d).total;
+}
+
+int moe_route(const moe_dims* d, const uint16_t* x, const uint16_t* router_w, const uint16_t* router_scale,
+              const uint16_t* per_expert_scale, int32_t* idx_out, uint16_t* w_out, void* stream) {
+    int rc = check_dims(d);
+    if (rc) return rc;
+    if ((rc = check_ptrs({x, router_w, router_scale, per_expert_scale, idx_out, w_out}))) return rc;
+    if (d->T == 0) return MOE_OK;
+    DeviceInfo di;
+    if ((rc = device_info(&di))) return rc;
+    return route_impl(d, x, router_w, router_scale, per_expert_scale, idx_out, w_out,
+                      static_cast<cudaStream_t>(stream));
+}
+
+int moe_dispatch(const moe_dims* d, const int32_t* idx, int32_t* perm, int32_t* offsets, int32_t* inv,
+                 void* stream) {
+    int rc = check_dims(d);
+    if (rc) return rc;
+    if ((rc = check_ptrs({idx, perm, offsets, inv}))) return rc;
+    DeviceInfo di;
+    if ((rc = device_info(&di))) return rc;
+    DispatchArgs da{idx, perm, offsets, inv, nullptr, nullptr, d->T * d->k, d->E, 64};
+    return fail(launch_dispatch(da, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_experts(const moe_dims* d, const uint16_t* x, const int32_t* idx, const uint16_t* w,
+                const moe_qweight* gate_up, const moe_qweight* down, uint16_t* out, void* workspace,
+                size_t ws_bytes, void* stream) {
+    int rc = check_dims(d);
+    if (rc) return rc;
+    if ((rc = check_ptrs({x, idx, w, out}))) return rc;
+    if ((rc = check_qweight(gate_up)) || (rc = check_qweight(down))) return rc;
+    if (d->T == 0) return MOE_OK;
+    DeviceInfo di;
+    if ((rc = device_info(&di))) return rc;
+    const Layout L = layout(d);
+    uint8_t* ws = nullptr;
+    if ((rc = get_workspace(d, workspace, ws_bytes, L, &ws))) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    CallTimer tm(s);
+    tm.mark(0);
+    tm.mark(1);
+    return run_experts(d, x, idx, w, gate_up, down, out, ws, L, di, s, tm);
+}
+
+int moe_forward(const moe_dims* d, const uint16_t* x, const uint16_t* router_w, const uint16_t* router_scale,
+                const uint16_t* per_expert_scale, const moe_qweight* gate_up, const moe_qweight* down,
+                uint16_t* out, int32_t* idx_out, uint16_t* w_out, void* workspace, size_t ws_bytes,
+                void* stream) {
+    int rc = check_dims(d);
+    if (rc) return rc;
+    if ((rc = check_ptrs({x, router_w, router_scale, per_expert_scale, out}))) return rc;
+    if ((rc = check_qweight(gate_up)) || (rc = check_qweight(down))) return rc;
+    if ((idx_out && !aligned16(idx_out)) || (w_out && !aligned16(w_out))) return MOE_ERR_ALIGN;
+    if (d->T == 0) return MOE_OK;
+    DeviceInfo di;
+    if ((rc = device_info(&di))) return rc;
+    const Layout L = layout(d);
+    uint8_t* ws = nullptr;
+    if ((rc = get_workspace(d, workspace, ws_bytes, L, &ws))) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(ws + L.idx);
+    uint16_t* w = w_out ? w_out : reinterpret_cast<uint16_t*>(ws + L.w);
+    CallTimer tm(s);
+    tm.mark(0);
+    if ((rc = route_impl(d, x, router_w, router_scale, per_expert_scale, idx, w, s))) return rc;
+    tm.mark(1);
+    return run_experts(d, x, idx, w, gate_up, down, out, ws, L, di, s, tm);
+}
+
+int moe_forward_hostio(const moe_dims* d, const uint16_t* x_host, const uint16_t* router_w,
+                       const uint16_t* router_scale, const uint16_t* per_expert_scale, const moe_qweight* gate_up,
+                       const moe_qweight* down, uint16_t* out_host, void* workspace, size_t ws_bytes,
+                       void* stream) {
+    int rc = check_dims(d);
+    if (rc) return rc;
+    if (!x_host || !out_host) return MOE_ERR_NULL;
+    if ((rc = check_ptrs({router_w, router_scale, per_expert_scale}))) return rc;
+    if ((rc = check_qweight(gate_up)) || (rc = check_qweight(down))) return rc;
+    if (d->T == 0) return MOE_OK;
+    DeviceInfo di;
+    if ((rc = device_info(&di))) return rc;
+    const Layout L = layout(d);
+    uint8_t* ws = nullptr;
+    if ((rc = get_workspace(d, workspace, ws_bytes, L, &ws))) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint16_t* xdev = reinterpret_cast<uint16_t*>(ws + L.xdev);
+    uint16_t* odev = reinterpret_cast<uint16_t*>(ws + L.outdev);
+    const size_t bytes = (size_t)d->T * d->H * 2;
+    if (cudaMemcpyAsync(xdev, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;
+    rc = moe_forward(d, xdev, router_w, router_scale, per_expert_scale, gate_up, down, odev, nullptr, nullptr, ws,
+                     L.total, stream);
+    if (rc) return rc;
+    if (cudaMemcpyAsync(out_host, odev, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+    return fail(cudaStreamSynchronize(s));
+}
+
+int moe_timing_enable(int enable) {
+    Timing& t = timing();
+    std::lock_guard<std::mutex> lock(t.mu);
+    if (enable && t.ev.empty()) {
+        t.ev.resize((size_t)kMaxTimedCalls * (kStages + 1));
+        for (auto& e : t.ev)
+            if (cudaEventCreate(&e) != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    t.enabled = enable != 0;
+    t.calls = 0;
+    return MOE_OK;
+}
+
+int moe_timing_read(float* ms, int n, int* calls) {
+    Timing& t = timing();
+    std::lock_guard<std::mutex> lock(t.mu);
+    const int m = n < kStages ? n : kStages;
+    for (int i = 0; i < m; ++i) ms[i] = 0.f;
+    for (int c = 0; c < t.calls; ++c) {
+        cudaEvent_t* ev = &t.ev[(size_t)c * (kStages + 1)];
+        if (cudaEventSynchronize(ev[kStages]) != cudaSuccess) return -MOE_ERR_CUDA;
+        for (int i = 0; i < m; ++i) {
+            float v = 0.f;
+            if (cudaEventElapsedTime(&v, ev[i], ev[i + 1]) == cudaSuccess) ms[i] += v;
+        }
+    }
+    if (calls) *calls = t.calls;
+    t.calls = 0;
+    return m;
+}
+
+int moe_launches_per_forward(void) { return kStages; }
+
+int moe_device_error(void) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return -MOE_ERR_CUDA;
+    return router_error_word() | dispatch_error_word() | gemm_error_word();
+}
+
+}  // extern "C"

@@ -1,0 +1,226 @@
+// Router kernel: DiffRouter.forward of the DiffusionGemma language model
+// ("diffusion-gemma/model.ts"), fused into one launch.
+//
+// One thread-block cluster handles 16 tokens. Its CS = ceil(E/32) CTAs each
+//   1. compute the no-scale RMS norm of the 16 rows in fp32 (the norm's fp32
+//      semantics are the ones "diffusion-gemma/vision.ts" spells out in
+//      manualRms), then the two bf16 multiplies (router scale, H^-0.5) into
+//      shared memory;
+//   2. compute the bf16 scores of 32 experts with mma.sync m16n8k16 (fp32
+//      accumulate), and write them into the leader CTA's shared memory;
+// then the leader CTA picks the top k per token (value descending, ties to
+// the lower expert id), takes the fp32 softmax over the k picked scores and
+// multiplies by per_expert_scale[idx].
+#include <cooperative_groups.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace cg = cooperative_groups;
+
+namespace moe {
+
+namespace {
+
+constexpr int kTT = 16;        // tokens per cluster
+constexpr int kWarps = 4;      // warps per CTA
+constexpr int kExpPerCta = 32; // experts per CTA (8 per warp)
+
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// bf16 bits -> key that orders like the value (for finite values).
+__device__ __forceinline__ uint32_t order_key16(uint32_t b) { return (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u); }
+__device__ __forceinline__ uint32_t key16_to_bits(uint32_t k) { return (k & 0x8000u) ? (k & 0x7FFFu) : (~k & 0xFFFFu); }
+
+}  // namespace
+
+__global__ void __launch_bounds__(kWarps * 32) router_kernel(RouterArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int H = a.H, E = a.E, k = a.k;
+    const int rowstride = H + 8;  // bf16 elements; +16 B per row keeps the fragment reads conflict-free
+    uint16_t* n3 = reinterpret_cast<uint16_t*>(smem);
+    uint16_t* scores = n3 + kTT * rowstride;  // [kTT][E] bf16, used in the leader CTA
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int cs = (int)cluster.num_blocks();
+    const int rank = (int)cluster.block_rank();
+    const int tile = blockIdx.x / cs;
+    const int t0 = tile * kTT;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // ---- 1. no-scale RMS norm, x scale, x H^-0.5 (bf16 after each op) ----
+    for (int tl = warp; tl < kTT; tl += kWarps) {
+        const int t = t0 + tl;
+        uint16_t* dst = n3 + tl * rowstride;
+        if (t >= a.T) {
+            for (int h = lane * 8; h < H; h += 256) *reinterpret_cast<uint4*>(dst + h) = make_uint4(0, 0, 0, 0);
+            continue;
+        }
+        const uint16_t* xr = a.x + (size_t)t * H;
+        float ss = 0.f;
+        for (int h = lane * 8; h < H; h += 256) {
+            uint4 v = __ldg(reinterpret_cast<const uint4*>(xr + h));
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float lo = bf16_bits_to_f32(w[i] & 0xFFFFu), hi = bf16_bits_to_f32(w[i] >> 16);
+                ss = __fadd_rn(ss, __fmul_rn(lo, lo));
+                ss = __fadd_rn(ss, __fmul_rn(hi, hi));
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+        const float r = __frsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)H), a.eps));
+        for (int h = lane * 8; h < H; h += 256) {
+            uint4 v = __ldg(reinterpret_cast<const uint4*>(xr + h));
+            uint4 s = __ldg(reinterpret_cast<const uint4*>(a.router_scale + h));
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w}, sc[4] = {s.x, s.y, s.z, s.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float n_lo = bf16_bits_to_f32(f32_to_bf16_bits(__fmul_rn(bf16_bits_to_f32(w[i] & 0xFFFFu), r)));
+                float n_hi = bf16_bits_to_f32(f32_to_bf16_bits(__fmul_rn(bf16_bits_to_f32(w[i] >> 16), r)));
+                n_lo = bf16_bits_to_f32(f32_to_bf16_bits(__fmul_rn(n_lo, bf16_bits_to_f32(sc[i] & 0xFFFFu))));
+                n_hi = bf16_bits_to_f32(f32_to_bf16_bits(__fmul_rn(n_hi, bf16_bits_to_f32(sc[i] >> 16))));
+                o[i] = pack_bf16x2(__fmul_rn(n_lo, a.root), __fmul_rn(n_hi, a.root));
+            }
+            *reinterpret_cast<uint4*>(dst + h) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+    __syncthreads();
+
+    // ---- 2. scores for experts [e0, e0+8) of this warp: 16 tokens x 8 experts ----
+    // Inside each 64-wide K block, thread (g, q) owns K [16q, 16q+16) of its
+    // rows; mma step s takes K 16q+4s+{0,1} as fragment k {2q, 2q+1} and
+    // 16q+4s+{2,3} as k {2q+8, 2q+9}, identically for both operands, so the
+    // four steps sum the block's 64 products exactly once.
+    const int e0 = rank * kExpPerCta + warp * 8;
+    const int g = lane >> 2, q = lane & 3;
+    const int eg = e0 + g;
+    const uint16_t* wrow = a.router_w + (size_t)(eg < E ? eg : 0) * H;
+    const uint16_t* arow0 = n3 + g * rowstride;
+    const uint16_t* arow1 = n3 + (g + 8) * rowstride;
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    if (e0 < E) {
+        uint4 b0 = make_uint4(0, 0, 0, 0), b1 = b0;
+        if (eg < E) {
+            b0 = __ldg(reinterpret_cast<const uint4*>(wrow + 16 * q));
+            b1 = __ldg(reinterpret_cast<const uint4*>(wrow + 16 * q + 8));
+        }
+        for (int kb = 0; kb < H; kb += 64) {
+            uint4 nb0 = make_uint4(0, 0, 0, 0), nb1 = nb0;
+            if (eg < E && kb + 64 < H) {
+                nb0 = __ldg(reinterpret_cast<const uint4*>(wrow + kb + 64 + 16 * q));
+                nb1 = __ldg(reinterpret_cast<const uint4*>(wrow + kb + 64 + 16 * q + 8));
+            }
+            const uint4 x0 = *reinterpret_cast<const uint4*>(arow0 + kb + 16 * q);
+            const uint4 x1 = *reinterpret_cast<const uint4*>(arow0 + kb + 16 * q + 8);
+            const uint4 y0 = *reinterpret_cast<const uint4*>(arow1 + kb + 16 * q);
+            const uint4 y1 = *reinterpret_cast<const uint4*>(arow1 + kb + 16 * q + 8);
+            const uint32_t ar0[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            const uint32_t ar1[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+            const uint32_t br[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_bf16_16816(c, ar0[2 * s], ar1[2 * s], ar0[2 * s + 1], ar1[2 * s + 1], br[2 * s], br[2 * s + 1]);
+            b0 = nb0;
+            b1 = nb1;
+        }
+    }
+    // c0,c1: token g, experts e0+2q, e0+2q+1; c2,c3: token g+8.
+    uint16_t* lead = cluster.map_shared_rank(scores, 0);
+    {
+        const int ea = e0 + 2 * q;
+        if (ea < E) {
+            lead[g * E + ea] = (uint16_t)f32_to_bf16_bits(c[0]);
+            lead[(g + 8) * E + ea] = (uint16_t)f32_to_bf16_bits(c[2]);
+        }
+        if (ea + 1 < E) {
+            lead[g * E + ea + 1] = (uint16_t)f32_to_bf16_bits(c[1]);
+            lead[(g + 8) * E + ea + 1] = (uint16_t)f32_to_bf16_bits(c[3]);
+        }
+    }
+    cluster.sync();
+    if (rank != 0) return;
+
+    // ---- 3. top-k + precise softmax + per-expert scale (leader CTA) ----
+    for (int tl = warp; tl < kTT; tl += kWarps) {
+        const int t = t0 + tl;
+        if (t >= a.T) continue;
+        const uint16_t* sr = scores + tl * E;
+        uint32_t cand[8];  // keys of this lane's experts e = lane + 32 i
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = lane + 32 * i;
+            cand[i] = (e < E) ? ((order_key16(sr[e]) << 16) | (0xFFFFu - (uint32_t)e)) : 0u;
+        }
+        int my_idx = 0;
+        float my_s = 0.f;
+        float top_s = 0.f;
+        for (int j = 0; j < k; ++j) {
+            uint32_t best = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) best = max(best, cand[i]);
+            const uint32_t win = __reduce_max_sync(0xffffffffu, best);
+            const int e = (int)(0xFFFFu - (win & 0xFFFFu));
+            const float s = bf16_bits_to_f32(key16_to_bits(win >> 16));
+            if (j == 0) top_s = s;
+            if (lane == j) {
+                my_idx = e;
+                my_s = s;
+            }
+            if ((e & 31) == lane) cand[e >> 5] = 0u;
+        }
+        const float ex = (lane < k) ? expf(__fsub_rn(my_s, top_s)) : 0.f;
+        float sum = 0.f;
+        for (int j = 0; j < k; ++j) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, ex, j));
+        if (lane < k) {
+            const float p = bf16_bits_to_f32(f32_to_bf16_bits(__fdiv_rn(ex, sum)));
+            const float pes = bf16_bits_to_f32(a.per_expert_scale[my_idx]);
+            a.idx[(size_t)t * k + lane] = my_idx;
+            a.w[(size_t)t * k + lane] = (uint16_t)f32_to_bf16_bits(__fmul_rn(p, pes));
+        }
+    }
+}
+
+int router_error_word() {
+    int v = 0, z = 0;
+    if (cudaMemcpyFromSymbol(&v, g_error_word, sizeof(int)) != cudaSuccess) return 0;
+    cudaMemcpyToSymbol(g_error_word, &z, sizeof(int));
+    return v;
+}
+
+size_t router_smem_bytes(int H, int E) {
+    return (size_t)kTT * (H + 8) * 2 + (size_t)kTT * E * 2;
+}
+
+cudaError_t launch_router(const RouterArgs& a, cudaStream_t stream) {
+    if (a.T == 0) return cudaSuccess;
+    const int cs = (a.E + kExpPerCta - 1) / kExpPerCta;
+    const int tiles = (a.T + kTT - 1) / kTT;
+    const size_t smem = router_smem_bytes(a.H, a.E);
+    cudaError_t err = cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(tiles * cs, 1, 1);
+    cfg.blockDim = dim3(kWarps * 32, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, router_kernel, a);
+}
+
+}  // namespace moe

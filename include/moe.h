@@ -1,0 +1,172 @@
+/*
+ * libmoe -- routed 4-bit mixture-of-experts feed-forward on GB300 (sm_103a).
+ *
+ * The layer is the MoE branch of the DiffusionGemma-26B-A4B decoder/encoder
+ * layer ("diffusion-gemma/model.ts"): class DiffRouter picks k of E experts
+ * per token, class DiffExperts runs each picked expert's fused gate_up
+ * SwitchLinear, GeGLU and down SwitchLinear and sums the results with the
+ * routing weights.
+ *
+ * Conventions for every call below:
+ *  - bf16 tensors are passed as uint16_t bit patterns, row-major, contiguous.
+ *  - All tensor pointers are DEVICE pointers unless the name says _host.
+ *    The caller owns every buffer; the library never frees caller memory.
+ *  - Every device pointer must be 16-byte aligned (MOE_ERR_ALIGN otherwise).
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream). All work is
+ *    enqueued on it; no call synchronises the host except
+ *    moe_forward_hostio, moe_timing_read and moe_device_error.
+ *  - Argument errors are detected on the host before anything is enqueued
+ *    and leave the outputs untouched. A launch failure returns MOE_ERR_CUDA.
+ *  - Supported shapes: bits == 4, group == 64, H % 128 == 0, inter % 64 == 0,
+ *    1 <= k <= 32, k <= E <= 256, T >= 0 (T == 0 is a no-op).
+ *  - 4-bit weights use the affine layout that the pages' quantized linears
+ *    consume: w uint32 [E, N, K/8] with element K of row n in nibble K%8
+ *    (bits 4*(K%8)..+3, low nibble first) of word K/8; scales and biases
+ *    bf16 [E, N, K/64]; the dequantised weight is bf16(scale*q + bias) and
+ *    a linear computes out = in . W^T.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Shape of one layer call. eps is the RMS-norm epsilon of the router. */
+typedef struct moe_dims {
+    int32_t T;      /* tokens                                   */
+    int32_t H;      /* hidden size                              */
+    int32_t E;      /* experts                                  */
+    int32_t k;      /* experts per token (top-k)                */
+    int32_t inter;  /* moe_intermediate: gate_up has 2*inter rows */
+    int32_t group;  /* quantisation group along K (64)          */
+    int32_t bits;   /* 4                                        */
+    float eps;      /* router RMS-norm epsilon                  */
+} moe_dims;
+
+/* One 4-bit affine quantized SwitchLinear for all E experts.
+ * gate_up: N = 2*inter, K = H;  down: N = H, K = inter. */
+typedef struct moe_qweight {
+    const uint32_t* w;       /* [E, N, K/8]  */
+    const uint16_t* scales;  /* [E, N, K/64] */
+    const uint16_t* biases;  /* [E, N, K/64] */
+} moe_qweight;
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_NULL = 1,         /* a required pointer is NULL               */
+    MOE_ERR_SHAPE = 2,        /* sizes inconsistent or out of range        */
+    MOE_ERR_ALIGN = 3,        /* a pointer is not 16-byte aligned          */
+    MOE_ERR_UNSUPPORTED = 4,  /* bits/group/k/E outside the supported set  */
+    MOE_ERR_WORKSPACE = 5,    /* workspace too small                       */
+    MOE_ERR_CUDA = 6,         /* a CUDA call or launch failed              */
+    MOE_ERR_TIMEOUT = 7,      /* a kernel gave up waiting (see moe_device_error) */
+    MOE_ERR_DEVICE = 8        /* no usable sm_100-family GPU               */
+} moe_status;
+
+/* Human-readable name of a status code. Never NULL. */
+const char* moe_status_str(int status);
+
+/* Bytes of device workspace moe_experts / moe_forward / moe_forward_hostio
+ * need for these dims (0 for invalid dims). Holds the routing result, the
+ * expert-sorted permutation, the gathered expert inputs, the GeGLU
+ * activations and the per-slot expert outputs. */
+size_t moe_workspace_bytes(const moe_dims* d);
+
+/*
+ * Router (DiffRouter.forward): x [T,H] -> indices [T,k], weights [T,k].
+ *   normed = rms_norm(x, no weight, eps)   fp32 inside, bf16 out
+ *   normed = bf16(normed * router_scale)   per hidden dim
+ *   normed = bf16(normed * bf16(H^-0.5))
+ *   scores = bf16(normed . router_w^T)     [T,E]
+ *   idx    = the k largest scores, value descending, ties to the lower id
+ *   w      = bf16(bf16(softmax_fp32(scores[idx])) * per_expert_scale[idx])
+ * x [T,H], router_w [E,H], router_scale [H], per_expert_scale [E] (bf16);
+ * idx_out int32 [T,k], w_out bf16 [T,k].
+ */
+int moe_route(const moe_dims* d, const uint16_t* x, const uint16_t* router_w,
+              const uint16_t* router_scale, const uint16_t* per_expert_scale,
+              int32_t* idx_out, uint16_t* w_out, void* stream);
+
+/*
+ * Dispatch (the sorted path of DiffExperts.forward: argsort of the flat
+ * indices, its inverse, rows = order // k), as a stable counting sort of the
+ * flat slots f = t*k + j by expert id:
+ *   offsets[e] .. offsets[e+1]   slot range of expert e (offsets int32 [E+1])
+ *   perm[p] = f                  p-th slot in expert order (int32 [T*k])
+ *   inv[f]  = p                  inverse of perm (int32 [T*k])
+ * idx int32 [T,k] must hold ids in [0,E); a bad id is dropped and raised in
+ * moe_device_error. Bit-exact and deterministic.
+ */
+int moe_dispatch(const moe_dims* d, const int32_t* idx, int32_t* perm, int32_t* offsets,
+                 int32_t* inv, void* stream);
+
+/*
+ * Experts (DiffExperts.forward): x [T,H], idx [T,k], w [T,k] -> out [T,H].
+ * Per slot (t, j) with expert e = idx[t,j]:
+ *   z = bf16(x[t] . Wgu[e]^T)          [2*inter]
+ *   m = bf16(gelu_tanh(z[:inter]) * z[inter:])
+ *   y = bf16(m . Wdn[e]^T)             [H]
+ * out[t] = bf16( sum_j bf16(y_{t,j} * w[t,j]) ), fp32 sum in j order.
+ * x may differ from the router's input (the layer routes on the residual
+ * and feeds the experts its pre-feed-forward-norm-2 output).
+ * workspace: moe_workspace_bytes(d) bytes of device memory, or NULL to use
+ * a grow-only buffer the library owns per device (not safe for concurrent
+ * calls from several host threads). out may not alias x.
+ */
+int moe_experts(const moe_dims* d, const uint16_t* x, const int32_t* idx, const uint16_t* w,
+                const moe_qweight* gate_up, const moe_qweight* down, uint16_t* out,
+                void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * The whole layer: moe_route on x, then moe_experts on the same x.
+ * idx_out / w_out may be NULL (the routing then stays in the workspace).
+ */
+int moe_forward(const moe_dims* d, const uint16_t* x, const uint16_t* router_w,
+                const uint16_t* router_scale, const uint16_t* per_expert_scale,
+                const moe_qweight* gate_up, const moe_qweight* down, uint16_t* out,
+                int32_t* idx_out, uint16_t* w_out, void* workspace, size_t ws_bytes,
+                void* stream);
+
+/*
+ * The whole layer with HOST activations: copies x_host [T,H] to the device,
+ * runs moe_forward and copies out [T,H] back to out_host, then synchronises
+ * the stream. Weights and router parameters are device pointers. Host
+ * buffers should be pinned (cudaHostAlloc) for full copy speed. The device
+ * copies of x and out live in the workspace.
+ */
+int moe_forward_hostio(const moe_dims* d, const uint16_t* x_host, const uint16_t* router_w,
+                       const uint16_t* router_scale, const uint16_t* per_expert_scale,
+                       const moe_qweight* gate_up, const moe_qweight* down, uint16_t* out_host,
+                       void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Per-kernel timing. After moe_timing_enable(1), each moe_forward /
+ * moe_experts call records CUDA events around each of its kernels on its
+ * stream (at most 1024 calls are kept). moe_timing_read synchronises the
+ * recorded events and writes, for each stage, the summed milliseconds into
+ * ms[0..n) in the order: route, dispatch, gather, gate_up, down, combine,
+ * and the number of calls into *calls; it then clears the record.
+ * Returns the number of stages written.
+ */
+int moe_timing_enable(int enable);
+int moe_timing_read(float* ms, int n, int* calls);
+
+/* Number of kernel launches one moe_forward call makes. */
+int moe_launches_per_forward(void);
+
+/*
+ * Device-side error word of the current device: 0 if no kernel has given
+ * up waiting or dropped a bad expert id since the last read; otherwise a
+ * bit set (1: a pipeline wait timed out, 2: an expert id was out of range).
+ * Synchronises the device, then clears the word.
+ */
+int moe_device_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H_ */

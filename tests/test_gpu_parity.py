@@ -1,0 +1,209 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Every workload of the layer runs at full size on the GPU. The oracle checks
+the whole output where it finishes in seconds (tiny, decode, canvas) and a
+seeded sample of token rows otherwise (prefill, skew); routing and dispatch
+are checked in full everywhere. Comparison rules: tests/gpu_helpers.py.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import moe_synth as ms
+import oracle
+import gpu_helpers as gh
+
+pytestmark = pytest.mark.gpu
+
+FULL = ("tiny", "decode", "canvas")
+SAMPLED = ("prefill", "skew")
+ALL = FULL + SAMPLED
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_quantized_moe_layer_gb300 import build
+    build.build()
+    oracle.build()
+
+
+_cache = {}
+
+
+def layer(name):
+    if name not in _cache:
+        inp = ms.make_layer(name)
+        ref = gh.oracle_route(inp)
+        _cache[name] = (inp, gh.upload(inp), ref)
+    return _cache[name]
+
+
+def sample_rows(T, n=48, seed=0):
+    if T <= n:
+        return np.arange(T)
+    rng = np.random.default_rng(seed)
+    return np.sort(np.concatenate([[0, T - 1], rng.choice(np.arange(1, T - 1), n - 2, replace=False)]))
+
+
+@pytest.mark.parametrize("name", ALL)
+def test_route(name):
+    inp, g, ref = layer(name)
+    idx, w = gh.gpu_route(g)
+    ties, differ = gh.check_routing(inp.dims, ref, idx, w)
+    print(f"{name}: near-tie tokens {ties}, differing {differ} of {inp.dims.T}")
+
+
+@pytest.mark.parametrize("name", ALL)
+def test_dispatch(name):
+    inp, g, ref = layer(name)
+    d = inp.dims
+    perm, off, inv = gh.gpu_dispatch(g.d, ref["idx"])
+    operm, ooff, oinv = oracle.dispatch(d.T, d.k, d.E, ref["idx"])
+    assert np.array_equal(off, ooff)
+    assert np.array_equal(perm, operm)
+    assert np.array_equal(inv, oinv)
+
+
+@pytest.mark.parametrize("case", ["T1", "one_expert", "empty_experts", "k1"])
+def test_dispatch_edges(case):
+    rng = np.random.default_rng(5)
+    if case == "T1":
+        d = ms.Dims(T=1, H=256, E=8, k=2, inter=128)
+        idx = np.array([[7, 0]], np.int32)
+    elif case == "one_expert":
+        d = ms.Dims(T=4000, H=256, E=8, k=1, inter=128)
+        idx = np.full((d.T, 1), 3, np.int32)
+    elif case == "empty_experts":
+        d = ms.Dims(T=700, H=2816, E=128, k=8, inter=704)
+        idx = np.stack([rng.permutation(8)[:8] for _ in range(d.T)]).astype(np.int32)
+    else:
+        d = ms.Dims(T=4096, H=2816, E=128, k=1, inter=704)
+        idx = rng.integers(0, 128, (d.T, 1)).astype(np.int32)
+    import bit_quantized_moe_layer_gb300 as moe
+    perm, off, inv = gh.gpu_dispatch(moe.dims_of(d), idx)
+    operm, ooff, oinv = oracle.dispatch(d.T, d.k, d.E, idx)
+    assert np.array_equal(off, ooff) and np.array_equal(perm, operm) and np.array_equal(inv, oinv)
+
+
+@pytest.mark.parametrize("name", ALL)
+def test_experts(name):
+    """The experts path alone, fed the oracle's routing."""
+    inp, g, ref = layer(name)
+    out = gh.gpu_experts(g, ref["idx"], ref["w"])
+    rows = None if name in FULL else sample_rows(inp.dims.T)
+    want = gh.oracle_experts_rows(inp, ref["idx"], ref["w"], rows)
+    got = out if rows is None else out[rows]
+    stats = gh.compare_out(got, want, f"{name} experts")
+    print(f"{name} experts: {stats}")
+
+
+@pytest.mark.parametrize("name", ALL)
+def test_forward(name):
+    """The whole layer; tokens whose routing legitimately differs (near ties)
+    are excluded from the output comparison."""
+    inp, g, ref = layer(name)
+    out, idx, w = gh.gpu_forward(g)
+    gh.check_routing(inp.dims, ref, idx, w)
+    rows = np.arange(inp.dims.T) if name in FULL else sample_rows(inp.dims.T, seed=1)
+    same = np.array([set(idx[t]) == set(ref["idx"][t]) for t in rows])
+    rows = rows[same]
+    want = gh.oracle_experts_rows(inp, ref["idx"], ref["w"], rows)
+    stats = gh.compare_out(out[rows], want, f"{name} forward")
+    print(f"{name} forward: {stats}")
+
+
+@pytest.mark.parametrize("T", [1, 17, 33, 130])
+def test_ragged_token_counts(T):
+    """Token counts that leave partial router tiles and partial MMA tiles."""
+    inp = ms.make_layer("canvas", T=T, seed=3)
+    g = gh.upload(inp)
+    ref = gh.oracle_route(inp)
+    out, idx, w = gh.gpu_forward(g)
+    gh.check_routing(inp.dims, ref, idx, w)
+    same = np.array([set(idx[t]) == set(ref["idx"][t]) for t in range(T)])
+    want = gh.oracle_experts_rows(inp, ref["idx"], ref["w"], np.flatnonzero(same))
+    gh.compare_out(out[same], want, f"T={T}")
+
+
+def test_tiny_layer_ragged():
+    inp = ms.make_layer("tiny", T=37, seed=4)
+    g = gh.upload(inp)
+    ref = gh.oracle_route(inp)
+    out = gh.gpu_experts(g, ref["idx"], ref["w"])
+    gh.compare_out(out, gh.oracle_experts_rows(inp, ref["idx"], ref["w"]), "tiny T=37")
+
+
+def test_many_rows_one_expert():
+    """One expert receives more rows than a token tile holds (several tiles),
+    most experts receive none."""
+    inp = ms.make_layer("canvas", T=300, seed=6)
+    g = gh.upload(inp)
+    rng = np.random.default_rng(6)
+    idx = np.stack([np.concatenate([[5], rng.choice(np.r_[0:5, 6:12], 7, replace=False)])
+                    for _ in range(300)]).astype(np.int32)
+    w = ms.bf16_bits(rng.uniform(0.05, 0.3, (300, 8)))
+    out = gh.gpu_experts(g, idx, w)
+    rows = sample_rows(300, 40, seed=2)
+    gh.compare_out(out[rows], gh.oracle_experts_rows(inp, idx, w, rows), "many rows one expert")
+
+
+def test_single_expert_identity():
+    """E = 1, k = 1, per_expert_scale = 1: the layer is one dense 4-bit GeGLU MLP."""
+    d = ms.Dims(T=40, H=256, E=1, k=1, inter=128)
+    inp = dataclasses.replace(ms.make_custom(d, seed=7), pes=np.full(1, 0x3F80, np.uint16))
+    g = gh.upload(inp)
+    out, idx, w = gh.gpu_forward(g)
+    assert np.all(idx == 0) and np.all(w == 0x3F80)
+    ref = gh.oracle_route(inp)
+    gh.compare_out(out, gh.oracle_experts_rows(inp, ref["idx"], ref["w"]), "identity")
+
+
+def test_deterministic_and_workspace_forms():
+    inp, g, ref = layer("canvas")
+    a, _, _ = gh.gpu_forward(g)
+    b, _, _ = gh.gpu_forward(g)
+    assert np.array_equal(a, b), "two runs differ"
+    import bit_quantized_moe_layer_gb300 as moe
+    ws = torch.empty(moe.workspace_bytes(g.d), dtype=torch.uint8, device="cuda")
+    c, _, _ = gh.gpu_forward(g, workspace=ws)
+    assert np.array_equal(a, c), "caller workspace differs from library workspace"
+
+
+def test_hostio_matches_device_call():
+    import bit_quantized_moe_layer_gb300 as moe
+    inp, g, ref = layer("canvas")
+    a, _, _ = gh.gpu_forward(g)
+    x_host = torch.from_numpy(inp.x.view(np.int16).copy()).pin_memory()
+    out_host = torch.empty((g.d.T, g.d.H), dtype=torch.int16).pin_memory()
+    moe.moe_forward_hostio(g.d, x_host, g.layer.router_w, g.layer.router_scale, g.layer.pes,
+                           g.layer.gate_up, g.layer.down, out_host)
+    assert np.array_equal(out_host.numpy().view(np.uint16), a)
+
+
+def test_timing_and_error_word():
+    import bit_quantized_moe_layer_gb300 as moe
+    inp, g, ref = layer("canvas")
+    moe.timing_enable(True)
+    for _ in range(3):
+        gh.gpu_forward(g)
+    ms_per_stage, calls = moe.timing_read()
+    moe.timing_enable(False)
+    assert calls == 3
+    assert all(v > 0 for v in ms_per_stage.values()), ms_per_stage
+    assert moe.device_error() == 0
+
+
+def test_bad_expert_id_is_flagged_not_faulted():
+    """An out-of-range expert id is dropped by the dispatch kernel (bounds
+    checked) and reported through the device error word."""
+    import bit_quantized_moe_layer_gb300 as moe
+    d = moe.dims(4, 256, 8, 2, 128)
+    idx = np.array([[0, 1], [2, 8], [3, 4], [5, 6]], np.int32)
+    moe.device_error()
+    perm, off, inv = gh.gpu_dispatch(d, idx)
+    assert off[-1] == 7
+    assert moe.device_error() & 2
