@@ -35,12 +35,12 @@ constexpr int kThreads = 384;
 constexpr int kStageK = 256;
 constexpr int kPackedStageBytes = 128 * 128;  // 128 rows x 32 words
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kDCol0 = 256;              // D buffers at columns 256 and 384
+constexpr uint32_t kPCol0 = 256;              // partial-sum regions at columns 256 and 384
 
 struct Smem {
     uint64_t full[8], empty[8];
     uint64_t afull[2], aempty[2];
-    uint64_t dfull[2], dempty[2];
+    uint64_t pfull[2], pempty[2];  // per-stage partial accumulators in TMEM
     uint64_t sfull[2], sempty[2];
     uint32_t tmem_base;
     int abort_flag;
@@ -53,10 +53,14 @@ __host__ __device__ inline int scale_buf_bytes(int K) {
     return ((128 * (K / 64) * 2 * 2) + 1023) & ~1023;
 }
 
+// gelu_approx(u) = 0.5 u (1 + tanh(s)), s = sqrt(2/pi) (u + 0.044715 u^3),
+// evaluated as u / (1 + exp(-2 s)) (the same function: 0.5 (1 + tanh s) is
+// the logistic of 2 s). This form does not cancel for negative u, where
+// 1 + tanh(s) in fp32 loses every digit.
 __device__ __forceinline__ float gelu_tanh(float u) {
     const float c = 0.7978845608028654f;  // sqrt(2/pi)
-    const float inner = __fmul_rn(c, __fadd_rn(u, __fmul_rn(0.044715f, __fmul_rn(u, __fmul_rn(u, u)))));
-    return __fmul_rn(__fmul_rn(0.5f, u), __fadd_rn(1.0f, tanhf(inner)));
+    const float s = __fmul_rn(c, __fadd_rn(u, __fmul_rn(0.044715f, __fmul_rn(u, __fmul_rn(u, u)))));
+    return __fdiv_rn(u, __fadd_rn(1.0f, expf(__fmul_rn(-2.0f, s))));
 }
 
 // Position of element n inside its 8-block in the interleaved K order.
@@ -67,7 +71,7 @@ __device__ __forceinline__ int interleaved_pos(int n) {
 
 }  // namespace
 
-template <int MODE>
+template <int MODE, int NMAX>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap bmap,
                         GemmArgs a) {
@@ -76,7 +80,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 1024-byte aligned carve-up: [stages][packed | B atoms] then 2 scale buffers.
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
     const int NS = a.stages;
-    const int sbytes = stage_bytes(a.nmax);
+    const int sbytes = stage_bytes(NMAX);
     uint8_t* scale_base = base + (size_t)NS * sbytes;
     const int G = a.K / 64;  // groups per weight row
     const int sbuf_bytes = scale_buf_bytes(a.K);
@@ -92,8 +96,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sh.afull[i], 128);
             mbar_init(&sh.aempty[i], 1);
-            mbar_init(&sh.dfull[i], 1);
-            mbar_init(&sh.dempty[i], 128);
+            mbar_init(&sh.pfull[i], 1);
+            mbar_init(&sh.pempty[i], 128);
             mbar_init(&sh.sfull[i], 1);
             mbar_init(&sh.sempty[i], 4);
         }
@@ -162,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t* bst = st + kPackedStageBytes;
                     for (int at = 0; at < atoms; ++at)
                         for (int r = 0; r < nrows16; r += 16)
-                            tma_load_2d(bst + at * a.nmax * 128 + r * 128, &bmap, &sh.full[slot],
+                            tma_load_2d(bst + at * NMAX * 128 + r * 128, &bmap, &sh.full[slot],
                                         s * kStageK + at * 64, tl.p0 + r);
                 }
             }
@@ -172,35 +176,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ---------------------------------------------------- MMA issuer --
+        // Each 256-K stage accumulates into a fresh TMEM region (alternating
+        // between two); the epilogue adds the stage partials in fp32
+        // registers. Short tensor-core accumulation chains keep z close to
+        // the exactly rounded value.
         if (lane == 0) {
             uint32_t gs = 0;
-            int li = 0;
             bool ok = true;
-            for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x, ++li) {
+            for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x) {
                 const Tile tl = a.tiles[it / a.n_tiles];
                 const uint32_t nrows16 = (uint32_t)((tl.rows + 15) & ~15);
-                const int d = li & 1;
-                if (!(ok = mbar_wait(&sh.dempty[d], ((li >> 1) & 1) ^ 1, abort_flag))) break;
-                tc_fence_after();
                 const uint32_t idesc = idesc_bf16_m128(nrows16);
-                const uint32_t dcol = tmem + kDCol0 + d * 128;
                 for (int s = 0; s < nstages; ++s, ++gs) {
                     const int slot = gs % NS;
                     const int as = gs & 1;
+                    const int pr = gs & 1;
                     if (!(ok = mbar_wait(&sh.full[slot], (gs / NS) & 1, abort_flag))) break;
                     if (!(ok = mbar_wait(&sh.afull[as], (gs >> 1) & 1, abort_flag))) break;
+                    if (!(ok = mbar_wait(&sh.pempty[pr], ((gs >> 1) & 1) ^ 1, abort_flag))) break;
                     tc_fence_after();
                     const int kr = min(kStageK, K - s * kStageK);
                     const uint32_t bst = smem_u32(base + (size_t)slot * sbytes + kPackedStageBytes);
+                    const uint32_t pcol = tmem + kPCol0 + pr * 128;
                     for (int k16 = 0; k16 < kr / 16; ++k16) {
                         const int at = k16 >> 2, kk = k16 & 3;
-                        const uint64_t bdesc = sw128_kmajor_desc(bst + at * a.nmax * 128 + kk * 32);
-                        umma_ts(dcol, tmem + as * 128 + k16 * 8, bdesc, idesc, (s > 0 || k16 > 0) ? 1u : 0u);
+                        const uint64_t bdesc = sw128_kmajor_desc(bst + at * NMAX * 128 + kk * 32);
+                        umma_ts(pcol, tmem + as * 128 + k16 * 8, bdesc, idesc, k16 > 0 ? 1u : 0u);
                     }
                     umma_commit(&sh.empty[slot]);
                     umma_commit(&sh.aempty[as]);
+                    umma_commit(&sh.pfull[pr]);
                 }
-                if (ok) umma_commit(&sh.dfull[d]);
             }
         }
     } else if (warp >= 4 && warp < 8) {
@@ -262,50 +268,62 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------ epilogue --
         const int q = warp & 3;
         const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
-        int li = 0;
+        uint32_t gs = 0;
         bool ok = true;
-        for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x, ++li) {
+        for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x) {
             const Tile tl = a.tiles[it / a.n_tiles];
             const int j = it % a.n_tiles;
-            const int d = li & 1;
-            if (!(ok = mbar_wait(&sh.dfull[d], (li >> 1) & 1, abort_flag))) break;
-            tc_fence_after();
             const int nrows16 = (tl.rows + 15) & ~15;
-            for (int c0 = 0; c0 < nrows16; c0 += 16) {
-                uint32_t v[16];
-                tmem_ld16(tmem + lane_addr + kDCol0 + d * 128 + c0, v);
-                tmem_wait_ld();
-                if (MODE == kGateUp) {
-                    // lanes 0-15: gate rows, lanes 16-31: up rows of the same n
-                    const int n = 64 * j + 16 * q + (lane & 15);
-                    const int pos = interleaved_pos(n);
+            float acc[NMAX];
 #pragma unroll
-                    for (int jj = 0; jj < 16; jj += 2) {
-                        const uint32_t send = (lane < 16) ? v[jj + 1] : v[jj];
-                        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 16);
-                        const int tok = c0 + jj + (lane < 16 ? 0 : 1);
-                        const float gf = __uint_as_float(lane < 16 ? v[jj] : recv);
-                        const float uf = __uint_as_float(lane < 16 ? recv : v[jj + 1]);
+            for (int c = 0; c < NMAX; ++c) acc[c] = 0.f;
+            for (int s = 0; s < nstages; ++s, ++gs) {
+                const int pr = gs & 1;
+                if (!(ok = mbar_wait(&sh.pfull[pr], (gs >> 1) & 1, abort_flag))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int c0 = 0; c0 < NMAX; c0 += 16) {
+                    if (c0 < nrows16) {
+                        uint32_t v[16];
+                        tmem_ld16(tmem + lane_addr + kPCol0 + pr * 128 + c0, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) acc[c0 + jj] = __fadd_rn(acc[c0 + jj], __uint_as_float(v[jj]));
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&sh.pempty[pr]);
+            }
+            if (!ok) break;
+            if (MODE == kGateUp) {
+                // lanes 0-15: gate rows, lanes 16-31: up rows of the same n
+                const int n = 64 * j + 16 * q + (lane & 15);
+                const int pos = interleaved_pos(n);
+#pragma unroll
+                for (int jj = 0; jj < NMAX; jj += 2) {
+                    if (jj < nrows16) {
+                        const float send = (lane < 16) ? acc[jj + 1] : acc[jj];
+                        const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+                        const int tok = jj + (lane < 16 ? 0 : 1);
+                        const float gf = lane < 16 ? acc[jj] : recv;
+                        const float uf = lane < 16 ? recv : acc[jj + 1];
                         const float gb = bf16_bits_to_f32(f32_to_bf16_bits(gf));  // z is a bf16 tensor
                         const float ub = bf16_bits_to_f32(f32_to_bf16_bits(uf));
                         if (tok < tl.rows)
                             a.out[(size_t)(tl.p0 + tok) * a.out_ld + pos] =
                                 (uint16_t)f32_to_bf16_bits(__fmul_rn(gelu_tanh(gb), ub));
                     }
-                } else {
-                    const int h = 128 * j + 32 * q + lane;
+                }
+            } else {
+                const int h = 128 * j + 32 * q + lane;
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        const int tok = c0 + jj;
-                        if (tok < tl.rows) {
-                            const int f = a.perm[tl.p0 + tok];
-                            a.out[(size_t)f * a.out_ld + h] = (uint16_t)f32_to_bf16_bits(__uint_as_float(v[jj]));
-                        }
+                for (int jj = 0; jj < NMAX; ++jj) {
+                    if (jj < tl.rows) {
+                        const int f = a.perm[tl.p0 + jj];
+                        a.out[(size_t)f * a.out_ld + h] = (uint16_t)f32_to_bf16_bits(acc[jj]);
                     }
                 }
             }
-            tc_fence_before();
-            mbar_arrive(&sh.dempty[d]);
         }
     }
 
@@ -329,20 +347,33 @@ int gemm_max_stages(int mode, int K, int nmax) {
     return s;
 }
 
+template <int MODE, int NMAX>
+static cudaError_t launch_one(const CUtensorMap& wmap, const CUtensorMap& bmap, const GemmArgs& a, int grid,
+                              size_t smem, cudaStream_t stream) {
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, NMAX>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, 232448 - 2048);
+        if (err != cudaSuccess) return err;
+        attr_set[dev] = true;
+    }
+    grouped_gemm_kernel<MODE, NMAX><<<grid, kThreads, smem, stream>>>(wmap, bmap, a);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_gemm(int mode, const CUtensorMap& wmap, const CUtensorMap& bmap, const GemmArgs& a, int grid,
                         cudaStream_t stream) {
     const size_t smem = gemm_smem_bytes(mode, a.K, a.nmax, a.stages);
-    cudaError_t err;
-    if (mode == kGateUp) {
-        err = cudaFuncSetAttribute(grouped_gemm_kernel<kGateUp>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (err != cudaSuccess) return err;
-        grouped_gemm_kernel<kGateUp><<<grid, kThreads, smem, stream>>>(wmap, bmap, a);
-    } else {
-        err = cudaFuncSetAttribute(grouped_gemm_kernel<kDown>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (err != cudaSuccess) return err;
-        grouped_gemm_kernel<kDown><<<grid, kThreads, smem, stream>>>(wmap, bmap, a);
-    }
-    return cudaGetLastError();
+    if (a.nmax == 64)
+        return mode == kGateUp ? launch_one<kGateUp, 64>(wmap, bmap, a, grid, smem, stream)
+                               : launch_one<kDown, 64>(wmap, bmap, a, grid, smem, stream);
+    if (a.nmax == 128)
+        return mode == kGateUp ? launch_one<kGateUp, 128>(wmap, bmap, a, grid, smem, stream)
+                               : launch_one<kDown, 128>(wmap, bmap, a, grid, smem, stream);
+    return cudaErrorInvalidValue;
 }
 
 int gemm_error_word() {

@@ -21,7 +21,8 @@ struct RouterArgs {
     float root;  // bf16(H^-0.5) as a float
 };
 size_t router_smem_bytes(int H, int E);
-cudaError_t launch_router(const RouterArgs& a, cudaStream_t stream);
+// wmap: router_w as bf16 [E rows, H], box {64, 32}, 128B swizzle.
+cudaError_t launch_router(const CUtensorMap& wmap, const RouterArgs& a, cudaStream_t stream);
 int router_error_word();
 
 // A token tile of one expert: rows [p0, p0 + rows) of the expert-sorted slots.

@@ -32,7 +32,7 @@ int check_dims(const moe_dims* d) {
     if (!d) return MOE_ERR_NULL;
     if (d->T < 0 || d->H <= 0 || d->E <= 0 || d->k <= 0 || d->inter <= 0) return MOE_ERR_SHAPE;
     if (d->bits != 4 || d->group != 64) return MOE_ERR_UNSUPPORTED;
-    if (d->H % 128 != 0 || d->inter % 64 != 0 || d->H > 6144) return MOE_ERR_UNSUPPORTED;
+    if (d->H % 128 != 0 || d->inter % 64 != 0 || d->H > 5888) return MOE_ERR_UNSUPPORTED;
     if (d->k > 32 || d->k > d->E || d->E > 256) return MOE_ERR_UNSUPPORTED;
     if ((int64_t)d->T * d->k > (int64_t)1 << 28) return MOE_ERR_SHAPE;
     if (!(d->eps >= 0.0f) || isinf(d->eps)) return MOE_ERR_SHAPE;
@@ -276,7 +276,9 @@ int run_experts(const moe_dims* d, const uint16_t* x, const int32_t* idx, const 
 int route_impl(const moe_dims* d, const uint16_t* x, const uint16_t* rw, const uint16_t* rs, const uint16_t* pes,
                int32_t* idx, uint16_t* w, cudaStream_t s) {
     RouterArgs ra{x, rw, rs, pes, idx, w, d->T, d->H, d->E, d->k, d->eps, bf16_round(pow((double)d->H, -0.5))};
-    return fail(launch_router(ra, s));
+    CUtensorMap m_rw;
+    if (!make_map_2d(&m_rw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rw, d->H, d->E, 64, 32)) return MOE_ERR_CUDA;
+    return fail(launch_router(m_rw, ra, s));
 }
 
 int get_workspace(const moe_dims* d, void* workspace, size_t ws_bytes, const Layout& L, uint8_t** out) {

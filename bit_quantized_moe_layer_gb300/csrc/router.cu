@@ -7,7 +7,10 @@
 //      manualRms), then the two bf16 multiplies (router scale, H^-0.5) into
 //      shared memory;
 //   2. compute the bf16 scores of 32 experts with mma.sync m16n8k16 (fp32
-//      accumulate), and write them into the leader CTA's shared memory;
+//      accumulate), the 32 router-weight rows streamed by a producer warp
+//      through a TMA ring of 64-wide K blocks (128-byte swizzle) that starts
+//      filling while the norm runs, and write them into the leader CTA's
+//      shared memory;
 // then the leader CTA picks the top k per token (value descending, ties to
 // the lower expert id), takes the fp32 softmax over the k picked scores and
 // multiplies by per_expert_scale[idx].
@@ -23,8 +26,10 @@ namespace moe {
 namespace {
 
 constexpr int kTT = 16;        // tokens per cluster
-constexpr int kWarps = 4;      // warps per CTA
+constexpr int kWarps = 4;      // compute warps per CTA (+1 producer warp)
 constexpr int kExpPerCta = 32; // experts per CTA (8 per warp)
+constexpr int kRing = 8;       // K blocks of router weight in flight
+constexpr int kBlockBytes = kExpPerCta * 128;  // 32 rows x 64 bf16
 
 __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                                uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -41,12 +46,18 @@ __device__ __forceinline__ uint32_t key16_to_bits(uint32_t k) { return (k & 0x80
 
 }  // namespace
 
-__global__ void __launch_bounds__(kWarps * 32) router_kernel(RouterArgs a) {
-    extern __shared__ __align__(16) uint8_t smem[];
+__global__ void __launch_bounds__((kWarps + 1) * 32) router_kernel(const __grid_constant__ CUtensorMap wmap,
+                                                                    RouterArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ uint64_t full[kRing], empty[kRing];
+    __shared__ int abort_flag_s;
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int H = a.H, E = a.E, k = a.k;
     const int rowstride = H + 8;  // bf16 elements; +16 B per row keeps the fragment reads conflict-free
-    uint16_t* n3 = reinterpret_cast<uint16_t*>(smem);
+    uint8_t* ring = smem;                                          // kRing x 4 KB, 1024-aligned
+    uint16_t* n3 = reinterpret_cast<uint16_t*>(smem + kRing * kBlockBytes);
     uint16_t* scores = n3 + kTT * rowstride;  // [kTT][E] bf16, used in the leader CTA
+    volatile int* abort_flag = &abort_flag_s;
 
     cg::cluster_group cluster = cg::this_cluster();
     const int cs = (int)cluster.num_blocks();
@@ -54,6 +65,37 @@ __global__ void __launch_bounds__(kWarps * 32) router_kernel(RouterArgs a) {
     const int tile = blockIdx.x / cs;
     const int t0 = tile * kTT;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nkb = H / 64;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kRing; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kWarps);
+        }
+        abort_flag_s = 0;
+        fence_barrier_init();
+    }
+    // All CTAs of the cluster have started (and initialised their barriers)
+    // before any of them writes into the leader's shared memory.
+    cluster.sync();
+
+    if (warp == kWarps) {
+        // ---- producer: router-weight rows [32 rank, 32 rank + 32), one 64-wide K block per stage ----
+        if (lane == 0) {
+            prefetch_tensormap(&wmap);
+            int kb = 0;
+            for (; kb < nkb; ++kb) {
+                const int slot = kb % kRing;
+                if (!mbar_wait(&empty[slot], ((kb / kRing) & 1) ^ 1, abort_flag)) break;
+                mbar_arrive_expect_tx(&full[slot], kBlockBytes);
+                tma_load_2d(ring + slot * kBlockBytes, &wmap, &full[slot], kb * 64, rank * kExpPerCta);
+            }
+            for (int b = (kb > kRing ? kb - kRing : 0); b < kb; ++b)  // no copies in flight at exit
+                mbar_wait(&full[b % kRing], (b / kRing) & 1, abort_flag);
+        }
+        cluster.sync();
+        return;
+    }
 
     // ---- 1. no-scale RMS norm, x scale, x H^-0.5 (bf16 after each op) ----
     for (int tl = warp; tl < kTT; tl += kWarps) {
@@ -103,36 +145,29 @@ __global__ void __launch_bounds__(kWarps * 32) router_kernel(RouterArgs a) {
     // four steps sum the block's 64 products exactly once.
     const int e0 = rank * kExpPerCta + warp * 8;
     const int g = lane >> 2, q = lane & 3;
-    const int eg = e0 + g;
-    const uint16_t* wrow = a.router_w + (size_t)(eg < E ? eg : 0) * H;
     const uint16_t* arow0 = n3 + g * rowstride;
     const uint16_t* arow1 = n3 + (g + 8) * rowstride;
+    const int brow = warp * 8 + g;  // row of this lane's expert in a ring block
     float c[4] = {0.f, 0.f, 0.f, 0.f};
-    if (e0 < E) {
-        uint4 b0 = make_uint4(0, 0, 0, 0), b1 = b0;
-        if (eg < E) {
-            b0 = __ldg(reinterpret_cast<const uint4*>(wrow + 16 * q));
-            b1 = __ldg(reinterpret_cast<const uint4*>(wrow + 16 * q + 8));
-        }
-        for (int kb = 0; kb < H; kb += 64) {
-            uint4 nb0 = make_uint4(0, 0, 0, 0), nb1 = nb0;
-            if (eg < E && kb + 64 < H) {
-                nb0 = __ldg(reinterpret_cast<const uint4*>(wrow + kb + 64 + 16 * q));
-                nb1 = __ldg(reinterpret_cast<const uint4*>(wrow + kb + 64 + 16 * q + 8));
-            }
-            const uint4 x0 = *reinterpret_cast<const uint4*>(arow0 + kb + 16 * q);
-            const uint4 x1 = *reinterpret_cast<const uint4*>(arow0 + kb + 16 * q + 8);
-            const uint4 y0 = *reinterpret_cast<const uint4*>(arow1 + kb + 16 * q);
-            const uint4 y1 = *reinterpret_cast<const uint4*>(arow1 + kb + 16 * q + 8);
-            const uint32_t ar0[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-            const uint32_t ar1[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
-            const uint32_t br[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+    for (int kb = 0; kb < nkb; ++kb) {
+        const int slot = kb % kRing;
+        if (!mbar_wait(&full[slot], (kb / kRing) & 1, abort_flag)) break;
+        const uint8_t* blk = ring + slot * kBlockBytes + brow * 128;
+        const uint4 b0 = *reinterpret_cast<const uint4*>(blk + (((2 * q) ^ (brow & 7)) << 4));
+        const uint4 b1 = *reinterpret_cast<const uint4*>(blk + (((2 * q + 1) ^ (brow & 7)) << 4));
+        const int kk = kb * 64;
+        const uint4 x0 = *reinterpret_cast<const uint4*>(arow0 + kk + 16 * q);
+        const uint4 x1 = *reinterpret_cast<const uint4*>(arow0 + kk + 16 * q + 8);
+        const uint4 y0 = *reinterpret_cast<const uint4*>(arow1 + kk + 16 * q);
+        const uint4 y1 = *reinterpret_cast<const uint4*>(arow1 + kk + 16 * q + 8);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+        const uint32_t ar0[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        const uint32_t ar1[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+        const uint32_t br[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-            for (int s = 0; s < 4; ++s)
-                mma_bf16_16816(c, ar0[2 * s], ar1[2 * s], ar0[2 * s + 1], ar1[2 * s + 1], br[2 * s], br[2 * s + 1]);
-            b0 = nb0;
-            b1 = nb1;
-        }
+        for (int s = 0; s < 4; ++s)
+            mma_bf16_16816(c, ar0[2 * s], ar1[2 * s], ar0[2 * s + 1], ar1[2 * s + 1], br[2 * s], br[2 * s + 1]);
     }
     // c0,c1: token g, experts e0+2q, e0+2q+1; c2,c3: token g+8.
     uint16_t* lead = cluster.map_shared_rank(scores, 0);
@@ -198,19 +233,26 @@ int router_error_word() {
 }
 
 size_t router_smem_bytes(int H, int E) {
-    return (size_t)kTT * (H + 8) * 2 + (size_t)kTT * E * 2;
+    return 1024 + (size_t)kRing * kBlockBytes + (size_t)kTT * (H + 8) * 2 + (size_t)kTT * E * 2;
 }
 
-cudaError_t launch_router(const RouterArgs& a, cudaStream_t stream) {
+cudaError_t launch_router(const CUtensorMap& wmap, const RouterArgs& a, cudaStream_t stream) {
     if (a.T == 0) return cudaSuccess;
     const int cs = (a.E + kExpPerCta - 1) / kExpPerCta;
     const int tiles = (a.T + kTT - 1) / kTT;
     const size_t smem = router_smem_bytes(a.H, a.E);
-    cudaError_t err = cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        cudaError_t err = cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448 - 1024);
+        if (err != cudaSuccess) return err;
+        attr_set[dev] = true;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(tiles * cs, 1, 1);
-    cfg.blockDim = dim3(kWarps * 32, 1, 1);
+    cfg.blockDim = dim3((kWarps + 1) * 32, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -220,7 +262,7 @@ cudaError_t launch_router(const RouterArgs& a, cudaStream_t stream) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, router_kernel, a);
+    return cudaLaunchKernelEx(&cfg, router_kernel, wmap, a);
 }
 
 }  // namespace moe

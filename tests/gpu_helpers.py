@@ -2,12 +2,14 @@
 inputs and compare with the CPU oracle.
 
 Comparison rules (stated once here, used by every GPU test):
-  * routing indices: bit-exact, except on "near-tie" tokens where the
-    oracle's exact k-th and (k+1)-th logits differ by less than 1e-3
-    relative; those tokens are counted and must still hold a valid top-k
-    (the oracle's first k-1 experts plus one whose logit is within the
-    near-tie band of the k-th);
-  * routing weights: within 1 bf16 ulp where the indices agree;
+  * routing indices: the set of k experts per token is bit-exact, except on
+    "near-tie" tokens where the oracle's exact k-th and (k+1)-th logits
+    differ by less than 1e-3 relative; those tokens are counted and must
+    still hold a valid top-k (one swap, between experts inside the band).
+    The pages' top-k (argpartition) is an unordered set; the emitted order
+    must be score descending with ties to the lower id, allowing a swap of
+    neighbours whose oracle scores are one bf16 ulp apart;
+  * routing weights: within 1 bf16 ulp, per (token, expert);
   * permutation, offsets, inverse: bit-exact;
   * layer output: |gpu - oracle| <= max(2e-2 * RMS(oracle), 1 bf16 ulp of
     the oracle value) per element, and RMS(gpu - oracle) <= 1e-3 * RMS.
@@ -139,9 +141,13 @@ def check_routing(d, ref, idx, w):
             assert len(extra) == 1 and len(missing) == 1, f"near-tie token {t}: more than one swap"
             assert band(lg[t, extra.pop()], lg[t, missing.pop()]), f"near-tie token {t}: swap outside the band"
             continue
-        for j in range(k - 1):  # order: descending, except inside the near-tie band
+        sc = f64(ref["scores"][t])
+        for j in range(k - 1):  # emitted order: score descending, ties to the lower id
             a, b = idx[t, j], idx[t, j + 1]
-            assert lg[t, a] >= lg[t, b] or band(lg[t, a], lg[t, b]), f"token {t}: order {idx[t]}"
+            ok = sc[a] > sc[b] or (sc[a] == sc[b] and a < b)
+            # a one-ulp rounding flip of a GPU score may swap two neighbours
+            ok = ok or abs(sc[a] - sc[b]) <= float(bf16_ulp(np.array([max(abs(sc[a]), abs(sc[b]))]))[0])
+            assert ok, f"token {t}: order {idx[t]} vs oracle {ref['idx'][t]}"
         gw = dict(zip(idx[t].tolist(), f64(w[t]).tolist()))
         for j, e in enumerate(ref["idx"][t].tolist()):
             o = float(f64(ref["w"][t, j]))
