@@ -226,4 +226,10 @@ __device__ __forceinline__ uint32_t fma_bf16x2(uint32_t a, uint32_t b, uint32_t 
 
 __device__ __forceinline__ int elect_lane0() { return (threadIdx.x & 31) == 0; }
 
+// Cluster-wide barrier (all threads of all CTAs of the cluster). Non-aligned
+// form; callers still reconverge their warp first (__syncwarp).
+__device__ __forceinline__ void cluster_barrier() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
 }  // namespace moe

@@ -53,14 +53,28 @@ __host__ __device__ inline int scale_buf_bytes(int K) {
     return ((128 * (K / 64) * 2 * 2) + 1023) & ~1023;
 }
 
-// gelu_approx(u) = 0.5 u (1 + tanh(s)), s = sqrt(2/pi) (u + 0.044715 u^3),
-// evaluated as u / (1 + exp(-2 s)) (the same function: 0.5 (1 + tanh s) is
-// the logistic of 2 s). This form does not cancel for negative u, where
-// 1 + tanh(s) in fp32 loses every digit.
-__device__ __forceinline__ float gelu_tanh(float u) {
+// bf16(gelu_approx(g) * up) for bf16 g, up, where gelu_approx(g) =
+// 0.5 g (1 + tanh(s)), s = sqrt(2/pi) (g + 0.044715 g^3). 0.5 (1 + tanh s) is
+// the logistic of 2s, evaluated in that form so it keeps its relative
+// accuracy where 1 + tanh(s) cancels (s << 0). p = g*up is exact in fp32.
+// For s >= 0 the value is p - p*t with t = 1 - logistic(2s) > 0, formed by a
+// fused multiply-add rounded toward zero: the exact value lies strictly
+// between 0 and p, so an exact bf16 tie of p (large g, where t is below
+// fp32's resolution of 1) rounds toward zero as the exact value does.
+__device__ __forceinline__ uint32_t geglu_bf16(float g, float up) {
     const float c = 0.7978845608028654f;  // sqrt(2/pi)
-    const float s = __fmul_rn(c, __fadd_rn(u, __fmul_rn(0.044715f, __fmul_rn(u, __fmul_rn(u, u)))));
-    return __fdiv_rn(u, __fadd_rn(1.0f, expf(__fmul_rn(-2.0f, s))));
+    const float s = __fmul_rn(c, __fadd_rn(g, __fmul_rn(0.044715f, __fmul_rn(g, __fmul_rn(g, g)))));
+    const float p = __fmul_rn(g, up);
+    float m;
+    if (s < 0.f) {
+        const float e = expf(__fmul_rn(2.0f, s));
+        m = __fmul_rn(p, __fdiv_rn(e, __fadd_rn(1.0f, e)));
+    } else {
+        const float e = expf(__fmul_rn(-2.0f, s));
+        const float t = fmaxf(__fdiv_rn(e, __fadd_rn(1.0f, e)), 1e-30f);
+        m = __fmaf_rz(-p, t, p);
+    }
+    return f32_to_bf16_bits(m);
 }
 
 // Position of element n inside its 8-block in the interleaved K order.
@@ -310,8 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float gb = bf16_bits_to_f32(f32_to_bf16_bits(gf));  // z is a bf16 tensor
                         const float ub = bf16_bits_to_f32(f32_to_bf16_bits(uf));
                         if (tok < tl.rows)
-                            a.out[(size_t)(tl.p0 + tok) * a.out_ld + pos] =
-                                (uint16_t)f32_to_bf16_bits(__fmul_rn(gelu_tanh(gb), ub));
+                            a.out[(size_t)(tl.p0 + tok) * a.out_ld + pos] = (uint16_t)geglu_bf16(gb, ub);
                     }
                 }
             } else {
@@ -327,6 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
+    __syncwarp();  // role warps diverge (one elected lane); reconverge before the block barrier
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {

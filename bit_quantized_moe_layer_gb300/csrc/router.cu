@@ -77,7 +77,7 @@ __global__ void __launch_bounds__((kWarps + 1) * 32) router_kernel(const __grid_
     }
     // All CTAs of the cluster have started (and initialised their barriers)
     // before any of them writes into the leader's shared memory.
-    cluster.sync();
+    cluster_barrier();
 
     if (warp == kWarps) {
         // ---- producer: router-weight rows [32 rank, 32 rank + 32), one 64-wide K block per stage ----
@@ -93,7 +93,8 @@ __global__ void __launch_bounds__((kWarps + 1) * 32) router_kernel(const __grid_
             for (int b = (kb > kRing ? kb - kRing : 0); b < kb; ++b)  // no copies in flight at exit
                 mbar_wait(&full[b % kRing], (b / kRing) & 1, abort_flag);
         }
-        cluster.sync();
+        __syncwarp();
+        cluster_barrier();
         return;
     }
 
@@ -136,7 +137,9 @@ __global__ void __launch_bounds__((kWarps + 1) * 32) router_kernel(const __grid_
             *reinterpret_cast<uint4*>(dst + h) = make_uint4(o[0], o[1], o[2], o[3]);
         }
     }
-    __syncthreads();
+    // The compute warps only (the producer warp never comes here): named
+    // barrier 1 over kWarps * 32 threads.
+    asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
 
     // ---- 2. scores for experts [e0, e0+8) of this warp: 16 tokens x 8 experts ----
     // Inside each 64-wide K block, thread (g, q) owns K [16q, 16q+16) of its
@@ -182,7 +185,8 @@ __global__ void __launch_bounds__((kWarps + 1) * 32) router_kernel(const __grid_
             lead[(g + 8) * E + ea + 1] = (uint16_t)f32_to_bf16_bits(c[3]);
         }
     }
-    cluster.sync();
+    __syncwarp();
+    cluster_barrier();
     if (rank != 0) return;
 
     // ---- 3. top-k + precise softmax + per-expert scale (leader CTA) ----

@@ -14,10 +14,12 @@
  *  - Every tensor the pages hold in the model dtype is rounded to bf16
  *    (round to nearest even) exactly where the pages produce it.
  *  - Where the pages fix the arithmetic precision it is followed: the RMS
- *    norm is fp32 (manualRms: x_f32 * rsqrt(mean(x^2) + eps), cast back) and
- *    the routing softmax is fp32 ("precise" softmax).
+ *    norm is fp32 (manualRms: x_f32 * rsqrt(mean(x^2) + eps), cast back;
+ *    the fp32 mean is the exact mean rounded once) and the routing softmax
+ *    is fp32 ("precise" softmax).
  *  - Where the pages are silent (matmul accumulation, GeGLU internals, the
- *    k-way sum of the combine) the oracle computes in double and rounds once.
+ *    k-way sum of the combine) the oracle computes in double and rounds once
+ *    to the bf16 of the exact value.
  *  - A 4-bit weight dequantises to the model dtype: w = bf16(S*q + B), as the
  *    pages' `dequantize` of a quantized table yields a bf16 matmul operand
  *    (DiffusionGemmaModel.dequantEmbedWeight, used by softEmbeddings).
@@ -143,16 +145,18 @@ int oracle_route(const oracle_dims* d, const uint16_t* x, const uint16_t* router
 #pragma omp for schedule(static)
         for (int t = 0; t < T; ++t) {
             const uint16_t* xt = x + (size_t)t * H;
-            /* RMSNormNoScale in fp32: mean of squares, + eps, rsqrt. */
-            float ss = 0.0f;
+            /* RMSNormNoScale in fp32: mean of squares, + eps, rsqrt. The fp32
+             * mean is the exact mean rounded once to fp32 (the squares of bf16
+             * values and their sum are exact in double for these sizes). */
+            double ss = 0.0;
             for (int h = 0; h < H; ++h) {
-                float v = bf(xt[h]);
+                double v = bf(xt[h]);
                 ss += v * v;
             }
 #if ORACLE_MUTANT == 1
-            float mean = ss / (float)(H - 1); /* planted: wrong divisor */
+            float mean = (float)(ss / (double)(H - 1)); /* planted: wrong divisor */
 #else
-            float mean = ss / (float)H;
+            float mean = (float)(ss / (double)H);
 #endif
             float denom = mean + d->eps;
             float r = (float)(1.0 / sqrt((double)denom)); /* rsqrt, rounded to fp32 */
@@ -272,10 +276,28 @@ static void dequant_expert(const uint32_t* w, const uint16_t* sc, const uint16_t
     }
 }
 
-/* gelu_approx(u) = 0.5 u (1 + tanh(sqrt(2/pi) (u + 0.044715 u^3))) */
-static double gelu_tanh(double u) {
+/* bf16(gelu_approx(g) * up), one rounding, where
+ *   gelu_approx(g) = 0.5 g (1 + tanh(s)),  s = sqrt(2/pi) (g + 0.044715 g^3)
+ * (the tanh approximation of GELU). 0.5 (1 + tanh(s)) equals the logistic
+ * function of 2s; evaluated that way it keeps its relative accuracy where
+ * 1 + tanh(s) cancels (s << 0). For s >= 0 the exact product lies strictly
+ * between 0 and g*up (the logistic is < 1); where double cannot tell the
+ * logistic from 1 (s > ~18.7) the product is moved one double ulp toward
+ * zero, which rounds an exact bf16 tie of g*up the way the exact value does
+ * and changes no other result. */
+static uint16_t geglu_bf16(double g, double up) {
     const double c = sqrt(2.0 / 3.14159265358979323846);
-    return 0.5 * u * (1.0 + tanh(c * (u + 0.044715 * u * u * u)));
+    const double s = c * (g + 0.044715 * g * g * g);
+    const double p = g * up; /* exact: a product of two bf16 values */
+    double v;
+    if (s < 0.0) {
+        const double e = exp(2.0 * s);
+        v = p * (e / (1.0 + e));
+    } else {
+        v = p / (1.0 + exp(-2.0 * s));
+        if (v == p && p != 0.0) v = nextafter(p, 0.0);
+    }
+    return bf16_from_double(v);
 }
 
 /*
@@ -332,9 +354,9 @@ int oracle_experts(const oracle_dims* d, const uint16_t* x, const int32_t* idx, 
                 }
                 for (int n = 0; n < I; ++n) {
 #if ORACLE_MUTANT == 6
-                    m[n] = bf16_from_double(gelu_tanh(bf(z[n + I])) * (double)bf(z[n])); /* planted: halves swapped */
+                    m[n] = geglu_bf16(bf(z[n + I]), bf(z[n])); /* planted: halves swapped */
 #else
-                    m[n] = bf16_from_double(gelu_tanh(bf(z[n])) * (double)bf(z[n + I]));
+                    m[n] = geglu_bf16(bf(z[n]), bf(z[n + I]));
 #endif
                 }
                 uint16_t* yf = y_all + (size_t)f * H;

@@ -79,6 +79,18 @@ def dense_dequant(w_words, s_bits, b_bits, K: int, g: int) -> np.ndarray:
     return f64(torch_bf16_bits(v32))
 
 
+def geglu_exact(gate, up) -> np.ndarray:
+    """gelu_approx(gate) * up in 100-digit arithmetic (mpmath), as float64."""
+    import mpmath
+    mpmath.mp.dps = 100
+    c = mpmath.sqrt(2 / mpmath.pi)
+    out = np.empty(len(gate))
+    for i, (g, u) in enumerate(zip(gate, up)):
+        g = mpmath.mpf(float(g))
+        out[i] = float(g / 2 * (1 + mpmath.tanh(c * (g + mpmath.mpf("0.044715") * g ** 3))) * mpmath.mpf(float(u)))
+    return out
+
+
 def small_dims(**kw) -> ms.Dims:
     base = dict(T=16, H=256, E=8, k=2, inter=128, group=64)
     base.update(kw)
@@ -252,46 +264,66 @@ def check_experts_brute_force(lib):
         wgu = dense_dequant(inp.gu_w[e], inp.gu_s[e], inp.gu_b[e], H, d.group)
         wdn = dense_dequant(inp.dn_w[e], inp.dn_s[e], inp.dn_b[e], I, d.group)
         assert_nearest_bf16(z[f], wgu @ x[t], f"gate_up output, slot {f}")
-        zz = torch.from_numpy(f64(z[f]))
-        mm = torch.nn.functional.gelu(zz[:I], approximate="tanh") * zz[I:]
-        assert_nearest_bf16(m[f], mm.numpy(), f"GeGLU output, slot {f}", rel_slack=1e-12)
+        zz = f64(z[f])
+        assert_nearest_bf16(m[f], geglu_exact(zz[:I], zz[I:]), f"GeGLU output, slot {f}")
         assert_nearest_bf16(y[f], wdn @ f64(m[f]), f"down output, slot {f}")
     prods = f64(torch_bf16_bits(ms.bits_to_f32(y) * ms.bits_to_f32(rt["w"]).reshape(-1, 1)))
     assert_nearest_bf16(out, prods.reshape(d.T, d.k, H).sum(1), "combine")
 
 
-def check_experts_one_hot(lib):
-    """Closed form. All codes 8 with S = 1, B = -8 make every weight 0, except
-    gate (n0, K0) = +1, up (I+n0, K1) = +2 and down (h0, n0) = +3. With k = 1
-    and pes = 1 the weight is 1, so out[t, h0] = bf16(3 m), with
-    m = bf16(gelu_tanh(x[t,K0]) * 2 x[t,K1]), and out is 0 elsewhere."""
-    d = small_dims(T=4, E=2, k=1)
-    inp = ms.make_custom(d, seed=9)
+def _one_hot_layer(lib, xrows, gate_code, up_code, down_code, n0=37, K0=70, K1=201, h0=133):
+    """Layer whose weights are all 0 (codes 8, S = 1, B = -8) except gate
+    (n0, K0), up (I+n0, K1) and down (h0, n0), whose codes set multipliers
+    code-8. k = 1, weight 1. Returns out [T, H] bits."""
+    d = small_dims(T=len(xrows), E=1, k=1)
     I, H, g = d.inter, d.H, d.group
-    n0, K0, K1, h0 = 37, 70, 201, 133
-    gu_w = np.full((d.E, 2 * I, H // 8), 0x88888888, np.uint32)
-    dn_w = np.full((d.E, H, I // 8), 0x88888888, np.uint32)
-    for e in range(d.E):
-        gu_w[e, n0, K0 // 8] = np.uint32(0x88888888 ^ (0x1 << (4 * (K0 % 8))))   # 8 -> 9
-        gu_w[e, I + n0, K1 // 8] = np.uint32(0x88888888 ^ (0x2 << (4 * (K1 % 8))))  # 8 -> 10
-        dn_w[e, h0, n0 // 8] = np.uint32(0x88888888 ^ (0x3 << (4 * (n0 % 8))))   # 8 -> 11
-    ones_g = lambda n, kk: np.full((d.E, n, kk // g), 0x3F80, np.uint16)
-    m8_g = lambda n, kk: np.full((d.E, n, kk // g), 0xC100, np.uint16)          # -8.0
+    gu_w = np.full((1, 2 * I, H // 8), 0x88888888, np.uint32)
+    dn_w = np.full((1, H, I // 8), 0x88888888, np.uint32)
+    gu_w[0, n0, K0 // 8] = np.uint32(0x88888888 ^ ((8 ^ gate_code) << (4 * (K0 % 8))))
+    gu_w[0, I + n0, K1 // 8] = np.uint32(0x88888888 ^ ((8 ^ up_code) << (4 * (K1 % 8))))
+    dn_w[0, h0, n0 // 8] = np.uint32(0x88888888 ^ ((8 ^ down_code) << (4 * (n0 % 8))))
+    ones_g = lambda n, kk: np.full((1, n, kk // g), 0x3F80, np.uint16)
+    m8_g = lambda n, kk: np.full((1, n, kk // g), 0xC100, np.uint16)  # -8.0
+    x = np.zeros((d.T, H), np.uint16)
+    x[:, K0] = xrows[:, 0]
+    x[:, K1] = xrows[:, 1]
     idx = np.zeros((d.T, 1), np.int32)
-    idx[1::2] = 1
     w = np.full((d.T, 1), 0x3F80, np.uint16)
-    out = oracle.experts(d, inp.x, idx, w, (gu_w, ones_g(2 * I, H), m8_g(2 * I, H)),
-                         (dn_w, ones_g(H, I), m8_g(H, I)), lib=lib)
-    x = f64(inp.x)
-    for t in range(d.T):
-        gate = torch.tensor(x[t, K0], dtype=torch.float64)
-        mval = (torch.nn.functional.gelu(gate, approximate="tanh") * 2.0 * x[t, K1]).item()
-        mbits = np.array([oracle.bf16_from_double(mval, lib)], np.uint16)  # helper pinned above
-        assert_nearest_bf16(mbits, [mval], "m")
-        mb = f64(mbits)[0]
-        want = np.zeros(H)
-        want[h0] = f64(torch_bf16_bits(np.float32(3.0 * mb)))[0]
+    return oracle.experts(d, x, idx, w, (gu_w, ones_g(2 * I, H), m8_g(2 * I, H)),
+                          (dn_w, ones_g(H, I), m8_g(H, I)), lib=lib or oracle.load()), h0
+
+
+def check_experts_one_hot(lib):
+    """Closed form: with gate multiplier 1, up 2 and down 3, out[t, h0] =
+    bf16(3 m), m = bf16(gelu_tanh(x[t,K0]) * 2 x[t,K1]), and out is 0 elsewhere."""
+    rng = np.random.default_rng(9)
+    xr = ms.bf16_bits(rng.standard_normal((6, 2)) * 2)
+    out, h0 = _one_hot_layer(lib, xr, 9, 10, 11)
+    for t in range(len(xr)):
+        gate, up = f64(xr[t, 0]), 2.0 * f64(xr[t, 1])
+        mex = geglu_exact(np.array([gate]), np.array([up]))
+        mbits = torch_bf16_bits(np.float32(mex))  # float32 first: exact enough away from ties
+        assert_nearest_bf16(mbits, mex, "m")
+        want = np.zeros(out.shape[1])
+        want[h0] = f64(torch_bf16_bits(np.float32(3.0 * f64(mbits)[0])))[0]
         assert np.array_equal(f64(out[t]), want), f"one-hot layer, token {t}"
+
+
+def check_geglu_ties(lib):
+    """gelu_tanh(g) < g for g > 0, so where g*up is exactly halfway between two
+    bf16 values, the exact product lies below the tie and rounds toward zero:
+    g=5.5, up=2.0625: g*up = 11.34375 (between 11.3125 and 11.375) -> 11.3125;
+    g=7.5, up=1.03125 (7.734375, between 7.71875 and 7.75) -> 7.71875, where
+    double arithmetic can no longer tell the logistic factor from 1."""
+    cases = [(5.5, 2.0625, 11.3125), (7.5, 1.03125, 7.71875), (-5.5, -2.0625, -0.0)]
+    xr = ms.bf16_bits(np.array([[g, u] for g, u, _ in cases], np.float32))
+    out, h0 = _one_hot_layer(lib, xr, 9, 9, 9)
+    for t, (g, u, want) in enumerate(cases):
+        got = f64(out[t, h0])
+        if want == 0.0:
+            assert abs(got) < 1e-6, f"g={g}: {got}"
+        else:
+            assert got == want, f"GeGLU tie g={g} up={u}: got {got}, want {want}"
 
 
 def check_single_expert_identity(lib):
@@ -343,6 +375,6 @@ ALL_CHECKS = [
     check_router_constant_row, check_router_zero_row, check_router_scale_invariance,
     check_router_exact_math, check_router_logits_topk, check_router_weights,
     check_dispatch,
-    check_experts_brute_force, check_experts_one_hot, check_single_expert_identity,
+    check_experts_brute_force, check_experts_one_hot, check_geglu_ties, check_single_expert_identity,
     check_expert_relabel, check_token_permutation,
 ]

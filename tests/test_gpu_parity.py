@@ -207,3 +207,34 @@ def test_bad_expert_id_is_flagged_not_faulted():
     perm, off, inv = gh.gpu_dispatch(d, idx)
     assert off[-1] == 7
     assert moe.device_error() & 2
+
+
+def test_geglu_ties_and_tails_exact():
+    """Exact bf16 ties of gate*up (large gates) and the far negative tail go
+    through the CUDA GeGLU epilogue exactly as through the oracle."""
+    import oracle_checks as oc
+    rng = np.random.default_rng(11)
+    gates = [5.5, 7.5, -5.5, 9.0, -7.0625, -12.0, 3.0, 0.0]
+    ups = [2.0625, 1.03125, -2.0625, 1.5, -1.3671875, 4.0, 2.0, 1.0]
+    xr = np.concatenate([ms.bf16_bits(np.array(list(zip(gates, ups)), np.float32)),
+                         ms.bf16_bits(rng.standard_normal((24, 2)) * 3)])
+    want, h0 = oc._one_hot_layer(None, xr, 9, 9, 9)
+    d = ms.Dims(T=len(xr), H=256, E=1, k=1, inter=128)
+    I, H = d.inter, d.H
+    # the same one-hot layer on the GPU
+    gu_w = np.full((1, 2 * I, H // 8), 0x88888888, np.uint32)
+    dn_w = np.full((1, H, I // 8), 0x88888888, np.uint32)
+    n0, K0, K1 = 37, 70, 201
+    gu_w[0, n0, K0 // 8] = np.uint32(0x88888888 ^ (1 << (4 * (K0 % 8))))
+    gu_w[0, I + n0, K1 // 8] = np.uint32(0x88888888 ^ (1 << (4 * (K1 % 8))))
+    dn_w[0, h0, n0 // 8] = np.uint32(0x88888888 ^ (1 << (4 * (n0 % 8))))
+    ones = lambda n, kk: np.full((1, n, kk // 64), 0x3F80, np.uint16)
+    m8 = lambda n, kk: np.full((1, n, kk // 64), 0xC100, np.uint16)
+    x = np.zeros((d.T, H), np.uint16)
+    x[:, K0], x[:, K1] = xr[:, 0], xr[:, 1]
+    inp = ms.LayerInputs(d, x, np.zeros((1, H), np.uint16), np.full(H, 0x3F80, np.uint16),
+                         np.full(1, 0x3F80, np.uint16), gu_w, ones(2 * I, H), m8(2 * I, H),
+                         dn_w, ones(H, I), m8(H, I))
+    g = gh.upload(inp)
+    out = gh.gpu_experts(g, np.zeros((d.T, 1), np.int32), np.full((d.T, 1), 0x3F80, np.uint16))
+    assert np.array_equal(out, want), np.flatnonzero((out != want).any(1))
