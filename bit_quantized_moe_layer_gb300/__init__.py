@@ -28,7 +28,7 @@ STATUS = {0: "ok", 1: "null pointer", 2: "bad shape", 3: "pointer not 16-byte al
 
 # Every function the public header declares.
 EXPORTS = ("moe_status_str", "moe_workspace_bytes", "moe_route", "moe_dispatch", "moe_experts",
-           "moe_forward", "moe_forward_hostio", "moe_timing_enable", "moe_timing_read",
+           "moe_experts_noalloc", "moe_forward", "moe_forward_hostio", "moe_timing_enable", "moe_timing_read",
            "moe_launches_per_forward", "moe_device_error")
 
 
@@ -69,13 +69,14 @@ def load(path: str = LIB_PATH):
     lib.moe_route.argtypes = [D, P, P, P, P, P, P, P]
     lib.moe_dispatch.argtypes = [D, P, P, P, P, P]
     lib.moe_experts.argtypes = [D, P, P, P, Q, Q, P, P, Z, P]
+    lib.moe_experts_noalloc.argtypes = [D, P, P, P, Q, Q, P, P]
     lib.moe_forward.argtypes = [D, P, P, P, P, Q, Q, P, P, P, P, Z, P]
     lib.moe_forward_hostio.argtypes = [D, P, P, P, P, Q, Q, P, P, Z, P]
     lib.moe_timing_enable.argtypes = [I]
     lib.moe_timing_read.argtypes = [ctypes.POINTER(ctypes.c_float), I, ctypes.POINTER(I)]
     lib.moe_launches_per_forward.argtypes = []
     lib.moe_device_error.argtypes = []
-    for fn in ("moe_route", "moe_dispatch", "moe_experts", "moe_forward", "moe_forward_hostio",
+    for fn in ("moe_route", "moe_dispatch", "moe_experts", "moe_experts_noalloc", "moe_forward", "moe_forward_hostio",
                "moe_timing_enable", "moe_timing_read", "moe_launches_per_forward", "moe_device_error"):
         getattr(lib, fn).restype = I
     _lib = lib
@@ -135,6 +136,13 @@ def moe_experts(d: Dims, x, idx, w, gate_up: QWeight, down: QWeight, out, worksp
     _check("moe_experts", load().moe_experts(ctypes.byref(d), _ptr(x), _ptr(idx), _ptr(w),
                                              ctypes.byref(gate_up), ctypes.byref(down), _ptr(out),
                                              _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def moe_experts_noalloc(d: Dims, x, idx, w, gate_up: QWeight, down: QWeight, out, stream=None):
+    """moe_experts with the library's fixed scratch (no allocation)."""
+    _check("moe_experts_noalloc", load().moe_experts_noalloc(ctypes.byref(d), _ptr(x), _ptr(idx), _ptr(w),
+                                                             ctypes.byref(gate_up), ctypes.byref(down),
+                                                             _ptr(out), _stream(stream)))
 
 
 def moe_forward(d: Dims, x, router_w, router_scale, per_expert_scale, gate_up: QWeight, down: QWeight,

@@ -294,6 +294,31 @@ int get_workspace(const moe_dims* d, void* workspace, size_t ws_bytes, const Lay
     return rc;
 }
 
+// ------------------------------------------------------ fixed scratch ----
+// Scratch of moe_experts_noalloc: a fixed array in the library's device
+// image, so that call never allocates. Every GPU that loads the library holds
+// it until the process exits. Host code must not use the array's name as a
+// device address (on the host it only stands for the symbol); the device
+// address comes from cudaGetSymbolAddress, once per device.
+constexpr size_t kNoAllocScratchBytes = MOE_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+int noalloc_scratch(uint8_t** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_DEVICE;
+    static std::mutex mu;
+    static std::vector<void*> ptrs;
+    std::lock_guard<std::mutex> lock(mu);
+    if ((int)ptrs.size() <= dev) ptrs.resize(dev + 1, nullptr);
+    if (!ptrs[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+        ptrs[dev] = p;
+    }
+    *out = static_cast<uint8_t*>(ptrs[dev]);
+    return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -354,6 +379,29 @@ int moe_experts(const moe_dims* d, const uint16_t* x, const int32_t* idx, const 
     const Layout L = layout(d);
     uint8_t* ws = nullptr;
     if ((rc = get_workspace(d, workspace, ws_bytes, L, &ws))) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    CallTimer tm(s);
+    tm.mark(0);
+    tm.mark(1);
+    return run_experts(d, x, idx, w, gate_up, down, out, ws, L, di, s, tm);
+}
+
+int moe_experts_noalloc(const moe_dims* d, const uint16_t* x, const int32_t* idx, const uint16_t* w,
+                        const moe_qweight* gate_up, const moe_qweight* down, uint16_t* out, void* stream) {
+    int rc = check_dims(d);
+    if (rc) return rc;
+    if ((rc = check_ptrs({x, idx, w, out}))) return rc;
+    if ((rc = check_qweight(gate_up)) || (rc = check_qweight(down))) return rc;
+    const Layout L = layout(d);
+    if (L.total > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE;  // beyond the fixed scratch
+    if (d->T == 0) return MOE_OK;
+    DeviceInfo di;
+    if ((rc = device_info(&di))) return rc;
+    uint8_t* ws = nullptr;
+    if ((rc = noalloc_scratch(&ws))) return rc;
+    // Nothing in the scratch has to start at zero: every region the kernels
+    // read (routing copy, permutation, offsets, tile list, gathered inputs,
+    // GeGLU output, expert outputs) is written earlier in the same call.
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     CallTimer tm(s);
     tm.mark(0);

@@ -123,6 +123,35 @@ int moe_experts(const moe_dims* d, const uint16_t* x, const int32_t* idx, const 
                 void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * moe_experts without any allocation. (The pages have no counterpart: this
+ * call exists for callers of this library, not for the layer.)
+ *
+ * Some callers cannot let a library call cudaMalloc: their device memory is
+ * fully reserved by their own allocator or pool, or they cannot afford the
+ * device-wide synchronisation that cudaMalloc and cudaFree may cause inside
+ * a latency-critical loop. This call computes exactly what moe_experts
+ * computes (same kernels, same results), but its scratch is a fixed array of
+ * MOE_NOALLOC_SCRATCH_BYTES bytes inside the library's device image, which
+ * every GPU that loads the library holds until the process exits. No
+ * cudaMalloc, cudaFree or allocating routine is called.
+ *  - Inputs and outputs are the caller's device buffers, as for moe_experts.
+ *  - Dims whose scratch (moe_workspace_bytes(d)) exceeds
+ *    MOE_NOALLOC_SCRATCH_BYTES are rejected with MOE_ERR_WORKSPACE before
+ *    anything is enqueued (the canvas layer, T=256, H=2816, k=8, fits).
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - All calls on a device share the one array and it keeps the last call's
+ *    contents; nothing in it needs to start at zero. Calls whose work
+ *    overlaps on the GPU (other streams, other host threads) race on it:
+ *    serialise them.
+ */
+#define MOE_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+int moe_experts_noalloc(const moe_dims* d, const uint16_t* x, const int32_t* idx, const uint16_t* w,
+                        const moe_qweight* gate_up, const moe_qweight* down, uint16_t* out,
+                        void* stream);
+
+/*
  * The whole layer: moe_route on x, then moe_experts on the same x.
  * idx_out / w_out may be NULL (the routing then stays in the workspace).
  */
