@@ -77,21 +77,28 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
-// Bounded wait on an mbarrier phase. Returns false if the phase has not
-// completed within ~2 s (then it raises the device error word and the CTA's
-// shared abort flag) or if another warp of the CTA has already aborted, so a
-// broken pipeline ends the kernel instead of hanging the GPU. Callers treat
-// false as "stop issuing work and fall through to the exit path".
+// Bounded wait on an mbarrier phase. Spins briefly, then backs off with
+// short sleeps so that waiting warps leave most issue slots to the warps that
+// work. Returns false if the phase has not completed within ~2 s (then it
+// raises the device error word and the CTA's shared abort flag) or if another
+// warp of the CTA has already aborted, so a broken pipeline ends the kernel
+// instead of hanging the GPU. Callers treat false as "stop issuing work and
+// fall through to the exit path".
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
         if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (global_timer_ns() - t0 > 2000000000ull) {
-            *abort_flag = 1;
-            atomicOr(&g_error_word, kErrTimeout);
-            return false;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t n = 0;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        __nanosleep(32);
+        if ((n & 255u) == 255u) {
+            if (*abort_flag) return false;
+            if (global_timer_ns() - t0 > 2000000000ull) {
+                *abort_flag = 1;
+                atomicOr(&g_error_word, kErrTimeout);
+                return false;
+            }
         }
     }
 }
@@ -224,7 +231,16 @@ __device__ __forceinline__ uint32_t fma_bf16x2(uint32_t a, uint32_t b, uint32_t 
     return d;
 }
 
-__device__ __forceinline__ int elect_lane0() { return (threadIdx.x & 31) == 0; }
+// One lane of a converged warp (elect.sync). Issue TMA and tcgen05 work from
+// inside `if (elect_one())` in a loop the whole warp runs: the operands stay
+// warp-uniform, which keeps the issue cost of each instruction low.
+__device__ __forceinline__ uint32_t elect_one() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .b32 rx;\n\t.reg .pred px;\n\telect.sync rx|px, 0xffffffff;\n\tselp.b32 %0, 1, 0, px;\n\t}"
+        : "=r"(pred));
+    return pred;
+}
 
 // Cluster-wide barrier (all threads of all CTAs of the cluster). Non-aligned
 // form; callers still reconverge their warp first (__syncwarp).

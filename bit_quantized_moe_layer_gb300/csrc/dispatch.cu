@@ -16,75 +16,117 @@ constexpr int kDispatchThreads = 1024;
 constexpr int kMaxE = 256;
 }  // namespace
 
-// One CTA. Pass 1 counts slots per expert; a serial scan gives the offsets
-// and the token tiles; pass 2 walks the slots in chunks of 1024 in slot
-// order and places each at offsets[e] + (earlier slots of e), which makes
-// the sort stable and the output unique.
+// One CTA of 32 warps; warp w owns the contiguous slot range
+// [w*per, (w+1)*per). Pass 1: per-warp histograms (warp match-any, one add
+// per group of equal ids). Then per expert an exclusive scan over warps, a
+// scan over experts (offsets and token-tile bases) and the tile list. Pass 2:
+// each warp walks its range again in slot order and places each slot at its
+// warp's running base for that expert plus its rank among equal ids in the
+// 32-slot group. Warps cover the slots in order, so the sort is stable and
+// the result unique.
 __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs a) {
-    __shared__ int cnt[kMaxE];
-    __shared__ int base[kMaxE];
-    __shared__ int wcnt[kDispatchThreads / 32][kMaxE];
+    constexpr int kW = kDispatchThreads / 32;
+    __shared__ int wh[kW][kMaxE + 1];
+    __shared__ int cnt[kMaxE], off[kMaxE + 1], tbase[kMaxE + 1];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int S = a.S, E = a.E;
-    for (int e = tid; e < E; e += kDispatchThreads) cnt[e] = 0;
-    __syncthreads();
-    for (int f = tid; f < S; f += kDispatchThreads) {
-        const int e = a.idx[f];
-        if (e < 0 || e >= E) {
-            atomicOr(&g_error_word, kErrBadExpert);
-            continue;
-        }
-        atomicAdd(&cnt[e], 1);
-    }
-    __syncthreads();
-    if (tid == 0) {
-        int run = 0, nt = 0;
-        for (int e = 0; e < E; ++e) {
-            a.offsets[e] = run;
-            base[e] = run;
-            if (a.tiles) {
-                for (int p = 0; p < cnt[e]; p += a.nmax) {
-                    Tile t;
-                    t.e = e;
-                    t.p0 = run + p;
-                    t.rows = min(a.nmax, cnt[e] - p);
-                    t.pad = 0;
-                    a.tiles[nt++] = t;
-                }
-            }
-            run += cnt[e];
-        }
-        a.offsets[E] = run;
-        if (a.num_tiles) *a.num_tiles = nt;
-    }
-    __syncthreads();
     const unsigned lt_mask = (1u << lane) - 1u;
-    for (int c0 = 0; c0 < S; c0 += kDispatchThreads) {
-        const int f = c0 + tid;
-        int e = (f < S) ? a.idx[f] : -1;
+    for (int i = tid; i < kW * (kMaxE + 1); i += kDispatchThreads) (&wh[0][0])[i] = 0;
+    __syncthreads();
+    const int per = (S + kW - 1) / kW;
+    const int c0 = min(S, warp * per), c1 = min(S, c0 + per);
+    for (int b = c0; b < c1; b += 32) {
+        const int f = b + lane;
+        int e = (f < c1) ? a.idx[f] : -1;
+        if (f < c1 && (e < 0 || e >= E)) {
+            atomicOr(&g_error_word, kErrBadExpert);
+            e = -1;
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && (peers & lt_mask) == 0) wh[warp][e] += __popc(peers);
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += kDispatchThreads) {
+        int run = 0;
+        for (int w = 0; w < kW; ++w) {
+            const int v = wh[w][e];
+            wh[w][e] = run;
+            run += v;
+        }
+        cnt[e] = run;
+    }
+    __syncthreads();
+    if (warp == 0) {  // scan over experts: lane owns experts [8 lane, 8 lane + 8)
+        int lc[8], lt[8], sc = 0, st = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int e = lane * 8 + j;
+            lc[j] = (e < E) ? cnt[e] : 0;
+            lt[j] = (lc[j] + a.nmax - 1) / a.nmax;
+            sc += lc[j];
+            st += lt[j];
+        }
+        int ic = sc, it = st;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int vc = __shfl_up_sync(0xffffffffu, ic, o), vt = __shfl_up_sync(0xffffffffu, it, o);
+            if (lane >= o) {
+                ic += vc;
+                it += vt;
+            }
+        }
+        int rc = ic - sc, rt = it - st;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int e = lane * 8 + j;
+            if (e < E) {
+                off[e] = rc;
+                tbase[e] = rt;
+            }
+            rc += lc[j];
+            rt += lt[j];
+        }
+        if (lane == 31) {
+            off[E] = ic;
+            tbase[E] = it;
+        }
+    }
+    __syncthreads();
+    for (int e = tid; e <= E; e += kDispatchThreads) a.offsets[e] = off[e];
+    if (a.tiles) {
+        for (int e = tid; e < E; e += kDispatchThreads) {
+            for (int i = 0; tbase[e] + i < tbase[e + 1]; ++i) {
+                Tile t;
+                t.e = e;
+                t.p0 = off[e] + i * a.nmax;
+                t.rows = min(a.nmax, cnt[e] - i * a.nmax);
+                t.pad = 0;
+                a.tiles[tbase[e] + i] = t;
+            }
+        }
+        if (tid == 0 && a.num_tiles) {
+            int mx = 0;
+            for (int e = 0; e < E; ++e) mx = max(mx, min(cnt[e], a.nmax));
+            a.num_tiles[0] = tbase[E];
+            a.num_tiles[1] = mx;  // rows of the largest token tile
+        }
+    }
+    for (int i = tid; i < kW * E; i += kDispatchThreads) wh[i / E][i % E] += off[i % E];
+    __syncthreads();
+    for (int b = c0; b < c1; b += 32) {
+        const int f = b + lane;
+        int e = (f < c1) ? a.idx[f] : -1;
         if (e >= E) e = -1;
-        for (int x = lane; x < E; x += 32) wcnt[warp][x] = 0;
-        __syncwarp();
         const unsigned peers = __match_any_sync(0xffffffffu, e);
         const int rank = __popc(peers & lt_mask);
-        if (e >= 0 && rank == 0) wcnt[warp][e] = __popc(peers);
-        __syncthreads();
-        if (tid < E) {  // exclusive scan over warps, per expert
-            int s = base[tid];
-            for (int w = 0; w < kDispatchThreads / 32; ++w) {
-                const int v = wcnt[w][tid];
-                wcnt[w][tid] = s;
-                s += v;
-            }
-            base[tid] = s;
-        }
-        __syncthreads();
         if (e >= 0) {
-            const int p = wcnt[warp][e] + rank;
+            const int p = wh[warp][e] + rank;
             a.perm[p] = f;
             a.inv[f] = p;
         }
-        __syncthreads();
+        __syncwarp();
+        if (e >= 0 && rank == 0) wh[warp][e] += __popc(peers);
+        __syncwarp();
     }
 }
 

@@ -9,21 +9,31 @@
 // HBM once and the tensor cores stay far from busy.
 //
 // Persistent kernel, one CTA per SM, work item = (token tile of one expert,
-// 128-row weight tile). Warp roles:
-//   warp 0      TMA producer: packed weights (128 rows x 128 B per stage,
-//               128 B swizzle) and the token tile of the B operand; the
-//               item's scales and biases by one bulk copy per block of rows.
-//   warp 1      TMEM owner and MMA issuer (one thread).
-//   warps 4-7   dequant: thread = weight row = TMEM lane. Reads 8 nibbles per
-//               word from shared memory, makes exact bf16 codes with the
-//               0x4300 magic (128+q) minus 128, then bf16(S*q + B) with one
-//               fused multiply-add, and stores the row's 256-K slice into the
-//               A-operand ring in tensor memory (tcgen05.st).
-//   warps 8-11  epilogue: tcgen05.ld of the fp32 accumulator, bf16 rounding,
-//               GeGLU (gate_up) or the scatter to flat slots (down).
-// A stage is 256 of K. The dequantised pair order inside each 8-element block
-// is (0,4),(1,5),(2,6),(3,7); the B operands (gathered x, GeGLU output) are
-// stored in that same K order, so the MMA sums the same products.
+// 128-row weight tile), K in stages of 256. Warp roles:
+//   warp 0        TMA producer of the packed weights (128 rows x 128 B per
+//                 stage, 128 B swizzle) into a deep ring that the dequant
+//                 warps release as soon as they have read a slot, and of the
+//                 item's scales and biases (bulk copies, double-buffered);
+//   warp 1        TMEM owner and MMA issuer (one thread);
+//   warp 2        TMA producer of the B operand (the token tile, 16-row boxes)
+//                 into a ring that the MMA's completion releases; its slots
+//                 are sized at run time for the largest token tile of the
+//                 call, so small tiles get a deep ring;
+//   dequant warps thread = weight row = TMEM lane; DQG groups of four warps
+//                 split each stage's four 64-wide K atoms. A packed word holds
+//                 8 codes; the 0x4300 magic gives 128+q per bf16 half, minus
+//                 128 gives q exactly, and one fma.rn.bf16x2 with the group's
+//                 scale and bias gives bf16(S*q + B) with a single rounding.
+//                 The row's slice goes to a two-slot A ring in TMEM
+//                 (tcgen05.st); the MMA reads A from TMEM, B from shared memory.
+//   4 epilogue    each stage accumulates into a fresh TMEM region (256/NMAX
+//     warps       regions rotate); these warps add the stage partials in fp32
+//                 registers (short tensor-core accumulation chains keep the
+//                 result close to the exactly rounded one), then apply GeGLU
+//                 (gate_up) or scatter y to flat slots (down).
+// The dequantised pair order inside each 8-element K block is (0,4),(1,5),
+// (2,6),(3,7); the B operands (gathered x, GeGLU output) are stored in that
+// same K order, so the MMA sums the same products.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -31,23 +41,23 @@ namespace moe {
 
 namespace {
 
-constexpr int kThreads = 384;
 constexpr int kStageK = 256;
 constexpr int kPackedStageBytes = 128 * 128;  // 128 rows x 32 words
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kPCol0 = 256;              // partial-sum regions at columns 256 and 384
+constexpr uint32_t kPCol0 = 256;              // partial-sum regions fill columns 256..511
+constexpr int kMaxPackedStages = 8;
+constexpr int kMaxBStages = 8;
 
 struct Smem {
-    uint64_t full[8], empty[8];
-    uint64_t afull[2], aempty[2];
-    uint64_t pfull[2], pempty[2];  // per-stage partial accumulators in TMEM
-    uint64_t sfull[2], sempty[2];
+    uint64_t wfull[kMaxPackedStages], wempty[kMaxPackedStages];  // packed-weight ring
+    uint64_t bfull[kMaxBStages], bempty[kMaxBStages];            // B-operand ring
+    uint64_t afull[2], aempty[2];                                // A ring in TMEM
+    uint64_t dfull[4], dempty[4];                                // partial-sum regions in TMEM
+    uint64_t sfull[2], sempty[2];                                // scale/bias buffers
     uint32_t tmem_base;
     int abort_flag;
 };
 
-__host__ __device__ constexpr int b_stage_bytes(int nmax) { return 4 * nmax * 128; }
-__host__ __device__ constexpr int stage_bytes(int nmax) { return kPackedStageBytes + b_stage_bytes(nmax); }
 __host__ __device__ inline int scale_buf_bytes(int K) {
     // scales + biases for 128 rows, rounded up to 1 KB
     return ((128 * (K / 64) * 2 * 2) + 1023) & ~1023;
@@ -83,19 +93,48 @@ __device__ __forceinline__ int interleaved_pos(int n) {
     return (n & ~7) | (r < 4 ? 2 * r : 2 * r - 7);
 }
 
+// Dequantise one 64-wide K atom (8 packed words) of a weight row with its
+// group's scale and bias (bf16 bits) into 32 bf16x2 TMEM columns.
+__device__ __forceinline__ void dequant_atom(const uint4 c0, const uint4 c1, uint32_t S1, uint32_t B1,
+                                             uint32_t (&r)[32]) {
+    const uint32_t S2 = S1 | (S1 << 16), B2 = B1 | (B1 << 16);
+    const uint32_t wd[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t w = wd[i];
+        const uint32_t sh4[4] = {w, w >> 4, w >> 8, w >> 12};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t t = lop3_and_or(sh4[c], 0x000F000Fu, 0x43004300u);  // 128+q
+            const uint32_t qv = fma_bf16x2(t, 0x3F803F80u, 0xC300C300u);       // q exactly
+            r[4 * i + c] = fma_bf16x2(qv, S2, B2);                            // bf16(S q + B)
+        }
+    }
+}
+
 }  // namespace
 
-template <int MODE, int NMAX>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int MODE, int NMAX, int DQG>
+__global__ void __launch_bounds__((8 + 4 * DQG) * 32, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap bmap,
                         GemmArgs a) {
+    constexpr int kDqWarps = 4 * DQG;
+    constexpr int kEpiWarp0 = 4 + kDqWarps;
+    constexpr int kAtomsPerGroup = (4 + DQG - 1) / DQG;
+    constexpr int kRegions = 256 / NMAX;  // partial-sum regions of NMAX columns
     extern __shared__ __align__(1024) uint8_t dsmem[];
     __shared__ Smem sh;
-    // 1024-byte aligned carve-up: [stages][packed | B atoms] then 2 scale buffers.
+    // 1024-byte aligned carve-up: packed ring | B ring | 2 scale buffers.
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
-    const int NS = a.stages;
-    const int sbytes = stage_bytes(NMAX);
-    uint8_t* scale_base = base + (size_t)NS * sbytes;
+    const int NP = a.wstages;
+    // B slot: 4 atoms of brows x 128 B, brows = the largest tile's rows
+    // rounded up to 16 (each atom stays 1024-byte aligned).
+    const int brows = min(NMAX, max(16, (a.num_tiles[1] + 15) & ~15));
+    const int bslot_bytes = 4 * brows * 128;
+    const int NB = min(kMaxBStages, a.bregion / bslot_bytes);
+    uint8_t* wring = base;
+    uint8_t* bring = base + (size_t)NP * kPackedStageBytes;
+    uint8_t* scale_base = bring + (size_t)a.bregion;
     const int G = a.K / 64;  // groups per weight row
     const int sbuf_bytes = scale_buf_bytes(a.K);
 
@@ -103,24 +142,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort_flag = &sh.abort_flag;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(&sh.full[s], 1);
-            mbar_init(&sh.empty[s], 5);  // 4 dequant warps + 1 MMA commit
+        for (int s = 0; s < NP; ++s) {
+            mbar_init(&sh.wfull[s], 1);
+            mbar_init(&sh.wempty[s], kDqWarps);
+        }
+        for (int s = 0; s < NB; ++s) {
+            mbar_init(&sh.bfull[s], 1);
+            mbar_init(&sh.bempty[s], 1);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&sh.afull[i], 128);
+            mbar_init(&sh.afull[i], 32 * kDqWarps);
             mbar_init(&sh.aempty[i], 1);
-            mbar_init(&sh.pfull[i], 1);
-            mbar_init(&sh.pempty[i], 128);
             mbar_init(&sh.sfull[i], 1);
-            mbar_init(&sh.sempty[i], 4);
+            mbar_init(&sh.sempty[i], kDqWarps);
+        }
+        for (int i = 0; i < kRegions; ++i) {
+            mbar_init(&sh.dfull[i], 1);
+            mbar_init(&sh.dempty[i], 128);
         }
         sh.abort_flag = 0;
         fence_barrier_init();
-    }
-    if (warp == 0 && lane == 0) {
-        prefetch_tensormap(&wmap);
-        prefetch_tensormap(&bmap);
     }
     if (warp == 1) {
         tmem_alloc(&sh.tmem_base, kTmemCols);
@@ -136,96 +177,122 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nstages = (K + kStageK - 1) / kStageK;
 
     if (warp == 0) {
-        // ------------------------------------------------------ producer --
-        if (lane == 0) {
-            uint32_t gs = 0;
-            int li = 0;
-            bool ok = true;
-            for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x, ++li) {
-                const Tile tl = a.tiles[it / a.n_tiles];
-                const int j = it % a.n_tiles;
-                const int nrows16 = (tl.rows + 15) & ~15;
-                // scales / biases of the item's 128 weight rows
-                const int sb = li & 1;
-                if (!(ok = mbar_wait(&sh.sempty[sb], ((li >> 1) & 1) ^ 1, abort_flag))) break;
-                uint8_t* sbuf = scale_base + sb * sbuf_bytes;
-                const uint32_t half = (uint32_t)(64 * G * 2);  // bytes of 64 rows
+        // ------------------------------------- packed weights + scales --
+        // The whole warp runs the loop; one elected lane issues the copies.
+        if (elect_one()) prefetch_tensormap(&wmap);
+        uint32_t gs = 0;
+        int li = 0;
+        bool ok = true;
+        for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x, ++li) {
+            const Tile tl = a.tiles[it / a.n_tiles];
+            const int j = it % a.n_tiles;
+            const int sb = li & 1;
+            if (!(ok = mbar_wait(&sh.sempty[sb], ((li >> 1) & 1) ^ 1, abort_flag))) break;
+            uint8_t* sbuf = scale_base + sb * sbuf_bytes;
+            const uint32_t half = (uint32_t)(64 * G * 2);  // bytes of 64 rows
+            if (elect_one()) {
+                mbar_arrive_expect_tx(&sh.sfull[sb], 4 * half);
                 if (MODE == kGateUp) {
                     const size_t r_gate = (size_t)tl.e * a.N + 64 * j;
                     const size_t r_up = (size_t)tl.e * a.N + a.inter + 64 * j;
-                    mbar_arrive_expect_tx(&sh.sfull[sb], 4 * half);
                     bulk_load(sbuf, a.scales + r_gate * G, half, &sh.sfull[sb]);
                     bulk_load(sbuf + half, a.scales + r_up * G, half, &sh.sfull[sb]);
                     bulk_load(sbuf + 2 * half, a.biases + r_gate * G, half, &sh.sfull[sb]);
                     bulk_load(sbuf + 3 * half, a.biases + r_up * G, half, &sh.sfull[sb]);
                 } else {
                     const size_t r0 = (size_t)tl.e * a.N + 128 * j;
-                    mbar_arrive_expect_tx(&sh.sfull[sb], 4 * half);
                     bulk_load(sbuf, a.scales + r0 * G, 2 * half, &sh.sfull[sb]);
                     bulk_load(sbuf + 2 * half, a.biases + r0 * G, 2 * half, &sh.sfull[sb]);
                 }
-                for (int s = 0; s < nstages; ++s, ++gs) {
-                    const int slot = gs % NS;
-                    if (!(ok = mbar_wait(&sh.empty[slot], ((gs / NS) & 1) ^ 1, abort_flag))) break;
-                    uint8_t* st = base + (size_t)slot * sbytes;
-                    const int kr = min(kStageK, K - s * kStageK);
-                    const int atoms = kr / 64;
-                    mbar_arrive_expect_tx(&sh.full[slot], kPackedStageBytes + atoms * nrows16 * 128);
+            }
+            __syncwarp();
+            for (int s = 0; s < nstages; ++s, ++gs) {
+                const int slot = gs % NP;
+                if (!(ok = mbar_wait(&sh.wempty[slot], ((gs / NP) & 1) ^ 1, abort_flag))) break;
+                uint8_t* st = wring + (size_t)slot * kPackedStageBytes;
+                if (elect_one()) {
+                    mbar_arrive_expect_tx(&sh.wfull[slot], kPackedStageBytes);
                     if (MODE == kGateUp) {
-                        tma_load_2d(st, &wmap, &sh.full[slot], s * 32, tl.e * a.N + 64 * j);
-                        tma_load_2d(st + 64 * 128, &wmap, &sh.full[slot], s * 32, tl.e * a.N + a.inter + 64 * j);
+                        tma_load_2d(st, &wmap, &sh.wfull[slot], s * 32, tl.e * a.N + 64 * j);
+                        tma_load_2d(st + 64 * 128, &wmap, &sh.wfull[slot], s * 32, tl.e * a.N + a.inter + 64 * j);
                     } else {
-                        tma_load_2d(st, &wmap, &sh.full[slot], s * 32, tl.e * a.N + 128 * j);
+                        tma_load_2d(st, &wmap, &sh.wfull[slot], s * 32, tl.e * a.N + 128 * j);
                     }
-                    uint8_t* bst = st + kPackedStageBytes;
+                }
+                __syncwarp();
+            }
+        }
+        // Do not leave while copies into shared memory are in flight.
+        for (uint32_t g = (gs > (uint32_t)NP ? gs - NP : 0); g < gs; ++g)
+            mbar_wait(&sh.wfull[g % NP], (g / NP) & 1, abort_flag);
+        if (li > 0) mbar_wait(&sh.sfull[(li - 1) & 1], ((li - 1) >> 1) & 1, abort_flag);
+    } else if (warp == 2) {
+        // ---------------------------------------------------- B operand --
+        if (elect_one()) prefetch_tensormap(&bmap);
+        uint32_t gs = 0;
+        bool ok = true;
+        for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x) {
+            const Tile tl = a.tiles[it / a.n_tiles];
+            const int nrows16 = (tl.rows + 15) & ~15;
+            for (int s = 0; s < nstages; ++s, ++gs) {
+                const int slot = gs % NB;
+                if (!(ok = mbar_wait(&sh.bempty[slot], ((gs / NB) & 1) ^ 1, abort_flag))) break;
+                uint8_t* bst = bring + (size_t)slot * bslot_bytes;
+                const int atoms = min(kStageK, K - s * kStageK) / 64;
+                if (elect_one()) {
+                    mbar_arrive_expect_tx(&sh.bfull[slot], atoms * nrows16 * 128);
                     for (int at = 0; at < atoms; ++at)
                         for (int r = 0; r < nrows16; r += 16)
-                            tma_load_2d(bst + at * NMAX * 128 + r * 128, &bmap, &sh.full[slot],
+                            tma_load_2d(bst + at * brows * 128 + r * 128, &bmap, &sh.bfull[slot],
                                         s * kStageK + at * 64, tl.p0 + r);
                 }
+                __syncwarp();
             }
-            // Do not leave while copies into shared memory are in flight.
-            for (uint32_t g = (gs > (uint32_t)NS ? gs - NS : 0); g < gs; ++g)
-                mbar_wait(&sh.full[g % NS], (g / NS) & 1, abort_flag);
         }
+        for (uint32_t g = (gs > (uint32_t)NB ? gs - NB : 0); g < gs; ++g)
+            mbar_wait(&sh.bfull[g % NB], (g / NB) & 1, abort_flag);
     } else if (warp == 1) {
         // ---------------------------------------------------- MMA issuer --
-        // Each 256-K stage accumulates into a fresh TMEM region (alternating
-        // between two); the epilogue adds the stage partials in fp32
-        // registers. Short tensor-core accumulation chains keep z close to
-        // the exactly rounded value.
-        if (lane == 0) {
-            uint32_t gs = 0;
-            bool ok = true;
-            for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x) {
-                const Tile tl = a.tiles[it / a.n_tiles];
-                const uint32_t nrows16 = (uint32_t)((tl.rows + 15) & ~15);
-                const uint32_t idesc = idesc_bf16_m128(nrows16);
-                for (int s = 0; s < nstages; ++s, ++gs) {
-                    const int slot = gs % NS;
-                    const int as = gs & 1;
-                    const int pr = gs & 1;
-                    if (!(ok = mbar_wait(&sh.full[slot], (gs / NS) & 1, abort_flag))) break;
-                    if (!(ok = mbar_wait(&sh.afull[as], (gs >> 1) & 1, abort_flag))) break;
-                    if (!(ok = mbar_wait(&sh.pempty[pr], ((gs >> 1) & 1) ^ 1, abort_flag))) break;
-                    tc_fence_after();
-                    const int kr = min(kStageK, K - s * kStageK);
-                    const uint32_t bst = smem_u32(base + (size_t)slot * sbytes + kPackedStageBytes);
-                    const uint32_t pcol = tmem + kPCol0 + pr * 128;
-                    for (int k16 = 0; k16 < kr / 16; ++k16) {
-                        const int at = k16 >> 2, kk = k16 & 3;
-                        const uint64_t bdesc = sw128_kmajor_desc(bst + at * NMAX * 128 + kk * 32);
-                        umma_ts(pcol, tmem + as * 128 + k16 * 8, bdesc, idesc, k16 > 0 ? 1u : 0u);
+        // The whole warp runs the loop; one elected lane issues the MMAs of a
+        // stage and the three commits (a commit tracks its own thread's MMAs).
+        uint32_t gs = 0;
+        bool ok = true;
+        for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x) {
+            const Tile tl = a.tiles[it / a.n_tiles];
+            const uint32_t nrows16 = (uint32_t)((tl.rows + 15) & ~15);
+            const uint32_t idesc = idesc_bf16_m128(nrows16);
+            for (int s = 0; s < nstages; ++s, ++gs) {
+                const int bslot = gs % NB;
+                const int as = gs & 1;
+                const int pr = gs % kRegions;
+                if (!(ok = mbar_wait(&sh.bfull[bslot], (gs / NB) & 1, abort_flag))) break;
+                if (!(ok = mbar_wait(&sh.afull[as], (gs >> 1) & 1, abort_flag))) break;
+                if (!(ok = mbar_wait(&sh.dempty[pr], ((gs / kRegions) & 1) ^ 1, abort_flag))) break;
+                tc_fence_after();
+                const int nk = min(kStageK, K - s * kStageK) / 16;
+                const uint64_t bdesc0 = sw128_kmajor_desc(smem_u32(bring + (size_t)bslot * bslot_bytes));
+                const uint32_t pcol = tmem + kPCol0 + pr * NMAX;
+                const uint32_t acol = tmem + as * 128;
+                const uint32_t atom_step = (uint32_t)(brows * 128) >> 4;  // descriptor units (16 B)
+                if (elect_one()) {
+#pragma unroll
+                    for (int k16 = 0; k16 < 16; ++k16) {
+                        if (k16 < nk) {
+                            const uint64_t bdesc = bdesc0 + (uint64_t)((k16 >> 2) * atom_step + (k16 & 3) * 2);
+                            umma_ts(pcol, acol + k16 * 8, bdesc, idesc, k16 > 0 ? 1u : 0u);
+                        }
                     }
-                    umma_commit(&sh.empty[slot]);
+                    umma_commit(&sh.bempty[bslot]);
                     umma_commit(&sh.aempty[as]);
-                    umma_commit(&sh.pfull[pr]);
+                    umma_commit(&sh.dfull[pr]);
                 }
+                __syncwarp();
             }
         }
-    } else if (warp >= 4 && warp < 8) {
+    } else if (warp >= 4 && warp < kEpiWarp0) {
         // ------------------------------------------------------- dequant --
         const int q = warp & 3;
+        const int grp = (warp - 4) >> 2;  // this group's atoms: grp, grp + DQG, ...
         int row;  // row in the packed stage and the scale buffer
         if (MODE == kGateUp)
             row = (lane < 16) ? (16 * q + lane) : (64 + 16 * q + (lane - 16));
@@ -238,47 +305,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x, ++li) {
             const int sb = li & 1;
             if (!(ok = mbar_wait(&sh.sfull[sb], (li >> 1) & 1, abort_flag))) break;
-            const uint16_t* sS = reinterpret_cast<const uint16_t*>(scale_base + sb * sbuf_bytes);
+            const uint16_t* sS = reinterpret_cast<const uint16_t*>(scale_base + sb * sbuf_bytes) + row * G;
             const uint16_t* sB = sS + 128 * G;
             for (int s = 0; s < nstages; ++s, ++gs) {
-                const int slot = gs % NS;
+                const int slot = gs % NP;
                 const int as = gs & 1;
-                if (!(ok = mbar_wait(&sh.full[slot], (gs / NS) & 1, abort_flag))) break;
+                if (!(ok = mbar_wait(&sh.wfull[slot], (gs / NP) & 1, abort_flag))) break;
+                const uint8_t* pst = wring + (size_t)slot * kPackedStageBytes + row * 128;
+                const int atoms = min(kStageK, K - s * kStageK) / 64;
+                // Read this group's packed words and scales first (the slot is
+                // released right after), then wait for the TMEM slot.
+                uint4 c[2 * kAtomsPerGroup];
+                uint32_t Sv[kAtomsPerGroup], Bv[kAtomsPerGroup];
+#pragma unroll
+                for (int i = 0; i < kAtomsPerGroup; ++i) {
+                    const int at = grp + i * DQG;
+                    if (at < atoms) {
+                        c[2 * i] = *reinterpret_cast<const uint4*>(pst + (((2 * at) ^ (row & 7)) << 4));
+                        c[2 * i + 1] = *reinterpret_cast<const uint4*>(pst + (((2 * at + 1) ^ (row & 7)) << 4));
+                        Sv[i] = sS[s * 4 + at];
+                        Bv[i] = sB[s * 4 + at];
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.wempty[slot]);
                 if (!(ok = mbar_wait(&sh.aempty[as], ((gs >> 1) & 1) ^ 1, abort_flag))) break;
                 tc_fence_after();
-                const uint8_t* pst = base + (size_t)slot * sbytes + row * 128;
-                const int kr = min(kStageK, K - s * kStageK);
-                for (int at = 0; at < kr / 64; ++at) {
-                    const int g = s * 4 + at;
-                    const uint32_t S1 = sS[row * G + g], B1 = sB[row * G + g];
-                    const uint32_t S2 = S1 | (S1 << 16), B2 = B1 | (B1 << 16);
-                    const uint4 c0 = *reinterpret_cast<const uint4*>(pst + (((2 * at) ^ (row & 7)) << 4));
-                    const uint4 c1 = *reinterpret_cast<const uint4*>(pst + (((2 * at + 1) ^ (row & 7)) << 4));
-                    const uint32_t wd[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-                    uint32_t r[32];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const uint32_t w = wd[i];
-                        const uint32_t sh4[4] = {w, w >> 4, w >> 8, w >> 12};
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const uint32_t t = lop3_and_or(sh4[c], 0x000F000Fu, 0x43004300u);  // 128+q
-                            const uint32_t qv = fma_bf16x2(t, 0x3F803F80u, 0xC300C300u);       // q exactly
-                            r[4 * i + c] = fma_bf16x2(qv, S2, B2);                            // bf16(S q + B)
-                        }
+                for (int i = 0; i < kAtomsPerGroup; ++i) {
+                    const int at = grp + i * DQG;
+                    if (at < atoms) {
+                        uint32_t r[32];
+                        dequant_atom(c[2 * i], c[2 * i + 1], Sv[i], Bv[i], r);
+                        tmem_st32(tmem + lane_addr + as * 128 + at * 32, r);
                     }
-                    tmem_st32(tmem + lane_addr + as * 128 + at * 32, r);
                 }
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(&sh.afull[as]);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sh.empty[slot]);
             }
             __syncwarp();
             if (ok && lane == 0) mbar_arrive(&sh.sempty[sb]);
         }
-    } else if (warp >= 8) {
+    } else if (warp >= kEpiWarp0) {
         // ------------------------------------------------------ epilogue --
         const int q = warp & 3;
         const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
@@ -292,21 +361,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 0; c < NMAX; ++c) acc[c] = 0.f;
             for (int s = 0; s < nstages; ++s, ++gs) {
-                const int pr = gs & 1;
-                if (!(ok = mbar_wait(&sh.pfull[pr], (gs >> 1) & 1, abort_flag))) break;
+                const int pr = gs % kRegions;
+                if (!(ok = mbar_wait(&sh.dfull[pr], (gs / kRegions) & 1, abort_flag))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int c0 = 0; c0 < NMAX; c0 += 16) {
                     if (c0 < nrows16) {
                         uint32_t v[16];
-                        tmem_ld16(tmem + lane_addr + kPCol0 + pr * 128 + c0, v);
+                        tmem_ld16(tmem + lane_addr + kPCol0 + pr * NMAX + c0, v);
                         tmem_wait_ld();
 #pragma unroll
                         for (int jj = 0; jj < 16; ++jj) acc[c0 + jj] = __fadd_rn(acc[c0 + jj], __uint_as_float(v[jj]));
                     }
                 }
                 tc_fence_before();
-                mbar_arrive(&sh.pempty[pr]);
+                mbar_arrive(&sh.dempty[pr]);
             }
             if (!ok) break;
             if (MODE == kGateUp) {
@@ -349,19 +418,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-size_t gemm_smem_bytes(int mode, int K, int nmax, int stages) {
-    (void)mode;
-    return 1024 /* alignment slack */ + (size_t)stages * stage_bytes(nmax) + 2 * (size_t)scale_buf_bytes(K);
+size_t gemm_smem_bytes(int K, int wstages, int bregion) {
+    return 1024 /* alignment slack */ + (size_t)wstages * kPackedStageBytes + (size_t)bregion +
+           2 * (size_t)scale_buf_bytes(K);
 }
 
-int gemm_max_stages(int mode, int K, int nmax) {
+// Shared-memory split: a packed-weight ring of 5 or 6 stages, the rest for
+// the B ring (at least two slots of the largest possible token tile).
+void gemm_stages(int K, int nmax, int* wstages, int* bregion) {
     const size_t limit = 232448 - 2048;  // 227 KB per CTA minus the static part
-    int s = 8;
-    while (s > 1 && gemm_smem_bytes(mode, K, nmax, s) > limit) --s;
-    return s;
+    const int min_b = 2 * 4 * nmax * 128;
+    int nw = 6;
+    while (nw > 2 && gemm_smem_bytes(K, nw, min_b) > limit) --nw;
+    if (nw > 5 && K > 1024) nw = 5;
+    *wstages = nw;
+    *bregion = (int)((limit - gemm_smem_bytes(K, nw, 0)) & ~size_t(1023));
 }
 
-template <int MODE, int NMAX>
+template <int MODE, int NMAX, int DQG>
 static cudaError_t launch_one(const CUtensorMap& wmap, const CUtensorMap& bmap, const GemmArgs& a, int grid,
                               size_t smem, cudaStream_t stream) {
     static bool attr_set[64] = {};
@@ -369,24 +443,24 @@ static cudaError_t launch_one(const CUtensorMap& wmap, const CUtensorMap& bmap, 
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, NMAX>,
+        cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, NMAX, DQG>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, 232448 - 2048);
         if (err != cudaSuccess) return err;
         attr_set[dev] = true;
     }
-    grouped_gemm_kernel<MODE, NMAX><<<grid, kThreads, smem, stream>>>(wmap, bmap, a);
+    grouped_gemm_kernel<MODE, NMAX, DQG><<<grid, (8 + 4 * DQG) * 32, smem, stream>>>(wmap, bmap, a);
     return cudaGetLastError();
 }
 
 cudaError_t launch_gemm(int mode, const CUtensorMap& wmap, const CUtensorMap& bmap, const GemmArgs& a, int grid,
                         cudaStream_t stream) {
-    const size_t smem = gemm_smem_bytes(mode, a.K, a.nmax, a.stages);
-    if (a.nmax == 64)
-        return mode == kGateUp ? launch_one<kGateUp, 64>(wmap, bmap, a, grid, smem, stream)
-                               : launch_one<kDown, 64>(wmap, bmap, a, grid, smem, stream);
-    if (a.nmax == 128)
-        return mode == kGateUp ? launch_one<kGateUp, 128>(wmap, bmap, a, grid, smem, stream)
-                               : launch_one<kDown, 128>(wmap, bmap, a, grid, smem, stream);
+    const size_t smem = gemm_smem_bytes(a.K, a.wstages, a.bregion);
+    if (a.nmax == 64)  // two dequant groups (16 warps)
+        return mode == kGateUp ? launch_one<kGateUp, 64, 2>(wmap, bmap, a, grid, smem, stream)
+                               : launch_one<kDown, 64, 2>(wmap, bmap, a, grid, smem, stream);
+    if (a.nmax == 128)  // the 128-column epilogue needs the registers of a 12-warp block
+        return mode == kGateUp ? launch_one<kGateUp, 128, 1>(wmap, bmap, a, grid, smem, stream)
+                               : launch_one<kDown, 128, 1>(wmap, bmap, a, grid, smem, stream);
     return cudaErrorInvalidValue;
 }
 

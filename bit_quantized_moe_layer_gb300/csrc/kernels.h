@@ -22,7 +22,9 @@ struct RouterArgs {
 };
 size_t router_smem_bytes(int H, int E);
 // wmap: router_w as bf16 [E rows, H], box {64, 32}, 128B swizzle.
-cudaError_t launch_router(const CUtensorMap& wmap, const RouterArgs& a, cudaStream_t stream);
+// xmap: x as bf16 [T rows, H], box {64, 16}, 128B swizzle.
+cudaError_t launch_router(const CUtensorMap& wmap, const CUtensorMap& xmap, const RouterArgs& a,
+                          cudaStream_t stream);
 int router_error_word();
 
 // A token tile of one expert: rows [p0, p0 + rows) of the expert-sorted slots.
@@ -37,7 +39,7 @@ struct DispatchArgs {
     int32_t* offsets;    // [E+1]
     int32_t* inv;        // [S]
     Tile* tiles;         // [max_tiles] (may be null)
-    int32_t* num_tiles;  // [1] (may be null)
+    int32_t* num_tiles;  // [2]: tile count, rows of the largest tile (may be null)
     int S, E, nmax;      // nmax: rows per token tile
 };
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream);
@@ -59,7 +61,7 @@ struct GemmArgs {
     const uint16_t* scales;   // [E, N, K/64]
     const uint16_t* biases;   // [E, N, K/64]
     const Tile* tiles;
-    const int32_t* num_tiles;
+    const int32_t* num_tiles; // [0] tile count, [1] rows of the largest tile
     const int32_t* perm;      // down: flat slot of each sorted row
     uint16_t* out;            // gate_up: mid [S, inter]; down: y [S, H] by flat slot
     int K;                    // reduction length (H or inter)
@@ -68,12 +70,13 @@ struct GemmArgs {
     int out_ld;               // row length of out (inter or H)
     int nmax;                 // rows per token tile (64 or 128)
     int n_tiles;              // weight-row tiles per token tile
-    int stages;               // smem pipeline depth
+    int wstages;              // packed-weight ring depth (shared memory)
+    int bregion;              // bytes of shared memory for the B-operand ring
 };
 // wmap: packed weights as uint32 [E*N rows, K/8], box {32, 64 or 128}, 128B swizzle.
 // bmap: B operand (xs or mid) as bf16 [S rows, K], box {64, 16}, 128B swizzle.
-size_t gemm_smem_bytes(int mode, int K, int nmax, int stages);
-int gemm_max_stages(int mode, int K, int nmax);
+size_t gemm_smem_bytes(int K, int wstages, int bregion);
+void gemm_stages(int K, int nmax, int* wstages, int* bregion);
 cudaError_t launch_gemm(int mode, const CUtensorMap& wmap, const CUtensorMap& bmap, const GemmArgs& a,
                         int grid, cudaStream_t stream);
 int gemm_error_word();

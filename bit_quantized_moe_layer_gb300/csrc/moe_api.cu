@@ -32,7 +32,7 @@ int check_dims(const moe_dims* d) {
     if (!d) return MOE_ERR_NULL;
     if (d->T < 0 || d->H <= 0 || d->E <= 0 || d->k <= 0 || d->inter <= 0) return MOE_ERR_SHAPE;
     if (d->bits != 4 || d->group != 64) return MOE_ERR_UNSUPPORTED;
-    if (d->H % 128 != 0 || d->inter % 64 != 0 || d->H > 5888) return MOE_ERR_UNSUPPORTED;
+    if (d->H % 128 != 0 || d->inter % 64 != 0 || d->H > 5504) return MOE_ERR_UNSUPPORTED;
     if (d->k > 32 || d->k > d->E || d->E > 256) return MOE_ERR_UNSUPPORTED;
     if ((int64_t)d->T * d->k > (int64_t)1 << 28) return MOE_ERR_SHAPE;
     if (!(d->eps >= 0.0f) || isinf(d->eps)) return MOE_ERR_SHAPE;
@@ -137,7 +137,7 @@ Layout layout(const moe_dims* d) {
     L.inv = take(S * 4);
     L.offsets = take((size_t)(d->E + 1) * 4);
     L.tiles = take((size_t)L.max_tiles * sizeof(Tile));
-    L.ntiles = take(4);
+    L.ntiles = take(8);
     L.xs = take(S * d->H * 2);
     L.mid = take(S * d->inter * 2);
     L.y = take(S * d->H * 2);
@@ -244,7 +244,7 @@ int run_experts(const moe_dims* d, const uint16_t* x, const int32_t* idx, const 
     ga.out_ld = I;
     ga.nmax = nmax;
     ga.n_tiles = I / 64;
-    ga.stages = gemm_max_stages(kGateUp, H, nmax);
+    gemm_stages(H, nmax, &ga.wstages, &ga.bregion);
     int grid = di.sms;
     if ((long)L.max_tiles * ga.n_tiles < grid) grid = L.max_tiles * ga.n_tiles;
     rc = fail(launch_gemm(kGateUp, m_gu, m_xs, ga, grid, s));
@@ -260,7 +260,7 @@ int run_experts(const moe_dims* d, const uint16_t* x, const int32_t* idx, const 
     gd.inter = I;
     gd.out_ld = H;
     gd.n_tiles = H / 128;
-    gd.stages = gemm_max_stages(kDown, I, nmax);
+    gemm_stages(I, nmax, &gd.wstages, &gd.bregion);
     grid = di.sms;
     if ((long)L.max_tiles * gd.n_tiles < grid) grid = L.max_tiles * gd.n_tiles;
     rc = fail(launch_gemm(kDown, m_dn, m_mid, gd, grid, s));
@@ -276,9 +276,11 @@ int run_experts(const moe_dims* d, const uint16_t* x, const int32_t* idx, const 
 int route_impl(const moe_dims* d, const uint16_t* x, const uint16_t* rw, const uint16_t* rs, const uint16_t* pes,
                int32_t* idx, uint16_t* w, cudaStream_t s) {
     RouterArgs ra{x, rw, rs, pes, idx, w, d->T, d->H, d->E, d->k, d->eps, bf16_round(pow((double)d->H, -0.5))};
-    CUtensorMap m_rw;
-    if (!make_map_2d(&m_rw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rw, d->H, d->E, 64, 32)) return MOE_ERR_CUDA;
-    return fail(launch_router(m_rw, ra, s));
+    CUtensorMap m_rw, m_x;
+    if (!make_map_2d(&m_rw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rw, d->H, d->E, 64, 32) ||
+        !make_map_2d(&m_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, d->H, d->T, 64, 16))
+        return MOE_ERR_CUDA;
+    return fail(launch_router(m_rw, m_x, ra, s));
 }
 
 int get_workspace(const moe_dims* d, void* workspace, size_t ws_bytes, const Layout& L, uint8_t** out) {

@@ -1,16 +1,18 @@
 // Router kernel: DiffRouter.forward of the DiffusionGemma language model
 // ("diffusion-gemma/model.ts"), fused into one launch.
 //
-// One thread-block cluster handles 16 tokens. Its CS = ceil(E/32) CTAs each
-//   1. compute the no-scale RMS norm of the 16 rows in fp32 (the norm's fp32
-//      semantics are the ones "diffusion-gemma/vision.ts" spells out in
-//      manualRms), then the two bf16 multiplies (router scale, H^-0.5) into
-//      shared memory;
-//   2. compute the bf16 scores of 32 experts with mma.sync m16n8k16 (fp32
-//      accumulate), the 32 router-weight rows streamed by a producer warp
-//      through a TMA ring of 64-wide K blocks (128-byte swizzle) that starts
-//      filling while the norm runs, and write them into the leader CTA's
-//      shared memory;
+// One thread-block cluster handles 16 tokens; its CS = ceil(E/32) CTAs each
+// own 32 experts. In every CTA a producer warp brings, by TMA with the
+// 128-byte swizzle, the 16 x H activation tile (16-row x 64-column boxes)
+// and, through an 8-deep ring, 64-wide K blocks of its 32 router-weight rows.
+// Four compute warps
+//   1. apply the no-scale RMS norm in fp32 to the tile in shared memory, in
+//      place (the fp32 semantics are the ones "diffusion-gemma/vision.ts"
+//      spells out in manualRms), followed by the two bf16 multiplies (router
+//      scale, H^-0.5);
+//   2. compute 16 tokens x 32 experts of scores with mma.sync m16n8k16 (fp32
+//      accumulate), round them to bf16 and write them into the leader CTA's
+//      shared memory (distributed shared memory);
 // then the leader CTA picks the top k per token (value descending, ties to
 // the lower expert id), takes the fp32 softmax over the k picked scores and
 // multiplies by per_expert_scale[idx].
@@ -30,6 +32,7 @@ constexpr int kWarps = 4;      // compute warps per CTA (+1 producer warp)
 constexpr int kExpPerCta = 32; // experts per CTA (8 per warp)
 constexpr int kRing = 8;       // K blocks of router weight in flight
 constexpr int kBlockBytes = kExpPerCta * 128;  // 32 rows x 64 bf16
+constexpr int kXBoxBytes = kTT * 128;          // 16 rows x 64 bf16
 
 __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                                uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -44,34 +47,39 @@ __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint3
 __device__ __forceinline__ uint32_t order_key16(uint32_t b) { return (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u); }
 __device__ __forceinline__ uint32_t key16_to_bits(uint32_t k) { return (k & 0x8000u) ? (k & 0x7FFFu) : (~k & 0xFFFFu); }
 
+// Byte offset of 16-byte chunk c (0..7) of row r inside a 128-byte-swizzled
+// box of 128-byte rows.
+__device__ __forceinline__ int sw128(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
+
 }  // namespace
 
 __global__ void __launch_bounds__((kWarps + 1) * 32) router_kernel(const __grid_constant__ CUtensorMap wmap,
+                                                                    const __grid_constant__ CUtensorMap xmap,
                                                                     RouterArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    __shared__ uint64_t full[kRing], empty[kRing];
+    __shared__ uint64_t full[kRing], empty[kRing], xfull;
     __shared__ int abort_flag_s;
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int H = a.H, E = a.E, k = a.k;
-    const int rowstride = H + 8;  // bf16 elements; +16 B per row keeps the fragment reads conflict-free
-    uint8_t* ring = smem;                                          // kRing x 4 KB, 1024-aligned
-    uint16_t* n3 = reinterpret_cast<uint16_t*>(smem + kRing * kBlockBytes);
-    uint16_t* scores = n3 + kTT * rowstride;  // [kTT][E] bf16, used in the leader CTA
+    const int nkb = H / 64;
+    uint8_t* ring = smem;                      // kRing x 4 KB
+    uint8_t* xt = smem + kRing * kBlockBytes;  // nkb boxes of 16 rows x 128 B (swizzled)
+    uint16_t* rscale = reinterpret_cast<uint16_t*>(xt + nkb * kXBoxBytes);  // router_scale [H]
+    uint16_t* scores = rscale + H;                                             // [kTT][E], leader CTA
     volatile int* abort_flag = &abort_flag_s;
 
     cg::cluster_group cluster = cg::this_cluster();
     const int cs = (int)cluster.num_blocks();
     const int rank = (int)cluster.block_rank();
-    const int tile = blockIdx.x / cs;
-    const int t0 = tile * kTT;
+    const int t0 = (blockIdx.x / cs) * kTT;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nkb = H / 64;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kRing; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], kWarps);
         }
+        mbar_init(&xfull, 1);
         abort_flag_s = 0;
         fence_barrier_init();
     }
@@ -80,9 +88,13 @@ __global__ void __launch_bounds__((kWarps + 1) * 32) router_kernel(const __grid_
     cluster_barrier();
 
     if (warp == kWarps) {
-        // ---- producer: router-weight rows [32 rank, 32 rank + 32), one 64-wide K block per stage ----
+        // ---- producer ----
         if (lane == 0) {
+            prefetch_tensormap(&xmap);
             prefetch_tensormap(&wmap);
+            mbar_arrive_expect_tx(&xfull, nkb * kXBoxBytes + H * 2);
+            bulk_load(rscale, a.router_scale, H * 2, &xfull);
+            for (int kb = 0; kb < nkb; ++kb) tma_load_2d(xt + kb * kXBoxBytes, &xmap, &xfull, kb * 64, t0);
             int kb = 0;
             for (; kb < nkb; ++kb) {
                 const int slot = kb % kRing;
@@ -90,51 +102,50 @@ __global__ void __launch_bounds__((kWarps + 1) * 32) router_kernel(const __grid_
                 mbar_arrive_expect_tx(&full[slot], kBlockBytes);
                 tma_load_2d(ring + slot * kBlockBytes, &wmap, &full[slot], kb * 64, rank * kExpPerCta);
             }
-            for (int b = (kb > kRing ? kb - kRing : 0); b < kb; ++b)  // no copies in flight at exit
-                mbar_wait(&full[b % kRing], (b / kRing) & 1, abort_flag);
+            // no copies in flight at exit
+            mbar_wait(&xfull, 0, abort_flag);
+            for (int b = (kb > kRing ? kb - kRing : 0); b < kb; ++b) mbar_wait(&full[b % kRing], (b / kRing) & 1, abort_flag);
         }
         __syncwarp();
         cluster_barrier();
         return;
     }
 
-    // ---- 1. no-scale RMS norm, x scale, x H^-0.5 (bf16 after each op) ----
-    for (int tl = warp; tl < kTT; tl += kWarps) {
-        const int t = t0 + tl;
-        uint16_t* dst = n3 + tl * rowstride;
-        if (t >= a.T) {
-            for (int h = lane * 8; h < H; h += 256) *reinterpret_cast<uint4*>(dst + h) = make_uint4(0, 0, 0, 0);
-            continue;
-        }
-        const uint16_t* xr = a.x + (size_t)t * H;
+    // ---- 1. no-scale RMS norm, x scale, x H^-0.5 (bf16 after each op), in place ----
+    const bool have_x = mbar_wait(&xfull, 0, abort_flag);
+    const int nchunks = nkb * 8;  // 16-byte chunks per row
+    for (int r = warp; r < kTT && have_x; r += kWarps) {
         float ss = 0.f;
-        for (int h = lane * 8; h < H; h += 256) {
-            uint4 v = __ldg(reinterpret_cast<const uint4*>(xr + h));
+#pragma unroll 4
+        for (int i = lane; i < nchunks; i += 32) {
+            const uint4 v = *reinterpret_cast<const uint4*>(xt + (i >> 3) * kXBoxBytes + sw128(r, i & 7));
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                float lo = bf16_bits_to_f32(w[i] & 0xFFFFu), hi = bf16_bits_to_f32(w[i] >> 16);
+            for (int j = 0; j < 4; ++j) {
+                const float lo = bf16_bits_to_f32(w[j] & 0xFFFFu), hi = bf16_bits_to_f32(w[j] >> 16);
                 ss = __fadd_rn(ss, __fmul_rn(lo, lo));
                 ss = __fadd_rn(ss, __fmul_rn(hi, hi));
             }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
-        const float r = __frsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)H), a.eps));
-        for (int h = lane * 8; h < H; h += 256) {
-            uint4 v = __ldg(reinterpret_cast<const uint4*>(xr + h));
-            uint4 s = __ldg(reinterpret_cast<const uint4*>(a.router_scale + h));
+        const float rs = __frsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)H), a.eps));
+#pragma unroll 4
+        for (int i = lane; i < nchunks; i += 32) {
+            uint4* p = reinterpret_cast<uint4*>(xt + (i >> 3) * kXBoxBytes + sw128(r, i & 7));
+            const uint4 v = *p;
+            const uint4 s = reinterpret_cast<const uint4*>(rscale)[i];
             const uint32_t w[4] = {v.x, v.y, v.z, v.w}, sc[4] = {s.x, s.y, s.z, s.w};
             uint32_t o[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                float n_lo = bf16_bits_to_f32(f32_to_bf16_bits(__fmul_rn(bf16_bits_to_f32(w[i] & 0xFFFFu), r)));
-                float n_hi = bf16_bits_to_f32(f32_to_bf16_bits(__fmul_rn(bf16_bits_to_f32(w[i] >> 16), r)));
-                n_lo = bf16_bits_to_f32(f32_to_bf16_bits(__fmul_rn(n_lo, bf16_bits_to_f32(sc[i] & 0xFFFFu))));
-                n_hi = bf16_bits_to_f32(f32_to_bf16_bits(__fmul_rn(n_hi, bf16_bits_to_f32(sc[i] >> 16))));
-                o[i] = pack_bf16x2(__fmul_rn(n_lo, a.root), __fmul_rn(n_hi, a.root));
+            for (int j = 0; j < 4; ++j) {
+                float n_lo = bf16_bits_to_f32(f32_to_bf16_bits(__fmul_rn(bf16_bits_to_f32(w[j] & 0xFFFFu), rs)));
+                float n_hi = bf16_bits_to_f32(f32_to_bf16_bits(__fmul_rn(bf16_bits_to_f32(w[j] >> 16), rs)));
+                n_lo = bf16_bits_to_f32(f32_to_bf16_bits(__fmul_rn(n_lo, bf16_bits_to_f32(sc[j] & 0xFFFFu))));
+                n_hi = bf16_bits_to_f32(f32_to_bf16_bits(__fmul_rn(n_hi, bf16_bits_to_f32(sc[j] >> 16))));
+                o[j] = pack_bf16x2(__fmul_rn(n_lo, a.root), __fmul_rn(n_hi, a.root));
             }
-            *reinterpret_cast<uint4*>(dst + h) = make_uint4(o[0], o[1], o[2], o[3]);
+            *p = make_uint4(o[0], o[1], o[2], o[3]);
         }
     }
     // The compute warps only (the producer warp never comes here): named
@@ -143,28 +154,26 @@ __global__ void __launch_bounds__((kWarps + 1) * 32) router_kernel(const __grid_
 
     // ---- 2. scores for experts [e0, e0+8) of this warp: 16 tokens x 8 experts ----
     // Inside each 64-wide K block, thread (g, q) owns K [16q, 16q+16) of its
-    // rows; mma step s takes K 16q+4s+{0,1} as fragment k {2q, 2q+1} and
-    // 16q+4s+{2,3} as k {2q+8, 2q+9}, identically for both operands, so the
-    // four steps sum the block's 64 products exactly once.
+    // rows (chunks 2q and 2q+1); mma step s takes K 16q+4s+{0,1} as fragment
+    // k {2q, 2q+1} and 16q+4s+{2,3} as k {2q+8, 2q+9}, identically for both
+    // operands, so the four steps sum the block's 64 products exactly once.
     const int e0 = rank * kExpPerCta + warp * 8;
     const int g = lane >> 2, q = lane & 3;
-    const uint16_t* arow0 = n3 + g * rowstride;
-    const uint16_t* arow1 = n3 + (g + 8) * rowstride;
     const int brow = warp * 8 + g;  // row of this lane's expert in a ring block
     float c[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int kb = 0; kb < nkb; ++kb) {
+    for (int kb = 0; kb < nkb && have_x; ++kb) {
         const int slot = kb % kRing;
         if (!mbar_wait(&full[slot], (kb / kRing) & 1, abort_flag)) break;
-        const uint8_t* blk = ring + slot * kBlockBytes + brow * 128;
-        const uint4 b0 = *reinterpret_cast<const uint4*>(blk + (((2 * q) ^ (brow & 7)) << 4));
-        const uint4 b1 = *reinterpret_cast<const uint4*>(blk + (((2 * q + 1) ^ (brow & 7)) << 4));
-        const int kk = kb * 64;
-        const uint4 x0 = *reinterpret_cast<const uint4*>(arow0 + kk + 16 * q);
-        const uint4 x1 = *reinterpret_cast<const uint4*>(arow0 + kk + 16 * q + 8);
-        const uint4 y0 = *reinterpret_cast<const uint4*>(arow1 + kk + 16 * q);
-        const uint4 y1 = *reinterpret_cast<const uint4*>(arow1 + kk + 16 * q + 8);
+        const uint8_t* blk = ring + slot * kBlockBytes;
+        const uint4 b0 = *reinterpret_cast<const uint4*>(blk + sw128(brow, 2 * q));
+        const uint4 b1 = *reinterpret_cast<const uint4*>(blk + sw128(brow, 2 * q + 1));
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
+        const uint8_t* xb = xt + kb * kXBoxBytes;
+        const uint4 x0 = *reinterpret_cast<const uint4*>(xb + sw128(g, 2 * q));
+        const uint4 x1 = *reinterpret_cast<const uint4*>(xb + sw128(g, 2 * q + 1));
+        const uint4 y0 = *reinterpret_cast<const uint4*>(xb + sw128(g + 8, 2 * q));
+        const uint4 y1 = *reinterpret_cast<const uint4*>(xb + sw128(g + 8, 2 * q + 1));
         const uint32_t ar0[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
         const uint32_t ar1[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
         const uint32_t br[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
@@ -215,7 +224,9 @@ __global__ void __launch_bounds__((kWarps + 1) * 32) router_kernel(const __grid_
                 my_idx = e;
                 my_s = s;
             }
-            if ((e & 31) == lane) cand[e >> 5] = 0u;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (cand[i] == win) cand[i] = 0u;
         }
         const float ex = (lane < k) ? expf(__fsub_rn(my_s, top_s)) : 0.f;
         float sum = 0.f;
@@ -237,10 +248,11 @@ int router_error_word() {
 }
 
 size_t router_smem_bytes(int H, int E) {
-    return 1024 + (size_t)kRing * kBlockBytes + (size_t)kTT * (H + 8) * 2 + (size_t)kTT * E * 2;
+    return 1024 + (size_t)kRing * kBlockBytes + (size_t)(H / 64) * kXBoxBytes + (size_t)H * 2 + (size_t)kTT * E * 2;
 }
 
-cudaError_t launch_router(const CUtensorMap& wmap, const RouterArgs& a, cudaStream_t stream) {
+cudaError_t launch_router(const CUtensorMap& wmap, const CUtensorMap& xmap, const RouterArgs& a,
+                          cudaStream_t stream) {
     if (a.T == 0) return cudaSuccess;
     const int cs = (a.E + kExpPerCta - 1) / kExpPerCta;
     const int tiles = (a.T + kTT - 1) / kTT;
@@ -266,7 +278,7 @@ cudaError_t launch_router(const CUtensorMap& wmap, const RouterArgs& a, cudaStre
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, router_kernel, wmap, a);
+    return cudaLaunchKernelEx(&cfg, router_kernel, wmap, xmap, a);
 }
 
 }  // namespace moe

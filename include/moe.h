@@ -17,7 +17,7 @@
  *    moe_forward_hostio, moe_timing_read and moe_device_error.
  *  - Argument errors are detected on the host before anything is enqueued
  *    and leave the outputs untouched. A launch failure returns MOE_ERR_CUDA.
- *  - Supported shapes: bits == 4, group == 64, H % 128 == 0, H <= 5888,
+ *  - Supported shapes: bits == 4, group == 64, H % 128 == 0, H <= 5504,
  *    inter % 64 == 0,
  *    1 <= k <= 32, k <= E <= 256, T >= 0 (T == 0 is a no-op).
  *  - 4-bit weights use the affine layout that the pages' quantized linears
