@@ -52,7 +52,7 @@ struct Smem {
     uint64_t wfull[kMaxPackedStages], wempty[kMaxPackedStages];  // packed-weight ring
     uint64_t bfull[kMaxBStages], bempty[kMaxBStages];            // B-operand ring
     uint64_t afull[2], aempty[2];                                // A ring in TMEM
-    uint64_t dfull[4], dempty[4];                                // partial-sum regions in TMEM
+    uint64_t dfull[16], dempty[16];                              // partial-sum regions in TMEM
     uint64_t sfull[2], sempty[2];                                // scale/bias buffers
     uint32_t tmem_base;
     int abort_flag;
@@ -114,22 +114,28 @@ __device__ __forceinline__ void dequant_atom(const uint4 c0, const uint4 c1, uin
 
 }  // namespace
 
-template <int MODE, int NMAX, int DQG>
-__global__ void __launch_bounds__((8 + 4 * DQG) * 32, 1)
+template <int MODE, int NMAX, int DQG, int EPW>
+__global__ void __launch_bounds__((4 + 4 * DQG + 4 * EPW) * 32, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap bmap,
                         GemmArgs a) {
     constexpr int kDqWarps = 4 * DQG;
     constexpr int kEpiWarp0 = 4 + kDqWarps;
-    constexpr int kAtomsPerGroup = (4 + DQG - 1) / DQG;
-    constexpr int kRegions = 256 / NMAX;  // partial-sum regions of NMAX columns
+    constexpr int kEpiWarps = 4 * EPW;
+    constexpr int kAtomsPerGroup = 4 / DQG;
+    constexpr int kAccChunks = NMAX / 16 / EPW;  // 16-column chunks one epilogue warp accumulates
     extern __shared__ __align__(1024) uint8_t dsmem[];
     __shared__ Smem sh;
     // 1024-byte aligned carve-up: packed ring | B ring | 2 scale buffers.
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
     const int NP = a.wstages;
-    // B slot: 4 atoms of brows x 128 B, brows = the largest tile's rows
-    // rounded up to 16 (each atom stays 1024-byte aligned).
-    const int brows = min(NMAX, max(16, (a.num_tiles[1] + 15) & ~15));
+    // brows: the largest token tile's rows rounded up to a power of two
+    // (16..NMAX). It sizes the B slots (4 atoms of brows x 128 B, each atom
+    // 1024-byte aligned) and the partial-sum regions (brows TMEM columns
+    // each, 256 / brows of them).
+    const int maxrows = a.num_tiles[1];
+    int brows = 16;
+    while (brows < maxrows && brows < NMAX) brows <<= 1;
+    const int nreg = 256 / brows;
     const int bslot_bytes = 4 * brows * 128;
     const int NB = min(kMaxBStages, a.bregion / bslot_bytes);
     uint8_t* wring = base;
@@ -144,21 +150,24 @@ __global__ void __launch_bounds__((8 + 4 * DQG) * 32, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < NP; ++s) {
             mbar_init(&sh.wfull[s], 1);
-            mbar_init(&sh.wempty[s], kDqWarps);
+            mbar_init(&sh.wempty[s], kDqWarps / 2);  // read by one stage group
         }
         for (int s = 0; s < NB; ++s) {
             mbar_init(&sh.bfull[s], 1);
             mbar_init(&sh.bempty[s], 1);
         }
+        // An item's scales are read by both stage groups when it has two
+        // or more K stages, by one group when it has a single stage.
+        const int nst = (a.K + kStageK - 1) / kStageK;
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&sh.afull[i], 32 * kDqWarps);
+            mbar_init(&sh.afull[i], kDqWarps / 2 + 1);  // one stage group + the stage gate (warp 3)
             mbar_init(&sh.aempty[i], 1);
             mbar_init(&sh.sfull[i], 1);
-            mbar_init(&sh.sempty[i], kDqWarps);
+            mbar_init(&sh.sempty[i], nst >= 2 ? kDqWarps : kDqWarps / 2);
         }
-        for (int i = 0; i < kRegions; ++i) {
+        for (int i = 0; i < nreg; ++i) {
             mbar_init(&sh.dfull[i], 1);
-            mbar_init(&sh.dempty[i], 128);
+            mbar_init(&sh.dempty[i], kEpiWarps);
         }
         sh.abort_flag = 0;
         fence_barrier_init();
@@ -172,7 +181,7 @@ __global__ void __launch_bounds__((8 + 4 * DQG) * 32, 1)
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
 
-    const int num_items = (*a.num_tiles) * a.n_tiles;
+    const int num_items = a.num_tiles[0] * a.n_tiles;
     const int K = a.K;
     const int nstages = (K + kStageK - 1) / kStageK;
 
@@ -180,7 +189,8 @@ __global__ void __launch_bounds__((8 + 4 * DQG) * 32, 1)
         // ------------------------------------- packed weights + scales --
         // The whole warp runs the loop; one elected lane issues the copies.
         if (elect_one()) prefetch_tensormap(&wmap);
-        uint32_t gs = 0;
+        int slot = 0;
+        uint32_t ph = 0, issued = 0;
         int li = 0;
         bool ok = true;
         for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x, ++li) {
@@ -206,9 +216,8 @@ __global__ void __launch_bounds__((8 + 4 * DQG) * 32, 1)
                 }
             }
             __syncwarp();
-            for (int s = 0; s < nstages; ++s, ++gs) {
-                const int slot = gs % NP;
-                if (!(ok = mbar_wait(&sh.wempty[slot], ((gs / NP) & 1) ^ 1, abort_flag))) break;
+            for (int s = 0; s < nstages; ++s) {
+                if (!(ok = mbar_wait(&sh.wempty[slot], ph ^ 1, abort_flag))) break;
                 uint8_t* st = wring + (size_t)slot * kPackedStageBytes;
                 if (elect_one()) {
                     mbar_arrive_expect_tx(&sh.wfull[slot], kPackedStageBytes);
@@ -220,23 +229,28 @@ __global__ void __launch_bounds__((8 + 4 * DQG) * 32, 1)
                     }
                 }
                 __syncwarp();
+                ++issued;
+                if (++slot == NP) {
+                    slot = 0;
+                    ph ^= 1;
+                }
             }
         }
         // Do not leave while copies into shared memory are in flight.
-        for (uint32_t g = (gs > (uint32_t)NP ? gs - NP : 0); g < gs; ++g)
+        for (uint32_t g = (issued > (uint32_t)NP ? issued - NP : 0); g < issued; ++g)
             mbar_wait(&sh.wfull[g % NP], (g / NP) & 1, abort_flag);
         if (li > 0) mbar_wait(&sh.sfull[(li - 1) & 1], ((li - 1) >> 1) & 1, abort_flag);
     } else if (warp == 2) {
         // ---------------------------------------------------- B operand --
         if (elect_one()) prefetch_tensormap(&bmap);
-        uint32_t gs = 0;
+        int slot = 0;
+        uint32_t ph = 0, issued = 0;
         bool ok = true;
         for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x) {
             const Tile tl = a.tiles[it / a.n_tiles];
             const int nrows16 = (tl.rows + 15) & ~15;
-            for (int s = 0; s < nstages; ++s, ++gs) {
-                const int slot = gs % NB;
-                if (!(ok = mbar_wait(&sh.bempty[slot], ((gs / NB) & 1) ^ 1, abort_flag))) break;
+            for (int s = 0; s < nstages; ++s) {
+                if (!(ok = mbar_wait(&sh.bempty[slot], ph ^ 1, abort_flag))) break;
                 uint8_t* bst = bring + (size_t)slot * bslot_bytes;
                 const int atoms = min(kStageK, K - s * kStageK) / 64;
                 if (elect_one()) {
@@ -247,33 +261,40 @@ __global__ void __launch_bounds__((8 + 4 * DQG) * 32, 1)
                                         s * kStageK + at * 64, tl.p0 + r);
                 }
                 __syncwarp();
+                ++issued;
+                if (++slot == NB) {
+                    slot = 0;
+                    ph ^= 1;
+                }
             }
         }
-        for (uint32_t g = (gs > (uint32_t)NB ? gs - NB : 0); g < gs; ++g)
+        for (uint32_t g = (issued > (uint32_t)NB ? issued - NB : 0); g < issued; ++g)
             mbar_wait(&sh.bfull[g % NB], (g / NB) & 1, abort_flag);
     } else if (warp == 1) {
         // ---------------------------------------------------- MMA issuer --
         // The whole warp runs the loop; one elected lane issues the MMAs of a
         // stage and the three commits (a commit tracks its own thread's MMAs).
         uint32_t gs = 0;
+        int bslot = 0, pr = 0;
         bool ok = true;
+        Tile tl_next = {};
+        if (blockIdx.x < num_items) tl_next = a.tiles[blockIdx.x / a.n_tiles];
+        const uint32_t atom_step = (uint32_t)(brows * 128) >> 4;  // descriptor units (16 B)
         for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x) {
-            const Tile tl = a.tiles[it / a.n_tiles];
+            const Tile tl = tl_next;
+            if (it + (int)gridDim.x < num_items) tl_next = a.tiles[(it + gridDim.x) / a.n_tiles];
             const uint32_t nrows16 = (uint32_t)((tl.rows + 15) & ~15);
             const uint32_t idesc = idesc_bf16_m128(nrows16);
             for (int s = 0; s < nstages; ++s, ++gs) {
-                const int bslot = gs % NB;
                 const int as = gs & 1;
-                const int pr = gs % kRegions;
-                if (!(ok = mbar_wait(&sh.bfull[bslot], (gs / NB) & 1, abort_flag))) break;
+                // afull also carries the gate warp's arrival: the B slot is
+                // full and the partial region is free.
                 if (!(ok = mbar_wait(&sh.afull[as], (gs >> 1) & 1, abort_flag))) break;
-                if (!(ok = mbar_wait(&sh.dempty[pr], ((gs / kRegions) & 1) ^ 1, abort_flag))) break;
                 tc_fence_after();
                 const int nk = min(kStageK, K - s * kStageK) / 16;
                 const uint64_t bdesc0 = sw128_kmajor_desc(smem_u32(bring + (size_t)bslot * bslot_bytes));
-                const uint32_t pcol = tmem + kPCol0 + pr * NMAX;
+                const uint32_t pcol = tmem + kPCol0 + (uint32_t)(pr * brows);
                 const uint32_t acol = tmem + as * 128;
-                const uint32_t atom_step = (uint32_t)(brows * 128) >> 4;  // descriptor units (16 B)
                 if (elect_one()) {
 #pragma unroll
                     for (int k16 = 0; k16 < 16; ++k16) {
@@ -287,95 +308,176 @@ __global__ void __launch_bounds__((8 + 4 * DQG) * 32, 1)
                     umma_commit(&sh.dfull[pr]);
                 }
                 __syncwarp();
+                if (++bslot == NB) bslot = 0;
+                if (++pr == nreg) pr = 0;
+            }
+        }
+    } else if (warp == 3) {
+        // --------------------------------------------------- stage gate --
+        // Folds the MMA's other two conditions into the A-slot barrier, so
+        // the MMA issuer waits once per stage: for stage g this warp waits
+        // for the B slot to be full and the partial region to be free, and
+        // for the previous phase of afull[g & 1] (stage g - 2) to complete
+        // so that its arrival counts toward stage g.
+        uint32_t gs = 0, bph = 0, dph = 0;
+        int bslot = 0, pr = 0;
+        bool ok = true;
+        const uint32_t total = (blockIdx.x < num_items)
+                                   ? (uint32_t)((num_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1) * nstages
+                                   : 0u;
+        for (; gs < total && ok; ++gs) {
+            const int as = gs & 1;
+            if (gs >= 2 && !(ok = mbar_wait(&sh.afull[as], ((gs >> 1) - 1) & 1, abort_flag))) break;
+            if (!(ok = mbar_wait(&sh.bfull[bslot], bph, abort_flag))) break;
+            if (!(ok = mbar_wait(&sh.dempty[pr], dph ^ 1, abort_flag))) break;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.afull[as]);
+            if (++bslot == NB) {
+                bslot = 0;
+                bph ^= 1;
+            }
+            if (++pr == nreg) {
+                pr = 0;
+                dph ^= 1;
             }
         }
     } else if (warp >= 4 && warp < kEpiWarp0) {
         // ------------------------------------------------------- dequant --
+        // Two stage groups of kDqWarps / 2 warps: group p dequantises the
+        // stages g with g % 2 == p into A slot p, so one group's waits and
+        // loads overlap the other group's arithmetic. Within a group, warp
+        // (q, sub) covers TMEM lanes 32q..32q+31 and the atoms sub, sub + 2
+        // (DQG / 2 == 2) or all four (DQG / 2 == 1) of its stages.
+        constexpr int kSub = DQG / 2;                // warps per lane quarter in a group
+        constexpr int kAtomsPerWarp = 4 / kSub;
+        const int dgrp = (warp - 4) / (4 * kSub);
+        const int sub = ((warp - 4) >> 2) % kSub;
         const int q = warp & 3;
-        const int grp = (warp - 4) >> 2;  // this group's atoms: grp, grp + DQG, ...
         int row;  // row in the packed stage and the scale buffer
         if (MODE == kGateUp)
             row = (lane < 16) ? (16 * q + lane) : (64 + 16 * q + (lane - 16));
         else
             row = 32 * q + lane;
         const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
-        uint32_t gs = 0;
-        int li = 0;
-        bool ok = true;
-        for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x, ++li) {
-            const int sb = li & 1;
-            if (!(ok = mbar_wait(&sh.sfull[sb], (li >> 1) & 1, abort_flag))) break;
+        const uint32_t total = (blockIdx.x < num_items)
+                                   ? (uint32_t)((num_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1) * nstages
+                                   : 0u;
+        // Fetch cursor over this CTA's stages (item ordinal li, stage s, ring slot).
+        int f_s = 0, f_li = 0, f_slot = 0, waited_li = -1;
+        uint32_t f_ph = 0;
+        auto step = [&]() {
+            if (++f_slot == NP) {
+                f_slot = 0;
+                f_ph ^= 1;
+            }
+            if (++f_s == nstages) {
+                f_s = 0;
+                ++f_li;
+            }
+        };
+        if (dgrp == 1) step();
+        uint4 c[2 * kAtomsPerWarp];
+        uint32_t Sv[kAtomsPerWarp], Bv[kAtomsPerWarp];
+        int atoms = 0;
+        // Reads the cursor's stage into c/Sv/Bv, releases its ring slot (and
+        // the item's scale buffer after this warp's last stage of the item),
+        // and moves the cursor to the group's next stage.
+        auto fetch = [&]() -> bool {
+            const int sb = f_li & 1;
+            if (f_li != waited_li) {
+                if (!mbar_wait(&sh.sfull[sb], (f_li >> 1) & 1, abort_flag)) return false;
+                waited_li = f_li;
+            }
+            if (!mbar_wait(&sh.wfull[f_slot], f_ph, abort_flag)) return false;
             const uint16_t* sS = reinterpret_cast<const uint16_t*>(scale_base + sb * sbuf_bytes) + row * G;
             const uint16_t* sB = sS + 128 * G;
-            for (int s = 0; s < nstages; ++s, ++gs) {
-                const int slot = gs % NP;
-                const int as = gs & 1;
-                if (!(ok = mbar_wait(&sh.wfull[slot], (gs / NP) & 1, abort_flag))) break;
-                const uint8_t* pst = wring + (size_t)slot * kPackedStageBytes + row * 128;
-                const int atoms = min(kStageK, K - s * kStageK) / 64;
-                // Read this group's packed words and scales first (the slot is
-                // released right after), then wait for the TMEM slot.
-                uint4 c[2 * kAtomsPerGroup];
-                uint32_t Sv[kAtomsPerGroup], Bv[kAtomsPerGroup];
+            const uint8_t* pst = wring + (size_t)f_slot * kPackedStageBytes + row * 128;
+            atoms = min(kStageK, K - f_s * kStageK) / 64;
 #pragma unroll
-                for (int i = 0; i < kAtomsPerGroup; ++i) {
-                    const int at = grp + i * DQG;
-                    if (at < atoms) {
-                        c[2 * i] = *reinterpret_cast<const uint4*>(pst + (((2 * at) ^ (row & 7)) << 4));
-                        c[2 * i + 1] = *reinterpret_cast<const uint4*>(pst + (((2 * at + 1) ^ (row & 7)) << 4));
-                        Sv[i] = sS[s * 4 + at];
-                        Bv[i] = sB[s * 4 + at];
-                    }
+            for (int i = 0; i < kAtomsPerWarp; ++i) {
+                const int at = sub + i * kSub;
+                if (at < atoms) {
+                    c[2 * i] = *reinterpret_cast<const uint4*>(pst + (((2 * at) ^ (row & 7)) << 4));
+                    c[2 * i + 1] = *reinterpret_cast<const uint4*>(pst + (((2 * at + 1) ^ (row & 7)) << 4));
+                    Sv[i] = sS[f_s * 4 + at];
+                    Bv[i] = sB[f_s * 4 + at];
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sh.wempty[slot]);
-                if (!(ok = mbar_wait(&sh.aempty[as], ((gs >> 1) & 1) ^ 1, abort_flag))) break;
-                tc_fence_after();
-#pragma unroll
-                for (int i = 0; i < kAtomsPerGroup; ++i) {
-                    const int at = grp + i * DQG;
-                    if (at < atoms) {
-                        uint32_t r[32];
-                        dequant_atom(c[2 * i], c[2 * i + 1], Sv[i], Bv[i], r);
-                        tmem_st32(tmem + lane_addr + as * 128 + at * 32, r);
-                    }
-                }
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(&sh.afull[as]);
             }
+            const int li = f_li;
+            const int slot = f_slot;
+            step();
+            step();
             __syncwarp();
-            if (ok && lane == 0) mbar_arrive(&sh.sempty[sb]);
+            if (lane == 0) {
+                mbar_arrive(&sh.wempty[slot]);
+                if (f_li != li) mbar_arrive(&sh.sempty[sb]);  // this warp's last read of the item's scales
+            }
+            return true;
+        };
+        bool ok = true;
+        if ((uint32_t)dgrp < total) ok = fetch();
+        for (uint32_t gs = dgrp; gs < total && ok; gs += 2) {
+            const int as = dgrp;
+            if (!(ok = mbar_wait(&sh.aempty[as], ((gs >> 1) & 1) ^ 1, abort_flag))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int i = 0; i < kAtomsPerWarp; ++i) {
+                const int at = sub + i * kSub;
+                if (at < atoms) {
+                    uint32_t r[32];
+                    dequant_atom(c[2 * i], c[2 * i + 1], Sv[i], Bv[i], r);
+                    tmem_st32(tmem + lane_addr + as * 128 + at * 32, r);
+                }
+            }
+            if (gs + 2 < total && !(ok = fetch())) break;  // next stage's words while the stores drain
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.afull[as]);
         }
+        tmem_wait_st();
     } else if (warp >= kEpiWarp0) {
         // ------------------------------------------------------ epilogue --
+        // Warp (q, h): TMEM lanes 32q..32q+31, the 16-column chunks h, h+EPW, ...
         const int q = warp & 3;
+        const int h = (warp - kEpiWarp0) >> 2;
         const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
-        uint32_t gs = 0;
+        uint32_t dph = 0;
+        int pr = 0;
         bool ok = true;
         for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x) {
             const Tile tl = a.tiles[it / a.n_tiles];
             const int j = it % a.n_tiles;
             const int nrows16 = (tl.rows + 15) & ~15;
-            float acc[NMAX];
+            int pf[NMAX / 32];  // down: flat slot of sorted row 32 i + lane
+            if (MODE == kDown) {
 #pragma unroll
-            for (int c = 0; c < NMAX; ++c) acc[c] = 0.f;
-            for (int s = 0; s < nstages; ++s, ++gs) {
-                const int pr = gs % kRegions;
-                if (!(ok = mbar_wait(&sh.dfull[pr], (gs / kRegions) & 1, abort_flag))) break;
+                for (int i = 0; i < NMAX / 32; ++i) pf[i] = (32 * i + lane < tl.rows) ? a.perm[tl.p0 + 32 * i + lane] : 0;
+            }
+            float acc[kAccChunks * 16];
+#pragma unroll
+            for (int c = 0; c < kAccChunks * 16; ++c) acc[c] = 0.f;
+            for (int s = 0; s < nstages; ++s) {
+                if (!(ok = mbar_wait(&sh.dfull[pr], dph, abort_flag))) break;
                 tc_fence_after();
+                const uint32_t pcol = tmem + lane_addr + kPCol0 + (uint32_t)(pr * brows);
 #pragma unroll
-                for (int c0 = 0; c0 < NMAX; c0 += 16) {
-                    if (c0 < nrows16) {
+                for (int cl = 0; cl < kAccChunks; ++cl)
+                    if ((cl * EPW + h) * 16 < nrows16) {
                         uint32_t v[16];
-                        tmem_ld16(tmem + lane_addr + kPCol0 + pr * NMAX + c0, v);
+                        tmem_ld16(pcol + (cl * EPW + h) * 16, v);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int jj = 0; jj < 16; ++jj) acc[c0 + jj] = __fadd_rn(acc[c0 + jj], __uint_as_float(v[jj]));
+                        for (int jj = 0; jj < 16; ++jj)
+                            acc[cl * 16 + jj] = __fadd_rn(acc[cl * 16 + jj], __uint_as_float(v[jj]));
                     }
-                }
                 tc_fence_before();
-                mbar_arrive(&sh.dempty[pr]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.dempty[pr]);
+                if (++pr == nreg) {
+                    pr = 0;
+                    dph ^= 1;
+                }
             }
             if (!ok) break;
             if (MODE == kGateUp) {
@@ -383,26 +485,35 @@ __global__ void __launch_bounds__((8 + 4 * DQG) * 32, 1)
                 const int n = 64 * j + 16 * q + (lane & 15);
                 const int pos = interleaved_pos(n);
 #pragma unroll
-                for (int jj = 0; jj < NMAX; jj += 2) {
-                    if (jj < nrows16) {
-                        const float send = (lane < 16) ? acc[jj + 1] : acc[jj];
-                        const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
-                        const int tok = jj + (lane < 16 ? 0 : 1);
-                        const float gf = lane < 16 ? acc[jj] : recv;
-                        const float uf = lane < 16 ? recv : acc[jj + 1];
-                        const float gb = bf16_bits_to_f32(f32_to_bf16_bits(gf));  // z is a bf16 tensor
-                        const float ub = bf16_bits_to_f32(f32_to_bf16_bits(uf));
-                        if (tok < tl.rows)
-                            a.out[(size_t)(tl.p0 + tok) * a.out_ld + pos] = (uint16_t)geglu_bf16(gb, ub);
+                for (int cl = 0; cl < kAccChunks; ++cl) {
+                    const int c0 = (cl * EPW + h) * 16;
+                    if (c0 < nrows16) {
+#pragma unroll
+                        for (int jj = 0; jj < 16; jj += 2) {
+                            const float send = (lane < 16) ? acc[cl * 16 + jj + 1] : acc[cl * 16 + jj];
+                            const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+                            const int tok = c0 + jj + (lane < 16 ? 0 : 1);
+                            const float gf = lane < 16 ? acc[cl * 16 + jj] : recv;
+                            const float uf = lane < 16 ? recv : acc[cl * 16 + jj + 1];
+                            const float gb = bf16_bits_to_f32(f32_to_bf16_bits(gf));  // z is a bf16 tensor
+                            const float ub = bf16_bits_to_f32(f32_to_bf16_bits(uf));
+                            if (tok < tl.rows)
+                                a.out[(size_t)(tl.p0 + tok) * a.out_ld + pos] = (uint16_t)geglu_bf16(gb, ub);
+                        }
                     }
                 }
             } else {
-                const int h = 128 * j + 32 * q + lane;
+                const int hrow = 128 * j + 32 * q + lane;
 #pragma unroll
-                for (int jj = 0; jj < NMAX; ++jj) {
-                    if (jj < tl.rows) {
-                        const int f = a.perm[tl.p0 + jj];
-                        a.out[(size_t)f * a.out_ld + h] = (uint16_t)f32_to_bf16_bits(acc[jj]);
+                for (int cl = 0; cl < kAccChunks; ++cl) {
+                    const int c0 = (cl * EPW + h) * 16;
+                    if (c0 < nrows16) {
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) {
+                            const int tok = c0 + jj;
+                            const int f = __shfl_sync(0xffffffffu, pf[tok >> 5], tok & 31);
+                            if (tok < tl.rows) a.out[(size_t)f * a.out_ld + hrow] = (uint16_t)f32_to_bf16_bits(acc[cl * 16 + jj]);
+                        }
                     }
                 }
             }
@@ -435,7 +546,7 @@ void gemm_stages(int K, int nmax, int* wstages, int* bregion) {
     *bregion = (int)((limit - gemm_smem_bytes(K, nw, 0)) & ~size_t(1023));
 }
 
-template <int MODE, int NMAX, int DQG>
+template <int MODE, int NMAX, int DQG, int EPW>
 static cudaError_t launch_one(const CUtensorMap& wmap, const CUtensorMap& bmap, const GemmArgs& a, int grid,
                               size_t smem, cudaStream_t stream) {
     static bool attr_set[64] = {};
@@ -443,24 +554,24 @@ static cudaError_t launch_one(const CUtensorMap& wmap, const CUtensorMap& bmap, 
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, NMAX, DQG>,
+        cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, NMAX, DQG, EPW>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, 232448 - 2048);
         if (err != cudaSuccess) return err;
         attr_set[dev] = true;
     }
-    grouped_gemm_kernel<MODE, NMAX, DQG><<<grid, (8 + 4 * DQG) * 32, smem, stream>>>(wmap, bmap, a);
+    grouped_gemm_kernel<MODE, NMAX, DQG, EPW><<<grid, (4 + 4 * DQG + 4 * EPW) * 32, smem, stream>>>(wmap, bmap, a);
     return cudaGetLastError();
 }
 
 cudaError_t launch_gemm(int mode, const CUtensorMap& wmap, const CUtensorMap& bmap, const GemmArgs& a, int grid,
                         cudaStream_t stream) {
     const size_t smem = gemm_smem_bytes(a.K, a.wstages, a.bregion);
-    if (a.nmax == 64)  // two dequant groups (16 warps)
-        return mode == kGateUp ? launch_one<kGateUp, 64, 2>(wmap, bmap, a, grid, smem, stream)
-                               : launch_one<kDown, 64, 2>(wmap, bmap, a, grid, smem, stream);
-    if (a.nmax == 128)  // the 128-column epilogue needs the registers of a 12-warp block
-        return mode == kGateUp ? launch_one<kGateUp, 128, 1>(wmap, bmap, a, grid, smem, stream)
-                               : launch_one<kDown, 128, 1>(wmap, bmap, a, grid, smem, stream);
+    if (a.nmax == 64)  // 16 dequant warps (one atom each per stage), 8 epilogue warps: 28 warps
+        return mode == kGateUp ? launch_one<kGateUp, 64, 4, 2>(wmap, bmap, a, grid, smem, stream)
+                               : launch_one<kDown, 64, 4, 2>(wmap, bmap, a, grid, smem, stream);
+    if (a.nmax == 128)  // 8 dequant warps, 16 epilogue warps of 32 columns: 28 warps
+        return mode == kGateUp ? launch_one<kGateUp, 128, 2, 4>(wmap, bmap, a, grid, smem, stream)
+                               : launch_one<kDown, 128, 2, 4>(wmap, bmap, a, grid, smem, stream);
     return cudaErrorInvalidValue;
 }
 
