@@ -19,10 +19,12 @@ struct RouterArgs {
     int T, H, E, k;
     float eps;
     float root;  // bf16(H^-0.5) as a float
+    int tt;      // tokens per cluster (16, 32 or 64), from router_tokens_per_cluster
 };
-size_t router_smem_bytes(int H, int E);
-// wmap: router_w as bf16 [E rows, H], box {64, 32}, 128B swizzle.
-// xmap: x as bf16 [T rows, H], box {64, 16}, 128B swizzle.
+size_t router_smem_bytes(int H, int E, int tt);
+int router_tokens_per_cluster(int T, int H, int E);
+// wmap: router_w as bf16 [E rows, H], box {64, min(E, 128)}, 128B swizzle.
+// xmap: x as bf16 [T rows, H], box {64, tt}, 128B swizzle.
 cudaError_t launch_router(const CUtensorMap& wmap, const CUtensorMap& xmap, const RouterArgs& a,
                           cudaStream_t stream);
 int router_error_word();

@@ -275,10 +275,13 @@ int run_experts(const moe_dims* d, const uint16_t* x, const int32_t* idx, const 
 
 int route_impl(const moe_dims* d, const uint16_t* x, const uint16_t* rw, const uint16_t* rs, const uint16_t* pes,
                int32_t* idx, uint16_t* w, cudaStream_t s) {
-    RouterArgs ra{x, rw, rs, pes, idx, w, d->T, d->H, d->E, d->k, d->eps, bf16_round(pow((double)d->H, -0.5))};
+    const int tt = router_tokens_per_cluster(d->T, d->H, d->E);
+    RouterArgs ra{x,    rw,   rs,   pes,  idx,    w,
+                  d->T, d->H, d->E, d->k, d->eps, bf16_round(pow((double)d->H, -0.5)),
+                  tt};
     CUtensorMap m_rw, m_x;
-    if (!make_map_2d(&m_rw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rw, d->H, d->E, 64, 32) ||
-        !make_map_2d(&m_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, d->H, d->T, 64, 16))
+    if (!make_map_2d(&m_rw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rw, d->H, d->E, 64, d->E < 128 ? d->E : 128) ||
+        !make_map_2d(&m_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, d->H, d->T, 64, tt))
         return MOE_ERR_CUDA;
     return fail(launch_router(m_rw, m_x, ra, s));
 }

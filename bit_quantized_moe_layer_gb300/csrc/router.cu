@@ -1,22 +1,33 @@
 // Router kernel: DiffRouter.forward of the DiffusionGemma language model
 // ("diffusion-gemma/model.ts"), fused into one launch.
 //
-// One thread-block cluster handles 16 tokens; its CS = ceil(E/32) CTAs each
-// own 32 experts. In every CTA a producer warp brings, by TMA with the
-// 128-byte swizzle, the 16 x H activation tile (16-row x 64-column boxes)
-// and, through an 8-deep ring, 64-wide K blocks of its 32 router-weight rows.
-// Four compute warps
-//   1. apply the no-scale RMS norm in fp32 to the tile in shared memory, in
-//      place (the fp32 semantics are the ones "diffusion-gemma/vision.ts"
-//      spells out in manualRms), followed by the two bf16 multiplies (router
-//      scale, H^-0.5);
-//   2. compute 16 tokens x 32 experts of scores with mma.sync m16n8k16 (fp32
-//      accumulate), round them to bf16 and write them into the leader CTA's
-//      shared memory (distributed shared memory);
-// then the leader CTA picks the top k per token (value descending, ties to
-// the lower expert id), takes the fp32 softmax over the k picked scores and
-// multiplies by per_expert_scale[idx].
+// One thread-block cluster of 8 CTAs handles TT tokens (TT = 16, 32 or 64).
+// The hidden dimension is split into 64-wide blocks shared out over the
+// cluster: CTA r loads, by TMA with the 128-byte swizzle, its blocks of the
+// TT activation rows and of every router-weight row, all at once. Then
+//   1. each CTA sums the squares of its slice per token (fp32 with an
+//      error-free two-sum, so the partial sum keeps ~48 bits) and sends the
+//      partial to every CTA of the cluster (distributed shared memory);
+//   2. every CTA adds the 8 partials in CTA order, forms the fp32 mean as the
+//      two-float sum divided by H and rounded once (the fp32 RMS-norm
+//      semantics "diffusion-gemma/vision.ts" spells out in manualRms), and normalises
+//      its slice in place, then the two bf16 multiplies (router scale,
+//      H^-0.5), bf16 after each op;
+//   3. each CTA computes partial scores of all TT tokens x E experts over its
+//      slice on the tensor cores (tcgen05.mma, 128 experts on the TMEM lanes,
+//      fp32 accumulate) and sends each token's partials to the CTA that owns
+//      the token (TT/8 tokens per CTA);
+//   4. the owner adds the 8 partials in CTA order, rounds to bf16, picks the
+//      top k (value descending, ties to the lower expert id), takes the fp32
+//      softmax over the k picked scores and multiplies by
+//      per_expert_scale[idx].
+// Every CTA passes the same three cluster barriers whatever happens, so a
+// wait that times out (error word set) cannot leave the cluster hung.
 #include <cooperative_groups.h>
+
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -27,21 +38,11 @@ namespace moe {
 
 namespace {
 
-constexpr int kTT = 16;        // tokens per cluster
-constexpr int kWarps = 4;      // compute warps per CTA (+1 producer warp)
-constexpr int kExpPerCta = 32; // experts per CTA (8 per warp)
-constexpr int kRing = 8;       // K blocks of router weight in flight
-constexpr int kBlockBytes = kExpPerCta * 128;  // 32 rows x 64 bf16
-constexpr int kXBoxBytes = kTT * 128;          // 16 rows x 64 bf16
-
-__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                               uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-        "{%0, %1, %2, %3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
+constexpr int kCS = 8;          // CTAs per cluster
+constexpr int kWarps = 16;      // warps per CTA
+constexpr int kChunkE = 128;    // experts per router-weight chunk in shared memory
+constexpr int kWBlockBytes = kChunkE * 128;  // one 64-wide K block of a chunk
+constexpr uint32_t kTmemCols = 64;           // >= the largest TT
 
 // bf16 bits -> key that orders like the value (for finite values).
 __device__ __forceinline__ uint32_t order_key16(uint32_t b) { return (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u); }
@@ -51,90 +52,169 @@ __device__ __forceinline__ uint32_t key16_to_bits(uint32_t k) { return (k & 0x80
 // box of 128-byte rows.
 __device__ __forceinline__ int sw128(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
 
+// Error-free transformation of a + b (Knuth's two-sum): s + e == a + b exactly.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+    s = __fadd_rn(a, b);
+    const float bp = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
+}
+
+// (hi, lo) += v, keeping hi + lo within ~2^-48 of the exact running sum.
+__device__ __forceinline__ void acc2(float& hi, float& lo, float v) {
+    float s, e;
+    two_sum(hi, v, s, e);
+    hi = s;
+    lo = __fadd_rn(lo, e);
+}
+
+// K blocks [kb0, kb0 + cnt) of the H / 64 blocks owned by cluster rank r.
+__host__ __device__ inline void kslice(int nkb, int r, int& kb0, int& cnt) {
+    const int base = nkb / kCS, rem = nkb % kCS;
+    cnt = base + (r < rem ? 1 : 0);
+    kb0 = r * base + (r < rem ? r : rem);
+}
+
+struct RouterSmem {
+    uint8_t *xt, *wt, *rsl;  // x slice boxes, weight-chunk blocks, router_scale slice
+    float2* pss;             // [kCS][TT] partial sums of squares, by source CTA
+    float* red;              // [kCS][TT/kCS][E] partial scores of my tokens, by source CTA
+    uint16_t* sc;            // [TT/kCS][E] bf16 scores of my tokens
+};
+
+__host__ __device__ inline size_t take_bytes(size_t& off, size_t bytes, size_t align) {
+    off = (off + align - 1) & ~(align - 1);
+    const size_t at = off;
+    off += bytes;
+    return at;
+}
+
+// Carve-up of the dynamic shared memory (from a 1024-byte aligned base);
+// returns its size.
+__host__ __device__ inline size_t router_layout(int H, int E, int TT, uint8_t* base, RouterSmem* s) {
+    const int nkbmax = (H / 64 + kCS - 1) / kCS;
+    size_t off = 0;
+    const size_t xt = take_bytes(off, (size_t)nkbmax * TT * 128, 1024);
+    const size_t wt = take_bytes(off, (size_t)nkbmax * kWBlockBytes, 1024);
+    const size_t rsl = take_bytes(off, (size_t)nkbmax * 128, 16);
+    const size_t pss = take_bytes(off, (size_t)kCS * TT * sizeof(float2), 16);
+    const size_t red = take_bytes(off, (size_t)TT * E * sizeof(float), 16);
+    const size_t sc = take_bytes(off, (size_t)(TT / kCS) * E * 2, 16);
+    if (s) {
+        s->xt = base + xt;
+        s->wt = base + wt;
+        s->rsl = base + rsl;
+        s->pss = reinterpret_cast<float2*>(base + pss);
+        s->red = reinterpret_cast<float*>(base + red);
+        s->sc = reinterpret_cast<uint16_t*>(base + sc);
+    }
+    return off;
+}
+
 }  // namespace
 
-__global__ void __launch_bounds__((kWarps + 1) * 32) router_kernel(const __grid_constant__ CUtensorMap wmap,
-                                                                    const __grid_constant__ CUtensorMap xmap,
-                                                                    RouterArgs a) {
+__global__ void __launch_bounds__(kWarps * 32) router_kernel(const __grid_constant__ CUtensorMap wmap,
+                                                              const __grid_constant__ CUtensorMap xmap,
+                                                              RouterArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    __shared__ uint64_t full[kRing], empty[kRing], xfull;
+    __shared__ uint64_t full, wfull, mdone;
+    __shared__ uint32_t tmem_base;
     __shared__ int abort_flag_s;
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int H = a.H, E = a.E, k = a.k;
-    const int nkb = H / 64;
-    uint8_t* ring = smem;                      // kRing x 4 KB
-    uint8_t* xt = smem + kRing * kBlockBytes;  // nkb boxes of 16 rows x 128 B (swizzled)
-    uint16_t* rscale = reinterpret_cast<uint16_t*>(xt + nkb * kXBoxBytes);  // router_scale [H]
-    uint16_t* scores = rscale + H;                                             // [kTT][E], leader CTA
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int H = a.H, E = a.E, k = a.k, TT = a.tt;
+    RouterSmem sm;
+    router_layout(H, E, TT, base, &sm);
     volatile int* abort_flag = &abort_flag_s;
 
     cg::cluster_group cluster = cg::this_cluster();
-    const int cs = (int)cluster.num_blocks();
     const int rank = (int)cluster.block_rank();
-    const int t0 = (blockIdx.x / cs) * kTT;
+    const int t0 = (blockIdx.x / kCS) * TT;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int kb0, cnt;
+    kslice(H / 64, rank, kb0, cnt);
+    const int nch = (E + kChunkE - 1) / kChunkE;
+    const int eb = E < kChunkE ? E : kChunkE;  // rows of a weight box
+    const int tpc = TT / kCS;                  // tokens owned by each CTA
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kRing; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], kWarps);
-        }
-        mbar_init(&xfull, 1);
+        prefetch_tensormap(&xmap);
+        prefetch_tensormap(&wmap);
+        mbar_init(&full, 1);
+        mbar_init(&wfull, 1);
+        mbar_init(&mdone, 1);
         abort_flag_s = 0;
         fence_barrier_init();
     }
-    // All CTAs of the cluster have started (and initialised their barriers)
-    // before any of them writes into the leader's shared memory.
-    cluster_barrier();
-
-    if (warp == kWarps) {
-        // ---- producer ----
-        if (lane == 0) {
-            prefetch_tensormap(&xmap);
-            prefetch_tensormap(&wmap);
-            mbar_arrive_expect_tx(&xfull, nkb * kXBoxBytes + H * 2);
-            bulk_load(rscale, a.router_scale, H * 2, &xfull);
-            for (int kb = 0; kb < nkb; ++kb) tma_load_2d(xt + kb * kXBoxBytes, &xmap, &xfull, kb * 64, t0);
-            int kb = 0;
-            for (; kb < nkb; ++kb) {
-                const int slot = kb % kRing;
-                if (!mbar_wait(&empty[slot], ((kb / kRing) & 1) ^ 1, abort_flag)) break;
-                mbar_arrive_expect_tx(&full[slot], kBlockBytes);
-                tma_load_2d(ring + slot * kBlockBytes, &wmap, &full[slot], kb * 64, rank * kExpPerCta);
-            }
-            // no copies in flight at exit
-            mbar_wait(&xfull, 0, abort_flag);
-            for (int b = (kb > kRing ? kb - kRing : 0); b < kb; ++b) mbar_wait(&full[b % kRing], (b / kRing) & 1, abort_flag);
-        }
+    __syncthreads();
+    if (warp == 0) {  // scores accumulator: 128 lanes (experts) x TT columns (tokens)
+        tmem_alloc(&tmem_base, kTmemCols);
+        tmem_relinquish();
+    } else if (warp == 1) {
+        // The copies only write this CTA's shared memory: start them before
+        // waiting for the rest of the cluster, one lane per copy.
+        if (lane == 0) mbar_arrive_expect_tx(&full, (uint32_t)cnt * (TT * 128 + eb * 128 + 128));
         __syncwarp();
-        cluster_barrier();
-        return;
+        if (lane < cnt) tma_load_2d(sm.xt + lane * TT * 128, &xmap, &full, (kb0 + lane) * 64, t0);
+        if (lane >= 16 && lane - 16 < cnt)
+            tma_load_2d(sm.wt + (lane - 16) * kWBlockBytes, &wmap, &full, (kb0 + lane - 16) * 64, 0);
+        if (lane == 31 && cnt > 0) bulk_load(sm.rsl, a.router_scale + (size_t)kb0 * 64, cnt * 128, &full);
     }
+    // Cluster barrier 0: every CTA's barriers exist before any remote write.
+    tc_fence_before();
+    cluster_barrier();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+    const bool have = mbar_wait(&full, 0, abort_flag);
 
-    // ---- 1. no-scale RMS norm, x scale, x H^-0.5 (bf16 after each op), in place ----
-    const bool have_x = mbar_wait(&xfull, 0, abort_flag);
-    const int nchunks = nkb * 8;  // 16-byte chunks per row
-    for (int r = warp; r < kTT && have_x; r += kWarps) {
-        float ss = 0.f;
-#pragma unroll 4
-        for (int i = lane; i < nchunks; i += 32) {
-            const uint4 v = *reinterpret_cast<const uint4*>(xt + (i >> 3) * kXBoxBytes + sw128(r, i & 7));
+    // ---- 1. partial sums of squares of this slice, to every CTA ----
+    for (int t = warp; t < TT; t += kWarps) {
+        float hi = 0.f, lo = 0.f;
+        for (int i = lane; have && i < cnt * 8; i += 32) {
+            const uint4 v = *reinterpret_cast<const uint4*>(sm.xt + (i >> 3) * TT * 128 + sw128(t, i & 7));
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const float lo = bf16_bits_to_f32(w[j] & 0xFFFFu), hi = bf16_bits_to_f32(w[j] >> 16);
-                ss = __fadd_rn(ss, __fmul_rn(lo, lo));
-                ss = __fadd_rn(ss, __fmul_rn(hi, hi));
+                const float x0 = bf16_bits_to_f32(w[j] & 0xFFFFu), x1 = bf16_bits_to_f32(w[j] >> 16);
+                acc2(hi, lo, __fmul_rn(x0, x0));  // squares of bf16 values are exact in fp32
+                acc2(hi, lo, __fmul_rn(x1, x1));
             }
         }
+        // Butterfly: both lanes of a pair form the same (exact) two-sum, so
+        // every lane ends with the same value.
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
-        const float rs = __frsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)H), a.eps));
-#pragma unroll 4
-        for (int i = lane; i < nchunks; i += 32) {
-            uint4* p = reinterpret_cast<uint4*>(xt + (i >> 3) * kXBoxBytes + sw128(r, i & 7));
+        for (int o = 16; o > 0; o >>= 1) {
+            const float h2 = __shfl_xor_sync(0xffffffffu, hi, o), l2 = __shfl_xor_sync(0xffffffffu, lo, o);
+            float s, e;
+            two_sum(hi, h2, s, e);
+            hi = s;
+            lo = __fadd_rn(__fadd_rn(lo, l2), e);
+        }
+        if (lane < kCS) cluster.map_shared_rank(sm.pss, lane)[rank * TT + t] = make_float2(hi, lo);
+    }
+    __syncwarp();
+    cluster_barrier();  // 1: all partial sums of squares delivered
+
+    // ---- 2. rsqrt of the fp32 mean, normalise this slice in place ----
+    for (int t = warp; t < TT; t += kWarps) {
+        float hs = 0.f, ls = 0.f;
+        for (int src = 0; src < kCS; ++src) {  // CTA order: the same result in every CTA
+            const float2 p = sm.pss[src * TT + t];
+            acc2(hs, ls, p.x);
+            ls = __fadd_rn(ls, p.y);
+        }
+        // mean = (hs + ls) / H rounded once to fp32, without fp64 (slow on
+        // this part): q = RN(hs / H); the residual hs - q H is exact (fma);
+        // adding (residual + ls) / H moves q by under half an ulp, so the
+        // sum rounds to the exactly rounded mean unless that mean lies within
+        // about 2^-40 (relative) of a rounding boundary.
+        const float Hf = (float)H;
+        const float q0 = __fdiv_rn(hs, Hf);
+        const float rsd = __fadd_rn(__fmaf_rn(-q0, Hf, hs), ls);
+        const float mean = __fadd_rn(q0, __fdiv_rn(rsd, Hf));
+        const float rs = __frsqrt_rn(__fadd_rn(mean, a.eps));
+        for (int i = lane; have && i < cnt * 8; i += 32) {
+            uint4* p = reinterpret_cast<uint4*>(sm.xt + (i >> 3) * TT * 128 + sw128(t, i & 7));
             const uint4 v = *p;
-            const uint4 s = reinterpret_cast<const uint4*>(rscale)[i];
+            const uint4 s = reinterpret_cast<const uint4*>(sm.rsl)[i];  // router_scale of the same 8 columns
             const uint32_t w[4] = {v.x, v.y, v.z, v.w}, sc[4] = {s.x, s.y, s.z, s.w};
             uint32_t o[4];
 #pragma unroll
@@ -148,61 +228,85 @@ __global__ void __launch_bounds__((kWarps + 1) * 32) router_kernel(const __grid_
             *p = make_uint4(o[0], o[1], o[2], o[3]);
         }
     }
-    // The compute warps only (the producer warp never comes here): named
-    // barrier 1 over kWarps * 32 threads.
-    asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
+    // The normalised tile was written by ordinary stores; the tensor core
+    // reads it through the async proxy.
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
 
-    // ---- 2. scores for experts [e0, e0+8) of this warp: 16 tokens x 8 experts ----
-    // Inside each 64-wide K block, thread (g, q) owns K [16q, 16q+16) of its
-    // rows (chunks 2q and 2q+1); mma step s takes K 16q+4s+{0,1} as fragment
-    // k {2q, 2q+1} and 16q+4s+{2,3} as k {2q+8, 2q+9}, identically for both
-    // operands, so the four steps sum the block's 64 products exactly once.
-    const int e0 = rank * kExpPerCta + warp * 8;
-    const int g = lane >> 2, q = lane & 3;
-    const int brow = warp * 8 + g;  // row of this lane's expert in a ring block
-    float c[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int kb = 0; kb < nkb && have_x; ++kb) {
-        const int slot = kb % kRing;
-        if (!mbar_wait(&full[slot], (kb / kRing) & 1, abort_flag)) break;
-        const uint8_t* blk = ring + slot * kBlockBytes;
-        const uint4 b0 = *reinterpret_cast<const uint4*>(blk + sw128(brow, 2 * q));
-        const uint4 b1 = *reinterpret_cast<const uint4*>(blk + sw128(brow, 2 * q + 1));
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
-        const uint8_t* xb = xt + kb * kXBoxBytes;
-        const uint4 x0 = *reinterpret_cast<const uint4*>(xb + sw128(g, 2 * q));
-        const uint4 x1 = *reinterpret_cast<const uint4*>(xb + sw128(g, 2 * q + 1));
-        const uint4 y0 = *reinterpret_cast<const uint4*>(xb + sw128(g + 8, 2 * q));
-        const uint4 y1 = *reinterpret_cast<const uint4*>(xb + sw128(g + 8, 2 * q + 1));
-        const uint32_t ar0[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-        const uint32_t ar1[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
-        const uint32_t br[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+    // ---- 3. partial scores over this slice, to the CTA owning each token ----
+    // D[e][t] = sum over this slice of W[e][h] * n[t][h], experts on the 128
+    // TMEM lanes and tokens on TT columns: one tcgen05.mma per 16 K (A = the
+    // weight chunk, B = the normalised tile, both K-major in shared memory).
+    const uint32_t idesc = idesc_bf16_m128((uint32_t)TT);
+    for (int ch = 0; ch < nch; ++ch) {
+        bool wok = have;
+        if (ch > 0) {
+            __syncthreads();  // every warp has read the previous chunk's scores
+            if (threadIdx.x == 0) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_arrive_expect_tx(&wfull, (uint32_t)cnt * eb * 128);
+                for (int i = 0; i < cnt; ++i)
+                    tma_load_2d(sm.wt + i * kWBlockBytes, &wmap, &wfull, (kb0 + i) * 64, ch * kChunkE);
+            }
+            wok = mbar_wait(&wfull, (ch - 1) & 1, abort_flag) && wok;
+        }
+        const bool mma = wok && cnt > 0;
+        if (warp == 0 && mma) {
+            tc_fence_after();
+            if (elect_one()) {
+                for (int kb = 0; kb < cnt; ++kb) {
+                    const uint64_t ad = sw128_kmajor_desc(smem_u32(sm.wt + kb * kWBlockBytes));
+                    const uint64_t bd = sw128_kmajor_desc(smem_u32(sm.xt + kb * TT * 128));
 #pragma unroll
-        for (int s = 0; s < 4; ++s)
-            mma_bf16_16816(c, ar0[2 * s], ar1[2 * s], ar0[2 * s + 1], ar1[2 * s + 1], br[2 * s], br[2 * s + 1]);
-    }
-    // c0,c1: token g, experts e0+2q, e0+2q+1; c2,c3: token g+8.
-    uint16_t* lead = cluster.map_shared_rank(scores, 0);
-    {
-        const int ea = e0 + 2 * q;
-        if (ea < E) {
-            lead[g * E + ea] = (uint16_t)f32_to_bf16_bits(c[0]);
-            lead[(g + 8) * E + ea] = (uint16_t)f32_to_bf16_bits(c[2]);
+                    for (int k16 = 0; k16 < 4; ++k16)
+                        umma_ss(tmem, ad + (uint64_t)(k16 * 2), bd + (uint64_t)(k16 * 2), idesc,
+                                (kb > 0 || k16 > 0) ? 1u : 0u);
+                }
+                umma_commit(&mdone);
+            }
+            __syncwarp();
         }
-        if (ea + 1 < E) {
-            lead[g * E + ea + 1] = (uint16_t)f32_to_bf16_bits(c[1]);
-            lead[(g + 8) * E + ea + 1] = (uint16_t)f32_to_bf16_bits(c[3]);
+        const bool got = mma && mbar_wait(&mdone, ch & 1, abort_flag);
+        tc_fence_after();
+        // Warp w reads TMEM lane quarter w % 4 (experts ch*128 + 32(w%4) +
+        // lane) and the 16 token columns 16 (w / 4) .. 16 (w / 4) + 15.
+        const int e = ch * kChunkE + (warp & 3) * 32 + lane;
+        const int c0 = (warp >> 2) * 16;
+        if (c0 < TT) {
+            uint32_t v[16];
+            if (got) {
+                tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)c0, v);
+                tmem_wait_ld();
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] = 0u;  // no K blocks here (or a wait timed out)
+            }
+            if (e < E) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int tok = c0 + j;
+                    cluster.map_shared_rank(sm.red, tok / tpc)[(size_t)(rank * tpc + tok % tpc) * E + e] =
+                        __uint_as_float(v[j]);
+                }
+            }
         }
+        tc_fence_before();
     }
     __syncwarp();
-    cluster_barrier();
-    if (rank != 0) return;
+    cluster_barrier();  // 2: all partial scores delivered; no remote access after this
 
-    // ---- 3. top-k + precise softmax + per-expert scale (leader CTA) ----
-    for (int tl = warp; tl < kTT; tl += kWarps) {
-        const int t = t0 + tl;
+    // ---- 4. my tokens: scores, top k, precise softmax, per-expert scale ----
+    for (int i = threadIdx.x; i < tpc * E; i += kWarps * 32) {
+        const int tl = i / E, e = i % E;
+        float s = 0.f;
+        for (int src = 0; src < kCS; ++src) s = __fadd_rn(s, sm.red[(size_t)(src * tpc + tl) * E + e]);
+        sm.sc[tl * E + e] = (uint16_t)f32_to_bf16_bits(s);
+    }
+    __syncthreads();
+    for (int tl = warp; tl < tpc; tl += kWarps) {
+        const int t = t0 + rank * tpc + tl;
         if (t >= a.T) continue;
-        const uint16_t* sr = scores + tl * E;
+        const uint16_t* sr = sm.sc + tl * E;
         uint32_t cand[8];  // keys of this lane's experts e = lane + 32 i
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -210,8 +314,7 @@ __global__ void __launch_bounds__((kWarps + 1) * 32) router_kernel(const __grid_
             cand[i] = (e < E) ? ((order_key16(sr[e]) << 16) | (0xFFFFu - (uint32_t)e)) : 0u;
         }
         int my_idx = 0;
-        float my_s = 0.f;
-        float top_s = 0.f;
+        float my_s = 0.f, top_s = 0.f;
         for (int j = 0; j < k; ++j) {
             uint32_t best = 0;
 #pragma unroll
@@ -238,6 +341,12 @@ __global__ void __launch_bounds__((kWarps + 1) * 32) router_kernel(const __grid_
             a.w[(size_t)t * k + lane] = (uint16_t)f32_to_bf16_bits(__fmul_rn(p, pes));
         }
     }
+    __syncwarp();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
 }
 
 int router_error_word() {
@@ -247,37 +356,84 @@ int router_error_word() {
     return v;
 }
 
-size_t router_smem_bytes(int H, int E) {
-    return 1024 + (size_t)kRing * kBlockBytes + (size_t)(H / 64) * kXBoxBytes + (size_t)H * 2 + (size_t)kTT * E * 2;
+namespace {
+constexpr size_t kRouterSmemLimit = 232448 - 1024;  // 227 KB per CTA minus the static part
 }
 
-cudaError_t launch_router(const CUtensorMap& wmap, const CUtensorMap& xmap, const RouterArgs& a,
-                          cudaStream_t stream) {
-    if (a.T == 0) return cudaSuccess;
-    const int cs = (a.E + kExpPerCta - 1) / kExpPerCta;
-    const int tiles = (a.T + kTT - 1) / kTT;
-    const size_t smem = router_smem_bytes(a.H, a.E);
+size_t router_smem_bytes(int H, int E, int tt) { return 1024 + router_layout(H, E, tt, nullptr, nullptr); }
+
+namespace {
+cudaError_t ensure_router_attr() {
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        cudaError_t err = cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448 - 1024);
+        cudaError_t err = cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)kRouterSmemLimit);
         if (err != cudaSuccess) return err;
         attr_set[dev] = true;
     }
+    return cudaSuccess;
+}
+
+cudaLaunchConfig_t router_config(int T, int tt, size_t smem, cudaStream_t stream, cudaLaunchAttribute* attr) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(tiles * cs, 1, 1);
-    cfg.blockDim = dim3((kWarps + 1) * 32, 1, 1);
+    cfg.gridDim = dim3((unsigned)(((T + tt - 1) / tt) * kCS), 1, 1);
+    cfg.blockDim = dim3(kWarps * 32, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.x = kCS;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    return cfg;
+}
+
+// Clusters of this kernel the device holds at once with `smem` bytes per CTA
+// (cached per device and size).
+int router_resident_clusters(size_t smem) {
+    static std::mutex mu;
+    static std::map<std::pair<int, size_t>, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || ensure_router_attr() != cudaSuccess) return 1;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find({dev, smem});
+    if (it != cache.end()) return it->second;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = router_config(kCS, 16, smem, nullptr, attr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, router_kernel, &cfg) != cudaSuccess || n < 1) n = 1;
+    cache[{dev, smem}] = n;
+    return n;
+}
+}  // namespace
+
+// Tokens per cluster: the smallest of 16, 32, 64 whose clusters all fit on
+// the device at once (one wave); the largest that fits in shared memory when
+// none does.
+int router_tokens_per_cluster(int T, int H, int E) {
+    int best = 16;
+    for (int tt = 16; tt <= 64; tt <<= 1) {
+        const size_t smem = router_smem_bytes(H, E, tt);
+        if (smem > kRouterSmemLimit) break;
+        best = tt;
+        if ((T + tt - 1) / tt <= router_resident_clusters(smem)) return tt;
+    }
+    return best;
+}
+
+cudaError_t launch_router(const CUtensorMap& wmap, const CUtensorMap& xmap, const RouterArgs& a,
+                          cudaStream_t stream) {
+    if (a.T == 0) return cudaSuccess;
+    const size_t smem = router_smem_bytes(a.H, a.E, a.tt);
+    if (smem > kRouterSmemLimit || a.tt % 16 != 0 || a.tt > 64) return cudaErrorInvalidValue;
+    cudaError_t err = ensure_router_attr();
+    if (err != cudaSuccess) return err;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = router_config(a.T, a.tt, smem, stream, attr);
     return cudaLaunchKernelEx(&cfg, router_kernel, wmap, xmap, a);
 }
 
