@@ -24,6 +24,7 @@ import hashlib
 import json
 import os
 import statistics
+import threading
 import subprocess
 import sys
 import time
@@ -67,54 +68,81 @@ def roofline_model(d: ms.Dims, touched: int, peaks):
 
 
 class ClockSampler:
-    """nvidia-smi clocks/throttle reasons sampled every 200 ms while running."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock, power and clock-event reasons of one GPU, read through NVML
+    (ctypes, read-only queries) every 2 ms while the timed region runs, plus
+    one reading at each end. Falls back to nothing when NVML is missing."""
+    # nvmlClocksEventReason bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, index: int):
-        self.index = index
-        self.proc = None
+    def __init__(self, index: int, uuid: str | None = None, period_s: float = 0.002):
+        self.index, self.uuid, self.period = index, uuid, period_s
+        self.rows, self.nvml, self.handle = [], None, None
+        self._stop = threading.Event()
+        self._thread = None
+
+    def _open(self):
+        import ctypes
+        for name in ("libnvidia-ml.so.1", "libnvidia-ml.so"):
+            try:
+                lib = ctypes.CDLL(name)
+                break
+            except OSError:
+                lib = None
+        if lib is None or lib.nvmlInit_v2() != 0:
+            return False
+        h = ctypes.c_void_p()
+        ok = False
+        if self.uuid:
+            ok = lib.nvmlDeviceGetHandleByUUID(self.uuid.encode(), ctypes.byref(h)) == 0
+        if not ok:
+            ok = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(h)) == 0
+        if not ok:
+            return False
+        self.nvml, self.handle, self.ct = lib, h, ctypes
+        mx = ctypes.c_uint()
+        self.max_mhz = float(mx.value) if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0 else None
+        return True
+
+    def _sample(self):
+        ct, lib, h = self.ct, self.nvml, self.handle
+        clk, pw, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if lib.nvmlDeviceGetClockInfo(h, 1, ct.byref(clk)) != 0:
+            return
+        fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        reasons = rs.value if fn(h, ct.byref(rs)) == 0 else 0
+        power = pw.value / 1e3 if lib.nvmlDeviceGetPowerUsage(h, ct.byref(pw)) == 0 else None
+        self.rows.append((float(clk.value), power, int(reasons)))
+
+    def _run(self):
+        while not self._stop.wait(self.period):
+            self._sample()
 
     def __enter__(self):
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
-                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.proc = None
+            if self._open():
+                self._sample()
+                self._thread = threading.Thread(target=self._run, daemon=True)
+                self._thread.start()
+        except (OSError, AttributeError):
+            self.nvml = None
         return self
 
     def __exit__(self, *exc):
-        self.lines = []
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                out, _ = self.proc.communicate(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join()
+            self._sample()
 
     def summary(self):
-        rows = []
-        for ln in self.lines:
-            f = [x.strip() for x in ln.split(",")]
-            try:
-                rows.append(dict(sm=float(f[1]), smmax=float(f[2]), power=float(f[3]),
-                                 hw=f[5], hwt=f[6], swt=f[7], pcap=f[8]))
-            except (ValueError, IndexError):
-                continue
-        if not rows:
+        if not self.rows:
             return None
-        reasons = set()
-        for r in rows:
-            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
-                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
-                if r[key].lower() == "active":
-                    reasons.add(name)
-        return dict(sm_mhz=statistics.median(r["sm"] for r in rows), sm_max_mhz=max(r["smmax"] for r in rows),
-                    power_w_max=max(r["power"] for r in rows), samples=len(rows), reasons=sorted(reasons))
+        reasons = sorted({name for _, _, r in self.rows for bit, name in self.REASONS.items() if r & bit})
+        powers = [p for _, p, _ in self.rows if p is not None]
+        return dict(sm_mhz=statistics.median(c for c, _, _ in self.rows), sm_max_mhz=self.max_mhz,
+                    power_w_max=max(powers) if powers else None, samples=len(self.rows), reasons=reasons,
+                    source="NVML every 2 ms during the timed region")
 
 
 def cores_available() -> int:
@@ -235,11 +263,17 @@ def run_ours(args, wl):
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    moe.timing_enable(True)
+    try:
+        uuid = str(torch.cuda.get_device_properties(local).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except (AttributeError, RuntimeError):
+        uuid = None
+    # Timed region 1: whole steps, events only around each step (the
+    # library's kernels run back to back with programmatic dependent launch).
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
+    with ClockSampler(local, uuid) as clk:
         for i in range(args.steps):
             flush.zero_()
             starts[i].record(stream)
@@ -248,6 +282,14 @@ def run_ours(args, wl):
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
+    # Timed region 2: the same steps with the library's per-kernel events on
+    # (they sit between the kernels, so this pass is only for the breakdown
+    # and the per-launch roofline of the dominant kernel).
+    moe.timing_enable(True)
+    for i in range(args.steps):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
     stage_ms, calls = moe.timing_read()
     moe.timing_enable(False)
     err = moe.device_error()
@@ -304,7 +346,8 @@ def run_ours(args, wl):
         roofline=dict(bound="hbm", achieved=achieved, peak=peaks["hbm"], unit="GB/s", frac=achieved / peaks["hbm"],
                       traffic=traffic_from_profile(f"gate_up:{wl.name}", src_hash), kernel="grouped_gemm gate_up",
                       bytes_per_launch=touched * gu_bytes, ms_per_launch=gu_ms,
-                      peak_source=f"{peaks['source']} hbm_gbs (copy)"),
+                      peak_source=f"{peaks['source']} hbm_gbs (copy)",
+                      timed="per-launch CUDA events in timed region 2 (same steps, library timing on)"),
         layer_roofline=dict(bound=model["bound"], t_roof_us=model["t_roof_s"] * 1e6, t_step_us=ms_step * 1e3,
                             frac=model["t_roof_s"] / (ms_step * 1e-3), bytes=model["bytes"], flops=model["flops"]),
         stages_ms_per_call={k: v / max(1, calls) for k, v in stage_ms.items()},
@@ -323,7 +366,7 @@ def run_ours(args, wl):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="canvas", choices=sorted(ms.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

@@ -255,6 +255,13 @@ __device__ __forceinline__ uint32_t elect_one() {
 
 // Cluster-wide barrier (all threads of all CTAs of the cluster). Non-aligned
 // form; callers still reconverge their warp first (__syncwarp).
+// Programmatic dependent launch: let the next kernel of the stream be
+// scheduled now (it still waits for this grid before touching memory), and
+// wait for the previous kernel's grid to complete and its memory to be
+// visible. Both are no-ops for a launch without the programmatic attribute.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void cluster_barrier() {
     asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }

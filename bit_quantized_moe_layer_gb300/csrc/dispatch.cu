@@ -28,6 +28,8 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
     constexpr int kW = kDispatchThreads / 32;
     __shared__ int wh[kW][kMaxE + 1];
     __shared__ int cnt[kMaxE], off[kMaxE + 1], tbase[kMaxE + 1];
+    pdl_trigger();
+    pdl_wait();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int S = a.S, E = a.E;
     const unsigned lt_mask = (1u << lane) - 1u;
@@ -46,14 +48,18 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
         if (e >= 0 && (peers & lt_mask) == 0) wh[warp][e] += __popc(peers);
     }
     __syncthreads();
-    for (int e = tid; e < E; e += kDispatchThreads) {
-        int run = 0;
-        for (int w = 0; w < kW; ++w) {
-            const int v = wh[w][e];
-            wh[w][e] = run;
-            run += v;
+    // Per expert, exclusive scan over the 32 warps' counts: warp ww scans the
+    // columns of experts ww, ww + 32, ..., lane = source warp.
+    for (int e = warp; e < E; e += kW) {
+        const int v = wh[lane][e];
+        int inc = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += u;
         }
-        cnt[e] = run;
+        wh[lane][e] = inc - v;
+        if (lane == 31) cnt[e] = inc;
     }
     __syncthreads();
     if (warp == 0) {  // scan over experts: lane owns experts [8 lane, 8 lane + 8)
@@ -104,11 +110,14 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
                 a.tiles[tbase[e] + i] = t;
             }
         }
-        if (tid == 0 && a.num_tiles) {
+        if (warp == 0 && a.num_tiles) {
             int mx = 0;
-            for (int e = 0; e < E; ++e) mx = max(mx, min(cnt[e], a.nmax));
-            a.num_tiles[0] = tbase[E];
-            a.num_tiles[1] = mx;  // rows of the largest token tile
+            for (int e = lane; e < E; e += 32) mx = max(mx, min(cnt[e], a.nmax));
+            mx = __reduce_max_sync(0xffffffffu, mx);
+            if (lane == 0) {
+                a.num_tiles[0] = tbase[E];
+                a.num_tiles[1] = mx;  // rows of the largest token tile
+            }
         }
     }
     for (int i = tid; i < kW * E; i += kDispatchThreads) wh[i / E][i % E] += off[i % E];
@@ -131,8 +140,7 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
 }
 
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
-    dispatch_kernel<<<1, kDispatchThreads, 0, stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(dispatch_kernel, dim3(1), dim3(kDispatchThreads), 0, stream, a);
 }
 
 // 8 bf16 (one 16-byte chunk) -> positions holding elements (0,4,1,5,2,6,3,7).
@@ -145,70 +153,72 @@ __device__ __forceinline__ uint4 interleave8(uint4 v) {
     return o;
 }
 
-__global__ void gather_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm,
-                              const int32_t* __restrict__ offsets, uint16_t* __restrict__ xs, int S, int k,
-                              int H, int E) {
+// One warp per sorted row p: t = perm[p] / k, then the warp's lanes copy the
+// row's 16-byte chunks (8 bf16 each), interleaved, lane-strided.
+constexpr int kRowWarps = 8;  // rows (gather) or tokens (combine) per 256-thread block
+
+__global__ void __launch_bounds__(kRowWarps * 32) gather_kernel(const uint16_t* __restrict__ x,
+                                                                const int32_t* __restrict__ perm,
+                                                                const int32_t* __restrict__ offsets,
+                                                                uint16_t* __restrict__ xs, int S, int k, int H,
+                                                                int E) {
+    pdl_trigger();
+    pdl_wait();
+    const int p = blockIdx.x * kRowWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (p >= S || p >= offsets[E]) return;
+    const int t = perm[p] / k;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+    uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)p * H);
     const int chunks = H / 8;
-    const int valid = offsets[E];
-    const long total = (long)S * chunks;
-    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
-        const int p = (int)(i / chunks), c = (int)(i % chunks);
-        if (p >= valid) continue;
-        const int t = perm[p] / k;
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H) + c);
-        reinterpret_cast<uint4*>(xs + (size_t)p * H)[c] = interleave8(v);
-    }
+#pragma unroll 4
+    for (int c = lane; c < chunks; c += 32) dst[c] = interleave8(__ldg(src + c));
 }
 
 cudaError_t launch_gather(const uint16_t* x, const int32_t* perm, const int32_t* offsets, uint16_t* xs,
                           int S, int k, int H, int E, cudaStream_t stream) {
     if (S == 0) return cudaSuccess;
-    const long total = (long)S * (H / 8);
-    const int threads = 256;
-    long blocks = (total + threads - 1) / threads;
-    if (blocks > 152 * 16) blocks = 152 * 16;
-    gather_kernel<<<(int)blocks, threads, 0, stream>>>(x, perm, offsets, xs, S, k, H, E);
-    return cudaGetLastError();
+    return launch_pdl(gather_kernel, dim3((S + kRowWarps - 1) / kRowWarps), dim3(kRowWarps * 32), 0, stream, x, perm,
+                      offsets, xs, S, k, H, E);
 }
 
-__global__ void combine_kernel(const uint16_t* __restrict__ y, const uint16_t* __restrict__ w,
-                               uint16_t* __restrict__ out, int T, int k, int H) {
+// One thread per (token t = blockIdx.x, 16-byte chunk c of H):
+// out[t] = bf16(sum_j bf16(y[t k + j] * w[t k + j])), the products rounded to
+// bf16 (the product of two bf16 arrays is a bf16 array) and summed in fp32
+// in j order.
+__global__ void __launch_bounds__(128) combine_kernel(const uint16_t* __restrict__ y,
+                                                      const uint16_t* __restrict__ w,
+                                                      uint16_t* __restrict__ out, int k, int H) {
+    pdl_trigger();
+    pdl_wait();
     const int chunks = H / 8;
-    const long total = (long)T * chunks;
-    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
-        const int t = (int)(i / chunks), c = (int)(i % chunks);
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int j = 0; j < k; ++j) {
-            const size_t f = (size_t)t * k + j;
-            const float wj = bf16_bits_to_f32(w[f]);
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(y + f * H) + c);
-            const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+    const int t = blockIdx.x, c = blockIdx.y * 128 + threadIdx.x;
+    if (c >= chunks) return;
+    const uint4* yt = reinterpret_cast<const uint4*>(y + (size_t)t * k * H) + c;
+    const uint16_t* wt = w + (size_t)t * k;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+    for (int j = 0; j < k; ++j) {
+        const float wj = bf16_bits_to_f32(__ldg(wt + j));
+        const uint4 v = __ldg(yt + (size_t)j * chunks);
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float lo = bf16_bits_to_f32(f32_to_bf16_bits(__fmul_rn(bf16_bits_to_f32(u[q] & 0xFFFFu), wj)));
-                const float hi = bf16_bits_to_f32(f32_to_bf16_bits(__fmul_rn(bf16_bits_to_f32(u[q] >> 16), wj)));
-                acc[2 * q] = __fadd_rn(acc[2 * q], lo);
-                acc[2 * q + 1] = __fadd_rn(acc[2 * q + 1], hi);
-            }
+        for (int q = 0; q < 4; ++q) {
+            const float lo = bf16_bits_to_f32(f32_to_bf16_bits(__fmul_rn(bf16_bits_to_f32(u[q] & 0xFFFFu), wj)));
+            const float hi = bf16_bits_to_f32(f32_to_bf16_bits(__fmul_rn(bf16_bits_to_f32(u[q] >> 16), wj)));
+            acc[2 * q] = __fadd_rn(acc[2 * q], lo);
+            acc[2 * q + 1] = __fadd_rn(acc[2 * q + 1], hi);
         }
-        uint4 o;
-        o.x = pack_bf16x2(acc[0], acc[1]);
-        o.y = pack_bf16x2(acc[2], acc[3]);
-        o.z = pack_bf16x2(acc[4], acc[5]);
-        o.w = pack_bf16x2(acc[6], acc[7]);
-        reinterpret_cast<uint4*>(out + (size_t)t * H)[c] = o;
     }
+    reinterpret_cast<uint4*>(out + (size_t)t * H)[c] =
+        make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                   pack_bf16x2(acc[6], acc[7]));
 }
 
 cudaError_t launch_combine(const uint16_t* y, const uint16_t* w, uint16_t* out, int T, int k, int H,
                            cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
-    const long total = (long)T * (H / 8);
-    const int threads = 256;
-    long blocks = (total + threads - 1) / threads;
-    if (blocks > 152 * 16) blocks = 152 * 16;
-    combine_kernel<<<(int)blocks, threads, 0, stream>>>(y, w, out, T, k, H);
-    return cudaGetLastError();
+    const dim3 grid((unsigned)T, (unsigned)((H / 8 + 127) / 128));
+    return launch_pdl(combine_kernel, grid, dim3(128), 0, stream, y, w, out, k, H);
 }
 
 int dispatch_error_word() {

@@ -125,6 +125,8 @@ __global__ void __launch_bounds__((4 + 4 * DQG + 4 * EPW) * 32, 1)
     constexpr int kAccChunks = NMAX / 16 / EPW;  // 16-column chunks one epilogue warp accumulates
     extern __shared__ __align__(1024) uint8_t dsmem[];
     __shared__ Smem sh;
+    pdl_trigger();
+    pdl_wait();
     // 1024-byte aligned carve-up: packed ring | B ring | 2 scale buffers.
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
     const int NP = a.wstages;
@@ -559,8 +561,8 @@ static cudaError_t launch_one(const CUtensorMap& wmap, const CUtensorMap& bmap, 
         if (err != cudaSuccess) return err;
         attr_set[dev] = true;
     }
-    grouped_gemm_kernel<MODE, NMAX, DQG, EPW><<<grid, (4 + 4 * DQG + 4 * EPW) * 32, smem, stream>>>(wmap, bmap, a);
-    return cudaGetLastError();
+    return launch_pdl(grouped_gemm_kernel<MODE, NMAX, DQG, EPW>, dim3(grid), dim3((4 + 4 * DQG + 4 * EPW) * 32),
+                      smem, stream, wmap, bmap, a);
 }
 
 cudaError_t launch_gemm(int mode, const CUtensorMap& wmap, const CUtensorMap& bmap, const GemmArgs& a, int grid,

@@ -119,6 +119,8 @@ __global__ void __launch_bounds__(kWarps * 32) router_kernel(const __grid_consta
     __shared__ uint64_t full, wfull, mdone;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag_s;
+    pdl_trigger();
+    pdl_wait();
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int H = a.H, E = a.E, k = a.k, TT = a.tt;
     RouterSmem sm;
@@ -387,8 +389,10 @@ cudaLaunchConfig_t router_config(int T, int tt, size_t smem, cudaStream_t stream
     attr[0].val.clusterDim.x = kCS;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cfg;
 }
 
@@ -402,7 +406,7 @@ int router_resident_clusters(size_t smem) {
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find({dev, smem});
     if (it != cache.end()) return it->second;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = router_config(kCS, 16, smem, nullptr, attr);
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, router_kernel, &cfg) != cudaSuccess || n < 1) n = 1;
@@ -432,7 +436,7 @@ cudaError_t launch_router(const CUtensorMap& wmap, const CUtensorMap& xmap, cons
     if (smem > kRouterSmemLimit || a.tt % 16 != 0 || a.tt > 64) return cudaErrorInvalidValue;
     cudaError_t err = ensure_router_attr();
     if (err != cudaSuccess) return err;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = router_config(a.T, a.tt, smem, stream, attr);
     return cudaLaunchKernelEx(&cfg, router_kernel, wmap, xmap, a);
 }
