@@ -77,28 +77,37 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
-// Bounded wait on an mbarrier phase. Spins briefly, then backs off with
-// short sleeps so that waiting warps leave most issue slots to the warps that
-// work. Returns false if the phase has not completed within ~2 s (then it
-// raises the device error word and the CTA's shared abort flag) or if another
-// warp of the CTA has already aborted, so a broken pipeline ends the kernel
-// instead of hanging the GPU. Callers treat false as "stop issuing work and
-// fall through to the exit path".
+// try_wait with a suspend-time hint: the warp sleeps in hardware until the
+// phase completes or about `ns` nanoseconds pass, issuing nothing meanwhile.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase. After one plain test, the warp sleeps
+// in hardware between tests (a waiting warp takes no issue slots from the
+// warps that work). Returns false if the phase has not completed within
+// ~2 s (then it raises the device error word and the CTA's shared abort
+// flag) or if another warp of the CTA has already aborted, so a broken
+// pipeline ends the kernel instead of hanging the GPU. Callers treat false
+// as "stop issuing work and fall through to the exit path".
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    for (uint32_t n = 0;; ++n) {
-        if (mbar_try_wait(bar, parity)) return true;
-        __nanosleep(32);
-        if ((n & 255u) == 255u) {
-            if (*abort_flag) return false;
-            if (global_timer_ns() - t0 > 2000000000ull) {
-                *abort_flag = 1;
-                atomicOr(&g_error_word, kErrTimeout);
-                return false;
-            }
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > 2000000000ull) {
+            *abort_flag = 1;
+            atomicOr(&g_error_word, kErrTimeout);
+            return false;
         }
     }
 }

@@ -11,26 +11,28 @@
 // Persistent kernel, one CTA per SM, work item = (token tile of one expert,
 // 128-row weight tile), K in stages of 256. Warp roles:
 //   warp 0        TMA producer of the packed weights (128 rows x 128 B per
-//                 stage, 128 B swizzle) into a deep ring that the dequant
-//                 warps release as soon as they have read a slot, and of the
-//                 item's scales and biases (bulk copies, double-buffered);
-//   warp 1        TMEM owner and MMA issuer (one thread);
+//                 stage, 128 B swizzle) into a ring of up to 8 stages, and of
+//                 the item's scales and biases (bulk copies, double-buffered);
+//   warp 1        TMEM owner and MMA issuer (one elected thread);
 //   warp 2        TMA producer of the B operand (the token tile, 16-row boxes)
 //                 into a ring that the MMA's completion releases; its slots
 //                 are sized at run time for the largest token tile of the
 //                 call, so small tiles get a deep ring;
-//   dequant warps thread = weight row = TMEM lane; DQG groups of four warps
-//                 split each stage's four 64-wide K atoms. A packed word holds
-//                 8 codes; the 0x4300 magic gives 128+q per bf16 half, minus
-//                 128 gives q exactly, and one fma.rn.bf16x2 with the group's
-//                 scale and bias gives bf16(S*q + B) with a single rounding.
-//                 The row's slice goes to a two-slot A ring in TMEM
-//                 (tcgen05.st); the MMA reads A from TMEM, B from shared memory.
-//   4 epilogue    each stage accumulates into a fresh TMEM region (256/NMAX
-//     warps       regions rotate); these warps add the stage partials in fp32
-//                 registers (short tensor-core accumulation chains keep the
-//                 result close to the exactly rounded one), then apply GeGLU
-//                 (gate_up) or scatter y to flat slots (down).
+//   warp 3        stage gate: waits for the B slot and (once per item) for a
+//                 free accumulator, then arrives on the A-slot barrier, so the
+//                 MMA issuer waits once per stage;
+//   dequant warps thread = weight row = TMEM lane, in two stage groups: group
+//                 p dequantises the stages g with g % 2 == p into A slot p of
+//                 TMEM (tcgen05.st), so one group's waits overlap the other's
+//                 arithmetic. A packed word holds 8 codes; the 0x4300 magic
+//                 gives 128+q per bf16 half, minus 128 gives q exactly, and
+//                 one fma.rn.bf16x2 with the group's scale and bias gives
+//                 bf16(S*q + B) with a single rounding. The MMA reads A from
+//                 TMEM and B from shared memory;
+//   epilogue      an item accumulates its whole K in one of two TMEM
+//     warps       accumulator buffers (fp32); once per item these warps read
+//                 it and apply GeGLU (gate_up) or scatter y to flat slots
+//                 (down) while the next item accumulates in the other buffer.
 // The dequantised pair order inside each 8-element K block is (0,4),(1,5),
 // (2,6),(3,7); the B operands (gathered x, GeGLU output) are stored in that
 // same K order, so the MMA sums the same products.
@@ -44,7 +46,7 @@ namespace {
 constexpr int kStageK = 256;
 constexpr int kPackedStageBytes = 128 * 128;  // 128 rows x 32 words
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kPCol0 = 256;              // partial-sum regions fill columns 256..511
+constexpr uint32_t kPCol0 = 256;              // two accumulator buffers of NMAX columns from column 256
 constexpr int kMaxPackedStages = 8;
 constexpr int kMaxBStages = 8;
 
@@ -52,7 +54,7 @@ struct Smem {
     uint64_t wfull[kMaxPackedStages], wempty[kMaxPackedStages];  // packed-weight ring
     uint64_t bfull[kMaxBStages], bempty[kMaxBStages];            // B-operand ring
     uint64_t afull[2], aempty[2];                                // A ring in TMEM
-    uint64_t dfull[16], dempty[16];                              // partial-sum regions in TMEM
+    uint64_t dfull[2], dempty[2];                                // accumulator buffers in TMEM
     uint64_t sfull[2], sempty[2];                                // scale/bias buffers
     uint32_t tmem_base;
     int abort_flag;
@@ -121,7 +123,6 @@ __global__ void __launch_bounds__((4 + 4 * DQG + 4 * EPW) * 32, 1)
     constexpr int kDqWarps = 4 * DQG;
     constexpr int kEpiWarp0 = 4 + kDqWarps;
     constexpr int kEpiWarps = 4 * EPW;
-    constexpr int kAtomsPerGroup = 4 / DQG;
     constexpr int kAccChunks = NMAX / 16 / EPW;  // 16-column chunks one epilogue warp accumulates
     extern __shared__ __align__(1024) uint8_t dsmem[];
     __shared__ Smem sh;
@@ -132,12 +133,10 @@ __global__ void __launch_bounds__((4 + 4 * DQG + 4 * EPW) * 32, 1)
     const int NP = a.wstages;
     // brows: the largest token tile's rows rounded up to a power of two
     // (16..NMAX). It sizes the B slots (4 atoms of brows x 128 B, each atom
-    // 1024-byte aligned) and the partial-sum regions (brows TMEM columns
-    // each, 256 / brows of them).
+    // 1024-byte aligned), so small tiles get a deep B ring.
     const int maxrows = a.num_tiles[1];
     int brows = 16;
     while (brows < maxrows && brows < NMAX) brows <<= 1;
-    const int nreg = 256 / brows;
     const int bslot_bytes = 4 * brows * 128;
     const int NB = min(kMaxBStages, a.bregion / bslot_bytes);
     uint8_t* wring = base;
@@ -167,7 +166,7 @@ __global__ void __launch_bounds__((4 + 4 * DQG + 4 * EPW) * 32, 1)
             mbar_init(&sh.sfull[i], 1);
             mbar_init(&sh.sempty[i], nst >= 2 ? kDqWarps : kDqWarps / 2);
         }
-        for (int i = 0; i < nreg; ++i) {
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&sh.dfull[i], 1);
             mbar_init(&sh.dempty[i], kEpiWarps);
         }
@@ -275,72 +274,70 @@ __global__ void __launch_bounds__((4 + 4 * DQG + 4 * EPW) * 32, 1)
     } else if (warp == 1) {
         // ---------------------------------------------------- MMA issuer --
         // The whole warp runs the loop; one elected lane issues the MMAs of a
-        // stage and the three commits (a commit tracks its own thread's MMAs).
+        // stage and the commits (a commit tracks its own thread's MMAs). An
+        // item accumulates its whole K into accumulator buffer li & 1.
         uint32_t gs = 0;
-        int bslot = 0, pr = 0;
+        int bslot = 0, li = 0;
         bool ok = true;
         Tile tl_next = {};
         if (blockIdx.x < num_items) tl_next = a.tiles[blockIdx.x / a.n_tiles];
         const uint32_t atom_step = (uint32_t)(brows * 128) >> 4;  // descriptor units (16 B)
-        for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x) {
+        for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x, ++li) {
             const Tile tl = tl_next;
             if (it + (int)gridDim.x < num_items) tl_next = a.tiles[(it + gridDim.x) / a.n_tiles];
             const uint32_t nrows16 = (uint32_t)((tl.rows + 15) & ~15);
             const uint32_t idesc = idesc_bf16_m128(nrows16);
+            const int db = li & 1;
+            const uint32_t dcol = tmem + kPCol0 + (uint32_t)(db * NMAX);
             for (int s = 0; s < nstages; ++s, ++gs) {
                 const int as = gs & 1;
                 // afull also carries the gate warp's arrival: the B slot is
-                // full and the partial region is free.
+                // full and (at an item's first stage) the accumulator is free.
                 if (!(ok = mbar_wait(&sh.afull[as], (gs >> 1) & 1, abort_flag))) break;
                 tc_fence_after();
                 const int nk = min(kStageK, K - s * kStageK) / 16;
                 const uint64_t bdesc0 = sw128_kmajor_desc(smem_u32(bring + (size_t)bslot * bslot_bytes));
-                const uint32_t pcol = tmem + kPCol0 + (uint32_t)(pr * brows);
                 const uint32_t acol = tmem + as * 128;
                 if (elect_one()) {
 #pragma unroll
                     for (int k16 = 0; k16 < 16; ++k16) {
                         if (k16 < nk) {
                             const uint64_t bdesc = bdesc0 + (uint64_t)((k16 >> 2) * atom_step + (k16 & 3) * 2);
-                            umma_ts(pcol, acol + k16 * 8, bdesc, idesc, k16 > 0 ? 1u : 0u);
+                            umma_ts(dcol, acol + k16 * 8, bdesc, idesc, (s > 0 || k16 > 0) ? 1u : 0u);
                         }
                     }
                     umma_commit(&sh.bempty[bslot]);
                     umma_commit(&sh.aempty[as]);
-                    umma_commit(&sh.dfull[pr]);
+                    if (s == nstages - 1) umma_commit(&sh.dfull[db]);
                 }
                 __syncwarp();
                 if (++bslot == NB) bslot = 0;
-                if (++pr == nreg) pr = 0;
             }
         }
     } else if (warp == 3) {
         // --------------------------------------------------- stage gate --
-        // Folds the MMA's other two conditions into the A-slot barrier, so
-        // the MMA issuer waits once per stage: for stage g this warp waits
-        // for the B slot to be full and the partial region to be free, and
-        // for the previous phase of afull[g & 1] (stage g - 2) to complete
-        // so that its arrival counts toward stage g.
-        uint32_t gs = 0, bph = 0, dph = 0;
-        int bslot = 0, pr = 0;
+        // Folds the MMA's other conditions into the A-slot barrier, so the
+        // MMA issuer waits once per stage: for stage g this warp waits for
+        // the B slot to be full, at an item's first stage for the item's
+        // accumulator buffer to be free, and for the previous phase of
+        // afull[g & 1] (stage g - 2) to complete so that its arrival counts
+        // toward stage g.
+        uint32_t gs = 0, bph = 0;
+        int bslot = 0;
         bool ok = true;
-        const uint32_t total = (blockIdx.x < num_items)
-                                   ? (uint32_t)((num_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1) * nstages
-                                   : 0u;
-        for (; gs < total && ok; ++gs) {
-            const int as = gs & 1;
-            if (gs >= 2 && !(ok = mbar_wait(&sh.afull[as], ((gs >> 1) - 1) & 1, abort_flag))) break;
-            if (!(ok = mbar_wait(&sh.bfull[bslot], bph, abort_flag))) break;
-            if (!(ok = mbar_wait(&sh.dempty[pr], dph ^ 1, abort_flag))) break;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.afull[as]);
-            if (++bslot == NB) {
-                bslot = 0;
-                bph ^= 1;
-            }
-            if (++pr == nreg) {
-                pr = 0;
-                dph ^= 1;
+        const int my_items = (blockIdx.x < num_items) ? (num_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+        for (int li = 0; li < my_items && ok; ++li) {
+            for (int s = 0; s < nstages; ++s, ++gs) {
+                const int as = gs & 1;
+                if (gs >= 2 && !(ok = mbar_wait(&sh.afull[as], ((gs >> 1) - 1) & 1, abort_flag))) break;
+                if (!(ok = mbar_wait(&sh.bfull[bslot], bph, abort_flag))) break;
+                if (s == 0 && li >= 2 && !(ok = mbar_wait(&sh.dempty[li & 1], ((li >> 1) - 1) & 1, abort_flag))) break;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.afull[as]);
+                if (++bslot == NB) {
+                    bslot = 0;
+                    bph ^= 1;
+                }
             }
         }
     } else if (warp >= 4 && warp < kEpiWarp0) {
@@ -381,9 +378,13 @@ __global__ void __launch_bounds__((4 + 4 * DQG + 4 * EPW) * 32, 1)
         uint4 c[2 * kAtomsPerWarp];
         uint32_t Sv[kAtomsPerWarp], Bv[kAtomsPerWarp];
         int atoms = 0;
-        // Reads the cursor's stage into c/Sv/Bv, releases its ring slot (and
-        // the item's scale buffer after this warp's last stage of the item),
-        // and moves the cursor to the group's next stage.
+        // The ring slot (and scale buffer) whose words c/Sv/Bv hold: released
+        // after the A-slot wait that follows the loads, by when they have
+        // landed in registers.
+        int held_slot = 0, held_sb = 0;
+        bool held_last = false;
+        // Issues the loads of the cursor's stage into c/Sv/Bv and moves the
+        // cursor to the group's next stage.
         auto fetch = [&]() -> bool {
             const int sb = f_li & 1;
             if (f_li != waited_li) {
@@ -406,14 +407,11 @@ __global__ void __launch_bounds__((4 + 4 * DQG + 4 * EPW) * 32, 1)
                 }
             }
             const int li = f_li;
-            const int slot = f_slot;
+            held_slot = f_slot;
+            held_sb = sb;
             step();
             step();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&sh.wempty[slot]);
-                if (f_li != li) mbar_arrive(&sh.sempty[sb]);  // this warp's last read of the item's scales
-            }
+            held_last = (f_li != li);  // this warp's last read of the item's scales
             return true;
         };
         bool ok = true;
@@ -422,6 +420,11 @@ __global__ void __launch_bounds__((4 + 4 * DQG + 4 * EPW) * 32, 1)
             const int as = dgrp;
             if (!(ok = mbar_wait(&sh.aempty[as], ((gs >> 1) & 1) ^ 1, abort_flag))) break;
             tc_fence_after();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&sh.wempty[held_slot]);
+                if (held_last) mbar_arrive(&sh.sempty[held_sb]);
+            }
 #pragma unroll
             for (int i = 0; i < kAtomsPerWarp; ++i) {
                 const int at = sub + i * kSub;
@@ -431,11 +434,13 @@ __global__ void __launch_bounds__((4 + 4 * DQG + 4 * EPW) * 32, 1)
                     tmem_st32(tmem + lane_addr + as * 128 + at * 32, r);
                 }
             }
-            if (gs + 2 < total && !(ok = fetch())) break;  // next stage's words while the stores drain
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.afull[as]);
+            // the group's next stage: its loads land while this warp waits
+            // for that stage's A slot
+            if (gs + 2 < total && !(ok = fetch())) break;
         }
         tmem_wait_st();
     } else if (warp >= kEpiWarp0) {
@@ -444,10 +449,9 @@ __global__ void __launch_bounds__((4 + 4 * DQG + 4 * EPW) * 32, 1)
         const int q = warp & 3;
         const int h = (warp - kEpiWarp0) >> 2;
         const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
-        uint32_t dph = 0;
-        int pr = 0;
         bool ok = true;
-        for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x) {
+        int li = 0;
+        for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x, ++li) {
             const Tile tl = a.tiles[it / a.n_tiles];
             const int j = it % a.n_tiles;
             const int nrows16 = (tl.rows + 15) & ~15;
@@ -456,31 +460,25 @@ __global__ void __launch_bounds__((4 + 4 * DQG + 4 * EPW) * 32, 1)
 #pragma unroll
                 for (int i = 0; i < NMAX / 32; ++i) pf[i] = (32 * i + lane < tl.rows) ? a.perm[tl.p0 + 32 * i + lane] : 0;
             }
+            // The item's accumulator (buffer li & 1) holds the whole K; read
+            // this warp's chunks, then hand the buffer back before the math.
+            const int db = li & 1;
+            if (!(ok = mbar_wait(&sh.dfull[db], (li >> 1) & 1, abort_flag))) break;
+            tc_fence_after();
+            const uint32_t dcol = tmem + lane_addr + kPCol0 + (uint32_t)(db * NMAX);
+            uint32_t raw[kAccChunks][16];
+#pragma unroll
+            for (int cl = 0; cl < kAccChunks; ++cl)
+                if ((cl * EPW + h) * 16 < nrows16) tmem_ld16(dcol + (cl * EPW + h) * 16, raw[cl]);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.dempty[db]);
             float acc[kAccChunks * 16];
 #pragma unroll
-            for (int c = 0; c < kAccChunks * 16; ++c) acc[c] = 0.f;
-            for (int s = 0; s < nstages; ++s) {
-                if (!(ok = mbar_wait(&sh.dfull[pr], dph, abort_flag))) break;
-                tc_fence_after();
-                const uint32_t pcol = tmem + lane_addr + kPCol0 + (uint32_t)(pr * brows);
+            for (int cl = 0; cl < kAccChunks; ++cl)
 #pragma unroll
-                for (int cl = 0; cl < kAccChunks; ++cl)
-                    if ((cl * EPW + h) * 16 < nrows16) {
-                        uint32_t v[16];
-                        tmem_ld16(pcol + (cl * EPW + h) * 16, v);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int jj = 0; jj < 16; ++jj)
-                            acc[cl * 16 + jj] = __fadd_rn(acc[cl * 16 + jj], __uint_as_float(v[jj]));
-                    }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sh.dempty[pr]);
-                if (++pr == nreg) {
-                    pr = 0;
-                    dph ^= 1;
-                }
-            }
+                for (int jj = 0; jj < 16; ++jj) acc[cl * 16 + jj] = __uint_as_float(raw[cl][jj]);
             if (!ok) break;
             if (MODE == kGateUp) {
                 // lanes 0-15: gate rows, lanes 16-31: up rows of the same n
@@ -536,14 +534,14 @@ size_t gemm_smem_bytes(int K, int wstages, int bregion) {
            2 * (size_t)scale_buf_bytes(K);
 }
 
-// Shared-memory split: a packed-weight ring of 5 or 6 stages, the rest for
-// the B ring (at least two slots of the largest possible token tile).
+// Shared-memory split: the deepest packed-weight ring (up to 8 stages) that
+// leaves the B ring at least two slots of the largest possible token tile;
+// the rest goes to the B ring.
 void gemm_stages(int K, int nmax, int* wstages, int* bregion) {
     const size_t limit = 232448 - 2048;  // 227 KB per CTA minus the static part
     const int min_b = 2 * 4 * nmax * 128;
-    int nw = 6;
+    int nw = kMaxPackedStages;
     while (nw > 2 && gemm_smem_bytes(K, nw, min_b) > limit) --nw;
-    if (nw > 5 && K > 1024) nw = 5;
     *wstages = nw;
     *bregion = (int)((limit - gemm_smem_bytes(K, nw, 0)) & ~size_t(1023));
 }
