@@ -91,18 +91,27 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
     return ok != 0;
 }
 
-// Bounded wait on an mbarrier phase. After one plain test, the warp sleeps
-// in hardware between tests (a waiting warp takes no issue slots from the
-// warps that work). Returns false if the phase has not completed within
-// ~2 s (then it raises the device error word and the CTA's shared abort
-// flag) or if another warp of the CTA has already aborted, so a broken
-// pipeline ends the kernel instead of hanging the GPU. Callers treat false
-// as "stop issuing work and fall through to the exit path".
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+// Bounded wait on an mbarrier phase. After one plain test the warp sleeps
+// between tests, so a waiting warp takes (almost) no issue slots from the
+// warps that work: with sleep_ns == 0 in hardware (try_wait with a suspend
+// hint: woken soon after the phase completes, for waits on the critical
+// path), otherwise for sleep_ns between tests (for warps with slack).
+// Returns false if the phase has not completed within ~2 s (then it raises
+// the device error word and the CTA's shared abort flag) or if another warp
+// of the CTA has already aborted, so a broken pipeline ends the kernel
+// instead of hanging the GPU. Callers treat false as "stop issuing work and
+// fall through to the exit path".
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          uint32_t sleep_ns = 0) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (;;) {
-        if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+        if (sleep_ns == 0) {
+            if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+        } else {
+            __nanosleep(sleep_ns);
+            if (mbar_try_wait(bar, parity)) return true;
+        }
         if (*abort_flag) return false;
         if (global_timer_ns() - t0 > 2000000000ull) {
             *abort_flag = 1;

@@ -46,14 +46,17 @@ namespace {
 constexpr int kStageK = 256;
 constexpr int kPackedStageBytes = 128 * 128;  // 128 rows x 32 words
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kPCol0 = 256;              // two accumulator buffers of NMAX columns from column 256
 constexpr int kMaxPackedStages = 8;
 constexpr int kMaxBStages = 8;
+constexpr int kMaxGroups = 3;  // dequant stage groups (A slots)
+// Sleep between tests for waits with slack (producers, gate, epilogue).
+constexpr uint32_t kSleepRing = 200;   // ns: producers and the stage gate
+constexpr uint32_t kSleepEpi = 1000;   // ns: the epilogue has a whole item of slack
 
 struct Smem {
     uint64_t wfull[kMaxPackedStages], wempty[kMaxPackedStages];  // packed-weight ring
     uint64_t bfull[kMaxBStages], bempty[kMaxBStages];            // B-operand ring
-    uint64_t afull[2], aempty[2];                                // A ring in TMEM
+    uint64_t afull[kMaxGroups], aempty[kMaxGroups];              // A slots in TMEM, one per stage group
     uint64_t dfull[2], dempty[2];                                // accumulator buffers in TMEM
     uint64_t sfull[2], sempty[2];                                // scale/bias buffers
     uint32_t tmem_base;
@@ -116,14 +119,19 @@ __device__ __forceinline__ void dequant_atom(const uint4 c0, const uint4 c1, uin
 
 }  // namespace
 
-template <int MODE, int NMAX, int DQG, int EPW>
-__global__ void __launch_bounds__((4 + 4 * DQG + 4 * EPW) * 32, 1)
+// NG stage groups of GW dequant warps (A slot g of TMEM for group g), EPW
+// epilogue warps per TMEM lane quarter.
+template <int MODE, int NMAX, int NG, int GW, int EPW>
+__global__ void __launch_bounds__((4 + NG * GW + 4 * EPW) * 32, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap bmap,
                         GemmArgs a) {
-    constexpr int kDqWarps = 4 * DQG;
+    constexpr int kDqWarps = NG * GW;
     constexpr int kEpiWarp0 = 4 + kDqWarps;
     constexpr int kEpiWarps = 4 * EPW;
-    constexpr int kAccChunks = NMAX / 16 / EPW;  // 16-column chunks one epilogue warp accumulates
+    constexpr int kAccChunks = NMAX / 16 / EPW;  // 16-column chunks of one epilogue warp
+    constexpr uint32_t kD0 = NG * 128;           // accumulator buffers after the A slots
+    static_assert(kD0 + 2 * NMAX <= kTmemCols, "TMEM columns");
+    static_assert(GW % 4 == 0 && NG <= kMaxGroups, "group shape");
     extern __shared__ __align__(1024) uint8_t dsmem[];
     __shared__ Smem sh;
     pdl_trigger();
@@ -151,20 +159,23 @@ __global__ void __launch_bounds__((4 + 4 * DQG + 4 * EPW) * 32, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < NP; ++s) {
             mbar_init(&sh.wfull[s], 1);
-            mbar_init(&sh.wempty[s], kDqWarps / 2);  // read by one stage group
+            mbar_init(&sh.wempty[s], GW);  // read by one stage group
         }
         for (int s = 0; s < NB; ++s) {
             mbar_init(&sh.bfull[s], 1);
             mbar_init(&sh.bempty[s], 1);
         }
-        // An item's scales are read by both stage groups when it has two
-        // or more K stages, by one group when it has a single stage.
+        // An item's scales are read by every stage group when it has NG or
+        // more K stages (the host only picks NG = 3 then), by one group when
+        // it has a single stage (NG = 2).
         const int nst = (a.K + kStageK - 1) / kStageK;
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&sh.afull[i], kDqWarps / 2 + 1);  // one stage group + the stage gate (warp 3)
+        for (int i = 0; i < NG; ++i) {
+            mbar_init(&sh.afull[i], GW + 1);  // one stage group + the stage gate (warp 3)
             mbar_init(&sh.aempty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&sh.sfull[i], 1);
-            mbar_init(&sh.sempty[i], nst >= 2 ? kDqWarps : kDqWarps / 2);
+            mbar_init(&sh.sempty[i], nst >= NG ? kDqWarps : GW);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sh.dfull[i], 1);
@@ -198,7 +209,7 @@ __global__ void __launch_bounds__((4 + 4 * DQG + 4 * EPW) * 32, 1)
             const Tile tl = a.tiles[it / a.n_tiles];
             const int j = it % a.n_tiles;
             const int sb = li & 1;
-            if (!(ok = mbar_wait(&sh.sempty[sb], ((li >> 1) & 1) ^ 1, abort_flag))) break;
+            if (!(ok = mbar_wait(&sh.sempty[sb], ((li >> 1) & 1) ^ 1, abort_flag, kSleepRing))) break;
             uint8_t* sbuf = scale_base + sb * sbuf_bytes;
             const uint32_t half = (uint32_t)(64 * G * 2);  // bytes of 64 rows
             if (elect_one()) {
@@ -218,7 +229,7 @@ __global__ void __launch_bounds__((4 + 4 * DQG + 4 * EPW) * 32, 1)
             }
             __syncwarp();
             for (int s = 0; s < nstages; ++s) {
-                if (!(ok = mbar_wait(&sh.wempty[slot], ph ^ 1, abort_flag))) break;
+                if (!(ok = mbar_wait(&sh.wempty[slot], ph ^ 1, abort_flag, kSleepRing))) break;
                 uint8_t* st = wring + (size_t)slot * kPackedStageBytes;
                 if (elect_one()) {
                     mbar_arrive_expect_tx(&sh.wfull[slot], kPackedStageBytes);
@@ -251,7 +262,7 @@ __global__ void __launch_bounds__((4 + 4 * DQG + 4 * EPW) * 32, 1)
             const Tile tl = a.tiles[it / a.n_tiles];
             const int nrows16 = (tl.rows + 15) & ~15;
             for (int s = 0; s < nstages; ++s) {
-                if (!(ok = mbar_wait(&sh.bempty[slot], ph ^ 1, abort_flag))) break;
+                if (!(ok = mbar_wait(&sh.bempty[slot], ph ^ 1, abort_flag, kSleepRing))) break;
                 uint8_t* bst = bring + (size_t)slot * bslot_bytes;
                 const int atoms = min(kStageK, K - s * kStageK) / 64;
                 if (elect_one()) {
@@ -276,8 +287,8 @@ __global__ void __launch_bounds__((4 + 4 * DQG + 4 * EPW) * 32, 1)
         // The whole warp runs the loop; one elected lane issues the MMAs of a
         // stage and the commits (a commit tracks its own thread's MMAs). An
         // item accumulates its whole K into accumulator buffer li & 1.
-        uint32_t gs = 0;
-        int bslot = 0, li = 0;
+        int bslot = 0, li = 0, as = 0;
+        uint32_t aph = 0;  // A slot of the stage and the phase of its barrier
         bool ok = true;
         Tile tl_next = {};
         if (blockIdx.x < num_items) tl_next = a.tiles[blockIdx.x / a.n_tiles];
@@ -288,12 +299,11 @@ __global__ void __launch_bounds__((4 + 4 * DQG + 4 * EPW) * 32, 1)
             const uint32_t nrows16 = (uint32_t)((tl.rows + 15) & ~15);
             const uint32_t idesc = idesc_bf16_m128(nrows16);
             const int db = li & 1;
-            const uint32_t dcol = tmem + kPCol0 + (uint32_t)(db * NMAX);
-            for (int s = 0; s < nstages; ++s, ++gs) {
-                const int as = gs & 1;
+            const uint32_t dcol = tmem + kD0 + (uint32_t)(db * NMAX);
+            for (int s = 0; s < nstages; ++s) {
                 // afull also carries the gate warp's arrival: the B slot is
                 // full and (at an item's first stage) the accumulator is free.
-                if (!(ok = mbar_wait(&sh.afull[as], (gs >> 1) & 1, abort_flag))) break;
+                if (!(ok = mbar_wait(&sh.afull[as], aph, abort_flag))) break;
                 tc_fence_after();
                 const int nk = min(kStageK, K - s * kStageK) / 16;
                 const uint64_t bdesc0 = sw128_kmajor_desc(smem_u32(bring + (size_t)bslot * bslot_bytes));
@@ -312,6 +322,10 @@ __global__ void __launch_bounds__((4 + 4 * DQG + 4 * EPW) * 32, 1)
                 }
                 __syncwarp();
                 if (++bslot == NB) bslot = 0;
+                if (++as == NG) {
+                    as = 0;
+                    aph ^= 1;
+                }
             }
         }
     } else if (warp == 3) {
@@ -322,34 +336,40 @@ __global__ void __launch_bounds__((4 + 4 * DQG + 4 * EPW) * 32, 1)
         // accumulator buffer to be free, and for the previous phase of
         // afull[g & 1] (stage g - 2) to complete so that its arrival counts
         // toward stage g.
-        uint32_t gs = 0, bph = 0;
-        int bslot = 0;
+        uint32_t gs = 0, bph = 0, aph = 0;
+        int bslot = 0, as = 0;
         bool ok = true;
         const int my_items = (blockIdx.x < num_items) ? (num_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
         for (int li = 0; li < my_items && ok; ++li) {
             for (int s = 0; s < nstages; ++s, ++gs) {
-                const int as = gs & 1;
-                if (gs >= 2 && !(ok = mbar_wait(&sh.afull[as], ((gs >> 1) - 1) & 1, abort_flag))) break;
-                if (!(ok = mbar_wait(&sh.bfull[bslot], bph, abort_flag))) break;
-                if (s == 0 && li >= 2 && !(ok = mbar_wait(&sh.dempty[li & 1], ((li >> 1) - 1) & 1, abort_flag))) break;
+                // previous phase of afull[as]: stage gs - NG
+                if (gs >= NG && !(ok = mbar_wait(&sh.afull[as], aph ^ 1, abort_flag, kSleepRing))) break;
+                if (!(ok = mbar_wait(&sh.bfull[bslot], bph, abort_flag, kSleepRing))) break;
+                if (s == 0 && li >= 2 &&
+                    !(ok = mbar_wait(&sh.dempty[li & 1], ((li >> 1) - 1) & 1, abort_flag, kSleepRing)))
+                    break;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sh.afull[as]);
                 if (++bslot == NB) {
                     bslot = 0;
                     bph ^= 1;
                 }
+                if (++as == NG) {
+                    as = 0;
+                    aph ^= 1;
+                }
             }
         }
     } else if (warp >= 4 && warp < kEpiWarp0) {
         // ------------------------------------------------------- dequant --
-        // Two stage groups of kDqWarps / 2 warps: group p dequantises the
-        // stages g with g % 2 == p into A slot p, so one group's waits and
-        // loads overlap the other group's arithmetic. Within a group, warp
-        // (q, sub) covers TMEM lanes 32q..32q+31 and the atoms sub, sub + 2
-        // (DQG / 2 == 2) or all four (DQG / 2 == 1) of its stages.
-        constexpr int kSub = DQG / 2;                // warps per lane quarter in a group
+        // NG stage groups of GW warps: group p dequantises the stages g with
+        // g % NG == p into A slot p, so one group's waits and loads overlap
+        // the other groups' arithmetic. Within a group, warp (q, sub) covers
+        // TMEM lanes 32q..32q+31 and the atoms sub, sub + kSub, ... of its
+        // stages.
+        constexpr int kSub = GW / 4;                 // warps per lane quarter in a group
         constexpr int kAtomsPerWarp = 4 / kSub;
-        const int dgrp = (warp - 4) / (4 * kSub);
+        const int dgrp = (warp - 4) / GW;
         const int sub = ((warp - 4) >> 2) % kSub;
         const int q = warp & 3;
         int row;  // row in the packed stage and the scale buffer
@@ -374,7 +394,7 @@ __global__ void __launch_bounds__((4 + 4 * DQG + 4 * EPW) * 32, 1)
                 ++f_li;
             }
         };
-        if (dgrp == 1) step();
+        for (int i = 0; i < dgrp; ++i) step();
         uint4 c[2 * kAtomsPerWarp];
         uint32_t Sv[kAtomsPerWarp], Bv[kAtomsPerWarp];
         int atoms = 0;
@@ -409,16 +429,16 @@ __global__ void __launch_bounds__((4 + 4 * DQG + 4 * EPW) * 32, 1)
             const int li = f_li;
             held_slot = f_slot;
             held_sb = sb;
-            step();
-            step();
+            for (int i = 0; i < NG; ++i) step();
             held_last = (f_li != li);  // this warp's last read of the item's scales
             return true;
         };
         bool ok = true;
         if ((uint32_t)dgrp < total) ok = fetch();
-        for (uint32_t gs = dgrp; gs < total && ok; gs += 2) {
+        uint32_t aph = 0;  // phase of this group's A slot
+        for (uint32_t gs = dgrp; gs < total && ok; gs += NG, aph ^= 1) {
             const int as = dgrp;
-            if (!(ok = mbar_wait(&sh.aempty[as], ((gs >> 1) & 1) ^ 1, abort_flag))) break;
+            if (!(ok = mbar_wait(&sh.aempty[as], aph ^ 1, abort_flag))) break;
             tc_fence_after();
             __syncwarp();
             if (lane == 0) {
@@ -440,7 +460,7 @@ __global__ void __launch_bounds__((4 + 4 * DQG + 4 * EPW) * 32, 1)
             if (lane == 0) mbar_arrive(&sh.afull[as]);
             // the group's next stage: its loads land while this warp waits
             // for that stage's A slot
-            if (gs + 2 < total && !(ok = fetch())) break;
+            if (gs + NG < total && !(ok = fetch())) break;
         }
         tmem_wait_st();
     } else if (warp >= kEpiWarp0) {
@@ -460,63 +480,51 @@ __global__ void __launch_bounds__((4 + 4 * DQG + 4 * EPW) * 32, 1)
 #pragma unroll
                 for (int i = 0; i < NMAX / 32; ++i) pf[i] = (32 * i + lane < tl.rows) ? a.perm[tl.p0 + 32 * i + lane] : 0;
             }
-            // The item's accumulator (buffer li & 1) holds the whole K; read
-            // this warp's chunks, then hand the buffer back before the math.
+            // The item's accumulator (buffer li & 1) holds the whole K: this
+            // warp reads its 16-column chunks one at a time, then hands the
+            // buffer back (it is not needed again before item li + 2).
             const int db = li & 1;
-            if (!(ok = mbar_wait(&sh.dfull[db], (li >> 1) & 1, abort_flag))) break;
+            if (!(ok = mbar_wait(&sh.dfull[db], (li >> 1) & 1, abort_flag, kSleepEpi))) break;
             tc_fence_after();
-            const uint32_t dcol = tmem + lane_addr + kPCol0 + (uint32_t)(db * NMAX);
-            uint32_t raw[kAccChunks][16];
+            const uint32_t dcol = tmem + lane_addr + kD0 + (uint32_t)(db * NMAX);
 #pragma unroll
-            for (int cl = 0; cl < kAccChunks; ++cl)
-                if ((cl * EPW + h) * 16 < nrows16) tmem_ld16(dcol + (cl * EPW + h) * 16, raw[cl]);
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.dempty[db]);
-            float acc[kAccChunks * 16];
+            for (int cl = 0; cl < kAccChunks; ++cl) {
+                const int c0 = (cl * EPW + h) * 16;
+                if (c0 >= nrows16) continue;  // warp-uniform
+                uint32_t raw[16];
+                tmem_ld16(dcol + c0, raw);
+                tmem_wait_ld();
+                float v[16];
 #pragma unroll
-            for (int cl = 0; cl < kAccChunks; ++cl)
+                for (int jj = 0; jj < 16; ++jj) v[jj] = __uint_as_float(raw[jj]);
+                if (MODE == kGateUp) {
+                    // lanes 0-15: gate rows, lanes 16-31: up rows of the same n
+                    const int pos = interleaved_pos(64 * j + 16 * q + (lane & 15));
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) acc[cl * 16 + jj] = __uint_as_float(raw[cl][jj]);
-            if (!ok) break;
-            if (MODE == kGateUp) {
-                // lanes 0-15: gate rows, lanes 16-31: up rows of the same n
-                const int n = 64 * j + 16 * q + (lane & 15);
-                const int pos = interleaved_pos(n);
-#pragma unroll
-                for (int cl = 0; cl < kAccChunks; ++cl) {
-                    const int c0 = (cl * EPW + h) * 16;
-                    if (c0 < nrows16) {
-#pragma unroll
-                        for (int jj = 0; jj < 16; jj += 2) {
-                            const float send = (lane < 16) ? acc[cl * 16 + jj + 1] : acc[cl * 16 + jj];
-                            const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
-                            const int tok = c0 + jj + (lane < 16 ? 0 : 1);
-                            const float gf = lane < 16 ? acc[cl * 16 + jj] : recv;
-                            const float uf = lane < 16 ? recv : acc[cl * 16 + jj + 1];
-                            const float gb = bf16_bits_to_f32(f32_to_bf16_bits(gf));  // z is a bf16 tensor
-                            const float ub = bf16_bits_to_f32(f32_to_bf16_bits(uf));
-                            if (tok < tl.rows)
-                                a.out[(size_t)(tl.p0 + tok) * a.out_ld + pos] = (uint16_t)geglu_bf16(gb, ub);
-                        }
+                    for (int jj = 0; jj < 16; jj += 2) {
+                        const float send = (lane < 16) ? v[jj + 1] : v[jj];
+                        const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+                        const int tok = c0 + jj + (lane < 16 ? 0 : 1);
+                        const float gf = lane < 16 ? v[jj] : recv;
+                        const float uf = lane < 16 ? recv : v[jj + 1];
+                        const float gb = bf16_bits_to_f32(f32_to_bf16_bits(gf));  // z is a bf16 tensor
+                        const float ub = bf16_bits_to_f32(f32_to_bf16_bits(uf));
+                        if (tok < tl.rows)
+                            a.out[(size_t)(tl.p0 + tok) * a.out_ld + pos] = (uint16_t)geglu_bf16(gb, ub);
                     }
-                }
-            } else {
-                const int hrow = 128 * j + 32 * q + lane;
+                } else {
+                    const int hrow = 128 * j + 32 * q + lane;
 #pragma unroll
-                for (int cl = 0; cl < kAccChunks; ++cl) {
-                    const int c0 = (cl * EPW + h) * 16;
-                    if (c0 < nrows16) {
-#pragma unroll
-                        for (int jj = 0; jj < 16; ++jj) {
-                            const int tok = c0 + jj;
-                            const int f = __shfl_sync(0xffffffffu, pf[tok >> 5], tok & 31);
-                            if (tok < tl.rows) a.out[(size_t)f * a.out_ld + hrow] = (uint16_t)f32_to_bf16_bits(acc[cl * 16 + jj]);
-                        }
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int tok = c0 + jj;
+                        const int f = __shfl_sync(0xffffffffu, pf[tok >> 5], tok & 31);
+                        if (tok < tl.rows) a.out[(size_t)f * a.out_ld + hrow] = (uint16_t)f32_to_bf16_bits(v[jj]);
                     }
                 }
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.dempty[db]);
         }
     }
 
@@ -546,7 +554,7 @@ void gemm_stages(int K, int nmax, int* wstages, int* bregion) {
     *bregion = (int)((limit - gemm_smem_bytes(K, nw, 0)) & ~size_t(1023));
 }
 
-template <int MODE, int NMAX, int DQG, int EPW>
+template <int MODE, int NMAX, int NG, int GW, int EPW>
 static cudaError_t launch_one(const CUtensorMap& wmap, const CUtensorMap& bmap, const GemmArgs& a, int grid,
                               size_t smem, cudaStream_t stream) {
     static bool attr_set[64] = {};
@@ -554,25 +562,35 @@ static cudaError_t launch_one(const CUtensorMap& wmap, const CUtensorMap& bmap, 
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, NMAX, DQG, EPW>,
+        cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, NMAX, NG, GW, EPW>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, 232448 - 2048);
         if (err != cudaSuccess) return err;
         attr_set[dev] = true;
     }
-    return launch_pdl(grouped_gemm_kernel<MODE, NMAX, DQG, EPW>, dim3(grid), dim3((4 + 4 * DQG + 4 * EPW) * 32),
+    return launch_pdl(grouped_gemm_kernel<MODE, NMAX, NG, GW, EPW>, dim3(grid), dim3((4 + NG * GW + 4 * EPW) * 32),
                       smem, stream, wmap, bmap, a);
+}
+
+template <int MODE>
+static cudaError_t launch_mode(const CUtensorMap& wmap, const CUtensorMap& bmap, const GemmArgs& a, int grid,
+                               size_t smem, cudaStream_t stream) {
+    const int nstages = (a.K + kStageK - 1) / kStageK;
+    if (a.nmax == 64) {
+        // two stage groups of 8 dequant warps + 8 epilogue warps (28 warps);
+        // three groups (32 warps, 64 registers a thread) measured slower
+        (void)nstages;
+        return launch_one<MODE, 64, 2, 8, 2>(wmap, bmap, a, grid, smem, stream);
+    }
+    if (a.nmax == 128)  // two groups of 4 dequant warps, 16 epilogue warps (28 warps)
+        return launch_one<MODE, 128, 2, 4, 4>(wmap, bmap, a, grid, smem, stream);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_gemm(int mode, const CUtensorMap& wmap, const CUtensorMap& bmap, const GemmArgs& a, int grid,
                         cudaStream_t stream) {
     const size_t smem = gemm_smem_bytes(a.K, a.wstages, a.bregion);
-    if (a.nmax == 64)  // 16 dequant warps (one atom each per stage), 8 epilogue warps: 28 warps
-        return mode == kGateUp ? launch_one<kGateUp, 64, 4, 2>(wmap, bmap, a, grid, smem, stream)
-                               : launch_one<kDown, 64, 4, 2>(wmap, bmap, a, grid, smem, stream);
-    if (a.nmax == 128)  // 8 dequant warps, 16 epilogue warps of 32 columns: 28 warps
-        return mode == kGateUp ? launch_one<kGateUp, 128, 2, 4>(wmap, bmap, a, grid, smem, stream)
-                               : launch_one<kDown, 128, 2, 4>(wmap, bmap, a, grid, smem, stream);
-    return cudaErrorInvalidValue;
+    return mode == kGateUp ? launch_mode<kGateUp>(wmap, bmap, a, grid, smem, stream)
+                           : launch_mode<kDown>(wmap, bmap, a, grid, smem, stream);
 }
 
 int gemm_error_word() {
