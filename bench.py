@@ -223,6 +223,30 @@ def traffic_from_profile(name: str, src_hash: str):
     return e.get("dram_bytes_per_launch")
 
 
+# ---------------------------------------------------------------- replicas --
+# The layer shards by tokens with no exchange: N GPUs run N independent
+# replicas (weak scaling), each on its own seeded batch of the same workload.
+def replica_layer(wl, rank: int):
+    """Rank r's batch: the workload's generator with seed + r."""
+    return ms.make_layer(wl, seed=wl.seed + rank)
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The slowest rank's time (all ranks block until every rank has it)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(tokens_per_rank: int, world: int, seconds: float) -> float:
+    """Tokens/s of the whole job: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank / seconds
+
+
 def run_ours(args, wl):
     import torch
     import torch.distributed as dist
@@ -240,7 +264,7 @@ def run_ours(args, wl):
     moe.load()
     peaks = load_peaks()
 
-    inp = ms.make_layer(wl, seed=wl.seed + rank)  # each replica its own batch
+    inp = replica_layer(wl, rank)
     d = moe.dims_of(inp.dims)
     layer = moe.to_device_layer(inp)
     x = torch.from_numpy(inp.x.view(np.int16).copy()).cuda()
@@ -294,11 +318,7 @@ def run_ours(args, wl):
     moe.timing_enable(False)
     err = moe.device_error()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms_step = statistics.mean(step_ms)
-    if world > 1:
-        t = torch.tensor([ms_step], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(statistics.mean(step_ms), world, "cuda")
 
     # end to end through the host-buffer call (x in, out back, copies inside)
     x_host = torch.from_numpy(inp.x.view(np.int16).copy()).pin_memory()
@@ -312,11 +332,7 @@ def run_ours(args, wl):
                                layer.down, out_host, ws, ws.numel(), stream)
         if i >= args.warmup:
             e2e_ms.append(1e3 * (time.perf_counter() - t0))
-    e2e_step = statistics.mean(e2e_ms)
-    if world > 1:
-        t = torch.tensor([e2e_step], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_step = float(t.item())
+    e2e_step = max_over_ranks(statistics.mean(e2e_ms), world, "cuda")
 
     if rank != 0:
         if world > 1:
@@ -329,7 +345,7 @@ def run_ours(args, wl):
     with open(os.path.join(ROOT, "bit_quantized_moe_layer_gb300", "csrc", "grouped_gemm.cu"), "rb") as fh:
         src_hash = hashlib.sha1(fh.read()).hexdigest()
     model = roofline_model(inp.dims, touched, peaks)
-    value = world * d.T / (ms_step * 1e-3)
+    value = whole_job_rate(d.T, world, ms_step * 1e-3)
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -352,7 +368,7 @@ def run_ours(args, wl):
                             frac=model["t_roof_s"] / (ms_step * 1e-3), bytes=model["bytes"], flops=model["flops"]),
         stages_ms_per_call={k: v / max(1, calls) for k, v in stage_ms.items()},
         cpu_baseline=cpu,
-        e2e=dict(value=world * d.T / (e2e_step * 1e-3), unit="tokens/s", h2d_bytes_per_step=d.T * d.H * 2,
+        e2e=dict(value=whole_job_rate(d.T, world, e2e_step * 1e-3), unit="tokens/s", h2d_bytes_per_step=d.T * d.H * 2,
                  d2h_bytes_per_step=d.T * d.H * 2, ms_per_step=e2e_step),
         gpu_launches=moe.launches_per_forward() * args.steps,
         clocks=clk.summary(),
