@@ -517,7 +517,10 @@ __global__ void __launch_bounds__((4 + NG * GW + 4 * EPW) * 32, 1)
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) {
                         const int tok = c0 + jj;
-                        const int f = __shfl_sync(0xffffffffu, pf[tok >> 5], tok & 31);
+                        int src = pf[0];  // select, not an indexed load: pf stays in registers
+#pragma unroll
+                        for (int i = 1; i < NMAX / 32; ++i) src = ((tok >> 5) == i) ? pf[i] : src;
+                        const int f = __shfl_sync(0xffffffffu, src, tok & 31);
                         if (tok < tl.rows) a.out[(size_t)f * a.out_ld + hrow] = (uint16_t)f32_to_bf16_bits(v[jj]);
                     }
                 }
@@ -576,10 +579,11 @@ static cudaError_t launch_mode(const CUtensorMap& wmap, const CUtensorMap& bmap,
                                size_t smem, cudaStream_t stream) {
     const int nstages = (a.K + kStageK - 1) / kStageK;
     if (a.nmax == 64) {
-        // two stage groups of 8 dequant warps + 8 epilogue warps (28 warps);
+        // two stage groups of 8 dequant warps + 4 epilogue warps (24 warps,
+        // up to 85 registers a thread: the dequantisation does not spill);
         // three groups (32 warps, 64 registers a thread) measured slower
         (void)nstages;
-        return launch_one<MODE, 64, 2, 8, 2>(wmap, bmap, a, grid, smem, stream);
+        return launch_one<MODE, 64, 2, 8, 1>(wmap, bmap, a, grid, smem, stream);
     }
     if (a.nmax == 128)  // two groups of 4 dequant warps, 16 epilogue warps (28 warps)
         return launch_one<MODE, 128, 2, 4, 4>(wmap, bmap, a, grid, smem, stream);
