@@ -105,18 +105,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
                                           uint32_t sleep_ns = 0) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    for (;;) {
+    for (uint32_t n = 1;; ++n) {
         if (sleep_ns == 0) {
             if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
         } else {
             __nanosleep(sleep_ns);
             if (mbar_try_wait(bar, parity)) return true;
         }
-        if (*abort_flag) return false;
-        if (global_timer_ns() - t0 > 2000000000ull) {
-            *abort_flag = 1;
-            atomicOr(&g_error_word, kErrTimeout);
-            return false;
+        if ((n & 15u) == 0) {  // the abort flag and the clock, every 16th test
+            if (*abort_flag) return false;
+            if (global_timer_ns() - t0 > 2000000000ull) {
+                *abort_flag = 1;
+                atomicOr(&g_error_word, kErrTimeout);
+                return false;
+            }
         }
     }
 }

@@ -398,6 +398,16 @@ __global__ void __launch_bounds__((4 + NG * GW + 4 * EPW) * 32, 1)
         uint4 c[2 * kAtomsPerWarp];
         uint32_t Sv[kAtomsPerWarp], Bv[kAtomsPerWarp];
         int atoms = 0;
+        // Per-thread constants: the swizzled offsets of this warp's atoms in
+        // its 128-byte row of a packed stage, and the TMEM column of each.
+        uint32_t woff[2 * kAtomsPerWarp];
+#pragma unroll
+        for (int i = 0; i < kAtomsPerWarp; ++i) {
+            const int at = sub + i * kSub;
+            woff[2 * i] = (uint32_t)row * 128u + ((uint32_t)((2 * at) ^ (row & 7)) << 4);
+            woff[2 * i + 1] = (uint32_t)row * 128u + ((uint32_t)((2 * at + 1) ^ (row & 7)) << 4);
+        }
+        const uint16_t* srow = reinterpret_cast<const uint16_t*>(scale_base) + row * G;  // buffer 0
         // The ring slot (and scale buffer) whose words c/Sv/Bv hold: released
         // after the A-slot wait that follows the loads, by when they have
         // landed in registers.
@@ -412,18 +422,18 @@ __global__ void __launch_bounds__((4 + NG * GW + 4 * EPW) * 32, 1)
                 waited_li = f_li;
             }
             if (!mbar_wait(&sh.wfull[f_slot], f_ph, abort_flag)) return false;
-            const uint16_t* sS = reinterpret_cast<const uint16_t*>(scale_base + sb * sbuf_bytes) + row * G;
+            const uint16_t* sS = srow + (sb * sbuf_bytes) / 2 + f_s * 4;
             const uint16_t* sB = sS + 128 * G;
-            const uint8_t* pst = wring + (size_t)f_slot * kPackedStageBytes + row * 128;
+            const uint8_t* pst = wring + (size_t)f_slot * kPackedStageBytes;
             atoms = min(kStageK, K - f_s * kStageK) / 64;
 #pragma unroll
             for (int i = 0; i < kAtomsPerWarp; ++i) {
                 const int at = sub + i * kSub;
                 if (at < atoms) {
-                    c[2 * i] = *reinterpret_cast<const uint4*>(pst + (((2 * at) ^ (row & 7)) << 4));
-                    c[2 * i + 1] = *reinterpret_cast<const uint4*>(pst + (((2 * at + 1) ^ (row & 7)) << 4));
-                    Sv[i] = sS[f_s * 4 + at];
-                    Bv[i] = sB[f_s * 4 + at];
+                    c[2 * i] = *reinterpret_cast<const uint4*>(pst + woff[2 * i]);
+                    c[2 * i + 1] = *reinterpret_cast<const uint4*>(pst + woff[2 * i + 1]);
+                    Sv[i] = sS[at];
+                    Bv[i] = sB[at];
                 }
             }
             const int li = f_li;
