@@ -370,7 +370,7 @@ def run_ours(args, wl):
         cpu_baseline=cpu,
         e2e=dict(value=whole_job_rate(d.T, world, e2e_step * 1e-3), unit="tokens/s", h2d_bytes_per_step=d.T * d.H * 2,
                  d2h_bytes_per_step=d.T * d.H * 2, ms_per_step=e2e_step),
-        gpu_launches=moe.launches_per_forward() * args.steps,
+        gpu_launches=moe.launches_per_forward(d) * args.steps,
         clocks=clk.summary(),
         device_error=err,
     )

@@ -74,7 +74,7 @@ def load(path: str = LIB_PATH):
     lib.moe_forward_hostio.argtypes = [D, P, P, P, P, Q, Q, P, P, Z, P]
     lib.moe_timing_enable.argtypes = [I]
     lib.moe_timing_read.argtypes = [ctypes.POINTER(ctypes.c_float), I, ctypes.POINTER(I)]
-    lib.moe_launches_per_forward.argtypes = []
+    lib.moe_launches_per_forward.argtypes = [ctypes.c_void_p]
     lib.moe_device_error.argtypes = []
     for fn in ("moe_route", "moe_dispatch", "moe_experts", "moe_experts_noalloc", "moe_forward", "moe_forward_hostio",
                "moe_timing_enable", "moe_timing_read", "moe_launches_per_forward", "moe_device_error"):
@@ -175,8 +175,8 @@ def timing_read() -> tuple[dict, int]:
     return {s: float(ms[i]) for i, s in enumerate(STAGES)}, calls.value
 
 
-def launches_per_forward() -> int:
-    return int(load().moe_launches_per_forward())
+def launches_per_forward(d: "Dims") -> int:
+    return int(load().moe_launches_per_forward(ctypes.byref(d)))
 
 
 def device_error() -> int:

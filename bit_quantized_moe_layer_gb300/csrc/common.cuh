@@ -19,6 +19,8 @@ static __device__ int g_error_word;
 
 constexpr int kErrTimeout = 1;
 constexpr int kErrBadExpert = 2;
+// Bits 8..15 of the error word: which wait timed out first (0: none).
+constexpr int kErrWhereShift = 8;
 
 // ------------------------------------------------------------------- bf16 --
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
@@ -102,7 +104,7 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 // instead of hanging the GPU. Callers treat false as "stop issuing work and
 // fall through to the exit path".
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          uint32_t sleep_ns = 0) {
+                                          uint32_t sleep_ns = 0, int where = 0) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t n = 1;; ++n) {
@@ -117,8 +119,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
             if (global_timer_ns() - t0 > 2000000000ull) {
                 *abort_flag = 1;
                 atomicOr(&g_error_word, kErrTimeout);
+                atomicCAS(&g_error_word, kErrTimeout, kErrTimeout | ((where & 0xFF) << kErrWhereShift));
                 return false;
             }
+        }
+    }
+}
+
+// Exit-path wait for this CTA's own asynchronous work (TMA copies into its
+// shared memory, MMAs into its TMEM) to finish before the CTA releases that
+// memory or exits. It ignores the abort flag (the work completes on its own
+// once issued) and gives up after ~200 ms.
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return;
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        __nanosleep(1000);
+        if (global_timer_ns() - t0 > 200000000ull) {
+            atomicOr(&g_error_word, kErrTimeout);
+            return;
         }
     }
 }

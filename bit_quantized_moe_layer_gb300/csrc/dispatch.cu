@@ -13,61 +13,59 @@ namespace moe {
 
 namespace {
 constexpr int kDispatchThreads = 1024;
+constexpr int kW = kDispatchThreads / 32;
 constexpr int kMaxE = 256;
-}  // namespace
 
-// One CTA of 32 warps; warp w owns the contiguous slot range
-// [w*per, (w+1)*per). Pass 1: per-warp histograms (warp match-any, one add
-// per group of equal ids). Then per expert an exclusive scan over warps, a
-// scan over experts (offsets and token-tile bases) and the tile list. Pass 2:
-// each warp walks its range again in slot order and places each slot at its
-// warp's running base for that expert plus its rank among equal ids in the
-// 32-slot group. Warps cover the slots in order, so the sort is stable and
-// the result unique.
-__global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs a) {
-    constexpr int kW = kDispatchThreads / 32;
-    __shared__ int wh[kW][kMaxE + 1];
-    __shared__ int cnt[kMaxE], off[kMaxE + 1], tbase[kMaxE + 1];
-    pdl_trigger();
-    pdl_wait();
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int S = a.S, E = a.E;
+struct DispatchSmem {
+    int wh[kW][kMaxE + 1];  // per-warp counts, then per-warp bases
+    int cnt[kMaxE], off[kMaxE + 1], tbase[kMaxE + 1];
+};
+
+// Counts of the slots [c0, c1) by expert into wh_row (warp match-any: one add
+// per group of equal ids). Out-of-range ids are dropped (and flagged once).
+__device__ __forceinline__ void warp_histogram(const int32_t* idx, int c0, int c1, int E, int* wh_row, int lane,
+                                               bool flag) {
     const unsigned lt_mask = (1u << lane) - 1u;
-    for (int i = tid; i < kW * (kMaxE + 1); i += kDispatchThreads) (&wh[0][0])[i] = 0;
-    __syncthreads();
-    const int per = (S + kW - 1) / kW;
-    const int c0 = min(S, warp * per), c1 = min(S, c0 + per);
     for (int b = c0; b < c1; b += 32) {
         const int f = b + lane;
-        int e = (f < c1) ? a.idx[f] : -1;
+        int e = (f < c1) ? idx[f] : -1;
         if (f < c1 && (e < 0 || e >= E)) {
-            atomicOr(&g_error_word, kErrBadExpert);
+            if (flag) atomicOr(&g_error_word, kErrBadExpert);
             e = -1;
         }
         const unsigned peers = __match_any_sync(0xffffffffu, e);
-        if (e >= 0 && (peers & lt_mask) == 0) wh[warp][e] += __popc(peers);
+        if (e >= 0 && (peers & lt_mask) == 0) wh_row[e] += __popc(peers);
     }
-    __syncthreads();
-    // Per expert, exclusive scan over the 32 warps' counts: warp ww scans the
-    // columns of experts ww, ww + 32, ..., lane = source warp.
+}
+
+// Per expert, exclusive scan of the 32 warps' counts in place (warp ww scans
+// experts ww, ww + 32, ..., lane = source warp); totals to cnt (if not null).
+__device__ __forceinline__ void scan_over_warps(DispatchSmem& sm, int* cnt, int E, int warp, int lane) {
     for (int e = warp; e < E; e += kW) {
-        const int v = wh[lane][e];
+        const int v = sm.wh[lane][e];
         int inc = v;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int u = __shfl_up_sync(0xffffffffu, inc, o);
             if (lane >= o) inc += u;
         }
-        wh[lane][e] = inc - v;
-        if (lane == 31) cnt[e] = inc;
+        sm.wh[lane][e] = inc - v;
+        if (cnt && lane == 31) cnt[e] = inc;
     }
-    __syncthreads();
-    if (warp == 0) {  // scan over experts: lane owns experts [8 lane, 8 lane + 8)
+}
+
+// From the per-expert totals in sm.cnt: offsets and token-tile bases (scan
+// over experts by warp 0), then offsets, the tile list and (tile count, rows
+// of the largest tile) to global memory. Every thread of the CTA calls it.
+__device__ __forceinline__ void finish_experts(const DispatchArgs& a, DispatchSmem& sm, int tid, int warp,
+                                               int lane) {
+    const int E = a.E;
+    if (warp == 0) {  // lane owns experts [8 lane, 8 lane + 8)
         int lc[8], lt[8], sc = 0, st = 0;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const int e = lane * 8 + j;
-            lc[j] = (e < E) ? cnt[e] : 0;
+            lc[j] = (e < E) ? sm.cnt[e] : 0;
             lt[j] = (lc[j] + a.nmax - 1) / a.nmax;
             sc += lc[j];
             st += lt[j];
@@ -86,61 +84,171 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
         for (int j = 0; j < 8; ++j) {
             const int e = lane * 8 + j;
             if (e < E) {
-                off[e] = rc;
-                tbase[e] = rt;
+                sm.off[e] = rc;
+                sm.tbase[e] = rt;
             }
             rc += lc[j];
             rt += lt[j];
         }
         if (lane == 31) {
-            off[E] = ic;
-            tbase[E] = it;
+            sm.off[E] = ic;
+            sm.tbase[E] = it;
         }
     }
     __syncthreads();
-    for (int e = tid; e <= E; e += kDispatchThreads) a.offsets[e] = off[e];
+    for (int e = tid; e <= E; e += blockDim.x) a.offsets[e] = sm.off[e];
     if (a.tiles) {
-        for (int e = tid; e < E; e += kDispatchThreads) {
-            for (int i = 0; tbase[e] + i < tbase[e + 1]; ++i) {
+        for (int e = tid; e < E; e += blockDim.x) {
+            for (int i = 0; sm.tbase[e] + i < sm.tbase[e + 1]; ++i) {
                 Tile t;
                 t.e = e;
-                t.p0 = off[e] + i * a.nmax;
-                t.rows = min(a.nmax, cnt[e] - i * a.nmax);
+                t.p0 = sm.off[e] + i * a.nmax;
+                t.rows = min(a.nmax, sm.cnt[e] - i * a.nmax);
                 t.pad = 0;
-                a.tiles[tbase[e] + i] = t;
+                a.tiles[sm.tbase[e] + i] = t;
             }
         }
         if (warp == 0 && a.num_tiles) {
             int mx = 0;
-            for (int e = lane; e < E; e += 32) mx = max(mx, min(cnt[e], a.nmax));
+            for (int e = lane; e < E; e += 32) mx = max(mx, min(sm.cnt[e], a.nmax));
             mx = __reduce_max_sync(0xffffffffu, mx);
             if (lane == 0) {
-                a.num_tiles[0] = tbase[E];
-                a.num_tiles[1] = mx;  // rows of the largest token tile
+                a.num_tiles[0] = sm.tbase[E];
+                a.num_tiles[1] = mx;
             }
         }
     }
-    for (int i = tid; i < kW * E; i += kDispatchThreads) wh[i / E][i % E] += off[i % E];
-    __syncthreads();
+}
+
+// Stable scatter of the slots [c0, c1) in slot order: slot f with expert e
+// goes to the warp's running base for e plus its rank among equal ids in its
+// 32-slot group.
+__device__ __forceinline__ void warp_scatter(const DispatchArgs& a, int c0, int c1, int* wh_row, int lane) {
+    const unsigned lt_mask = (1u << lane) - 1u;
     for (int b = c0; b < c1; b += 32) {
         const int f = b + lane;
         int e = (f < c1) ? a.idx[f] : -1;
-        if (e >= E) e = -1;
+        if (e >= a.E) e = -1;
         const unsigned peers = __match_any_sync(0xffffffffu, e);
         const int rank = __popc(peers & lt_mask);
         if (e >= 0) {
-            const int p = wh[warp][e] + rank;
+            const int p = wh_row[e] + rank;
             a.perm[p] = f;
             a.inv[f] = p;
         }
         __syncwarp();
-        if (e >= 0 && rank == 0) wh[warp][e] += __popc(peers);
+        if (e >= 0 && rank == 0) wh_row[e] += __popc(peers);
         __syncwarp();
     }
 }
 
+__device__ __forceinline__ void zero_warp_counts(DispatchSmem& sm, int tid) {
+    for (int i = tid; i < kW * (kMaxE + 1); i += kDispatchThreads) (&sm.wh[0][0])[i] = 0;
+}
+
+// Slot chunk of CTA c in the three-kernel path.
+__host__ __device__ inline int chunk_slots(int S) {
+    const int c = (S + kDispatchMaxChunks - 1) / kDispatchMaxChunks;
+    return max(2048, (c + 31) & ~31);
+}
+}  // namespace
+
+// One CTA of 32 warps sorts everything; warp w owns the contiguous slot range
+// [w*per, (w+1)*per). Warps cover the slots in order, so the sort is stable
+// and the result unique.
+__global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs a) {
+    __shared__ DispatchSmem sm;
+    pdl_trigger();
+    pdl_wait();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    zero_warp_counts(sm, tid);
+    __syncthreads();
+    const int per = (a.S + kW - 1) / kW;
+    const int c0 = min(a.S, warp * per), c1 = min(a.S, c0 + per);
+    warp_histogram(a.idx, c0, c1, a.E, sm.wh[warp], lane, true);
+    __syncthreads();
+    scan_over_warps(sm, sm.cnt, a.E, warp, lane);
+    __syncthreads();
+    finish_experts(a, sm, tid, warp, lane);
+    for (int i = tid; i < kW * a.E; i += kDispatchThreads) sm.wh[i / a.E][i % a.E] += sm.off[i % a.E];
+    __syncthreads();
+    warp_scatter(a, c0, c1, sm.wh[warp], lane);
+}
+
+// Three-kernel path for large S. 1: CTA c counts its slot chunk by expert.
+__global__ void __launch_bounds__(kDispatchThreads) dispatch_count_kernel(DispatchArgs a) {
+    __shared__ DispatchSmem sm;
+    pdl_trigger();
+    pdl_wait();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int chunk = chunk_slots(a.S);
+    const int s0 = blockIdx.x * chunk, s1 = min(a.S, s0 + chunk);
+    zero_warp_counts(sm, tid);
+    __syncthreads();
+    const int per = (s1 - s0 + kW - 1) / kW;
+    const int c0 = min(s1, s0 + warp * per), c1 = min(s1, c0 + per);
+    warp_histogram(a.idx, c0, c1, a.E, sm.wh[warp], lane, true);
+    __syncthreads();
+    for (int e = tid; e < a.E; e += kDispatchThreads) {
+        int t = 0;
+        for (int w = 0; w < kW; ++w) t += sm.wh[w][e];
+        a.chunk_hist[blockIdx.x * a.E + e] = t;
+    }
+}
+
+// 2: one CTA: per-expert totals and chunk prefixes, offsets, tiles; the
+// chunk histogram becomes each chunk's base position per expert.
+__global__ void __launch_bounds__(kDispatchThreads) dispatch_scan_kernel(DispatchArgs a) {
+    __shared__ DispatchSmem sm;
+    pdl_trigger();
+    pdl_wait();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nch = (a.S + chunk_slots(a.S) - 1) / chunk_slots(a.S);
+    for (int e = tid; e < a.E; e += kDispatchThreads) {
+        int run = 0;
+        for (int c = 0; c < nch; ++c) {
+            const int v = a.chunk_hist[c * a.E + e];
+            a.chunk_hist[c * a.E + e] = run;
+            run += v;
+        }
+        sm.cnt[e] = run;
+    }
+    __syncthreads();
+    finish_experts(a, sm, tid, warp, lane);
+    __syncthreads();
+    for (int i = tid; i < nch * a.E; i += kDispatchThreads) a.chunk_hist[i] += sm.off[i % a.E];
+}
+
+// 3: CTA c scatters its chunk from the chunk's per-expert bases.
+__global__ void __launch_bounds__(kDispatchThreads) dispatch_scatter_kernel(DispatchArgs a) {
+    __shared__ DispatchSmem sm;
+    pdl_trigger();
+    pdl_wait();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int chunk = chunk_slots(a.S);
+    const int s0 = blockIdx.x * chunk, s1 = min(a.S, s0 + chunk);
+    zero_warp_counts(sm, tid);
+    __syncthreads();
+    const int per = (s1 - s0 + kW - 1) / kW;
+    const int c0 = min(s1, s0 + warp * per), c1 = min(s1, c0 + per);
+    warp_histogram(a.idx, c0, c1, a.E, sm.wh[warp], lane, false);
+    __syncthreads();
+    scan_over_warps(sm, nullptr, a.E, warp, lane);
+    __syncthreads();
+    for (int i = tid; i < kW * a.E; i += kDispatchThreads)
+        sm.wh[i / a.E][i % a.E] += a.chunk_hist[blockIdx.x * a.E + i % a.E];
+    __syncthreads();
+    warp_scatter(a, c0, c1, sm.wh[warp], lane);
+}
+
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
-    return launch_pdl(dispatch_kernel, dim3(1), dim3(kDispatchThreads), 0, stream, a);
+    if (a.chunk_hist == nullptr || a.S <= kDispatchSingleMaxSlots)
+        return launch_pdl(dispatch_kernel, dim3(1), dim3(kDispatchThreads), 0, stream, a);
+    const int nch = (a.S + chunk_slots(a.S) - 1) / chunk_slots(a.S);  // <= kDispatchMaxChunks
+    cudaError_t e = launch_pdl(dispatch_count_kernel, dim3(nch), dim3(kDispatchThreads), 0, stream, a);
+    if (e == cudaSuccess) e = launch_pdl(dispatch_scan_kernel, dim3(1), dim3(kDispatchThreads), 0, stream, a);
+    if (e == cudaSuccess) e = launch_pdl(dispatch_scatter_kernel, dim3(nch), dim3(kDispatchThreads), 0, stream, a);
+    return e;
 }
 
 // 8 bf16 (one 16-byte chunk) -> positions holding elements (0,4,1,5,2,6,3,7).

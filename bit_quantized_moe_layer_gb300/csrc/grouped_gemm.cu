@@ -59,6 +59,7 @@ struct Smem {
     uint64_t afull[kMaxGroups], aempty[kMaxGroups];              // A slots in TMEM, one per stage group
     uint64_t dfull[2], dempty[2];                                // accumulator buffers in TMEM
     uint64_t sfull[2], sempty[2];                                // scale/bias buffers
+    uint64_t mdrain;  // the MMA issuer's final commit
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -181,6 +182,7 @@ __global__ void __launch_bounds__((4 + NG * GW + 4 * EPW) * 32, 1)
             mbar_init(&sh.dfull[i], 1);
             mbar_init(&sh.dempty[i], kEpiWarps);
         }
+        mbar_init(&sh.mdrain, 1);
         sh.abort_flag = 0;
         fence_barrier_init();
     }
@@ -209,7 +211,7 @@ __global__ void __launch_bounds__((4 + NG * GW + 4 * EPW) * 32, 1)
             const Tile tl = a.tiles[it / a.n_tiles];
             const int j = it % a.n_tiles;
             const int sb = li & 1;
-            if (!(ok = mbar_wait(&sh.sempty[sb], ((li >> 1) & 1) ^ 1, abort_flag, kSleepRing))) break;
+            if (!(ok = mbar_wait(&sh.sempty[sb], ((li >> 1) & 1) ^ 1, abort_flag, kSleepRing, 1))) break;
             uint8_t* sbuf = scale_base + sb * sbuf_bytes;
             const uint32_t half = (uint32_t)(64 * G * 2);  // bytes of 64 rows
             if (elect_one()) {
@@ -229,7 +231,7 @@ __global__ void __launch_bounds__((4 + NG * GW + 4 * EPW) * 32, 1)
             }
             __syncwarp();
             for (int s = 0; s < nstages; ++s) {
-                if (!(ok = mbar_wait(&sh.wempty[slot], ph ^ 1, abort_flag, kSleepRing))) break;
+                if (!(ok = mbar_wait(&sh.wempty[slot], ph ^ 1, abort_flag, kSleepRing, 2))) break;
                 uint8_t* st = wring + (size_t)slot * kPackedStageBytes;
                 if (elect_one()) {
                     mbar_arrive_expect_tx(&sh.wfull[slot], kPackedStageBytes);
@@ -250,8 +252,8 @@ __global__ void __launch_bounds__((4 + NG * GW + 4 * EPW) * 32, 1)
         }
         // Do not leave while copies into shared memory are in flight.
         for (uint32_t g = (issued > (uint32_t)NP ? issued - NP : 0); g < issued; ++g)
-            mbar_wait(&sh.wfull[g % NP], (g / NP) & 1, abort_flag);
-        if (li > 0) mbar_wait(&sh.sfull[(li - 1) & 1], ((li - 1) >> 1) & 1, abort_flag);
+            mbar_drain(&sh.wfull[g % NP], (g / NP) & 1);
+        for (int l = (li > 2 ? li - 2 : 0); l < li; ++l) mbar_drain(&sh.sfull[l & 1], (l >> 1) & 1);
     } else if (warp == 2) {
         // ---------------------------------------------------- B operand --
         if (elect_one()) prefetch_tensormap(&bmap);
@@ -262,7 +264,7 @@ __global__ void __launch_bounds__((4 + NG * GW + 4 * EPW) * 32, 1)
             const Tile tl = a.tiles[it / a.n_tiles];
             const int nrows16 = (tl.rows + 15) & ~15;
             for (int s = 0; s < nstages; ++s) {
-                if (!(ok = mbar_wait(&sh.bempty[slot], ph ^ 1, abort_flag, kSleepRing))) break;
+                if (!(ok = mbar_wait(&sh.bempty[slot], ph ^ 1, abort_flag, kSleepRing, 3))) break;
                 uint8_t* bst = bring + (size_t)slot * bslot_bytes;
                 const int atoms = min(kStageK, K - s * kStageK) / 64;
                 if (elect_one()) {
@@ -281,7 +283,7 @@ __global__ void __launch_bounds__((4 + NG * GW + 4 * EPW) * 32, 1)
             }
         }
         for (uint32_t g = (issued > (uint32_t)NB ? issued - NB : 0); g < issued; ++g)
-            mbar_wait(&sh.bfull[g % NB], (g / NB) & 1, abort_flag);
+            mbar_drain(&sh.bfull[g % NB], (g / NB) & 1);
     } else if (warp == 1) {
         // ---------------------------------------------------- MMA issuer --
         // The whole warp runs the loop; one elected lane issues the MMAs of a
@@ -303,7 +305,7 @@ __global__ void __launch_bounds__((4 + NG * GW + 4 * EPW) * 32, 1)
             for (int s = 0; s < nstages; ++s) {
                 // afull also carries the gate warp's arrival: the B slot is
                 // full and (at an item's first stage) the accumulator is free.
-                if (!(ok = mbar_wait(&sh.afull[as], aph, abort_flag))) break;
+                if (!(ok = mbar_wait(&sh.afull[as], aph, abort_flag, 0, 7))) break;
                 tc_fence_after();
                 const int nk = min(kStageK, K - s * kStageK) / 16;
                 const uint64_t bdesc0 = sw128_kmajor_desc(smem_u32(bring + (size_t)bslot * bslot_bytes));
@@ -328,6 +330,10 @@ __global__ void __launch_bounds__((4 + NG * GW + 4 * EPW) * 32, 1)
                 }
             }
         }
+        // Every MMA this thread issued completes before TMEM is released.
+        if (elect_one()) umma_commit(&sh.mdrain);
+        __syncwarp();
+        mbar_drain(&sh.mdrain, 0);
     } else if (warp == 3) {
         // --------------------------------------------------- stage gate --
         // Folds the MMA's other conditions into the A-slot barrier, so the
@@ -343,10 +349,10 @@ __global__ void __launch_bounds__((4 + NG * GW + 4 * EPW) * 32, 1)
         for (int li = 0; li < my_items && ok; ++li) {
             for (int s = 0; s < nstages; ++s, ++gs) {
                 // previous phase of afull[as]: stage gs - NG
-                if (gs >= NG && !(ok = mbar_wait(&sh.afull[as], aph ^ 1, abort_flag, kSleepRing))) break;
-                if (!(ok = mbar_wait(&sh.bfull[bslot], bph, abort_flag, kSleepRing))) break;
+                if (gs >= NG && !(ok = mbar_wait(&sh.afull[as], aph ^ 1, abort_flag, kSleepRing, 4))) break;
+                if (!(ok = mbar_wait(&sh.bfull[bslot], bph, abort_flag, kSleepRing, 5))) break;
                 if (s == 0 && li >= 2 &&
-                    !(ok = mbar_wait(&sh.dempty[li & 1], ((li >> 1) - 1) & 1, abort_flag, kSleepRing)))
+                    !(ok = mbar_wait(&sh.dempty[li & 1], ((li >> 1) - 1) & 1, abort_flag, kSleepRing, 6)))
                     break;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sh.afull[as]);
@@ -418,10 +424,10 @@ __global__ void __launch_bounds__((4 + NG * GW + 4 * EPW) * 32, 1)
         auto fetch = [&]() -> bool {
             const int sb = f_li & 1;
             if (f_li != waited_li) {
-                if (!mbar_wait(&sh.sfull[sb], (f_li >> 1) & 1, abort_flag)) return false;
+                if (!mbar_wait(&sh.sfull[sb], (f_li >> 1) & 1, abort_flag, 0, 8)) return false;
                 waited_li = f_li;
             }
-            if (!mbar_wait(&sh.wfull[f_slot], f_ph, abort_flag)) return false;
+            if (!mbar_wait(&sh.wfull[f_slot], f_ph, abort_flag, 0, 9)) return false;
             const uint16_t* sS = srow + (sb * sbuf_bytes) / 2 + f_s * 4;
             const uint16_t* sB = sS + 128 * G;
             const uint8_t* pst = wring + (size_t)f_slot * kPackedStageBytes;
@@ -448,7 +454,7 @@ __global__ void __launch_bounds__((4 + NG * GW + 4 * EPW) * 32, 1)
         uint32_t aph = 0;  // phase of this group's A slot
         for (uint32_t gs = dgrp; gs < total && ok; gs += NG, aph ^= 1) {
             const int as = dgrp;
-            if (!(ok = mbar_wait(&sh.aempty[as], aph ^ 1, abort_flag))) break;
+            if (!(ok = mbar_wait(&sh.aempty[as], aph ^ 1, abort_flag, 0, 10))) break;
             tc_fence_after();
             __syncwarp();
             if (lane == 0) {
@@ -494,7 +500,7 @@ __global__ void __launch_bounds__((4 + NG * GW + 4 * EPW) * 32, 1)
             // warp reads its 16-column chunks one at a time, then hands the
             // buffer back (it is not needed again before item li + 2).
             const int db = li & 1;
-            if (!(ok = mbar_wait(&sh.dfull[db], (li >> 1) & 1, abort_flag, kSleepEpi))) break;
+            if (!(ok = mbar_wait(&sh.dfull[db], (li >> 1) & 1, abort_flag, kSleepEpi, 11))) break;
             tc_fence_after();
             const uint32_t dcol = tmem + lane_addr + kD0 + (uint32_t)(db * NMAX);
 #pragma unroll
@@ -595,8 +601,9 @@ static cudaError_t launch_mode(const CUtensorMap& wmap, const CUtensorMap& bmap,
         (void)nstages;
         return launch_one<MODE, 64, 2, 8, 1>(wmap, bmap, a, grid, smem, stream);
     }
-    if (a.nmax == 128)  // two groups of 4 dequant warps, 16 epilogue warps (28 warps)
-        return launch_one<MODE, 128, 2, 4, 4>(wmap, bmap, a, grid, smem, stream);
+    if (a.nmax == 128)  // two groups of 8 dequant warps, 8 epilogue warps (28 warps): a
+                        // 128-token tile's GeGLU needs the wider epilogue
+        return launch_one<MODE, 128, 2, 8, 2>(wmap, bmap, a, grid, smem, stream);
     return cudaErrorInvalidValue;
 }
 

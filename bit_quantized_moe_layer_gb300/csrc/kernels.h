@@ -62,7 +62,12 @@ struct DispatchArgs {
     Tile* tiles;         // [max_tiles] (may be null)
     int32_t* num_tiles;  // [2]: tile count, rows of the largest tile (may be null)
     int S, E, nmax;      // nmax: rows per token tile
+    // Scratch of kDispatchMaxChunks x E ints for the three-kernel path (large
+    // S); null: one CTA does the whole sort.
+    int32_t* chunk_hist = nullptr;
 };
+constexpr int kDispatchMaxChunks = 64;
+constexpr int kDispatchSingleMaxSlots = 8192;  // above this the sort runs as three kernels
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream);
 
 // Gather: xs[p] = x[perm[p] / k] with each 8-element block of K stored in

@@ -115,7 +115,7 @@ float bf16_round(double x) {
 
 // ------------------------------------------------------------ workspace --
 struct Layout {
-    size_t idx, w, perm, inv, offsets, tiles, ntiles, xs, mid, y, xdev, outdev, total;
+    size_t idx, w, perm, inv, offsets, tiles, ntiles, dhist, xs, mid, y, xdev, outdev, total;
     int max_tiles;
 };
 
@@ -138,6 +138,7 @@ Layout layout(const moe_dims* d) {
     L.offsets = take((size_t)(d->E + 1) * 4);
     L.tiles = take((size_t)L.max_tiles * sizeof(Tile));
     L.ntiles = take(8);
+    L.dhist = take((size_t)kDispatchMaxChunks * d->E * 4);
     L.xs = take(S * d->H * 2);
     L.mid = take(S * d->inter * 2);
     L.y = take(S * d->H * 2);
@@ -223,7 +224,7 @@ int run_experts(const moe_dims* d, const uint16_t* x, const int32_t* idx, const 
         !make_map_2d(&m_mid, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, mid, I, S, 64, 16))
         return MOE_ERR_CUDA;
 
-    DispatchArgs da{idx, perm, offsets, inv, tiles, ntiles, S, E, nmax};
+    DispatchArgs da{idx, perm, offsets, inv, tiles, ntiles, S, E, nmax, reinterpret_cast<int32_t*>(ws + L.dhist)};
     int rc = fail(launch_dispatch(da, s));
     if (rc) return rc;
     tm.mark(2);
@@ -299,6 +300,24 @@ int get_workspace(const moe_dims* d, void* workspace, size_t ws_bytes, const Lay
     return rc;
 }
 
+// Scratch of moe_dispatch's large-input path (kDispatchMaxChunks x 256
+// ints), allocated once per device on first use and held until the process
+// exits.
+int dispatch_scratch(int32_t** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_DEVICE;
+    static std::mutex mu;
+    static std::vector<void*> bufs;
+    std::lock_guard<std::mutex> lock(mu);
+    if ((int)bufs.size() <= dev) bufs.resize(dev + 1, nullptr);
+    if (!bufs[dev] && cudaMalloc(&bufs[dev], (size_t)kDispatchMaxChunks * 256 * 4) != cudaSuccess) {
+        bufs[dev] = nullptr;
+        return MOE_ERR_CUDA;
+    }
+    *out = static_cast<int32_t*>(bufs[dev]);
+    return MOE_OK;
+}
+
 // ------------------------------------------------------ fixed scratch ----
 // Scratch of moe_experts_noalloc: a fixed array in the library's device
 // image, so that call never allocates. Every GPU that loads the library holds
@@ -367,7 +386,9 @@ int moe_dispatch(const moe_dims* d, const int32_t* idx, int32_t* perm, int32_t* 
     if ((rc = check_ptrs({idx, perm, offsets, inv}))) return rc;
     DeviceInfo di;
     if ((rc = device_info(&di))) return rc;
-    DispatchArgs da{idx, perm, offsets, inv, nullptr, nullptr, d->T * d->k, d->E, 64};
+    int32_t* scratch = nullptr;  // chunk histograms of the large-input path
+    if ((rc = dispatch_scratch(&scratch))) return rc;
+    DispatchArgs da{idx, perm, offsets, inv, nullptr, nullptr, d->T * d->k, d->E, 64, scratch};
     return fail(launch_dispatch(da, static_cast<cudaStream_t>(stream)));
 }
 
@@ -497,7 +518,10 @@ int moe_timing_read(float* ms, int n, int* calls) {
     return m;
 }
 
-int moe_launches_per_forward(void) { return kStages; }
+int moe_launches_per_forward(const moe_dims* d) {
+    if (check_dims(d) != MOE_OK) return 0;
+    return kStages + (((int64_t)d->T * d->k > kDispatchSingleMaxSlots) ? 2 : 0);
+}
 
 int moe_device_error(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return -MOE_ERR_CUDA;

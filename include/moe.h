@@ -100,7 +100,9 @@ int moe_route(const moe_dims* d, const uint16_t* x, const uint16_t* router_w,
  *   perm[p] = f                  p-th slot in expert order (int32 [T*k])
  *   inv[f]  = p                  inverse of perm (int32 [T*k])
  * idx int32 [T,k] must hold ids in [0,E); a bad id is dropped and raised in
- * moe_device_error. Bit-exact and deterministic.
+ * moe_device_error. Bit-exact and deterministic. For T*k > 8192 the sort runs
+ * as three kernels that need 64 KB of device scratch: this call allocates it
+ * once per device on first use and holds it until the process exits.
  */
 int moe_dispatch(const moe_dims* d, const int32_t* idx, int32_t* perm, int32_t* offsets,
                  int32_t* inv, void* stream);
@@ -185,13 +187,17 @@ int moe_forward_hostio(const moe_dims* d, const uint16_t* x_host, const uint16_t
 int moe_timing_enable(int enable);
 int moe_timing_read(float* ms, int n, int* calls);
 
-/* Number of kernel launches one moe_forward call makes. */
-int moe_launches_per_forward(void);
+/* Number of kernel launches one moe_forward call with these dims makes
+ * (6; 8 when T*k > 8192, where dispatch runs as three kernels); 0 if the
+ * dims are rejected. */
+int moe_launches_per_forward(const moe_dims* d);
 
 /*
  * Device-side error word of the current device: 0 if no kernel has given
  * up waiting or dropped a bad expert id since the last read; otherwise a
- * bit set (1: a pipeline wait timed out, 2: an expert id was out of range).
+ * bit set (1: a pipeline wait timed out, 2: an expert id was out of range)
+ * and, with bit 1, bits 8..15 naming the first wait that timed out (a
+ * diagnostic code of the grouped GEMM's pipeline, 0 if not recorded).
  * Synchronises the device, then clears the word.
  */
 int moe_device_error(void);
