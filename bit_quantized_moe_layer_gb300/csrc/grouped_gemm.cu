@@ -13,18 +13,19 @@
 //   warp 0        TMA producer of the packed weights (128 rows x 128 B per
 //                 stage, 128 B swizzle) into a ring of up to 8 stages, and of
 //                 the item's scales and biases (bulk copies, double-buffered);
-//   warp 1        TMEM owner and MMA issuer (one elected thread);
+//   warp 1        TMEM owner and MMA issuer (one elected thread): per stage
+//                 it waits for the A slot and the B slot, at an item's first
+//                 stage for a free accumulator buffer;
 //   warp 2        TMA producer of the B operand (the token tile, 16-row boxes)
 //                 into a ring that the MMA's completion releases; its slots
 //                 are sized at run time for the largest token tile of the
 //                 call, so small tiles get a deep ring;
-//   warp 3        stage gate: waits for the B slot and (once per item) for a
-//                 free accumulator, then arrives on the A-slot barrier, so the
-//                 MMA issuer waits once per stage;
-//   dequant warps thread = weight row = TMEM lane, in two stage groups: group
-//                 p dequantises the stages g with g % 2 == p into A slot p of
-//                 TMEM (tcgen05.st), so one group's waits overlap the other's
-//                 arithmetic. A packed word holds 8 codes; the 0x4300 magic
+//   dequant warps 8 warps, thread = weight row = TMEM lane; warp (q, p)
+//                 dequantises atoms 2p and 2p + 1 (64 K each) of lane
+//                 quarter q of every stage into the next slot of a ring of A
+//                 slots in TMEM (tcgen05.st), so the dequantisation runs up
+//                 to a few stages ahead of the MMA. A packed word holds 8
+//                 codes; the 0x4300 magic
 //                 gives 128+q per bf16 half, minus 128 gives q exactly, and
 //                 one fma.rn.bf16x2 with the group's scale and bias gives
 //                 bf16(S*q + B) with a single rounding. The MMA reads A from
@@ -48,15 +49,15 @@ constexpr int kPackedStageBytes = 128 * 128;  // 128 rows x 32 words
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxPackedStages = 8;
 constexpr int kMaxBStages = 8;
-constexpr int kMaxGroups = 3;  // dequant stage groups (A slots)
-// Sleep between tests for waits with slack (producers, gate, epilogue).
-constexpr uint32_t kSleepRing = 200;   // ns: producers and the stage gate
-constexpr uint32_t kSleepEpi = 1000;   // ns: the epilogue has a whole item of slack
+constexpr int kMaxASlots = 3;  // A-operand ring in TMEM (128 columns a slot)
+// Sleep between tests for waits with slack (producers, epilogue).
+constexpr uint32_t kSleepRing = 200;  // ns: the TMA producers
+constexpr uint32_t kSleepEpi = 1000;  // ns: the epilogue has a whole item of slack
 
 struct Smem {
     uint64_t wfull[kMaxPackedStages], wempty[kMaxPackedStages];  // packed-weight ring
     uint64_t bfull[kMaxBStages], bempty[kMaxBStages];            // B-operand ring
-    uint64_t afull[kMaxGroups], aempty[kMaxGroups];              // A slots in TMEM, one per stage group
+    uint64_t afull[kMaxASlots], aempty[kMaxASlots];              // A slots in TMEM
     uint64_t dfull[2], dempty[2];                                // accumulator buffers in TMEM
     uint64_t sfull[2], sempty[2];                                // scale/bias buffers
     uint64_t mdrain;  // the MMA issuer's final commit
@@ -120,19 +121,20 @@ __device__ __forceinline__ void dequant_atom(const uint4 c0, const uint4 c1, uin
 
 }  // namespace
 
-// NG stage groups of GW dequant warps (A slot g of TMEM for group g), EPW
-// epilogue warps per TMEM lane quarter.
-template <int MODE, int NMAX, int NG, int GW, int EPW>
-__global__ void __launch_bounds__((4 + NG * GW + 4 * EPW) * 32, 1)
+// NA A slots in TMEM (a ring the dequant warps fill ahead of the MMA), APW
+// atoms of a stage per dequant warp (16 / APW dequant warps), EPW epilogue
+// warps per TMEM lane quarter.
+template <int MODE, int NMAX, int NA, int APW, int EPW>
+__global__ void __launch_bounds__((3 + 16 / APW + 4 * EPW) * 32, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap bmap,
                         GemmArgs a) {
-    constexpr int kDqWarps = NG * GW;
-    constexpr int kEpiWarp0 = 4 + kDqWarps;
+    constexpr int kDqWarps = 16 / APW;
+    constexpr int kEpiWarp0 = 3 + kDqWarps;
     constexpr int kEpiWarps = 4 * EPW;
     constexpr int kAccChunks = NMAX / 16 / EPW;  // 16-column chunks of one epilogue warp
-    constexpr uint32_t kD0 = NG * 128;           // accumulator buffers after the A slots
+    constexpr uint32_t kD0 = NA * 128;           // accumulator buffers after the A slots
     static_assert(kD0 + 2 * NMAX <= kTmemCols, "TMEM columns");
-    static_assert(GW % 4 == 0 && NG <= kMaxGroups, "group shape");
+    static_assert(NA <= kMaxASlots, "A slots");
     extern __shared__ __align__(1024) uint8_t dsmem[];
     __shared__ Smem sh;
     pdl_trigger();
@@ -160,23 +162,19 @@ __global__ void __launch_bounds__((4 + NG * GW + 4 * EPW) * 32, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < NP; ++s) {
             mbar_init(&sh.wfull[s], 1);
-            mbar_init(&sh.wempty[s], GW);  // read by one stage group
+            mbar_init(&sh.wempty[s], kDqWarps);  // every dequant warp reads every stage
         }
         for (int s = 0; s < NB; ++s) {
             mbar_init(&sh.bfull[s], 1);
             mbar_init(&sh.bempty[s], 1);
         }
-        // An item's scales are read by every stage group when it has NG or
-        // more K stages (the host only picks NG = 3 then), by one group when
-        // it has a single stage (NG = 2).
-        const int nst = (a.K + kStageK - 1) / kStageK;
-        for (int i = 0; i < NG; ++i) {
-            mbar_init(&sh.afull[i], GW + 1);  // one stage group + the stage gate (warp 3)
+        for (int i = 0; i < NA; ++i) {
+            mbar_init(&sh.afull[i], kDqWarps);
             mbar_init(&sh.aempty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sh.sfull[i], 1);
-            mbar_init(&sh.sempty[i], nst >= NG ? kDqWarps : GW);
+            mbar_init(&sh.sempty[i], kDqWarps);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sh.dfull[i], 1);
@@ -198,7 +196,6 @@ __global__ void __launch_bounds__((4 + NG * GW + 4 * EPW) * 32, 1)
     const int num_items = a.num_tiles[0] * a.n_tiles;
     const int K = a.K;
     const int nstages = (K + kStageK - 1) / kStageK;
-
     if (warp == 0) {
         // ------------------------------------- packed weights + scales --
         // The whole warp runs the loop; one elected lane issues the copies.
@@ -290,7 +287,7 @@ __global__ void __launch_bounds__((4 + NG * GW + 4 * EPW) * 32, 1)
         // stage and the commits (a commit tracks its own thread's MMAs). An
         // item accumulates its whole K into accumulator buffer li & 1.
         int bslot = 0, li = 0, as = 0;
-        uint32_t aph = 0;  // A slot of the stage and the phase of its barrier
+        uint32_t bph = 0, aph = 0;  // phases of the B slot's and the A slot's barriers
         bool ok = true;
         Tile tl_next = {};
         if (blockIdx.x < num_items) tl_next = a.tiles[blockIdx.x / a.n_tiles];
@@ -302,10 +299,11 @@ __global__ void __launch_bounds__((4 + NG * GW + 4 * EPW) * 32, 1)
             const uint32_t idesc = idesc_bf16_m128(nrows16);
             const int db = li & 1;
             const uint32_t dcol = tmem + kD0 + (uint32_t)(db * NMAX);
+            // the accumulator buffer's previous item (li - 2) has been read out
+            if (li >= 2 && !(ok = mbar_wait(&sh.dempty[db], ((li >> 1) - 1) & 1, abort_flag, 0, 6))) break;
             for (int s = 0; s < nstages; ++s) {
-                // afull also carries the gate warp's arrival: the B slot is
-                // full and (at an item's first stage) the accumulator is free.
                 if (!(ok = mbar_wait(&sh.afull[as], aph, abort_flag, 0, 7))) break;
+                if (!(ok = mbar_wait(&sh.bfull[bslot], bph, abort_flag, 0, 5))) break;
                 tc_fence_after();
                 const int nk = min(kStageK, K - s * kStageK) / 16;
                 const uint64_t bdesc0 = sw128_kmajor_desc(smem_u32(bring + (size_t)bslot * bslot_bytes));
@@ -323,8 +321,11 @@ __global__ void __launch_bounds__((4 + NG * GW + 4 * EPW) * 32, 1)
                     if (s == nstages - 1) umma_commit(&sh.dfull[db]);
                 }
                 __syncwarp();
-                if (++bslot == NB) bslot = 0;
-                if (++as == NG) {
+                if (++bslot == NB) {
+                    bslot = 0;
+                    bph ^= 1;
+                }
+                if (++as == NA) {
                     as = 0;
                     aph ^= 1;
                 }
@@ -334,149 +335,84 @@ __global__ void __launch_bounds__((4 + NG * GW + 4 * EPW) * 32, 1)
         if (elect_one()) umma_commit(&sh.mdrain);
         __syncwarp();
         mbar_drain(&sh.mdrain, 0);
-    } else if (warp == 3) {
-        // --------------------------------------------------- stage gate --
-        // Folds the MMA's other conditions into the A-slot barrier, so the
-        // MMA issuer waits once per stage: for stage g this warp waits for
-        // the B slot to be full, at an item's first stage for the item's
-        // accumulator buffer to be free, and for the previous phase of
-        // afull[g & 1] (stage g - 2) to complete so that its arrival counts
-        // toward stage g.
-        uint32_t gs = 0, bph = 0, aph = 0;
-        int bslot = 0, as = 0;
-        bool ok = true;
-        const int my_items = (blockIdx.x < num_items) ? (num_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-        for (int li = 0; li < my_items && ok; ++li) {
-            for (int s = 0; s < nstages; ++s, ++gs) {
-                // previous phase of afull[as]: stage gs - NG
-                if (gs >= NG && !(ok = mbar_wait(&sh.afull[as], aph ^ 1, abort_flag, kSleepRing, 4))) break;
-                if (!(ok = mbar_wait(&sh.bfull[bslot], bph, abort_flag, kSleepRing, 5))) break;
-                if (s == 0 && li >= 2 &&
-                    !(ok = mbar_wait(&sh.dempty[li & 1], ((li >> 1) - 1) & 1, abort_flag, kSleepRing, 6)))
-                    break;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sh.afull[as]);
-                if (++bslot == NB) {
-                    bslot = 0;
-                    bph ^= 1;
-                }
-                if (++as == NG) {
-                    as = 0;
-                    aph ^= 1;
-                }
-            }
-        }
-    } else if (warp >= 4 && warp < kEpiWarp0) {
+    } else if (warp >= 3 && warp < kEpiWarp0) {
         // ------------------------------------------------------- dequant --
-        // NG stage groups of GW warps: group p dequantises the stages g with
-        // g % NG == p into A slot p, so one group's waits and loads overlap
-        // the other groups' arithmetic. Within a group, warp (q, sub) covers
-        // TMEM lanes 32q..32q+31 and the atoms sub, sub + kSub, ... of its
-        // stages.
-        constexpr int kSub = GW / 4;                 // warps per lane quarter in a group
-        constexpr int kAtomsPerWarp = 4 / kSub;
-        const int dgrp = (warp - 4) / GW;
-        const int sub = ((warp - 4) >> 2) % kSub;
+        // 16 / APW warps; warp (q, p) covers TMEM lanes 32q..32q+31 (q =
+        // warp % 4, the lane quarter a warp may access) and atoms p APW ..
+        // p APW + APW - 1 (64 K each) of every stage. Each stage goes into the
+        // next A slot of the ring, so the warps run up to NA stages ahead of
+        // the MMA.
+        const int dw = warp - 3;
         const int q = warp & 3;
+        const int at0 = (dw >> 2) * APW;
         int row;  // row in the packed stage and the scale buffer
         if (MODE == kGateUp)
             row = (lane < 16) ? (16 * q + lane) : (64 + 16 * q + (lane - 16));
         else
             row = 32 * q + lane;
         const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
-        const uint32_t total = (blockIdx.x < num_items)
-                                   ? (uint32_t)((num_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1) * nstages
-                                   : 0u;
-        // Fetch cursor over this CTA's stages (item ordinal li, stage s, ring slot).
-        int f_s = 0, f_li = 0, f_slot = 0, waited_li = -1;
-        uint32_t f_ph = 0;
-        auto step = [&]() {
-            if (++f_slot == NP) {
-                f_slot = 0;
-                f_ph ^= 1;
-            }
-            if (++f_s == nstages) {
-                f_s = 0;
-                ++f_li;
-            }
-        };
-        for (int i = 0; i < dgrp; ++i) step();
-        uint4 c[2 * kAtomsPerWarp];
-        uint32_t Sv[kAtomsPerWarp], Bv[kAtomsPerWarp];
-        int atoms = 0;
-        // Per-thread constants: the swizzled offsets of this warp's atoms in
-        // its 128-byte row of a packed stage, and the TMEM column of each.
-        uint32_t woff[2 * kAtomsPerWarp];
+        // shared addresses: this thread's 128-byte row in ring slot 0 with
+        // the swizzled offsets of its atoms, and its scale in buffer 0
+        uint32_t wo[2 * APW];
 #pragma unroll
-        for (int i = 0; i < kAtomsPerWarp; ++i) {
-            const int at = sub + i * kSub;
-            woff[2 * i] = (uint32_t)row * 128u + ((uint32_t)((2 * at) ^ (row & 7)) << 4);
-            woff[2 * i + 1] = (uint32_t)row * 128u + ((uint32_t)((2 * at + 1) ^ (row & 7)) << 4);
+        for (int i = 0; i < APW; ++i) {
+            const int at = at0 + i;
+            wo[2 * i] = smem_u32(wring) + (uint32_t)row * 128u + ((uint32_t)((2 * at) ^ (row & 7)) << 4);
+            wo[2 * i + 1] = smem_u32(wring) + (uint32_t)row * 128u + ((uint32_t)((2 * at + 1) ^ (row & 7)) << 4);
         }
-        const uint16_t* srow = reinterpret_cast<const uint16_t*>(scale_base) + row * G;  // buffer 0
-        // The ring slot (and scale buffer) whose words c/Sv/Bv hold: released
-        // after the A-slot wait that follows the loads, by when they have
-        // landed in registers.
-        int held_slot = 0, held_sb = 0;
-        bool held_last = false;
-        // Issues the loads of the cursor's stage into c/Sv/Bv and moves the
-        // cursor to the group's next stage.
-        auto fetch = [&]() -> bool {
-            const int sb = f_li & 1;
-            if (f_li != waited_li) {
-                if (!mbar_wait(&sh.sfull[sb], (f_li >> 1) & 1, abort_flag, 0, 8)) return false;
-                waited_li = f_li;
-            }
-            if (!mbar_wait(&sh.wfull[f_slot], f_ph, abort_flag, 0, 9)) return false;
-            const uint16_t* sS = srow + (sb * sbuf_bytes) / 2 + f_s * 4;
-            const uint16_t* sB = sS + 128 * G;
-            const uint8_t* pst = wring + (size_t)f_slot * kPackedStageBytes;
-            atoms = min(kStageK, K - f_s * kStageK) / 64;
-#pragma unroll
-            for (int i = 0; i < kAtomsPerWarp; ++i) {
-                const int at = sub + i * kSub;
-                if (at < atoms) {
-                    c[2 * i] = *reinterpret_cast<const uint4*>(pst + woff[2 * i]);
-                    c[2 * i + 1] = *reinterpret_cast<const uint4*>(pst + woff[2 * i + 1]);
-                    Sv[i] = sS[at];
-                    Bv[i] = sB[at];
-                }
-            }
-            const int li = f_li;
-            held_slot = f_slot;
-            held_sb = sb;
-            for (int i = 0; i < NG; ++i) step();
-            held_last = (f_li != li);  // this warp's last read of the item's scales
-            return true;
-        };
+        const uint32_t srow = smem_u32(scale_base) + (uint32_t)(row * G + at0) * 2u;
+        const uint32_t bias_off = (uint32_t)(128 * G * 2);
+        int wslot = 0, as = 0;
+        uint32_t wph = 0, aph = 0;
         bool ok = true;
-        if ((uint32_t)dgrp < total) ok = fetch();
-        uint32_t aph = 0;  // phase of this group's A slot
-        for (uint32_t gs = dgrp; gs < total && ok; gs += NG, aph ^= 1) {
-            const int as = dgrp;
-            if (!(ok = mbar_wait(&sh.aempty[as], aph ^ 1, abort_flag, 0, 10))) break;
-            tc_fence_after();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&sh.wempty[held_slot]);
-                if (held_last) mbar_arrive(&sh.sempty[held_sb]);
-            }
+        int li = 0;
+        for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x, ++li) {
+            const int sb = li & 1;
+            if (!(ok = mbar_wait(&sh.sfull[sb], (li >> 1) & 1, abort_flag, 0, 8))) break;
+            const uint32_t sS = srow + (uint32_t)(sb * sbuf_bytes);
+            for (int s = 0; s < nstages; ++s) {
+                const int atoms = min(kStageK, K - s * kStageK) / 64;
+                if (!(ok = mbar_wait(&sh.wfull[wslot], wph, abort_flag, 0, 9))) break;
+                uint4 c[2 * APW];
+                uint32_t S1[APW], B1[APW];
+                const uint32_t so = (uint32_t)(wslot * kPackedStageBytes);
 #pragma unroll
-            for (int i = 0; i < kAtomsPerWarp; ++i) {
-                const int at = sub + i * kSub;
-                if (at < atoms) {
-                    uint32_t r[32];
-                    dequant_atom(c[2 * i], c[2 * i + 1], Sv[i], Bv[i], r);
-                    tmem_st32(tmem + lane_addr + as * 128 + at * 32, r);
+                for (int i = 0; i < APW; ++i) {
+                    if (at0 + i < atoms) {  // warp-uniform
+                        c[2 * i] = lds128(wo[2 * i] + so);
+                        c[2 * i + 1] = lds128(wo[2 * i + 1] + so);
+                        S1[i] = lds_u16(sS + (uint32_t)(8 * s + 2 * i));
+                        B1[i] = lds_u16(sS + bias_off + (uint32_t)(8 * s + 2 * i));
+                    }
+                }
+                // The arrive releases the loads above: the slot (and, after
+                // the item's last stage, the scale buffer) may be refilled.
+                __syncwarp();
+                mbar_arrive_lane0(&sh.wempty[wslot]);
+                if (s == nstages - 1) mbar_arrive_lane0(&sh.sempty[sb]);
+                if (++wslot == NP) {
+                    wslot = 0;
+                    wph ^= 1;
+                }
+                if (!(ok = mbar_wait(&sh.aempty[as], aph ^ 1, abort_flag, 0, 10))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int i = 0; i < APW; ++i) {
+                    if (at0 + i < atoms) {
+                        uint32_t r[32];
+                        dequant_atom(c[2 * i], c[2 * i + 1], S1[i], B1[i], r);
+                        tmem_st32(tmem + lane_addr + as * 128 + (at0 + i) * 32, r);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                mbar_arrive_lane0(&sh.afull[as]);
+                if (++as == NA) {
+                    as = 0;
+                    aph ^= 1;
                 }
             }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.afull[as]);
-            // the group's next stage: its loads land while this warp waits
-            // for that stage's A slot
-            if (gs + NG < total && !(ok = fetch())) break;
         }
         tmem_wait_st();
     } else if (warp >= kEpiWarp0) {
@@ -543,7 +479,7 @@ __global__ void __launch_bounds__((4 + NG * GW + 4 * EPW) * 32, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.dempty[db]);
+            mbar_arrive_lane0(&sh.dempty[db]);
         }
     }
 
@@ -573,7 +509,7 @@ void gemm_stages(int K, int nmax, int* wstages, int* bregion) {
     *bregion = (int)((limit - gemm_smem_bytes(K, nw, 0)) & ~size_t(1023));
 }
 
-template <int MODE, int NMAX, int NG, int GW, int EPW>
+template <int MODE, int NMAX, int NA, int APW, int EPW>
 static cudaError_t launch_one(const CUtensorMap& wmap, const CUtensorMap& bmap, const GemmArgs& a, int grid,
                               size_t smem, cudaStream_t stream) {
     static bool attr_set[64] = {};
@@ -581,29 +517,25 @@ static cudaError_t launch_one(const CUtensorMap& wmap, const CUtensorMap& bmap, 
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, NMAX, NG, GW, EPW>,
+        cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, NMAX, NA, APW, EPW>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, 232448 - 2048);
         if (err != cudaSuccess) return err;
         attr_set[dev] = true;
     }
-    return launch_pdl(grouped_gemm_kernel<MODE, NMAX, NG, GW, EPW>, dim3(grid), dim3((4 + NG * GW + 4 * EPW) * 32),
+    return launch_pdl(grouped_gemm_kernel<MODE, NMAX, NA, APW, EPW>, dim3(grid), dim3((3 + 16 / APW + 4 * EPW) * 32),
                       smem, stream, wmap, bmap, a);
 }
 
 template <int MODE>
 static cudaError_t launch_mode(const CUtensorMap& wmap, const CUtensorMap& bmap, const GemmArgs& a, int grid,
                                size_t smem, cudaStream_t stream) {
-    const int nstages = (a.K + kStageK - 1) / kStageK;
-    if (a.nmax == 64) {
-        // two stage groups of 8 dequant warps + 4 epilogue warps (24 warps,
-        // up to 85 registers a thread: the dequantisation does not spill);
-        // three groups (32 warps, 64 registers a thread) measured slower
-        (void)nstages;
-        return launch_one<MODE, 64, 2, 8, 1>(wmap, bmap, a, grid, smem, stream);
-    }
-    if (a.nmax == 128)  // two groups of 8 dequant warps, 8 epilogue warps (28 warps): a
-                        // 128-token tile's GeGLU needs the wider epilogue
-        return launch_one<MODE, 128, 2, 8, 2>(wmap, bmap, a, grid, smem, stream);
+    // Eight dequant warps of two atoms each (fewer warps than one atom each:
+    // less barrier traffic per byte, measured faster). Token tiles of up to
+    // 64: three A slots and 4 epilogue warps (15 warps); up to 128: two A
+    // slots (TMEM holds 2 x 128 accumulator columns) and 8 epilogue warps, as
+    // a 128-token tile's GeGLU needs the wider epilogue (19 warps).
+    if (a.nmax == 64) return launch_one<MODE, 64, 3, 2, 1>(wmap, bmap, a, grid, smem, stream);
+    if (a.nmax == 128) return launch_one<MODE, 128, 2, 2, 2>(wmap, bmap, a, grid, smem, stream);
     return cudaErrorInvalidValue;
 }
 
