@@ -138,6 +138,26 @@ __global__ void __launch_bounds__((3 + 16 / APW + 4 * EPW) * 32, 1)
     extern __shared__ __align__(1024) uint8_t dsmem[];
     __shared__ Smem sh;
     pdl_trigger();
+    // Before waiting for the routing: warm L2 with the weights and scales of
+    // this CTA's first items (the preceding kernels leave HBM idle). Only
+    // global data that no earlier kernel writes is touched here.
+    if (threadIdx.x == 0 && a.prefetch_items > 0) {
+        const uint32_t row_bytes = (uint32_t)a.K / 2, G = (uint32_t)a.K / 64;
+        for (int i = 0; i < a.prefetch_items; ++i) {
+            const int it = blockIdx.x + i * gridDim.x;
+            const int e = (it / a.n_tiles) / a.tiles_per_expert, j = it % a.n_tiles;
+            if (e >= a.E) break;
+            const int nblk = (MODE == kGateUp) ? 2 : 1;  // gate and up halves, or one 128-row block
+            for (int h = 0; h < nblk; ++h) {
+                const size_t r0 = (MODE == kGateUp) ? (size_t)e * a.N + (size_t)h * a.inter + 64 * j
+                                                    : (size_t)e * a.N + 128 * j;
+                const uint32_t rows = (MODE == kGateUp) ? 64u : 128u;
+                prefetch_l2_bulk(a.w + r0 * row_bytes, rows * row_bytes);
+                prefetch_l2_bulk(a.scales + r0 * G, (rows * G * 2 + 15) & ~15u);
+                prefetch_l2_bulk(a.biases + r0 * G, (rows * G * 2 + 15) & ~15u);
+            }
+        }
+    }
     pdl_wait();
     // 1024-byte aligned carve-up: packed ring | B ring | 2 scale buffers.
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));

@@ -94,10 +94,19 @@ struct GemmArgs {
     int N;                    // rows of the weight (2*inter or H)
     int inter;                // gate_up: split point
     int out_ld;               // row length of out (inter or H)
+    int E;                    // experts
     int nmax;                 // rows per token tile (64 or 128)
     int n_tiles;              // weight-row tiles per token tile
     int wstages;              // packed-weight ring depth (shared memory)
     int bregion;              // bytes of shared memory for the B-operand ring
+    // L2 warm-up before the kernel waits for its producers: the packed
+    // weights (w, [E*N rows, K/2 bytes]) and scales of each CTA's first
+    // `prefetch_items` items, guessing that token tile t belongs to expert
+    // t / tiles_per_expert (0 items: none). A wrong guess costs only
+    // bandwidth that the preceding kernels leave idle.
+    const uint8_t* w;
+    int prefetch_items;
+    int tiles_per_expert;
 };
 // wmap: packed weights as uint32 [E*N rows, K/8], box {32, 64 or 128}, 128B swizzle.
 // bmap: B operand (xs or mid) as bf16 [S rows, K], box {64, 16}, 128B swizzle.

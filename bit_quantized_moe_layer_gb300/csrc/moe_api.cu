@@ -244,7 +244,14 @@ int run_experts(const moe_dims* d, const uint16_t* x, const int32_t* idx, const 
     ga.inter = I;
     ga.out_ld = I;
     ga.nmax = nmax;
+    ga.E = E;
     ga.n_tiles = I / 64;
+    // With small token tiles the kernels stream weights: warm L2 with each
+    // CTA's first two items while the router, dispatch and gather run
+    // (guess: one tile per expert, as when every expert has up to nmax rows).
+    ga.w = reinterpret_cast<const uint8_t*>(gu->w);
+    ga.prefetch_items = (nmax == 64) ? 2 : 0;
+    ga.tiles_per_expert = 1;
     gemm_stages(H, nmax, &ga.wstages, &ga.bregion);
     int grid = di.sms;
     if ((long)L.max_tiles * ga.n_tiles < grid) grid = L.max_tiles * ga.n_tiles;
@@ -255,6 +262,7 @@ int run_experts(const moe_dims* d, const uint16_t* x, const int32_t* idx, const 
     GemmArgs gd = ga;
     gd.scales = dn->scales;
     gd.biases = dn->biases;
+    gd.w = reinterpret_cast<const uint8_t*>(dn->w);
     gd.out = y;
     gd.K = I;
     gd.N = H;
