@@ -1,10 +1,12 @@
 // Router kernel: DiffRouter.forward of the DiffusionGemma language model
 // ("diffusion-gemma/model.ts"), fused into one launch.
 //
-// One thread-block cluster of 8 CTAs handles TT tokens (TT = 16, 32 or 64).
-// The hidden dimension is split into 64-wide blocks shared out over the
-// cluster: CTA r loads, by TMA with the 128-byte swizzle, its blocks of the
-// TT activation rows and of every router-weight row, all at once. Then
+// Thread-block clusters of 8 CTAs, persistent: as many as the device holds at
+// once (at most one per tile), each walking token tiles of TT tokens (TT =
+// 16, 32 or 64). The hidden dimension is split into 64-wide blocks shared out
+// over the cluster: CTA r loads once, by TMA with the 128-byte swizzle, its
+// blocks of every router-weight row (kept for all tiles when E <= 128), and
+// per tile its blocks of the TT activation rows. Per tile
 //   1. each CTA sums the squares of its slice per token (fp32 with an
 //      error-free two-sum, so the partial sum keeps ~48 bits) and sends the
 //      partial to every CTA of the cluster (distributed shared memory);
@@ -21,10 +23,12 @@
 //      top k (value descending, ties to the lower expert id), takes the fp32
 //      softmax over the k picked scores and multiplies by
 //      per_expert_scale[idx].
-// Every CTA passes the same three cluster barriers whatever happens, so a
-// wait that times out (error word set) cannot leave the cluster hung.
+// Every CTA passes the same cluster barriers (one at the start, two a tile)
+// whatever happens, so a wait that times out (error word set) cannot leave the
+// cluster hung. The next tile's activations load during step 4.
 #include <cooperative_groups.h>
 
+#include <algorithm>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -43,6 +47,7 @@ constexpr int kWarps = 16;      // warps per CTA
 constexpr int kChunkE = 128;    // experts per router-weight chunk in shared memory
 constexpr int kWBlockBytes = kChunkE * 128;  // one 64-wide K block of a chunk
 constexpr uint32_t kTmemCols = 64;           // >= the largest TT
+constexpr int kMaxRouterE = 256;             // top-k candidates: 8 per lane
 
 // bf16 bits -> key that orders like the value (for finite values).
 __device__ __forceinline__ uint32_t order_key16(uint32_t b) { return (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u); }
@@ -118,6 +123,7 @@ __global__ void __launch_bounds__(kWarps * 32) router_kernel(const __grid_consta
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ uint64_t full, wfull, mdone;
     __shared__ uint32_t tmem_base;
+    __shared__ uint16_t pes_s[kMaxRouterE];  // per_expert_scale
     __shared__ int abort_flag_s;
     pdl_trigger();
     pdl_wait();
@@ -129,7 +135,8 @@ __global__ void __launch_bounds__(kWarps * 32) router_kernel(const __grid_consta
 
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = (int)cluster.block_rank();
-    const int t0 = (blockIdx.x / kCS) * TT;
+    const int cl = (int)blockIdx.x / kCS, ncl = (int)gridDim.x / kCS;  // this cluster, clusters
+    const int ntiles = (a.T + TT - 1) / TT;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int kb0, cnt;
     kslice(H / 64, rank, kb0, cnt);
@@ -137,6 +144,7 @@ __global__ void __launch_bounds__(kWarps * 32) router_kernel(const __grid_consta
     const int eb = E < kChunkE ? E : kChunkE;  // rows of a weight box
     const int tpc = TT / kCS;                  // tokens owned by each CTA
 
+    for (int e = threadIdx.x; e < E; e += blockDim.x) pes_s[e] = a.per_expert_scale[e];
     if (threadIdx.x == 0) {
         prefetch_tensormap(&xmap);
         prefetch_tensormap(&wmap);
@@ -147,204 +155,236 @@ __global__ void __launch_bounds__(kWarps * 32) router_kernel(const __grid_consta
         fence_barrier_init();
     }
     __syncthreads();
+    // Copies of tile `tile`'s activation slice (and, with `weights`, of the
+    // first weight chunk and the router scale slice), one lane per copy. They
+    // only write this CTA's shared memory.
+    auto issue_loads = [&](int tile, bool weights) {
+        if (lane == 0)
+            mbar_arrive_expect_tx(&full, (uint32_t)cnt * (TT * 128 + (weights ? eb * 128 + 128 : 0)));
+        __syncwarp();
+        if (lane < cnt) tma_load_2d(sm.xt + lane * TT * 128, &xmap, &full, (kb0 + lane) * 64, tile * TT);
+        if (weights && lane >= 16 && lane - 16 < cnt)
+            tma_load_2d(sm.wt + (lane - 16) * kWBlockBytes, &wmap, &full, (kb0 + lane - 16) * 64, 0);
+        if (weights && lane == 31 && cnt > 0) bulk_load(sm.rsl, a.router_scale + (size_t)kb0 * 64, cnt * 128, &full);
+    };
     if (warp == 0) {  // scores accumulator: 128 lanes (experts) x TT columns (tokens)
         tmem_alloc(&tmem_base, kTmemCols);
         tmem_relinquish();
-    } else if (warp == 1) {
-        // The copies only write this CTA's shared memory: start them before
-        // waiting for the rest of the cluster, one lane per copy.
-        if (lane == 0) mbar_arrive_expect_tx(&full, (uint32_t)cnt * (TT * 128 + eb * 128 + 128));
-        __syncwarp();
-        if (lane < cnt) tma_load_2d(sm.xt + lane * TT * 128, &xmap, &full, (kb0 + lane) * 64, t0);
-        if (lane >= 16 && lane - 16 < cnt)
-            tma_load_2d(sm.wt + (lane - 16) * kWBlockBytes, &wmap, &full, (kb0 + lane - 16) * 64, 0);
-        if (lane == 31 && cnt > 0) bulk_load(sm.rsl, a.router_scale + (size_t)kb0 * 64, cnt * 128, &full);
+    } else if (warp == 1 && cl < ntiles) {
+        issue_loads(cl, true);
     }
     // Cluster barrier 0: every CTA's barriers exist before any remote write.
     tc_fence_before();
     cluster_barrier();
     tc_fence_after();
     const uint32_t tmem = tmem_base;
-    const bool have = mbar_wait(&full, 0, abort_flag);
+    const uint32_t rootb = f32_to_bf16_bits(a.root), root2 = rootb | (rootb << 16);
+    uint32_t ncommit = 0, nreload = 0;  // mdone and wfull phases used so far
 
-    // ---- 1. partial sums of squares of this slice, to every CTA ----
-    for (int t = warp; t < TT; t += kWarps) {
-        float hi = 0.f, lo = 0.f;
-        for (int i = lane; have && i < cnt * 8; i += 32) {
-            const uint4 v = *reinterpret_cast<const uint4*>(sm.xt + (i >> 3) * TT * 128 + sw128(t, i & 7));
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    // Persistent over token tiles: the cluster keeps its weight slice in
+    // shared memory (one chunk when E <= 128) and walks tiles cl, cl + ncl,
+    // ... Per tile two cluster barriers; the next tile's activations load
+    // while this tile's top k runs. Every CTA of the cluster walks the same
+    // tiles and passes the same barriers whatever happens.
+    int it = 0;
+    for (int tile = cl; tile < ntiles; tile += ncl, ++it) {
+        const int t0 = tile * TT;
+        const bool have = mbar_wait(&full, (uint32_t)it & 1, abort_flag);
+
+        // ---- 1. partial sums of squares of this slice, to every CTA ----
+        for (int t = warp; t < TT; t += kWarps) {
+            float hi = 0.f, lo = 0.f;
+            for (int i = lane; have && i < cnt * 8; i += 32) {
+                const uint4 v = *reinterpret_cast<const uint4*>(sm.xt + (i >> 3) * TT * 128 + sw128(t, i & 7));
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float x0 = bf16_bits_to_f32(w[j] & 0xFFFFu), x1 = bf16_bits_to_f32(w[j] >> 16);
-                acc2(hi, lo, __fmul_rn(x0, x0));  // squares of bf16 values are exact in fp32
-                acc2(hi, lo, __fmul_rn(x1, x1));
+                for (int j = 0; j < 4; ++j) {
+                    const float x0 = bf16_bits_to_f32(w[j] & 0xFFFFu), x1 = bf16_bits_to_f32(w[j] >> 16);
+                    acc2(hi, lo, __fmul_rn(x0, x0));  // squares of bf16 values are exact in fp32
+                    acc2(hi, lo, __fmul_rn(x1, x1));
+                }
+            }
+            // Butterfly: both lanes of a pair form the same (exact) two-sum,
+            // so every lane ends with the same value.
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float h2 = __shfl_xor_sync(0xffffffffu, hi, o), l2 = __shfl_xor_sync(0xffffffffu, lo, o);
+                float s, e;
+                two_sum(hi, h2, s, e);
+                hi = s;
+                lo = __fadd_rn(__fadd_rn(lo, l2), e);
+            }
+            if (lane < kCS) cluster.map_shared_rank(sm.pss, lane)[rank * TT + t] = make_float2(hi, lo);
+        }
+        __syncwarp();
+        cluster_barrier();  // A: all partial sums of squares delivered
+
+        // ---- 2. rsqrt of the fp32 mean, normalise this slice in place ----
+        for (int t = warp; t < TT; t += kWarps) {
+            float hs = 0.f, ls = 0.f;
+            for (int src = 0; src < kCS; ++src) {  // CTA order: the same result in every CTA
+                const float2 p = sm.pss[src * TT + t];
+                acc2(hs, ls, p.x);
+                ls = __fadd_rn(ls, p.y);
+            }
+            // mean = (hs + ls) / H rounded once to fp32, without fp64 (slow on
+            // this part): q = RN(hs / H); the residual hs - q H is exact
+            // (fma); adding (residual + ls) / H moves q by under half an ulp,
+            // so the sum rounds to the exactly rounded mean unless that mean
+            // lies within about 2^-40 (relative) of a rounding boundary.
+            const float Hf = (float)H;
+            const float q0 = __fdiv_rn(hs, Hf);
+            const float rsd = __fadd_rn(__fmaf_rn(-q0, Hf, hs), ls);
+            const float mean = __fadd_rn(q0, __fdiv_rn(rsd, Hf));
+            const float rs = __frsqrt_rn(__fadd_rn(mean, a.eps));
+            // bf16 after each op: x*rs in fp32 rounded once (cvt.rn), then the
+            // two bf16 x bf16 products, each exact in fp32 and rounded once
+            // (mul.rn.bf16x2), two elements an instruction.
+            for (int i = lane; have && i < cnt * 8; i += 32) {
+                uint4* p = reinterpret_cast<uint4*>(sm.xt + (i >> 3) * TT * 128 + sw128(t, i & 7));
+                const uint4 v = *p;
+                const uint4 s = reinterpret_cast<const uint4*>(sm.rsl)[i];  // router_scale of the same 8 columns
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w}, sc[4] = {s.x, s.y, s.z, s.w};
+                uint32_t o[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t n = pack_bf16x2(__fmul_rn(__uint_as_float(w[j] << 16), rs),
+                                                   __fmul_rn(__uint_as_float(w[j] & 0xFFFF0000u), rs));
+                    o[j] = mul_bf16x2(mul_bf16x2(n, sc[j]), root2);
+                }
+                *p = make_uint4(o[0], o[1], o[2], o[3]);
             }
         }
-        // Butterfly: both lanes of a pair form the same (exact) two-sum, so
-        // every lane ends with the same value.
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float h2 = __shfl_xor_sync(0xffffffffu, hi, o), l2 = __shfl_xor_sync(0xffffffffu, lo, o);
-            float s, e;
-            two_sum(hi, h2, s, e);
-            hi = s;
-            lo = __fadd_rn(__fadd_rn(lo, l2), e);
-        }
-        if (lane < kCS) cluster.map_shared_rank(sm.pss, lane)[rank * TT + t] = make_float2(hi, lo);
-    }
-    __syncwarp();
-    cluster_barrier();  // 1: all partial sums of squares delivered
+        // The normalised tile was written by ordinary stores; the tensor core
+        // reads it through the async proxy.
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncthreads();
 
-    // ---- 2. rsqrt of the fp32 mean, normalise this slice in place ----
-    for (int t = warp; t < TT; t += kWarps) {
-        float hs = 0.f, ls = 0.f;
-        for (int src = 0; src < kCS; ++src) {  // CTA order: the same result in every CTA
-            const float2 p = sm.pss[src * TT + t];
-            acc2(hs, ls, p.x);
-            ls = __fadd_rn(ls, p.y);
-        }
-        // mean = (hs + ls) / H rounded once to fp32, without fp64 (slow on
-        // this part): q = RN(hs / H); the residual hs - q H is exact (fma);
-        // adding (residual + ls) / H moves q by under half an ulp, so the
-        // sum rounds to the exactly rounded mean unless that mean lies within
-        // about 2^-40 (relative) of a rounding boundary.
-        const float Hf = (float)H;
-        const float q0 = __fdiv_rn(hs, Hf);
-        const float rsd = __fadd_rn(__fmaf_rn(-q0, Hf, hs), ls);
-        const float mean = __fadd_rn(q0, __fdiv_rn(rsd, Hf));
-        const float rs = __frsqrt_rn(__fadd_rn(mean, a.eps));
-        for (int i = lane; have && i < cnt * 8; i += 32) {
-            uint4* p = reinterpret_cast<uint4*>(sm.xt + (i >> 3) * TT * 128 + sw128(t, i & 7));
-            const uint4 v = *p;
-            const uint4 s = reinterpret_cast<const uint4*>(sm.rsl)[i];  // router_scale of the same 8 columns
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w}, sc[4] = {s.x, s.y, s.z, s.w};
-            uint32_t o[4];
+        // ---- 3. partial scores over this slice, to the CTA owning each token ----
+        // D[e][t] = sum over this slice of W[e][h] * n[t][h], experts on the
+        // 128 TMEM lanes and tokens on TT columns: one tcgen05.mma per 16 K
+        // (A = the weight chunk, B = the normalised tile, both K-major in
+        // shared memory).
+        const uint32_t idesc = idesc_bf16_m128((uint32_t)TT);
+        for (int ch = 0; ch < nch; ++ch) {
+            bool wok = have;
+            // With more than one chunk, chunk ch (and chunk 0 again from the
+            // second tile on) is reloaded into the weight buffer.
+            if (ch > 0 || (nch > 1 && it > 0)) {
+                __syncthreads();  // every warp has read the previous chunk's scores
+                if (threadIdx.x == 0) {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    mbar_arrive_expect_tx(&wfull, (uint32_t)cnt * eb * 128);
+                    for (int i = 0; i < cnt; ++i)
+                        tma_load_2d(sm.wt + i * kWBlockBytes, &wmap, &wfull, (kb0 + i) * 64, ch * kChunkE);
+                }
+                wok = mbar_wait(&wfull, nreload & 1, abort_flag) && wok;
+                ++nreload;
+            }
+            const bool mma = wok && cnt > 0;
+            if (warp == 0 && mma) {
+                tc_fence_after();
+                if (elect_one()) {
+                    for (int kb = 0; kb < cnt; ++kb) {
+                        const uint64_t ad = sw128_kmajor_desc(smem_u32(sm.wt + kb * kWBlockBytes));
+                        const uint64_t bd = sw128_kmajor_desc(smem_u32(sm.xt + kb * TT * 128));
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                float n_lo = bf16_bits_to_f32(f32_to_bf16_bits(__fmul_rn(bf16_bits_to_f32(w[j] & 0xFFFFu), rs)));
-                float n_hi = bf16_bits_to_f32(f32_to_bf16_bits(__fmul_rn(bf16_bits_to_f32(w[j] >> 16), rs)));
-                n_lo = bf16_bits_to_f32(f32_to_bf16_bits(__fmul_rn(n_lo, bf16_bits_to_f32(sc[j] & 0xFFFFu))));
-                n_hi = bf16_bits_to_f32(f32_to_bf16_bits(__fmul_rn(n_hi, bf16_bits_to_f32(sc[j] >> 16))));
-                o[j] = pack_bf16x2(__fmul_rn(n_lo, a.root), __fmul_rn(n_hi, a.root));
+                        for (int k16 = 0; k16 < 4; ++k16)
+                            umma_ss(tmem, ad + (uint64_t)(k16 * 2), bd + (uint64_t)(k16 * 2), idesc,
+                                    (kb > 0 || k16 > 0) ? 1u : 0u);
+                    }
+                    umma_commit(&mdone);
+                }
+                __syncwarp();
             }
-            *p = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-    }
-    // The normalised tile was written by ordinary stores; the tensor core
-    // reads it through the async proxy.
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    __syncthreads();
-
-    // ---- 3. partial scores over this slice, to the CTA owning each token ----
-    // D[e][t] = sum over this slice of W[e][h] * n[t][h], experts on the 128
-    // TMEM lanes and tokens on TT columns: one tcgen05.mma per 16 K (A = the
-    // weight chunk, B = the normalised tile, both K-major in shared memory).
-    const uint32_t idesc = idesc_bf16_m128((uint32_t)TT);
-    for (int ch = 0; ch < nch; ++ch) {
-        bool wok = have;
-        if (ch > 0) {
-            __syncthreads();  // every warp has read the previous chunk's scores
-            if (threadIdx.x == 0) {
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                mbar_arrive_expect_tx(&wfull, (uint32_t)cnt * eb * 128);
-                for (int i = 0; i < cnt; ++i)
-                    tma_load_2d(sm.wt + i * kWBlockBytes, &wmap, &wfull, (kb0 + i) * 64, ch * kChunkE);
-            }
-            wok = mbar_wait(&wfull, (ch - 1) & 1, abort_flag) && wok;
-        }
-        const bool mma = wok && cnt > 0;
-        if (warp == 0 && mma) {
+            // Every CTA of the cluster commits (or skips) the same MMAs, so
+            // the phase count stays in step; a skipped commit leaves the
+            // count unchanged.
+            const bool got = mma && mbar_wait(&mdone, ncommit & 1, abort_flag);
+            if (mma) ++ncommit;
             tc_fence_after();
-            if (elect_one()) {
-                for (int kb = 0; kb < cnt; ++kb) {
-                    const uint64_t ad = sw128_kmajor_desc(smem_u32(sm.wt + kb * kWBlockBytes));
-                    const uint64_t bd = sw128_kmajor_desc(smem_u32(sm.xt + kb * TT * 128));
+            // Warp w reads TMEM lane quarter w % 4 (experts ch*128 + 32(w%4) +
+            // lane) and the 16 token columns 16 (w / 4) .. 16 (w / 4) + 15.
+            const int e = ch * kChunkE + (warp & 3) * 32 + lane;
+            const int c0 = (warp >> 2) * 16;
+            if (c0 < TT) {
+                uint32_t v[16];
+                if (got) {
+                    tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)c0, v);
+                    tmem_wait_ld();
+                } else {
 #pragma unroll
-                    for (int k16 = 0; k16 < 4; ++k16)
-                        umma_ss(tmem, ad + (uint64_t)(k16 * 2), bd + (uint64_t)(k16 * 2), idesc,
-                                (kb > 0 || k16 > 0) ? 1u : 0u);
+                    for (int j = 0; j < 16; ++j) v[j] = 0u;  // no K blocks here (or a wait timed out)
                 }
-                umma_commit(&mdone);
-            }
-            __syncwarp();
-        }
-        const bool got = mma && mbar_wait(&mdone, ch & 1, abort_flag);
-        tc_fence_after();
-        // Warp w reads TMEM lane quarter w % 4 (experts ch*128 + 32(w%4) +
-        // lane) and the 16 token columns 16 (w / 4) .. 16 (w / 4) + 15.
-        const int e = ch * kChunkE + (warp & 3) * 32 + lane;
-        const int c0 = (warp >> 2) * 16;
-        if (c0 < TT) {
-            uint32_t v[16];
-            if (got) {
-                tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)c0, v);
-                tmem_wait_ld();
-            } else {
+                if (e < E) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) v[j] = 0u;  // no K blocks here (or a wait timed out)
-            }
-            if (e < E) {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int tok = c0 + j;
-                    cluster.map_shared_rank(sm.red, tok / tpc)[(size_t)(rank * tpc + tok % tpc) * E + e] =
-                        __uint_as_float(v[j]);
+                    for (int j = 0; j < 16; ++j) {
+                        const int tok = c0 + j;
+                        cluster.map_shared_rank(sm.red, tok / tpc)[(size_t)(rank * tpc + tok % tpc) * E + e] =
+                            __uint_as_float(v[j]);
+                    }
                 }
             }
+            tc_fence_before();
         }
-        tc_fence_before();
-    }
-    __syncwarp();
-    cluster_barrier();  // 2: all partial scores delivered; no remote access after this
+        __syncwarp();
+        cluster_barrier();  // B: all partial scores delivered; no remote access until A of the next tile
 
-    // ---- 4. my tokens: scores, top k, precise softmax, per-expert scale ----
-    for (int i = threadIdx.x; i < tpc * E; i += kWarps * 32) {
-        const int tl = i / E, e = i % E;
-        float s = 0.f;
-        for (int src = 0; src < kCS; ++src) s = __fadd_rn(s, sm.red[(size_t)(src * tpc + tl) * E + e]);
-        sm.sc[tl * E + e] = (uint16_t)f32_to_bf16_bits(s);
-    }
-    __syncthreads();
-    for (int tl = warp; tl < tpc; tl += kWarps) {
-        const int t = t0 + rank * tpc + tl;
-        if (t >= a.T) continue;
-        const uint16_t* sr = sm.sc + tl * E;
-        uint32_t cand[8];  // keys of this lane's experts e = lane + 32 i
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int e = lane + 32 * i;
-            cand[i] = (e < E) ? ((order_key16(sr[e]) << 16) | (0xFFFFu - (uint32_t)e)) : 0u;
+        // The activation buffer is free (the MMAs read it before their
+        // commit): load the next tile's slice while this tile's top k runs.
+        if (warp == 1 && tile + ncl < ntiles) issue_loads(tile + ncl, false);
+
+        // ---- 4. my tokens: scores, top k, precise softmax, per-expert scale ----
+        for (int i = threadIdx.x; i < tpc * E; i += kWarps * 32) {
+            const int tl = i / E, e = i % E;
+            float s = 0.f;
+            for (int src = 0; src < kCS; ++src) s = __fadd_rn(s, sm.red[(size_t)(src * tpc + tl) * E + e]);
+            sm.sc[tl * E + e] = (uint16_t)f32_to_bf16_bits(s);
         }
-        int my_idx = 0;
-        float my_s = 0.f, top_s = 0.f;
-        for (int j = 0; j < k; ++j) {
-            uint32_t best = 0;
+        __syncthreads();
+        for (int tl = warp; tl < tpc; tl += kWarps) {
+            const int t = t0 + rank * tpc + tl;
+            if (t >= a.T) continue;
+            const uint16_t* sr = sm.sc + tl * E;
+            uint32_t cand[8];  // keys of this lane's experts e = lane + 32 i
 #pragma unroll
-            for (int i = 0; i < 8; ++i) best = max(best, cand[i]);
-            const uint32_t win = __reduce_max_sync(0xffffffffu, best);
-            const int e = (int)(0xFFFFu - (win & 0xFFFFu));
-            const float s = bf16_bits_to_f32(key16_to_bits(win >> 16));
-            if (j == 0) top_s = s;
-            if (lane == j) {
-                my_idx = e;
-                my_s = s;
+            for (int i = 0; i < 8; ++i) {
+                const int e = lane + 32 * i;
+                cand[i] = (e < E) ? ((order_key16(sr[e]) << 16) | (0xFFFFu - (uint32_t)e)) : 0u;
             }
+            int my_idx = 0;
+            float my_s = 0.f, top_s = 0.f;
+            for (int j = 0; j < k; ++j) {
+                uint32_t best = 0;
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                if (cand[i] == win) cand[i] = 0u;
+                for (int i = 0; i < 8; ++i) best = max(best, cand[i]);
+                const uint32_t win = __reduce_max_sync(0xffffffffu, best);
+                const int e = (int)(0xFFFFu - (win & 0xFFFFu));
+                const float s = bf16_bits_to_f32(key16_to_bits(win >> 16));
+                if (j == 0) top_s = s;
+                if (lane == j) {
+                    my_idx = e;
+                    my_s = s;
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (cand[i] == win) cand[i] = 0u;
+            }
+            const float ex = (lane < k) ? expf(__fsub_rn(my_s, top_s)) : 0.f;
+            float sum = 0.f;
+            for (int j = 0; j < k; ++j) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, ex, j));
+            if (lane < k) {
+                const float p = bf16_bits_to_f32(f32_to_bf16_bits(__fdiv_rn(ex, sum)));
+                const float pes = bf16_bits_to_f32(pes_s[my_idx]);
+                a.idx[(size_t)t * k + lane] = my_idx;
+                a.w[(size_t)t * k + lane] = (uint16_t)f32_to_bf16_bits(__fmul_rn(p, pes));
+            }
         }
-        const float ex = (lane < k) ? expf(__fsub_rn(my_s, top_s)) : 0.f;
-        float sum = 0.f;
-        for (int j = 0; j < k; ++j) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, ex, j));
-        if (lane < k) {
-            const float p = bf16_bits_to_f32(f32_to_bf16_bits(__fdiv_rn(ex, sum)));
-            const float pes = bf16_bits_to_f32(a.per_expert_scale[my_idx]);
-            a.idx[(size_t)t * k + lane] = my_idx;
-            a.w[(size_t)t * k + lane] = (uint16_t)f32_to_bf16_bits(__fmul_rn(p, pes));
-        }
+        __syncwarp();
+        __syncthreads();  // sc and red are read; the next tile may overwrite them
     }
-    __syncwarp();
-    __syncthreads();
+    // The last tile's activation copies (if any were issued without a tile
+    // to use them) cannot be pending: loads are issued only for tiles walked.
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -379,9 +419,9 @@ cudaError_t ensure_router_attr() {
     return cudaSuccess;
 }
 
-cudaLaunchConfig_t router_config(int T, int tt, size_t smem, cudaStream_t stream, cudaLaunchAttribute* attr) {
+cudaLaunchConfig_t router_config(int clusters, size_t smem, cudaStream_t stream, cudaLaunchAttribute* attr) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(((T + tt - 1) / tt) * kCS), 1, 1);
+    cfg.gridDim = dim3((unsigned)(clusters * kCS), 1, 1);
     cfg.blockDim = dim3(kWarps * 32, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
@@ -407,7 +447,7 @@ int router_resident_clusters(size_t smem) {
     auto it = cache.find({dev, smem});
     if (it != cache.end()) return it->second;
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = router_config(kCS, 16, smem, nullptr, attr);
+    cudaLaunchConfig_t cfg = router_config(1, smem, nullptr, attr);
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, router_kernel, &cfg) != cudaSuccess || n < 1) n = 1;
     cache[{dev, smem}] = n;
@@ -436,8 +476,12 @@ cudaError_t launch_router(const CUtensorMap& wmap, const CUtensorMap& xmap, cons
     if (smem > kRouterSmemLimit || a.tt % 16 != 0 || a.tt > 64) return cudaErrorInvalidValue;
     cudaError_t err = ensure_router_attr();
     if (err != cudaSuccess) return err;
+    // Persistent clusters: as many as the device holds at once, at most one
+    // per token tile; each walks its share of the tiles.
+    const int ntiles = (a.T + a.tt - 1) / a.tt;
+    const int clusters = std::min(ntiles, router_resident_clusters(smem));
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = router_config(a.T, a.tt, smem, stream, attr);
+    cudaLaunchConfig_t cfg = router_config(clusters, smem, stream, attr);
     return cudaLaunchKernelEx(&cfg, router_kernel, wmap, xmap, a);
 }
 
