@@ -155,24 +155,59 @@ __host__ __device__ inline int chunk_slots(int S) {
 
 // One CTA of 32 warps sorts everything; warp w owns the contiguous slot range
 // [w*per, (w+1)*per). Warps cover the slots in order, so the sort is stable
-// and the result unique.
+// and the result unique. A lane keeps its (at most 8) expert ids in
+// registers from one round of loads for both passes.
 __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs a) {
     __shared__ DispatchSmem sm;
+    constexpr int kPerLane = kDispatchSingleMaxSlots / kDispatchThreads;  // 8
     pdl_trigger();
     pdl_wait();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    zero_warp_counts(sm, tid);
-    __syncthreads();
     const int per = (a.S + kW - 1) / kW;
     const int c0 = min(a.S, warp * per), c1 = min(a.S, c0 + per);
-    warp_histogram(a.idx, c0, c1, a.E, sm.wh[warp], lane, true);
+    int ev[kPerLane];
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) {
+        const int f = c0 + 32 * i + lane;
+        int e = (f < c1) ? a.idx[f] : -1;
+        if (f < c1 && (e < 0 || e >= a.E)) {
+            atomicOr(&g_error_word, kErrBadExpert);
+            e = -1;
+        }
+        ev[i] = e;
+    }
+    zero_warp_counts(sm, tid);
+    __syncthreads();
+    const unsigned lt_mask = (1u << lane) - 1u;
+    int* wh = sm.wh[warp];
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) {
+        if (c0 + 32 * i >= c1) break;  // warp-uniform
+        const unsigned peers = __match_any_sync(0xffffffffu, ev[i]);
+        if (ev[i] >= 0 && (peers & lt_mask) == 0) wh[ev[i]] += __popc(peers);
+    }
     __syncthreads();
     scan_over_warps(sm, sm.cnt, a.E, warp, lane);
     __syncthreads();
     finish_experts(a, sm, tid, warp, lane);
     for (int i = tid; i < kW * a.E; i += kDispatchThreads) sm.wh[i / a.E][i % a.E] += sm.off[i % a.E];
     __syncthreads();
-    warp_scatter(a, c0, c1, sm.wh[warp], lane);
+    // stable scatter in slot order from the warp's running bases
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) {
+        if (c0 + 32 * i >= c1) break;  // warp-uniform
+        const int f = c0 + 32 * i + lane, e = ev[i];
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(peers & lt_mask);
+        if (e >= 0) {
+            const int p = wh[e] + rank;
+            a.perm[p] = f;
+            a.inv[f] = p;
+        }
+        __syncwarp();
+        if (e >= 0 && rank == 0) wh[e] += __popc(peers);
+        __syncwarp();
+    }
 }
 
 // Three-kernel path for large S. 1: CTA c counts its slot chunk by expert.
@@ -242,8 +277,9 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_scatter_kernel(Disp
 }
 
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
-    if (a.chunk_hist == nullptr || a.S <= kDispatchSingleMaxSlots)
+    if (a.S <= kDispatchSingleMaxSlots)  // the one-CTA sort holds up to 8 slots a thread in registers
         return launch_pdl(dispatch_kernel, dim3(1), dim3(kDispatchThreads), 0, stream, a);
+    if (a.chunk_hist == nullptr) return cudaErrorInvalidValue;
     const int nch = (a.S + chunk_slots(a.S) - 1) / chunk_slots(a.S);  // <= kDispatchMaxChunks
     cudaError_t e = launch_pdl(dispatch_count_kernel, dim3(nch), dim3(kDispatchThreads), 0, stream, a);
     if (e == cudaSuccess) e = launch_pdl(dispatch_scan_kernel, dim3(1), dim3(kDispatchThreads), 0, stream, a);
@@ -306,15 +342,14 @@ __global__ void __launch_bounds__(128) combine_kernel(const uint16_t* __restrict
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
     for (int j = 0; j < k; ++j) {
-        const float wj = bf16_bits_to_f32(__ldg(wt + j));
+        const uint32_t wb = __ldg(wt + j), w2 = wb | (wb << 16);
         const uint4 v = __ldg(yt + (size_t)j * chunks);
         const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const float lo = bf16_bits_to_f32(f32_to_bf16_bits(__fmul_rn(bf16_bits_to_f32(u[q] & 0xFFFFu), wj)));
-            const float hi = bf16_bits_to_f32(f32_to_bf16_bits(__fmul_rn(bf16_bits_to_f32(u[q] >> 16), wj)));
-            acc[2 * q] = __fadd_rn(acc[2 * q], lo);
-            acc[2 * q + 1] = __fadd_rn(acc[2 * q + 1], hi);
+            const uint32_t p = mul_bf16x2(u[q], w2);  // bf16(y * w), both halves
+            acc[2 * q] = __fadd_rn(acc[2 * q], __uint_as_float(p << 16));
+            acc[2 * q + 1] = __fadd_rn(acc[2 * q + 1], __uint_as_float(p & 0xFFFF0000u));
         }
     }
     reinterpret_cast<uint4*>(out + (size_t)t * H)[c] =
