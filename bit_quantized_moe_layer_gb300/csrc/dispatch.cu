@@ -6,6 +6,8 @@
 //  - gather: the sorted path's take of x rows (rowIdx), stored in the K order
 //    the grouped GEMM's dequantised weights use;
 //  - combine: the un-sort, (y * weights[..., None]).sum(-2), per token.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -15,6 +17,7 @@ namespace {
 constexpr int kDispatchThreads = 1024;
 constexpr int kW = kDispatchThreads / 32;
 constexpr int kMaxE = 256;
+constexpr int kFusedMaxRows = 64;  // sorted rows a CTA of the fused dispatch + gather writes
 
 struct DispatchSmem {
     int wh[kW][kMaxE + 1];  // per-warp counts, then per-warp bases
@@ -58,7 +61,7 @@ __device__ __forceinline__ void scan_over_warps(DispatchSmem& sm, int* cnt, int 
 // over experts by warp 0), then offsets, the tile list and (tile count, rows
 // of the largest tile) to global memory. Every thread of the CTA calls it.
 __device__ __forceinline__ void finish_experts(const DispatchArgs& a, DispatchSmem& sm, int tid, int warp,
-                                               int lane) {
+                                               int lane, bool write_out = true) {
     const int E = a.E;
     if (warp == 0) {  // lane owns experts [8 lane, 8 lane + 8)
         int lc[8], lt[8], sc = 0, st = 0;
@@ -96,6 +99,7 @@ __device__ __forceinline__ void finish_experts(const DispatchArgs& a, DispatchSm
         }
     }
     __syncthreads();
+    if (!write_out) return;
     for (int e = tid; e <= E; e += blockDim.x) a.offsets[e] = sm.off[e];
     if (a.tiles) {
         for (int e = tid; e < E; e += blockDim.x) {
@@ -144,6 +148,16 @@ __device__ __forceinline__ void warp_scatter(const DispatchArgs& a, int c0, int 
 
 __device__ __forceinline__ void zero_warp_counts(DispatchSmem& sm, int tid) {
     for (int i = tid; i < kW * (kMaxE + 1); i += kDispatchThreads) (&sm.wh[0][0])[i] = 0;
+}
+
+// 8 bf16 (one 16-byte chunk) -> positions holding elements (0,4,1,5,2,6,3,7).
+__device__ __forceinline__ uint4 interleave8(uint4 v) {
+    uint4 o;
+    o.x = __byte_perm(v.x, v.z, 0x5410);
+    o.y = __byte_perm(v.x, v.z, 0x7632);
+    o.z = __byte_perm(v.y, v.w, 0x5410);
+    o.w = __byte_perm(v.y, v.w, 0x7632);
+    return o;
 }
 
 // Slot chunk of CTA c in the three-kernel path.
@@ -207,6 +221,84 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
         __syncwarp();
         if (e >= 0 && rank == 0) wh[e] += __popc(peers);
         __syncwarp();
+    }
+}
+
+// Dispatch fused with the gather (S <= kDispatchSingleMaxSlots): every CTA
+// redoes the whole counting sort in shared memory (2 K slots: cheap, and no
+// CTA waits for another), then writes the sorted rows [r0, r0 + rows) of its
+// own range: perm, inv and xs[p] = interleave(x[perm[p] / k]). CTA 0 also
+// writes the offsets and the tile list. The result equals dispatch_kernel's
+// followed by gather_kernel's.
+__global__ void __launch_bounds__(kDispatchThreads) dispatch_gather_kernel(DispatchArgs a,
+                                                                           const uint16_t* __restrict__ x,
+                                                                           uint16_t* __restrict__ xs, int k, int H,
+                                                                           int rows) {
+    __shared__ DispatchSmem sm;
+    __shared__ int32_t src_tok[kFusedMaxRows];  // token of each row of this CTA's range
+    constexpr int kPerLane = kDispatchSingleMaxSlots / kDispatchThreads;  // 8
+    pdl_trigger();
+    pdl_wait();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r0 = blockIdx.x * rows, r1 = r0 + rows;
+    const int per = (a.S + kW - 1) / kW;
+    const int c0 = min(a.S, warp * per), c1 = min(a.S, c0 + per);
+    int ev[kPerLane];
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) {
+        const int f = c0 + 32 * i + lane;
+        int e = (f < c1) ? a.idx[f] : -1;
+        if (f < c1 && (e < 0 || e >= a.E)) {
+            if (blockIdx.x == 0) atomicOr(&g_error_word, kErrBadExpert);
+            e = -1;
+        }
+        ev[i] = e;
+    }
+    zero_warp_counts(sm, tid);
+    for (int i = tid; i < rows; i += kDispatchThreads) src_tok[i] = -1;
+    __syncthreads();
+    const unsigned lt_mask = (1u << lane) - 1u;
+    int* wh = sm.wh[warp];
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) {
+        if (c0 + 32 * i >= c1) break;  // warp-uniform
+        const unsigned peers = __match_any_sync(0xffffffffu, ev[i]);
+        if (ev[i] >= 0 && (peers & lt_mask) == 0) wh[ev[i]] += __popc(peers);
+    }
+    __syncthreads();
+    scan_over_warps(sm, sm.cnt, a.E, warp, lane);
+    __syncthreads();
+    finish_experts(a, sm, tid, warp, lane, blockIdx.x == 0);
+    for (int i = tid; i < kW * a.E; i += kDispatchThreads) sm.wh[i / a.E][i % a.E] += sm.off[i % a.E];
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) {
+        if (c0 + 32 * i >= c1) break;  // warp-uniform
+        const int f = c0 + 32 * i + lane, e = ev[i];
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(peers & lt_mask);
+        if (e >= 0) {
+            const int p = wh[e] + rank;
+            if (p >= r0 && p < r1) {
+                a.perm[p] = f;
+                a.inv[f] = p;
+                src_tok[p - r0] = f / k;
+            }
+        }
+        __syncwarp();
+        if (e >= 0 && rank == 0) wh[e] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    // One warp a row: 16-byte chunks of x[t], interleaved, lane-strided.
+    const int chunks = H / 8;
+    for (int rr = warp; rr < rows; rr += kW) {
+        const int t = src_tok[rr];
+        if (t < 0) continue;  // past the last valid slot
+        const uint4* srow = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+        uint4* drow = reinterpret_cast<uint4*>(xs + (size_t)(r0 + rr) * H);
+#pragma unroll 4
+        for (int c = lane; c < chunks; c += 32) drow[c] = interleave8(__ldg(srow + c));
     }
 }
 
@@ -276,6 +368,17 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_scatter_kernel(Disp
     warp_scatter(a, c0, c1, sm.wh[warp], lane);
 }
 
+cudaError_t launch_dispatch_gather(const DispatchArgs& a, const uint16_t* x, uint16_t* xs, int k, int H, int sms,
+                                   cudaStream_t stream) {
+    if (a.S == 0) return cudaSuccess;
+    // One wave (a 1024-thread CTA of 64 registers fills an SM): at least 8
+    // rows (45 KB at H = 2816) a CTA, at most one CTA an SM.
+    const int rows = std::max(8, (a.S + sms - 1) / std::max(1, sms));
+    if (a.S > kDispatchSingleMaxSlots || rows > kFusedMaxRows) return cudaErrorInvalidValue;
+    const int grid = (a.S + rows - 1) / rows;
+    return launch_pdl(dispatch_gather_kernel, dim3(grid), dim3(kDispatchThreads), 0, stream, a, x, xs, k, H, rows);
+}
+
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
     if (a.S <= kDispatchSingleMaxSlots)  // the one-CTA sort holds up to 8 slots a thread in registers
         return launch_pdl(dispatch_kernel, dim3(1), dim3(kDispatchThreads), 0, stream, a);
@@ -287,15 +390,6 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
     return e;
 }
 
-// 8 bf16 (one 16-byte chunk) -> positions holding elements (0,4,1,5,2,6,3,7).
-__device__ __forceinline__ uint4 interleave8(uint4 v) {
-    uint4 o;
-    o.x = __byte_perm(v.x, v.z, 0x5410);
-    o.y = __byte_perm(v.x, v.z, 0x7632);
-    o.z = __byte_perm(v.y, v.w, 0x5410);
-    o.w = __byte_perm(v.y, v.w, 0x7632);
-    return o;
-}
 
 // One warp per sorted row p: t = perm[p] / k, then the warp's lanes copy the
 // row's 16-byte chunks (8 bf16 each), interleaved, lane-strided.

@@ -69,6 +69,10 @@ struct DispatchArgs {
 constexpr int kDispatchMaxChunks = 64;
 constexpr int kDispatchSingleMaxSlots = 8192;  // above this the sort runs as three kernels
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream);
+// Dispatch and gather in one launch (S <= kDispatchSingleMaxSlots): the same
+// perm, inv, offsets, tiles and xs as launch_dispatch then launch_gather.
+cudaError_t launch_dispatch_gather(const DispatchArgs& a, const uint16_t* x, uint16_t* xs, int k, int H, int sms,
+                                   cudaStream_t stream);
 
 // Gather: xs[p] = x[perm[p] / k] with each 8-element block of K stored in
 // the order (0,4,1,5,2,6,3,7), the order the grouped GEMM's dequantised

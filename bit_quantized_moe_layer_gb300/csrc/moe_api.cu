@@ -225,12 +225,20 @@ int run_experts(const moe_dims* d, const uint16_t* x, const int32_t* idx, const 
         return MOE_ERR_CUDA;
 
     DispatchArgs da{idx, perm, offsets, inv, tiles, ntiles, S, E, nmax, reinterpret_cast<int32_t*>(ws + L.dhist)};
-    int rc = fail(launch_dispatch(da, s));
-    if (rc) return rc;
-    tm.mark(2);
-    rc = fail(launch_gather(x, perm, offsets, xs, S, d->k, H, E, s));
-    if (rc) return rc;
-    tm.mark(3);
+    int rc;
+    if (S <= kDispatchSingleMaxSlots) {  // one launch: every CTA sorts, then gathers its rows
+        rc = fail(launch_dispatch_gather(da, x, xs, d->k, H, di.sms, s));
+        if (rc) return rc;
+        tm.mark(2);
+        tm.mark(3);
+    } else {
+        rc = fail(launch_dispatch(da, s));
+        if (rc) return rc;
+        tm.mark(2);
+        rc = fail(launch_gather(x, perm, offsets, xs, S, d->k, H, E, s));
+        if (rc) return rc;
+        tm.mark(3);
+    }
 
     GemmArgs ga{};
     ga.scales = gu->scales;
