@@ -536,7 +536,9 @@ int moe_timing_read(float* ms, int n, int* calls) {
 
 int moe_launches_per_forward(const moe_dims* d) {
     if (check_dims(d) != MOE_OK) return 0;
-    return kStages + (((int64_t)d->T * d->k > kDispatchSingleMaxSlots) ? 2 : 0);
+    // router, dispatch fused with the gather, gate_up, down, combine; above
+    // 8192 slots the dispatch runs as three kernels and the gather as its own
+    return ((int64_t)d->T * d->k > kDispatchSingleMaxSlots) ? 8 : 5;
 }
 
 int moe_device_error(void) {

@@ -188,8 +188,9 @@ int moe_timing_enable(int enable);
 int moe_timing_read(float* ms, int n, int* calls);
 
 /* Number of kernel launches one moe_forward call with these dims makes
- * (6; 8 when T*k > 8192, where dispatch runs as three kernels); 0 if the
- * dims are rejected. */
+ * (5: router, dispatch fused with the gather, gate_up, down, combine; 8 when
+ * T*k > 8192, where dispatch runs as three kernels and the gather as its
+ * own); 0 if the dims are rejected. */
 int moe_launches_per_forward(const moe_dims* d);
 
 /*
