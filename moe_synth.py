@@ -160,6 +160,14 @@ def make_layer(wl, T: int | None = None, seed: int | None = None) -> LayerInputs
     return LayerInputs(d, x, wr, sc, pes, gw, gs, gb, dw, ds, db)
 
 
+def make_branch_norms(d: Dims, seed: int = 0):
+    """Weights [H] of the MoE branch's two RMS norms (pre_feedforward_layernorm_2,
+    post_feedforward_layernorm_2) as bf16 bits, U(0.5, 1.5) like the router
+    scale (trained RMS-norm weights are O(1) and positive)."""
+    rng = _rng(seed, f"branch-norms:{d.H}")
+    return bf16_bits(rng.uniform(0.5, 1.5, d.H)), bf16_bits(rng.uniform(0.5, 1.5, d.H))
+
+
 def make_custom(d: Dims, seed: int = 0, **skew) -> LayerInputs:
     """Inputs for an arbitrary layer shape with the standard distributions."""
     return make_layer(Workload("custom", d, seed=seed, **skew))

@@ -67,6 +67,10 @@ def _declare(lib):
     lib.oracle_experts.restype = ctypes.c_int
     lib.oracle_forward.argtypes = [ctypes.POINTER(_Dims)] + [P] * 13 + [ctypes.c_int]
     lib.oracle_forward.restype = ctypes.c_int
+    lib.oracle_rms_norm.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_float, P, P, P]
+    lib.oracle_rms_norm.restype = ctypes.c_int
+    lib.oracle_moe_branch.argtypes = [ctypes.POINTER(_Dims)] + [P] * 16 + [ctypes.c_int]
+    lib.oracle_moe_branch.restype = ctypes.c_int
     return lib
 
 
@@ -166,3 +170,37 @@ def forward(inp, nthreads: int = 0, lib=None):
     if rc != 0:
         raise ValueError(f"oracle_forward rejected the inputs ({rc})")
     return out, idx, w
+
+
+def rms_norm(x, weight, eps: float, lib=None):
+    """RMSNorm with a weight (the decoder layer's plain nn.RMSNorm): x [T,H]
+    and weight [H] bf16 bits -> [T,H] bf16 bits."""
+    lib = lib or load()
+    x = _c(x, np.uint16)
+    T, H = x.shape
+    out = np.zeros((T, H), np.uint16)
+    rc = lib.oracle_rms_norm(T, H, ctypes.c_float(eps), _p(x), _p(_c(weight, np.uint16)), _p(out))
+    if rc != 0:
+        raise ValueError(f"oracle_rms_norm rejected the inputs ({rc})")
+    return out
+
+
+def moe_branch(inp, pre_norm_w, post_norm_w, taps: bool = False, nthreads: int = 0, lib=None):
+    """The decoder layer's MoE branch: route on the residual (inp.x), experts
+    on preFfNorm2(residual), postFfNorm2 of their combined output. Returns
+    (out, idx, w[, expert input])."""
+    lib = lib or load()
+    d = inp.dims
+    out = np.zeros((d.T, d.H), np.uint16)
+    idx = np.zeros((d.T, d.k), np.int32)
+    w = np.zeros((d.T, d.k), np.uint16)
+    xe = np.zeros((d.T, d.H), np.uint16) if taps else None
+    dims = _dims(d)
+    arrs = [inp.x, inp.router_w, inp.router_scale, inp.pes, pre_norm_w, post_norm_w, inp.gu_w, inp.gu_s,
+            inp.gu_b, inp.dn_w, inp.dn_s, inp.dn_b]
+    arrs = [np.ascontiguousarray(a) for a in arrs]
+    rc = lib.oracle_moe_branch(ctypes.byref(dims), *[_p(a) for a in arrs], _p(out), _p(idx), _p(w),
+                               _p(xe) if taps else None, nthreads)
+    if rc != 0:
+        raise ValueError(f"oracle_moe_branch rejected the inputs ({rc})")
+    return (out, idx, w, xe) if taps else (out, idx, w)

@@ -397,6 +397,68 @@ int oracle_experts(const oracle_dims* d, const uint16_t* x, const int32_t* idx, 
     return 0;
 }
 
+/* RMSNorm with a weight: the decoder layer's plain nn.RMSNorm (the weight is
+ * used as it is, no 1 + weight offset; "diffusion-gemma/model.ts", header
+ * notes and DiffusionGemmaDecoderLayer), in fp32 like the router's norm:
+ * r = rsqrt(mean(x^2) + eps) with the fp32 mean the exact mean rounded once,
+ * then bf16((x * r) * w), each fp32 product rounded, one bf16 rounding. */
+int oracle_rms_norm(int32_t T, int32_t H, float eps, const uint16_t* x, const uint16_t* weight,
+                    uint16_t* out) {
+    if (T < 0 || H <= 0) return -1;
+    for (int t = 0; t < T; ++t) {
+        const uint16_t* xt = x + (size_t)t * H;
+        double ss = 0.0;
+        for (int h = 0; h < H; ++h) {
+            double v = bf(xt[h]);
+            ss += v * v;
+        }
+        float mean = (float)(ss / (double)H);
+        float r = (float)(1.0 / sqrt((double)(mean + eps)));
+        for (int h = 0; h < H; ++h) {
+            float nv = bf(xt[h]) * r;
+#if ORACLE_MUTANT == 8
+            out[(size_t)t * H + h] = bf16_from_float(nv); /* planted: weight dropped */
+#else
+            out[(size_t)t * H + h] = bf16_from_float(nv * bf(weight[h]));
+#endif
+        }
+    }
+    return 0;
+}
+
+/* The MoE branch of a decoder layer (DiffusionGemmaDecoderLayer.forwardWith):
+ * the router reads the residual, the experts read preFfNorm2(residual), and
+ * the experts' combined output goes through postFfNorm2. */
+int oracle_moe_branch(const oracle_dims* d, const uint16_t* residual, const uint16_t* router_w,
+                      const uint16_t* router_scale, const uint16_t* per_expert_scale,
+                      const uint16_t* pre_norm_w, const uint16_t* post_norm_w, const uint32_t* gu_w,
+                      const uint16_t* gu_s, const uint16_t* gu_b, const uint32_t* dn_w, const uint16_t* dn_s,
+                      const uint16_t* dn_b, uint16_t* out, int32_t* idx_out, uint16_t* w_out,
+                      uint16_t* expert_in_tap, int nthreads) {
+    const size_t n = (size_t)d->T * d->H;
+    uint16_t* xe = (uint16_t*)malloc(sizeof(uint16_t) * (n ? n : 1));
+    uint16_t* ye = (uint16_t*)malloc(sizeof(uint16_t) * (n ? n : 1));
+#if ORACLE_MUTANT == 9
+    /* planted: the router reads the expert input instead of the residual */
+    int rc = oracle_rms_norm(d->T, d->H, d->eps, residual, pre_norm_w, xe);
+    if (!rc)
+        rc = oracle_route(d, xe, router_w, router_scale, per_expert_scale, idx_out, w_out, NULL, NULL, NULL,
+                          nthreads);
+#else
+    int rc = oracle_route(d, residual, router_w, router_scale, per_expert_scale, idx_out, w_out, NULL, NULL,
+                          NULL, nthreads);
+    if (!rc) rc = oracle_rms_norm(d->T, d->H, d->eps, residual, pre_norm_w, xe);
+#endif
+    if (!rc && expert_in_tap) memcpy(expert_in_tap, xe, sizeof(uint16_t) * n);
+    if (!rc)
+        rc = oracle_experts(d, xe, idx_out, w_out, gu_w, gu_s, gu_b, dn_w, dn_s, dn_b, ye, NULL, NULL, NULL,
+                            nthreads);
+    if (!rc) rc = oracle_rms_norm(d->T, d->H, d->eps, ye, post_norm_w, out);
+    free(xe);
+    free(ye);
+    return rc;
+}
+
 /* Router then experts on the same x: the layer as one call. */
 int oracle_forward(const oracle_dims* d, const uint16_t* x, const uint16_t* router_w,
                    const uint16_t* router_scale, const uint16_t* per_expert_scale,

@@ -370,6 +370,64 @@ def check_token_permutation(lib):
     assert np.array_equal(out_b, out_a[pi]), "token permutation"
 
 
+def check_rms_norm_exact_math(lib):
+    """RMSNorm with a weight: out = x / sqrt(mean(x^2) + eps) * w within
+    the error of its fp32 steps and one bf16 rounding (float64 reference)."""
+    d = small_dims(T=32, H=512)
+    x = ms.make_x(d, seed=20)
+    w = ms.make_branch_norms(d, seed=20)[0]
+    out = f64(oracle.rms_norm(x, w, d.eps, lib=lib))
+    xf = f64(x)
+    exact = xf / np.sqrt(np.mean(xf * xf, axis=1, keepdims=True) + d.eps) * f64(w)
+    tol = 2.0 ** -8 * np.abs(exact) + 1e-30
+    assert np.all(np.abs(out - exact) <= tol), "rms_norm far from x / rms * w"
+
+
+def check_rms_norm_invariances(lib):
+    """eps = 0: RMSNorm(2x) == RMSNorm(x) bit for bit; doubling the weight
+    doubles the output bit for bit (powers of two are exact)."""
+    d = small_dims(T=16, H=256)
+    x = ms.make_x(d, seed=21)
+    w = ms.make_branch_norms(d, seed=21)[1]
+    a = oracle.rms_norm(x, w, 0.0, lib=lib)
+    b = oracle.rms_norm(ms.bf16_bits(ms.bits_to_f32(x) * 2.0), w, 0.0, lib=lib)
+    assert np.array_equal(a, b), "rms_norm(2x) != rms_norm(x)"
+    c = oracle.rms_norm(x, ms.bf16_bits(ms.bits_to_f32(w) * 2.0), 0.0, lib=lib)
+    assert np.array_equal(f64(c), 2.0 * f64(a)), "rms_norm with 2w != 2 rms_norm"
+
+
+def check_rms_norm_constant_row(lib):
+    """A constant row c (eps = 0, weight 1) normalises to sign(c) exactly;
+    weight w then gives w itself."""
+    H = 384
+    for c in (0x3F80, 0xC0A0, 0x3C23):  # 1, -5, ~0.00995
+        x = np.full((2, H), c, np.uint16)
+        ones = np.full(H, 0x3F80, np.uint16)
+        want = 0xBF80 if c & 0x8000 else 0x3F80
+        assert np.all(oracle.rms_norm(x, ones, 0.0, lib=lib) == want), f"constant row {c:#06x}"
+        w = ms.make_branch_norms(small_dims(H=H), seed=22)[0]
+        got = oracle.rms_norm(x, w, 0.0, lib=lib)
+        sign = -1.0 if c & 0x8000 else 1.0
+        assert np.array_equal(f64(got), sign * np.tile(f64(w), (2, 1))), f"constant row {c:#06x}, weight"
+
+
+def check_moe_branch_wiring(lib):
+    """The branch is route(residual), experts(RMSNorm(residual, pre)) and
+    RMSNorm(., post) of their output, composed from the parts pinned above:
+    the router reads the residual, not the normalised expert input."""
+    d = small_dims(T=24, E=8, k=2)
+    inp = ms.make_custom(d, seed=23)
+    pre, post = ms.make_branch_norms(d, seed=23)
+    out, idx, w, xe = oracle.moe_branch(inp, pre, post, taps=True, lib=lib)
+    rt = oracle.route(d, inp.x, inp.router_w, inp.router_scale, inp.pes, lib=lib)
+    assert np.array_equal(idx, rt["idx"]) and np.array_equal(w, rt["w"]), "branch routing != route(residual)"
+    want_xe = oracle.rms_norm(inp.x, pre, d.eps, lib=lib)
+    assert np.array_equal(xe, want_xe), "branch expert input != RMSNorm(residual, pre)"
+    y = oracle.experts(d, want_xe, rt["idx"], rt["w"], (inp.gu_w, inp.gu_s, inp.gu_b),
+                       (inp.dn_w, inp.dn_s, inp.dn_b), lib=lib)
+    assert np.array_equal(out, oracle.rms_norm(y, post, d.eps, lib=lib)), "branch output != RMSNorm(experts, post)"
+
+
 ALL_CHECKS = [
     check_bf16_from_float, check_bf16_from_double,
     check_router_constant_row, check_router_zero_row, check_router_scale_invariance,
@@ -377,4 +435,5 @@ ALL_CHECKS = [
     check_dispatch,
     check_experts_brute_force, check_experts_one_hot, check_geglu_ties, check_single_expert_identity,
     check_expert_relabel, check_token_permutation,
+    check_rms_norm_exact_math, check_rms_norm_invariances, check_rms_norm_constant_row, check_moe_branch_wiring,
 ]

@@ -19,6 +19,8 @@ MUTANTS = {
     5: "nibbles read high-first",
     6: "gate and up halves swapped",
     7: "combine sums unrounded products",
+    8: "RMS norm with a weight drops the weight",
+    9: "MoE branch routes on the normalised expert input",
 }
 
 
