@@ -334,6 +334,30 @@ def run_ours(args, wl):
             e2e_ms.append(1e3 * (time.perf_counter() - t0))
     e2e_step = max_over_ranks(statistics.mean(e2e_ms), world, "cuda")
 
+    # The decoder layer's MoE branch (moe_forward_branch: the router on the
+    # residual, the experts on preFfNorm2(residual), postFfNorm2 of their
+    # output), timed like region 1.
+    pre_w, post_w = (torch.from_numpy(a.view(np.int16).copy()).cuda()
+                     for a in ms.make_branch_norms(inp.dims, wl.seed))
+    out_b = torch.empty_like(out)
+
+    def branch_step():
+        moe.moe_forward_branch(d, x, layer.router_w, layer.router_scale, layer.pes, pre_w, post_w, layer.gate_up,
+                               layer.down, out_b, idx, wts, None, ws, ws.numel(), stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        branch_step()
+    bstarts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    bends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        bstarts[i].record(stream)
+        branch_step()
+        bends[i].record(stream)
+    torch.cuda.synchronize()
+    branch_ms = max_over_ranks(statistics.mean(s_.elapsed_time(e_) for s_, e_ in zip(bstarts, bends)), world, "cuda")
+
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -371,6 +395,8 @@ def run_ours(args, wl):
         e2e=dict(value=whole_job_rate(d.T, world, e2e_step * 1e-3), unit="tokens/s", h2d_bytes_per_step=d.T * d.H * 2,
                  d2h_bytes_per_step=d.T * d.H * 2, ms_per_step=e2e_step),
         gpu_launches=moe.launches_per_forward(d) * args.steps,
+        branch=dict(call="moe_forward_branch (router on the residual, experts on preFfNorm2, postFfNorm2)",
+                    ms_per_step=branch_ms, value=whole_job_rate(d.T, world, branch_ms * 1e-3), unit="tokens/s"),
         clocks=clk.summary(),
         device_error=err,
     )

@@ -28,7 +28,8 @@ STATUS = {0: "ok", 1: "null pointer", 2: "bad shape", 3: "pointer not 16-byte al
 
 # Every function the public header declares.
 EXPORTS = ("moe_status_str", "moe_workspace_bytes", "moe_route", "moe_dispatch", "moe_experts",
-           "moe_experts_noalloc", "moe_forward", "moe_forward_hostio", "moe_timing_enable", "moe_timing_read",
+           "moe_experts_noalloc", "moe_forward", "moe_forward_branch", "moe_forward_hostio", "moe_timing_enable",
+           "moe_timing_read",
            "moe_launches_per_forward", "moe_device_error")
 
 
@@ -72,11 +73,13 @@ def load(path: str = LIB_PATH):
     lib.moe_experts_noalloc.argtypes = [D, P, P, P, Q, Q, P, P]
     lib.moe_forward.argtypes = [D, P, P, P, P, Q, Q, P, P, P, P, Z, P]
     lib.moe_forward_hostio.argtypes = [D, P, P, P, P, Q, Q, P, P, Z, P]
+    lib.moe_forward_branch.argtypes = [D, P, P, P, P, P, P, Q, Q, P, P, P, P, P, Z, P]
     lib.moe_timing_enable.argtypes = [I]
     lib.moe_timing_read.argtypes = [ctypes.POINTER(ctypes.c_float), I, ctypes.POINTER(I)]
     lib.moe_launches_per_forward.argtypes = [ctypes.c_void_p]
     lib.moe_device_error.argtypes = []
-    for fn in ("moe_route", "moe_dispatch", "moe_experts", "moe_experts_noalloc", "moe_forward", "moe_forward_hostio",
+    for fn in ("moe_route", "moe_dispatch", "moe_experts", "moe_experts_noalloc", "moe_forward", "moe_forward_branch",
+               "moe_forward_hostio",
                "moe_timing_enable", "moe_timing_read", "moe_launches_per_forward", "moe_device_error"):
         getattr(lib, fn).restype = I
     _lib = lib
@@ -151,6 +154,17 @@ def moe_forward(d: Dims, x, router_w, router_scale, per_expert_scale, gate_up: Q
         ctypes.byref(d), _ptr(x), _ptr(router_w), _ptr(router_scale), _ptr(per_expert_scale),
         ctypes.byref(gate_up), ctypes.byref(down), _ptr(out), _ptr(idx_out), _ptr(w_out),
         _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def moe_forward_branch(d: Dims, residual, router_w, router_scale, per_expert_scale, pre_norm_w, post_norm_w,
+                       gate_up: QWeight, down: QWeight, out, idx_out=None, w_out=None, expert_in_out=None,
+                       workspace=None, ws_bytes: int = 0, stream=None):
+    """The decoder layer's MoE branch: route on the residual, experts on
+    RMSNorm(residual, pre_norm_w), RMSNorm(., post_norm_w) of their output."""
+    _check("moe_forward_branch", load().moe_forward_branch(
+        ctypes.byref(d), _ptr(residual), _ptr(router_w), _ptr(router_scale), _ptr(per_expert_scale),
+        _ptr(pre_norm_w), _ptr(post_norm_w), ctypes.byref(gate_up), ctypes.byref(down), _ptr(out),
+        _ptr(idx_out), _ptr(w_out), _ptr(expert_in_out), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def moe_forward_hostio(d: Dims, x_host, router_w, router_scale, per_expert_scale, gate_up: QWeight,

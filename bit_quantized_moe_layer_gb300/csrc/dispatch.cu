@@ -451,6 +451,119 @@ __global__ void __launch_bounds__(128) combine_kernel(const uint16_t* __restrict
                    pack_bf16x2(acc[6], acc[7]));
 }
 
+// Error-free sum a + b = s + e (Knuth's two-sum).
+__device__ __forceinline__ void two_sum_f(float a, float b, float& s, float& e) {
+    s = __fadd_rn(a, b);
+    const float bp = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
+}
+
+// Combine followed by the MoE branch's post norm (postFfNorm2), one CTA a
+// token: c = the combined row (bf16, as combine_kernel), then
+// out = bf16((c * rsqrt(mean(c^2) + eps)) * post_w) with fp32 steps; the sum of
+// squares is carried as an error-free two-float sum, so the fp32 mean is the
+// exact mean rounded once (unless within ~2^-40 of a rounding boundary).
+constexpr int kNormThreads = 256;
+constexpr int kNormChunks = 4;  // 16-byte chunks a thread: H <= 8192
+__global__ void __launch_bounds__(kNormThreads) combine_norm_kernel(const uint16_t* __restrict__ y,
+                                                                    const uint16_t* __restrict__ w,
+                                                                    const uint16_t* __restrict__ post_w,
+                                                                    uint16_t* __restrict__ out, int k, int H,
+                                                                    float eps) {
+    __shared__ float2 part[kNormThreads / 32];
+    __shared__ float rs_s;
+    pdl_trigger();
+    pdl_wait();
+    const int chunks = H / 8, t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint4* yt = reinterpret_cast<const uint4*>(y + (size_t)t * k * H);
+    const uint16_t* wt = w + (size_t)t * k;
+    uint4 cv[kNormChunks];
+    float hi = 0.f, lo = 0.f;
+#pragma unroll
+    for (int q = 0; q < kNormChunks; ++q) {
+        const int c = tid + q * kNormThreads;
+        cv[q] = make_uint4(0, 0, 0, 0);
+        if (c >= chunks) continue;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int j = 0; j < k; ++j) {
+            const uint32_t wb = __ldg(wt + j), w2 = wb | (wb << 16);
+            const uint4 v = __ldg(yt + (size_t)j * chunks + c);
+            const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t p = mul_bf16x2(u[e], w2);
+                acc[2 * e] = __fadd_rn(acc[2 * e], __uint_as_float(p << 16));
+                acc[2 * e + 1] = __fadd_rn(acc[2 * e + 1], __uint_as_float(p & 0xFFFF0000u));
+            }
+        }
+        const uint32_t b0 = pack_bf16x2(acc[0], acc[1]), b1 = pack_bf16x2(acc[2], acc[3]),
+                       b2 = pack_bf16x2(acc[4], acc[5]), b3 = pack_bf16x2(acc[6], acc[7]);
+        cv[q] = make_uint4(b0, b1, b2, b3);
+        const uint32_t bb[4] = {b0, b1, b2, b3};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {  // squares of bf16 values are exact in fp32
+            const float l = __uint_as_float(bb[e] << 16), h = __uint_as_float(bb[e] & 0xFFFF0000u);
+            float s1, e1;
+            two_sum_f(hi, __fmul_rn(l, l), s1, e1);
+            hi = s1;
+            lo = __fadd_rn(lo, e1);
+            two_sum_f(hi, __fmul_rn(h, h), s1, e1);
+            hi = s1;
+            lo = __fadd_rn(lo, e1);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float h2 = __shfl_xor_sync(0xffffffffu, hi, o), l2 = __shfl_xor_sync(0xffffffffu, lo, o);
+        float s1, e1;
+        two_sum_f(hi, h2, s1, e1);
+        hi = s1;
+        lo = __fadd_rn(__fadd_rn(lo, l2), e1);
+    }
+    if (lane == 0) part[warp] = make_float2(hi, lo);
+    __syncthreads();
+    if (tid == 0) {
+        float hs = 0.f, ls = 0.f;
+        for (int i = 0; i < kNormThreads / 32; ++i) {  // warp order: the same result every call
+            float s1, e1;
+            two_sum_f(hs, part[i].x, s1, e1);
+            hs = s1;
+            ls = __fadd_rn(__fadd_rn(ls, part[i].y), e1);
+        }
+        // mean = (hs + ls) / H rounded once: q0 = RN(hs / H), the residual
+        // hs - q0 H is exact (fma), the correction moves q0 by under half an ulp
+        const float Hf = (float)H;
+        const float q0 = __fdiv_rn(hs, Hf);
+        const float rsd = __fadd_rn(__fmaf_rn(-q0, Hf, hs), ls);
+        const float mean = __fadd_rn(q0, __fdiv_rn(rsd, Hf));
+        rs_s = __frsqrt_rn(__fadd_rn(mean, eps));
+    }
+    __syncthreads();
+    const float rs = rs_s;
+#pragma unroll
+    for (int q = 0; q < kNormChunks; ++q) {
+        const int c = tid + q * kNormThreads;
+        if (c >= chunks) continue;
+        const uint4 pw = __ldg(reinterpret_cast<const uint4*>(post_w) + c);
+        const uint32_t xv[4] = {cv[q].x, cv[q].y, cv[q].z, cv[q].w}, wv[4] = {pw.x, pw.y, pw.z, pw.w};
+        uint32_t o4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            o4[e] = pack_bf16x2(
+                __fmul_rn(__fmul_rn(__uint_as_float(xv[e] << 16), rs), __uint_as_float(wv[e] << 16)),
+                __fmul_rn(__fmul_rn(__uint_as_float(xv[e] & 0xFFFF0000u), rs), __uint_as_float(wv[e] & 0xFFFF0000u)));
+        reinterpret_cast<uint4*>(out + (size_t)t * H)[c] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+    }
+}
+
+cudaError_t launch_combine_norm(const uint16_t* y, const uint16_t* w, const uint16_t* post_w, uint16_t* out, int T,
+                                int k, int H, float eps, cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    if (H / 8 > kNormThreads * kNormChunks) return cudaErrorInvalidValue;
+    return launch_pdl(combine_norm_kernel, dim3((unsigned)T), dim3(kNormThreads), 0, stream, y, w, post_w, out, k, H,
+                      eps);
+}
+
 cudaError_t launch_combine(const uint16_t* y, const uint16_t* w, uint16_t* out, int T, int k, int H,
                            cudaStream_t stream) {
     if (T == 0) return cudaSuccess;

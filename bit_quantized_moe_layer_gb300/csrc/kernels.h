@@ -39,6 +39,11 @@ struct RouterArgs {
     float eps;
     float root;  // bf16(H^-0.5) as a float
     int tt;      // tokens per cluster (16, 32 or 64), from router_tokens_per_cluster
+    // Optional (both or neither): the MoE branch's expert input
+    // xe = bf16((x * rsqrt(mean(x^2) + eps)) * pre_w), fp32 steps, from the
+    // same per-token rms the router computes.
+    const uint16_t* pre_w;  // [H] bf16
+    uint16_t* xe;           // [T, H] bf16
 };
 size_t router_smem_bytes(int H, int E, int tt);
 int router_tokens_per_cluster(int T, int H, int E);
@@ -83,6 +88,10 @@ cudaError_t launch_gather(const uint16_t* x, const int32_t* perm, const int32_t*
 // Combine: out[t] = bf16(sum_j bf16(y[t*k+j] * w[t*k+j])), fp32 sum in j order.
 cudaError_t launch_combine(const uint16_t* y, const uint16_t* w, uint16_t* out, int T, int k, int H,
                            cudaStream_t stream);
+// Combine, then the MoE branch's post norm: out[t] = bf16((c * rsqrt(mean(c^2)
+// + eps)) * post_w) of the combined bf16 row c (fp32 steps). H <= 8192.
+cudaError_t launch_combine_norm(const uint16_t* y, const uint16_t* w, const uint16_t* post_w, uint16_t* out, int T,
+                                int k, int H, float eps, cudaStream_t stream);
 int dispatch_error_word();
 
 // Grouped dequant-GEMM on tcgen05 (one expert per token tile).

@@ -142,7 +142,7 @@ Layout layout(const moe_dims* d) {
     L.xs = take(S * d->H * 2);
     L.mid = take(S * d->inter * 2);
     L.y = take(S * d->H * 2);
-    L.xdev = take((size_t)d->T * d->H * 2);
+    L.xdev = take((size_t)d->T * d->H * 2);  // host-I/O input, or the branch's expert input
     L.outdev = take((size_t)d->T * d->H * 2);
     L.total = o;
     return L;
@@ -204,7 +204,7 @@ int fail(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 // ------------------------------------------------------------- pipeline --
 int run_experts(const moe_dims* d, const uint16_t* x, const int32_t* idx, const uint16_t* w,
                 const moe_qweight* gu, const moe_qweight* dn, uint16_t* out, uint8_t* ws, const Layout& L,
-                const DeviceInfo& di, cudaStream_t s, CallTimer& tm) {
+                const DeviceInfo& di, cudaStream_t s, CallTimer& tm, const uint16_t* post_norm_w = nullptr) {
     const int S = d->T * d->k;
     const int E = d->E, H = d->H, I = d->inter;
     int32_t* perm = reinterpret_cast<int32_t*>(ws + L.perm);
@@ -284,18 +284,20 @@ int run_experts(const moe_dims* d, const uint16_t* x, const int32_t* idx, const 
     if (rc) return rc;
     tm.mark(5);
 
-    rc = fail(launch_combine(y, w, out, d->T, d->k, H, s));
+    rc = fail(post_norm_w ? launch_combine_norm(y, w, post_norm_w, out, d->T, d->k, H, d->eps, s)
+                          : launch_combine(y, w, out, d->T, d->k, H, s));
     if (rc) return rc;
     tm.mark(6);
     return MOE_OK;
 }
 
 int route_impl(const moe_dims* d, const uint16_t* x, const uint16_t* rw, const uint16_t* rs, const uint16_t* pes,
-               int32_t* idx, uint16_t* w, cudaStream_t s) {
+               int32_t* idx, uint16_t* w, cudaStream_t s, const uint16_t* pre_norm_w = nullptr,
+               uint16_t* xe = nullptr) {
     const int tt = router_tokens_per_cluster(d->T, d->H, d->E);
     RouterArgs ra{x,    rw,   rs,   pes,  idx,    w,
                   d->T, d->H, d->E, d->k, d->eps, bf16_round(pow((double)d->H, -0.5)),
-                  tt};
+                  tt,   pre_norm_w, xe};
     CUtensorMap m_rw, m_x;
     if (!make_map_2d(&m_rw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rw, d->H, d->E, 64, d->E < 128 ? d->E : 128) ||
         !make_map_2d(&m_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, d->H, d->T, 64, tt))
@@ -474,6 +476,38 @@ int moe_forward(const moe_dims* d, const uint16_t* x, const uint16_t* router_w, 
     if ((rc = route_impl(d, x, router_w, router_scale, per_expert_scale, idx, w, s))) return rc;
     tm.mark(1);
     return run_experts(d, x, idx, w, gate_up, down, out, ws, L, di, s, tm);
+}
+
+int moe_forward_branch(const moe_dims* d, const uint16_t* residual, const uint16_t* router_w,
+                       const uint16_t* router_scale, const uint16_t* per_expert_scale, const uint16_t* pre_norm_w,
+                       const uint16_t* post_norm_w, const moe_qweight* gate_up, const moe_qweight* down,
+                       uint16_t* out, int32_t* idx_out, uint16_t* w_out, uint16_t* expert_in_out, void* workspace,
+                       size_t ws_bytes, void* stream) {
+    int rc = check_dims(d);
+    if (rc) return rc;
+    if ((rc = check_ptrs({residual, router_w, router_scale, per_expert_scale, pre_norm_w, post_norm_w, out})))
+        return rc;
+    if ((rc = check_qweight(gate_up)) || (rc = check_qweight(down))) return rc;
+    if ((idx_out && !aligned16(idx_out)) || (w_out && !aligned16(w_out)) ||
+        (expert_in_out && !aligned16(expert_in_out)))
+        return MOE_ERR_ALIGN;
+    if (d->H > 8192) return MOE_ERR_UNSUPPORTED;  // the post norm's one-CTA-a-token row
+    if (d->T == 0) return MOE_OK;
+    DeviceInfo di;
+    if ((rc = device_info(&di))) return rc;
+    const Layout L = layout(d);
+    uint8_t* ws = nullptr;
+    if ((rc = get_workspace(d, workspace, ws_bytes, L, &ws))) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(ws + L.idx);
+    uint16_t* w = w_out ? w_out : reinterpret_cast<uint16_t*>(ws + L.w);
+    uint16_t* xe = expert_in_out ? expert_in_out : reinterpret_cast<uint16_t*>(ws + L.xdev);
+    CallTimer tm(s);
+    tm.mark(0);
+    if ((rc = route_impl(d, residual, router_w, router_scale, per_expert_scale, idx, w, s, pre_norm_w, xe)))
+        return rc;
+    tm.mark(1);
+    return run_experts(d, xe, idx, w, gate_up, down, out, ws, L, di, s, tm, post_norm_w);
 }
 
 int moe_forward_hostio(const moe_dims* d, const uint16_t* x_host, const uint16_t* router_w,

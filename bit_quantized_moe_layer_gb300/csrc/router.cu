@@ -81,6 +81,7 @@ __host__ __device__ inline void kslice(int nkb, int r, int& kb0, int& cnt) {
 
 struct RouterSmem {
     uint8_t *xt, *wt, *rsl;  // x slice boxes, weight-chunk blocks, router_scale slice
+    uint8_t* psl;            // expert-input norm weight slice (optional output xe)
     float2* pss;             // [kCS][TT] partial sums of squares, by source CTA
     float* red;              // [kCS][TT/kCS][E] partial scores of my tokens, by source CTA
     uint16_t* sc;            // [TT/kCS][E] bf16 scores of my tokens
@@ -101,6 +102,7 @@ __host__ __device__ inline size_t router_layout(int H, int E, int TT, uint8_t* b
     const size_t xt = take_bytes(off, (size_t)nkbmax * TT * 128, 1024);
     const size_t wt = take_bytes(off, (size_t)nkbmax * kWBlockBytes, 1024);
     const size_t rsl = take_bytes(off, (size_t)nkbmax * 128, 16);
+    const size_t psl = take_bytes(off, (size_t)nkbmax * 128, 16);
     const size_t pss = take_bytes(off, (size_t)kCS * TT * sizeof(float2), 16);
     const size_t red = take_bytes(off, (size_t)TT * E * sizeof(float), 16);
     const size_t sc = take_bytes(off, (size_t)(TT / kCS) * E * 2, 16);
@@ -108,6 +110,7 @@ __host__ __device__ inline size_t router_layout(int H, int E, int TT, uint8_t* b
         s->xt = base + xt;
         s->wt = base + wt;
         s->rsl = base + rsl;
+        s->psl = base + psl;
         s->pss = reinterpret_cast<float2*>(base + pss);
         s->red = reinterpret_cast<float*>(base + red);
         s->sc = reinterpret_cast<uint16_t*>(base + sc);
@@ -160,12 +163,14 @@ __global__ void __launch_bounds__(kWarps * 32) router_kernel(const __grid_consta
     // only write this CTA's shared memory.
     auto issue_loads = [&](int tile, bool weights) {
         if (lane == 0)
-            mbar_arrive_expect_tx(&full, (uint32_t)cnt * (TT * 128 + (weights ? eb * 128 + 128 : 0)));
+            mbar_arrive_expect_tx(&full, (uint32_t)cnt * (TT * 128 + (weights ? eb * 128 + 128 : 0) +
+                                                          (weights && a.xe ? 128 : 0)));
         __syncwarp();
         if (lane < cnt) tma_load_2d(sm.xt + lane * TT * 128, &xmap, &full, (kb0 + lane) * 64, tile * TT);
         if (weights && lane >= 16 && lane - 16 < cnt)
             tma_load_2d(sm.wt + (lane - 16) * kWBlockBytes, &wmap, &full, (kb0 + lane - 16) * 64, 0);
         if (weights && lane == 31 && cnt > 0) bulk_load(sm.rsl, a.router_scale + (size_t)kb0 * 64, cnt * 128, &full);
+        if (weights && a.xe && lane == 30 && cnt > 0) bulk_load(sm.psl, a.pre_w + (size_t)kb0 * 64, cnt * 128, &full);
     };
     if (warp == 0) {  // scores accumulator: 128 lanes (experts) x TT columns (tokens)
         tmem_alloc(&tmem_base, kTmemCols);
@@ -240,9 +245,23 @@ __global__ void __launch_bounds__(kWarps * 32) router_kernel(const __grid_consta
             // bf16 after each op: x*rs in fp32 rounded once (cvt.rn), then the
             // two bf16 x bf16 products, each exact in fp32 and rounded once
             // (mul.rn.bf16x2), two elements an instruction.
+            const bool xe_row = a.xe && t0 + t < a.T;
             for (int i = lane; have && i < cnt * 8; i += 32) {
                 uint4* p = reinterpret_cast<uint4*>(sm.xt + (i >> 3) * TT * 128 + sw128(t, i & 7));
                 const uint4 v = *p;
+                if (xe_row) {  // the expert input: bf16((x * rs) * pre_w), one rounding
+                    const uint4 pw = reinterpret_cast<const uint4*>(sm.psl)[i];
+                    const uint32_t xv[4] = {v.x, v.y, v.z, v.w}, wv[4] = {pw.x, pw.y, pw.z, pw.w};
+                    uint32_t e[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        e[j] = pack_bf16x2(
+                            __fmul_rn(__fmul_rn(__uint_as_float(xv[j] << 16), rs), __uint_as_float(wv[j] << 16)),
+                            __fmul_rn(__fmul_rn(__uint_as_float(xv[j] & 0xFFFF0000u), rs),
+                                      __uint_as_float(wv[j] & 0xFFFF0000u)));
+                    const size_t h = (size_t)(kb0 + (i >> 3)) * 64 + (i & 7) * 8;
+                    *reinterpret_cast<uint4*>(a.xe + (size_t)(t0 + t) * H + h) = make_uint4(e[0], e[1], e[2], e[3]);
+                }
                 const uint4 s = reinterpret_cast<const uint4*>(sm.rsl)[i];  // router_scale of the same 8 columns
                 const uint32_t w[4] = {v.x, v.y, v.z, v.w}, sc[4] = {s.x, s.y, s.z, s.w};
                 uint32_t o[4];

@@ -164,6 +164,30 @@ int moe_forward(const moe_dims* d, const uint16_t* x, const uint16_t* router_w,
                 void* stream);
 
 /*
+ * The MoE branch of the decoder layer (DiffusionGemmaDecoderLayer.forwardWith
+ * in "diffusion-gemma/model.ts"): the router reads the residual, the experts
+ * read preFfNorm2(residual), and the experts' combined output goes through
+ * postFfNorm2. Both norms are the layer's plain RMSNorm with the weight used
+ * as it is (no 1 + weight offset):
+ *   norm(v, w) = bf16((v * rsqrt(mean(v^2) + eps)) * w), fp32 steps, the
+ *                fp32 mean the exact mean rounded once.
+ *   idx, w      = moe_route(residual)
+ *   expert_in   = norm(residual, pre_norm_w)
+ *   out         = norm(experts(expert_in, idx, w), post_norm_w)
+ * residual [T,H], pre_norm_w [H], post_norm_w [H], out [T,H] (bf16).
+ * idx_out, w_out and expert_in_out ([T,H] bf16) may be NULL; when given they
+ * receive the routing and the experts' input. The expert input is written
+ * by the router kernel from the rms it computes anyway; the post norm runs
+ * in the combine kernel (one CTA a token). Same launches as moe_forward.
+ */
+int moe_forward_branch(const moe_dims* d, const uint16_t* residual, const uint16_t* router_w,
+                       const uint16_t* router_scale, const uint16_t* per_expert_scale,
+                       const uint16_t* pre_norm_w, const uint16_t* post_norm_w,
+                       const moe_qweight* gate_up, const moe_qweight* down, uint16_t* out,
+                       int32_t* idx_out, uint16_t* w_out, uint16_t* expert_in_out,
+                       void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * The whole layer with HOST activations: copies x_host [T,H] to the device,
  * runs moe_forward and copies out [T,H] back to out_host, then synchronises
  * the stream. Weights and router parameters are device pointers. Host
