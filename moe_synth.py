@@ -160,6 +160,14 @@ def make_layer(wl, T: int | None = None, seed: int | None = None) -> LayerInputs
     return LayerInputs(d, x, wr, sc, pes, gw, gs, gb, dw, ds, db)
 
 
+def make_router_q4(d: Dims, seed: int = 0):
+    """The router projection as a 4-bit group-64 weight (the pages'
+    QuantizedLinear): (w uint32 [E, H/8], scales [E, H/g], biases [E, H/g]),
+    with the experts' code, scale and bias recipe."""
+    w, s, b = make_qweight(1, d.E, d.H, d.group, seed, "router")
+    return w[0], s[0], b[0]
+
+
 def make_branch_norms(d: Dims, seed: int = 0):
     """Weights [H] of the MoE branch's two RMS norms (pre_feedforward_layernorm_2,
     post_feedforward_layernorm_2) as bf16 bits, U(0.5, 1.5) like the router

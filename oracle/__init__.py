@@ -67,6 +67,8 @@ def _declare(lib):
     lib.oracle_experts.restype = ctypes.c_int
     lib.oracle_forward.argtypes = [ctypes.POINTER(_Dims)] + [P] * 13 + [ctypes.c_int]
     lib.oracle_forward.restype = ctypes.c_int
+    lib.oracle_route_q4.argtypes = [ctypes.POINTER(_Dims)] + [P] * 10 + [ctypes.c_int]
+    lib.oracle_route_q4.restype = ctypes.c_int
     lib.oracle_rms_norm.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_float, P, P, P]
     lib.oracle_rms_norm.restype = ctypes.c_int
     lib.oracle_moe_branch.argtypes = [ctypes.POINTER(_Dims)] + [P] * 16 + [ctypes.c_int]
@@ -204,3 +206,26 @@ def moe_branch(inp, pre_norm_w, post_norm_w, taps: bool = False, nthreads: int =
     if rc != 0:
         raise ValueError(f"oracle_moe_branch rejected the inputs ({rc})")
     return (out, idx, w, xe) if taps else (out, idx, w)
+
+
+def route_q4(d, x, rq, router_scale, pes, taps: bool = False, nthreads: int = 0, lib=None):
+    """DiffRouter.forward with the 4-bit group-64 projection: rq = (w uint32
+    [E, H/8], scales [E, H/g], biases [E, H/g]). Returns dict(idx, w[, logits,
+    scores])."""
+    lib = lib or load()
+    x = _c(x, np.uint16)
+    idx = np.zeros((d.T, d.k), np.int32)
+    w = np.zeros((d.T, d.k), np.uint16)
+    logits = np.zeros((d.T, d.E), np.float64) if taps else None
+    scores = np.zeros((d.T, d.E), np.uint16) if taps else None
+    dims = _dims(d)
+    args = [_c(rq[0], np.uint32), _c(rq[1], np.uint16), _c(rq[2], np.uint16), _c(router_scale, np.uint16),
+            _c(pes, np.uint16)]
+    rc = lib.oracle_route_q4(ctypes.byref(dims), _p(x), *[_p(a) for a in args], _p(idx), _p(w),
+                             _p(logits) if taps else None, _p(scores) if taps else None, nthreads)
+    if rc != 0:
+        raise ValueError(f"oracle_route_q4 rejected the inputs ({rc})")
+    out = dict(idx=idx, w=w)
+    if taps:
+        out.update(logits=logits, scores=scores)
+    return out

@@ -276,6 +276,32 @@ static void dequant_expert(const uint32_t* w, const uint16_t* sc, const uint16_t
     }
 }
 
+/* The router with the pages' 4-bit group-64 projection (DiffRouter.proj is a
+ * QuantizedLinear): the weight [E, H] dequantises like the experts' weights,
+ * w = bf16(S * q + B), and the router is then the dense one on that weight. */
+int oracle_route_q4(const oracle_dims* d, const uint16_t* x, const uint32_t* rq_w, const uint16_t* rq_s,
+                    const uint16_t* rq_b, const uint16_t* router_scale, const uint16_t* per_expert_scale,
+                    int32_t* idx_out, uint16_t* w_out, double* logits_exact_tap, uint16_t* scores_tap,
+                    int nthreads) {
+    const int E = d->E, H = d->H, g = d->group;
+    if (E <= 0 || H <= 0 || g <= 0 || H % g || H % 8) return -1;
+    float* wf = (float*)malloc(sizeof(float) * (size_t)E * H);
+    uint16_t* wb = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)E * H);
+#if ORACLE_MUTANT == 10
+    uint16_t* zb = (uint16_t*)calloc((size_t)E * (H / g), sizeof(uint16_t)); /* planted: biases dropped */
+    dequant_expert(rq_w, rq_s, zb, E, H, g, wf);
+    free(zb);
+#else
+    dequant_expert(rq_w, rq_s, rq_b, E, H, g, wf);
+#endif
+    for (size_t i = 0; i < (size_t)E * H; ++i) wb[i] = bf16_from_float(wf[i]); /* exact: already bf16 */
+    int rc = oracle_route(d, x, wb, router_scale, per_expert_scale, idx_out, w_out, NULL, logits_exact_tap,
+                          scores_tap, nthreads);
+    free(wf);
+    free(wb);
+    return rc;
+}
+
 /* bf16(gelu_approx(g) * up), one rounding, where
  *   gelu_approx(g) = 0.5 g (1 + tanh(s)),  s = sqrt(2/pi) (g + 0.044715 g^3)
  * (the tanh approximation of GELU). 0.5 (1 + tanh(s)) equals the logistic

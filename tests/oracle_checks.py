@@ -428,6 +428,20 @@ def check_moe_branch_wiring(lib):
     assert np.array_equal(out, oracle.rms_norm(y, post, d.eps, lib=lib)), "branch output != RMSNorm(experts, post)"
 
 
+def check_route_q4(lib):
+    """The 4-bit router equals the dense router on the dequantised weight
+    bf16(S q + B), dequantised here independently (torch bf16 rounding of
+    the unpacked codes), bit for bit on indices, weights and scores."""
+    d = small_dims(T=32, H=256, E=16, k=4)
+    inp = ms.make_custom(d, seed=24)
+    rq = ms.make_router_q4(d, seed=24)
+    dense = torch_bf16_bits(dense_dequant(rq[0][None], rq[1][None], rq[2][None], d.H, d.group)[0])
+    a = oracle.route_q4(d, inp.x, rq, inp.router_scale, inp.pes, taps=True, lib=lib)
+    b = oracle.route(d, inp.x, dense, inp.router_scale, inp.pes, taps=True, lib=lib)
+    for key in ("idx", "w", "scores"):
+        assert np.array_equal(a[key], b[key]), f"4-bit router != dense router on the dequantised weight: {key}"
+
+
 ALL_CHECKS = [
     check_bf16_from_float, check_bf16_from_double,
     check_router_constant_row, check_router_zero_row, check_router_scale_invariance,
@@ -436,4 +450,5 @@ ALL_CHECKS = [
     check_experts_brute_force, check_experts_one_hot, check_geglu_ties, check_single_expert_identity,
     check_expert_relabel, check_token_permutation,
     check_rms_norm_exact_math, check_rms_norm_invariances, check_rms_norm_constant_row, check_moe_branch_wiring,
+    check_route_q4,
 ]

@@ -21,6 +21,7 @@ MUTANTS = {
     7: "combine sums unrounded products",
     8: "RMS norm with a weight drops the weight",
     9: "MoE branch routes on the normalised expert input",
+    10: "4-bit router drops the biases",
 }
 
 
