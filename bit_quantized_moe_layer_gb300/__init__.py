@@ -28,7 +28,8 @@ STATUS = {0: "ok", 1: "null pointer", 2: "bad shape", 3: "pointer not 16-byte al
 
 # Every function the public header declares.
 EXPORTS = ("moe_status_str", "moe_workspace_bytes", "moe_route", "moe_dispatch", "moe_experts",
-           "moe_experts_noalloc", "moe_forward", "moe_forward_branch", "moe_forward_hostio", "moe_timing_enable",
+           "moe_experts_noalloc", "moe_forward", "moe_forward_branch", "moe_forward_hostio", "moe_route_q4",
+           "moe_forward_q4router", "moe_timing_enable",
            "moe_timing_read",
            "moe_launches_per_forward", "moe_device_error")
 
@@ -74,12 +75,14 @@ def load(path: str = LIB_PATH):
     lib.moe_forward.argtypes = [D, P, P, P, P, Q, Q, P, P, P, P, Z, P]
     lib.moe_forward_hostio.argtypes = [D, P, P, P, P, Q, Q, P, P, Z, P]
     lib.moe_forward_branch.argtypes = [D, P, P, P, P, P, P, Q, Q, P, P, P, P, P, Z, P]
+    lib.moe_route_q4.argtypes = [D, P, Q, P, P, P, P, P]
+    lib.moe_forward_q4router.argtypes = [D, P, Q, P, P, Q, Q, P, P, P, P, Z, P]
     lib.moe_timing_enable.argtypes = [I]
     lib.moe_timing_read.argtypes = [ctypes.POINTER(ctypes.c_float), I, ctypes.POINTER(I)]
     lib.moe_launches_per_forward.argtypes = [ctypes.c_void_p]
     lib.moe_device_error.argtypes = []
     for fn in ("moe_route", "moe_dispatch", "moe_experts", "moe_experts_noalloc", "moe_forward", "moe_forward_branch",
-               "moe_forward_hostio",
+               "moe_forward_hostio", "moe_route_q4", "moe_forward_q4router",
                "moe_timing_enable", "moe_timing_read", "moe_launches_per_forward", "moe_device_error"):
         getattr(lib, fn).restype = I
     _lib = lib
@@ -154,6 +157,22 @@ def moe_forward(d: Dims, x, router_w, router_scale, per_expert_scale, gate_up: Q
         ctypes.byref(d), _ptr(x), _ptr(router_w), _ptr(router_scale), _ptr(per_expert_scale),
         ctypes.byref(gate_up), ctypes.byref(down), _ptr(out), _ptr(idx_out), _ptr(w_out),
         _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def moe_route_q4(d: Dims, x, router_q: QWeight, router_scale, per_expert_scale, idx_out, w_out, stream=None):
+    """moe_route with the 4-bit group-64 router projection."""
+    _check("moe_route_q4", load().moe_route_q4(ctypes.byref(d), _ptr(x), ctypes.byref(router_q), _ptr(router_scale),
+                                               _ptr(per_expert_scale), _ptr(idx_out), _ptr(w_out), _stream(stream)))
+
+
+def moe_forward_q4router(d: Dims, x, router_q: QWeight, router_scale, per_expert_scale, gate_up: QWeight,
+                         down: QWeight, out, idx_out=None, w_out=None, workspace=None, ws_bytes: int = 0,
+                         stream=None):
+    """moe_forward with the 4-bit group-64 router projection."""
+    _check("moe_forward_q4router", load().moe_forward_q4router(
+        ctypes.byref(d), _ptr(x), ctypes.byref(router_q), _ptr(router_scale), _ptr(per_expert_scale),
+        ctypes.byref(gate_up), ctypes.byref(down), _ptr(out), _ptr(idx_out), _ptr(w_out), _ptr(workspace),
+        ws_bytes, _stream(stream)))
 
 
 def moe_forward_branch(d: Dims, residual, router_w, router_scale, per_expert_scale, pre_norm_w, post_norm_w,

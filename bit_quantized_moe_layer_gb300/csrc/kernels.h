@@ -44,6 +44,13 @@ struct RouterArgs {
     // same per-token rms the router computes.
     const uint16_t* pre_w;  // [H] bf16
     uint16_t* xe;           // [T, H] bf16
+    // Optional: the projection as a 4-bit group-64 weight (the pages'
+    // QuantizedLinear) instead of router_w; E <= 128. Each CTA dequantises
+    // its slice once, w = bf16(S * q + B), into the layout the dense path
+    // copies in.
+    const uint32_t* rq_w;   // [E, H/8]
+    const uint16_t* rq_s;   // [E, H/64]
+    const uint16_t* rq_b;   // [E, H/64]
 };
 size_t router_smem_bytes(int H, int E, int tt);
 int router_tokens_per_cluster(int T, int H, int E);

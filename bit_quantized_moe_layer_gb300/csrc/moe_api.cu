@@ -293,14 +293,17 @@ int run_experts(const moe_dims* d, const uint16_t* x, const int32_t* idx, const 
 
 int route_impl(const moe_dims* d, const uint16_t* x, const uint16_t* rw, const uint16_t* rs, const uint16_t* pes,
                int32_t* idx, uint16_t* w, cudaStream_t s, const uint16_t* pre_norm_w = nullptr,
-               uint16_t* xe = nullptr) {
+               uint16_t* xe = nullptr, const moe_qweight* rq = nullptr) {
     const int tt = router_tokens_per_cluster(d->T, d->H, d->E);
     RouterArgs ra{x,    rw,   rs,   pes,  idx,    w,
                   d->T, d->H, d->E, d->k, d->eps, bf16_round(pow((double)d->H, -0.5)),
-                  tt,   pre_norm_w, xe};
+                  tt,   pre_norm_w, xe, rq ? rq->w : nullptr, rq ? rq->scales : nullptr,
+                  rq ? rq->biases : nullptr};
     CUtensorMap m_rw, m_x;
-    if (!make_map_2d(&m_rw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rw, d->H, d->E, 64, d->E < 128 ? d->E : 128) ||
-        !make_map_2d(&m_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, d->H, d->T, 64, tt))
+    if (!make_map_2d(&m_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, d->H, d->T, 64, tt)) return MOE_ERR_CUDA;
+    if (rq)
+        m_rw = m_x;  // not read: the 4-bit projection is dequantised in the kernel
+    else if (!make_map_2d(&m_rw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rw, d->H, d->E, 64, d->E < 128 ? d->E : 128))
         return MOE_ERR_CUDA;
     return fail(launch_router(m_rw, m_x, ra, s));
 }
@@ -474,6 +477,45 @@ int moe_forward(const moe_dims* d, const uint16_t* x, const uint16_t* router_w, 
     CallTimer tm(s);
     tm.mark(0);
     if ((rc = route_impl(d, x, router_w, router_scale, per_expert_scale, idx, w, s))) return rc;
+    tm.mark(1);
+    return run_experts(d, x, idx, w, gate_up, down, out, ws, L, di, s, tm);
+}
+
+int moe_route_q4(const moe_dims* d, const uint16_t* x, const moe_qweight* router_q, const uint16_t* router_scale,
+                 const uint16_t* per_expert_scale, int32_t* idx_out, uint16_t* w_out, void* stream) {
+    int rc = check_dims(d);
+    if (rc) return rc;
+    if ((rc = check_ptrs({x, router_scale, per_expert_scale, idx_out, w_out}))) return rc;
+    if ((rc = check_qweight(router_q))) return rc;
+    if (d->E > 128) return MOE_ERR_UNSUPPORTED;  // one dequantised chunk of experts
+    if (d->T == 0) return MOE_OK;
+    return route_impl(d, x, nullptr, router_scale, per_expert_scale, idx_out, w_out, static_cast<cudaStream_t>(stream),
+                      nullptr, nullptr, router_q);
+}
+
+int moe_forward_q4router(const moe_dims* d, const uint16_t* x, const moe_qweight* router_q,
+                         const uint16_t* router_scale, const uint16_t* per_expert_scale, const moe_qweight* gate_up,
+                         const moe_qweight* down, uint16_t* out, int32_t* idx_out, uint16_t* w_out, void* workspace,
+                         size_t ws_bytes, void* stream) {
+    int rc = check_dims(d);
+    if (rc) return rc;
+    if ((rc = check_ptrs({x, router_scale, per_expert_scale, out}))) return rc;
+    if ((rc = check_qweight(router_q)) || (rc = check_qweight(gate_up)) || (rc = check_qweight(down))) return rc;
+    if ((idx_out && !aligned16(idx_out)) || (w_out && !aligned16(w_out))) return MOE_ERR_ALIGN;
+    if (d->E > 128) return MOE_ERR_UNSUPPORTED;
+    if (d->T == 0) return MOE_OK;
+    DeviceInfo di;
+    if ((rc = device_info(&di))) return rc;
+    const Layout L = layout(d);
+    uint8_t* ws = nullptr;
+    if ((rc = get_workspace(d, workspace, ws_bytes, L, &ws))) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(ws + L.idx);
+    uint16_t* w = w_out ? w_out : reinterpret_cast<uint16_t*>(ws + L.w);
+    CallTimer tm(s);
+    tm.mark(0);
+    if ((rc = route_impl(d, x, nullptr, router_scale, per_expert_scale, idx, w, s, nullptr, nullptr, router_q)))
+        return rc;
     tm.mark(1);
     return run_experts(d, x, idx, w, gate_up, down, out, ws, L, di, s, tm);
 }

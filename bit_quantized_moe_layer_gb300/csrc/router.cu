@@ -148,9 +148,10 @@ __global__ void __launch_bounds__(kWarps * 32) router_kernel(const __grid_consta
     const int tpc = TT / kCS;                  // tokens owned by each CTA
 
     for (int e = threadIdx.x; e < E; e += blockDim.x) pes_s[e] = a.per_expert_scale[e];
+    const bool wq = a.rq_w != nullptr;  // 4-bit projection, dequantised below
     if (threadIdx.x == 0) {
         prefetch_tensormap(&xmap);
-        prefetch_tensormap(&wmap);
+        if (!wq) prefetch_tensormap(&wmap);
         mbar_init(&full, 1);
         mbar_init(&wfull, 1);
         mbar_init(&mdone, 1);
@@ -163,11 +164,11 @@ __global__ void __launch_bounds__(kWarps * 32) router_kernel(const __grid_consta
     // only write this CTA's shared memory.
     auto issue_loads = [&](int tile, bool weights) {
         if (lane == 0)
-            mbar_arrive_expect_tx(&full, (uint32_t)cnt * (TT * 128 + (weights ? eb * 128 + 128 : 0) +
+            mbar_arrive_expect_tx(&full, (uint32_t)cnt * (TT * 128 + (weights ? (wq ? 0 : eb * 128) + 128 : 0) +
                                                           (weights && a.xe ? 128 : 0)));
         __syncwarp();
         if (lane < cnt) tma_load_2d(sm.xt + lane * TT * 128, &xmap, &full, (kb0 + lane) * 64, tile * TT);
-        if (weights && lane >= 16 && lane - 16 < cnt)
+        if (weights && !wq && lane >= 16 && lane - 16 < cnt)
             tma_load_2d(sm.wt + (lane - 16) * kWBlockBytes, &wmap, &full, (kb0 + lane - 16) * 64, 0);
         if (weights && lane == 31 && cnt > 0) bulk_load(sm.rsl, a.router_scale + (size_t)kb0 * 64, cnt * 128, &full);
         if (weights && a.xe && lane == 30 && cnt > 0) bulk_load(sm.psl, a.pre_w + (size_t)kb0 * 64, cnt * 128, &full);
@@ -183,6 +184,29 @@ __global__ void __launch_bounds__(kWarps * 32) router_kernel(const __grid_consta
     cluster_barrier();
     tc_fence_after();
     const uint32_t tmem = tmem_base;
+    if (wq) {
+        // This CTA's blocks of the 4-bit projection, once: word j of row e in
+        // block kb holds elements 8j..8j+7 of that block (low nibble first),
+        // i.e. 16-byte chunk j of the row, stored at chunk j ^ (e % 8) as the
+        // 128-byte swizzle of the copies lays it out. w = bf16(S q + B): the
+        // product of a bf16 scale and a 4-bit code is exact, the sum rounds
+        // once to fp32 and once to bf16 (exact in fp32 for these operands).
+        const int G = H / 64, W8 = H / 8;
+        for (int i = threadIdx.x; i < E * cnt * 8; i += kWarps * 32) {
+            const int j = i & 7, kb = (i >> 3) % cnt, e = (i >> 3) / cnt;
+            const uint32_t word = __ldg(a.rq_w + (size_t)e * W8 + (size_t)(kb0 + kb) * 8 + j);
+            const float S = bf16_bits_to_f32(__ldg(a.rq_s + (size_t)e * G + kb0 + kb));
+            const float B = bf16_bits_to_f32(__ldg(a.rq_b + (size_t)e * G + kb0 + kb));
+            uint32_t v[4];
+#pragma unroll
+            for (int p = 0; p < 4; ++p)
+                v[p] = pack_bf16x2(__fmaf_rn(S, (float)((word >> (8 * p)) & 0xFu), B),
+                                   __fmaf_rn(S, (float)((word >> (8 * p + 4)) & 0xFu), B));
+            *reinterpret_cast<uint4*>(sm.wt + kb * kWBlockBytes + e * 128 + ((j ^ (e & 7)) << 4)) =
+                make_uint4(v[0], v[1], v[2], v[3]);
+        }
+        // visible to the MMAs (async proxy) after phase 2's proxy fence and barrier
+    }
     const uint32_t rootb = f32_to_bf16_bits(a.root), root2 = rootb | (rootb << 16);
     uint32_t ncommit = 0, nreload = 0;  // mdone and wfull phases used so far
 

@@ -164,6 +164,23 @@ int moe_forward(const moe_dims* d, const uint16_t* x, const uint16_t* router_w,
                 void* stream);
 
 /*
+ * The router with the pages' 4-bit projection (DiffRouter.proj is a
+ * QuantizedLinear): router_q is the [E, H] weight in the affine layout above
+ * (w uint32 [E, H/8], scales and biases bf16 [E, H/64]); the projection uses
+ * the dequantised weight bf16(S*q + B), otherwise as moe_route. E <= 128
+ * (MOE_ERR_UNSUPPORTED otherwise). moe_forward_q4router is moe_forward with
+ * this router.
+ */
+int moe_route_q4(const moe_dims* d, const uint16_t* x, const moe_qweight* router_q,
+                 const uint16_t* router_scale, const uint16_t* per_expert_scale,
+                 int32_t* idx_out, uint16_t* w_out, void* stream);
+int moe_forward_q4router(const moe_dims* d, const uint16_t* x, const moe_qweight* router_q,
+                         const uint16_t* router_scale, const uint16_t* per_expert_scale,
+                         const moe_qweight* gate_up, const moe_qweight* down, uint16_t* out,
+                         int32_t* idx_out, uint16_t* w_out, void* workspace, size_t ws_bytes,
+                         void* stream);
+
+/*
  * The MoE branch of the decoder layer (DiffusionGemmaDecoderLayer.forwardWith
  * in "diffusion-gemma/model.ts"): the router reads the residual, the experts
  * read preFfNorm2(residual), and the experts' combined output goes through
