@@ -176,6 +176,45 @@ def make_branch_norms(d: Dims, seed: int = 0):
     return bf16_bits(rng.uniform(0.5, 1.5, d.H)), bf16_bits(rng.uniform(0.5, 1.5, d.H))
 
 
+# The dense MLP's intermediate size is not on the pages; the decoder-sized
+# dense workloads use 2112 (three times moe_intermediate, a multiple of 64).
+DENSE_INTER = 2112
+
+
+@dataclasses.dataclass
+class DenseInputs:
+    """Inputs of the dense 4-bit GeGLU MLP and the two calls built on it."""
+    T: int
+    H: int
+    I: int
+    group: int
+    eps: float
+    x: np.ndarray        # uint16 [T,H]: the MLP input, the dense branch's h, or the self-conditioning signal
+    embeds: np.ndarray   # uint16 [T,H]: SelfConditioning's inputs_embeds
+    gate: tuple          # (w uint32 [I,H/8], scales [I,H/g], biases [I,H/g])
+    up: tuple            # same shapes as gate
+    down: tuple          # (w uint32 [H,I/8], scales [H,I/g], biases [H,I/g])
+    pre_w: np.ndarray    # uint16 [H]: preFfNorm / SelfConditioning.preNorm weight
+    post_w: np.ndarray   # uint16 [H]: postFfNorm1 weight
+
+
+def make_dense(T: int, H: int = 2816, I: int = DENSE_INTER, seed: int = 0, group: int = 64,
+               eps: float = 1e-6) -> DenseInputs:
+    """Dense-MLP inputs with the layer's distributions: activations and
+    embeddings ~ N(0,1), the experts' 4-bit code, scale and bias recipe for the
+    three linears, norm weights ~ U(0.5, 1.5)."""
+    d = Dims(T=T, H=H, E=1, k=1, inter=I, group=group, eps=eps)
+    x = make_x(d, seed)
+    embeds = bf16_bits(_rng(seed, f"embeds:{T}x{H}").standard_normal((T, H)))
+    tri = lambda a: (a[0][0], a[1][0], a[2][0])
+    gate = tri(make_qweight(1, I, H, group, seed, "dense_gate"))
+    up = tri(make_qweight(1, I, H, group, seed, "dense_up"))
+    down = tri(make_qweight(1, H, I, group, seed, "dense_down"))
+    rng = _rng(seed, f"dense-norms:{H}")
+    pre_w, post_w = bf16_bits(rng.uniform(0.5, 1.5, H)), bf16_bits(rng.uniform(0.5, 1.5, H))
+    return DenseInputs(T, H, I, group, eps, x, embeds, gate, up, down, pre_w, post_w)
+
+
 def make_custom(d: Dims, seed: int = 0, **skew) -> LayerInputs:
     """Inputs for an arbitrary layer shape with the standard distributions."""
     return make_layer(Workload("custom", d, seed=seed, **skew))

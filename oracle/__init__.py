@@ -73,7 +73,25 @@ def _declare(lib):
     lib.oracle_rms_norm.restype = ctypes.c_int
     lib.oracle_moe_branch.argtypes = [ctypes.POINTER(_Dims)] + [P] * 16 + [ctypes.c_int]
     lib.oracle_moe_branch.restype = ctypes.c_int
+    Q = ctypes.POINTER(_QLinear)
+    lib.oracle_dense_mlp.argtypes = [ctypes.c_int32] * 4 + [P, Q, Q, Q] + [P] * 4 + [ctypes.c_int]
+    lib.oracle_dense_mlp.restype = ctypes.c_int
+    lib.oracle_dense_branch.argtypes = [ctypes.c_int32] * 4 + [ctypes.c_float, P, P, P, Q, Q, Q, P, ctypes.c_int]
+    lib.oracle_dense_branch.restype = ctypes.c_int
+    lib.oracle_self_conditioning.argtypes = [ctypes.c_int32] * 4 + [ctypes.c_float, P, P, P, Q, Q, Q, P,
+                                                                    ctypes.c_int]
+    lib.oracle_self_conditioning.restype = ctypes.c_int
     return lib
+
+
+class _QLinear(ctypes.Structure):
+    _fields_ = [("w", ctypes.c_void_p), ("s", ctypes.c_void_p), ("b", ctypes.c_void_p)]
+
+
+def _qlinear(q):
+    """(w uint32 [N, K/8], scales [N, K/g], biases [N, K/g]) -> (struct, arrays kept alive)."""
+    arrs = (_c(q[0], np.uint32), _c(q[1], np.uint16), _c(q[2], np.uint16))
+    return _QLinear(*[a.ctypes.data for a in arrs]), arrs
 
 
 def _dims(d) -> _Dims:
@@ -228,4 +246,58 @@ def route_q4(d, x, rq, router_scale, pes, taps: bool = False, nthreads: int = 0,
     out = dict(idx=idx, w=w)
     if taps:
         out.update(logits=logits, scores=scores)
+    return out
+
+
+def dense_mlp(x, gate, up, down, group: int = 64, taps: bool = False, nthreads: int = 0, lib=None):
+    """The dense 4-bit GeGLU MLP (SelfConditioning's three QuantizedLinears and
+    geglu; the decoder layer's GegluMLP). gate, up: (w [I, H/8], scales, biases),
+    down: (w [H, I/8], ...). Returns out [T,H] bf16 bits, or (out, gate, up, m)
+    with the per-token [T,I] taps."""
+    lib = lib or load()
+    x = _c(x, np.uint16)
+    T, H = x.shape
+    I = np.asarray(gate[0]).shape[0]
+    out = np.zeros((T, H), np.uint16)
+    tg, tu, tm = ((np.zeros((T, I), np.uint16) for _ in range(3)) if taps else (None, None, None))
+    (qg, ag), (qu, au), (qd, ad) = _qlinear(gate), _qlinear(up), _qlinear(down)
+    rc = lib.oracle_dense_mlp(T, H, I, group, _p(x), ctypes.byref(qg), ctypes.byref(qu), ctypes.byref(qd), _p(out),
+                              _p(tg), _p(tu), _p(tm), nthreads)
+    if rc != 0:
+        raise ValueError(f"oracle_dense_mlp rejected the inputs ({rc})")
+    return (out, tg, tu, tm) if taps else out
+
+
+def dense_branch(h, pre_norm_w, post_norm_w, gate, up, down, eps: float, group: int = 64, nthreads: int = 0,
+                 lib=None):
+    """The decoder layer's dense branch: postFfNorm1(mlp(preFfNorm(h)))."""
+    lib = lib or load()
+    h = _c(h, np.uint16)
+    T, H = h.shape
+    I = np.asarray(gate[0]).shape[0]
+    out = np.zeros((T, H), np.uint16)
+    (qg, ag), (qu, au), (qd, ad) = _qlinear(gate), _qlinear(up), _qlinear(down)
+    pre, post = _c(pre_norm_w, np.uint16), _c(post_norm_w, np.uint16)
+    rc = lib.oracle_dense_branch(T, H, I, group, ctypes.c_float(eps), _p(h), _p(pre), _p(post), ctypes.byref(qg),
+                                 ctypes.byref(qu), ctypes.byref(qd), _p(out), nthreads)
+    if rc != 0:
+        raise ValueError(f"oracle_dense_branch rejected the inputs ({rc})")
+    return out
+
+
+def self_conditioning(embeds, signal, pre_norm_w, gate, up, down, eps: float, group: int = 64, nthreads: int = 0,
+                      lib=None):
+    """SelfConditioning.forward: RMSNormNoScale(embeds + mlp(preNorm(signal)))."""
+    lib = lib or load()
+    embeds, signal = _c(embeds, np.uint16), _c(signal, np.uint16)
+    T, H = signal.shape
+    assert embeds.shape == (T, H)
+    I = np.asarray(gate[0]).shape[0]
+    out = np.zeros((T, H), np.uint16)
+    (qg, ag), (qu, au), (qd, ad) = _qlinear(gate), _qlinear(up), _qlinear(down)
+    pre = _c(pre_norm_w, np.uint16)
+    rc = lib.oracle_self_conditioning(T, H, I, group, ctypes.c_float(eps), _p(embeds), _p(signal), _p(pre),
+                                      ctypes.byref(qg), ctypes.byref(qu), ctypes.byref(qd), _p(out), nthreads)
+    if rc != 0:
+        raise ValueError(f"oracle_self_conditioning rejected the inputs ({rc})")
     return out

@@ -6,7 +6,9 @@
  * table or helper with the CUDA library; neither includes the other.
  *
  * Source: the DiffusionGemma language-model page ("diffusion-gemma/model.ts"),
- * classes DiffRouter (router forward) and DiffExperts (experts forward), and
+ * classes DiffRouter (router forward), DiffExperts (experts forward),
+ * DiffusionGemmaDecoderLayer (the MoE and dense branches' norms) and
+ * SelfConditioning (the dense 4-bit GeGLU MLP), and
  * the vision page ("diffusion-gemma/vision.ts", manualRms) for the fp32
  * semantics of the no-scale RMS norm.
  *
@@ -48,6 +50,14 @@ typedef struct {
     int32_t T, H, E, k, inter, group, bits;
     float eps;
 } oracle_dims;
+
+/* One 4-bit QuantizedLinear [N, K]: packed codes [N, K/8] (low nibble
+ * first), group scales and biases [N, K/g] as bf16 bits. */
+typedef struct {
+    const uint32_t* w;
+    const uint16_t* s;
+    const uint16_t* b;
+} oracle_qlinear;
 
 /* ---------------------------------------------------------------- bf16 --- */
 
@@ -427,7 +437,9 @@ int oracle_experts(const oracle_dims* d, const uint16_t* x, const int32_t* idx, 
  * used as it is, no 1 + weight offset; "diffusion-gemma/model.ts", header
  * notes and DiffusionGemmaDecoderLayer), in fp32 like the router's norm:
  * r = rsqrt(mean(x^2) + eps) with the fp32 mean the exact mean rounded once,
- * then bf16((x * r) * w), each fp32 product rounded, one bf16 rounding. */
+ * then bf16((x * r) * w), each fp32 product rounded, one bf16 rounding.
+ * weight NULL: RMSNormNoScale (an RMSNorm built with a null weight, as
+ * SelfConditioning's post norm), bf16(x * r). */
 int oracle_rms_norm(int32_t T, int32_t H, float eps, const uint16_t* x, const uint16_t* weight,
                     uint16_t* out) {
     if (T < 0 || H <= 0) return -1;
@@ -445,7 +457,7 @@ int oracle_rms_norm(int32_t T, int32_t H, float eps, const uint16_t* x, const ui
 #if ORACLE_MUTANT == 8
             out[(size_t)t * H + h] = bf16_from_float(nv); /* planted: weight dropped */
 #else
-            out[(size_t)t * H + h] = bf16_from_float(nv * bf(weight[h]));
+            out[(size_t)t * H + h] = weight ? bf16_from_float(nv * bf(weight[h])) : bf16_from_float(nv);
 #endif
         }
     }
@@ -482,6 +494,121 @@ int oracle_moe_branch(const oracle_dims* d, const uint16_t* residual, const uint
     if (!rc) rc = oracle_rms_norm(d->T, d->H, d->eps, ye, post_norm_w, out);
     free(xe);
     free(ye);
+    return rc;
+}
+
+/* ---------------------------------------------------------- dense MLP --- */
+
+/*
+ * The dense 4-bit GeGLU MLP: x [T,H] -> [T,H] through three QuantizedLinears
+ * (gate_proj and up_proj [I,H], down_proj [H,I], each a 4-bit group-g affine
+ * weight) and the compiled geglu between them. SelfConditioning.forward
+ * ("diffusion-gemma/model.ts") prints these steps; the decoder layer's
+ * GegluMLP is imported from a file the pages do not print and is read as
+ * the same three linears and geglu. Per token t:
+ *   gate = bf16(x[t] . W_gate^T), up = bf16(x[t] . W_up^T)     [I] each
+ *   m    = bf16(gelu_approx(gate) * up)                         one rounding
+ *   out  = bf16(m . W_down^T)                                   [H]
+ * Optional taps (NULL to skip): gate, up, m [T,I].
+ * Returns 0, or -1 on bad sizes.
+ */
+int oracle_dense_mlp(int32_t T, int32_t H, int32_t I, int32_t g, const uint16_t* x, const oracle_qlinear* gate,
+                     const oracle_qlinear* up, const oracle_qlinear* down, uint16_t* out, uint16_t* gate_tap,
+                     uint16_t* up_tap, uint16_t* m_tap, int nthreads) {
+    if (T < 0 || H <= 0 || I <= 0 || g <= 0 || H % 8 || I % 8 || H % g || I % g) return -1;
+    set_threads(nthreads);
+    float* wg = (float*)malloc(sizeof(float) * (size_t)I * H);
+    float* wu = (float*)malloc(sizeof(float) * (size_t)I * H);
+    float* wd = (float*)malloc(sizeof(float) * (size_t)H * I);
+    dequant_expert(gate->w, gate->s, gate->b, I, H, g, wg);
+    dequant_expert(up->w, up->s, up->b, I, H, g, wu);
+    dequant_expert(down->w, down->s, down->b, H, I, g, wd);
+#pragma omp parallel
+    {
+        uint16_t* gv = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)I);
+        uint16_t* uv = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)I);
+        uint16_t* m = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)I);
+#pragma omp for schedule(dynamic, 1)
+        for (int t = 0; t < T; ++t) {
+            const uint16_t* xt = x + (size_t)t * H;
+            for (int n = 0; n < I; ++n) {
+                double ag = 0.0, au = 0.0;
+                for (int h = 0; h < H; ++h) {
+                    ag += (double)bf(xt[h]) * (double)wg[(size_t)n * H + h];
+                    au += (double)bf(xt[h]) * (double)wu[(size_t)n * H + h];
+                }
+                gv[n] = bf16_from_double(ag);
+                uv[n] = bf16_from_double(au);
+            }
+            for (int n = 0; n < I; ++n) {
+#if ORACLE_MUTANT == 11
+                m[n] = geglu_bf16(bf(uv[n]), bf(gv[n])); /* planted: gate and up linears swapped */
+#else
+                m[n] = geglu_bf16(bf(gv[n]), bf(uv[n]));
+#endif
+            }
+            for (int h = 0; h < H; ++h) {
+                double acc = 0.0;
+                for (int n = 0; n < I; ++n) acc += (double)bf(m[n]) * (double)wd[(size_t)h * I + n];
+                out[(size_t)t * H + h] = bf16_from_double(acc);
+            }
+            if (gate_tap) memcpy(gate_tap + (size_t)t * I, gv, sizeof(uint16_t) * I);
+            if (up_tap) memcpy(up_tap + (size_t)t * I, uv, sizeof(uint16_t) * I);
+            if (m_tap) memcpy(m_tap + (size_t)t * I, m, sizeof(uint16_t) * I);
+        }
+        free(gv);
+        free(uv);
+        free(m);
+    }
+    free(wg);
+    free(wu);
+    free(wd);
+    return 0;
+}
+
+/* The decoder layer's dense branch (DiffusionGemmaDecoderLayer.forwardWith):
+ * postFfNorm1(mlp(preFfNorm(h))), the two norms plain RMSNorms with their
+ * weights (pre_feedforward_layernorm, post_feedforward_layernorm_1). */
+int oracle_dense_branch(int32_t T, int32_t H, int32_t I, int32_t g, float eps, const uint16_t* h,
+                        const uint16_t* pre_norm_w, const uint16_t* post_norm_w, const oracle_qlinear* gate,
+                        const oracle_qlinear* up, const oracle_qlinear* down, uint16_t* out, int nthreads) {
+    const size_t n = (size_t)T * (H > 0 ? H : 0);
+    uint16_t* xn = (uint16_t*)malloc(sizeof(uint16_t) * (n ? n : 1));
+    uint16_t* y = (uint16_t*)malloc(sizeof(uint16_t) * (n ? n : 1));
+    int rc = oracle_rms_norm(T, H, eps, h, pre_norm_w, xn);
+    if (!rc) rc = oracle_dense_mlp(T, H, I, g, xn, gate, up, down, y, NULL, NULL, NULL, nthreads);
+#if ORACLE_MUTANT == 13
+    if (!rc) rc = oracle_rms_norm(T, H, eps, y, pre_norm_w, out); /* planted: post norm takes the pre norm's weight */
+#else
+    if (!rc) rc = oracle_rms_norm(T, H, eps, y, post_norm_w, out);
+#endif
+    free(xn);
+    free(y);
+    return rc;
+}
+
+/* SelfConditioning.forward ("diffusion-gemma/model.ts"):
+ *   s   = mlp(preNorm(signal))          preNorm: RMSNorm with its weight
+ *   out = postNorm(bf16(embeds + s))    postNorm: RMSNormNoScale
+ * The add is a bf16 op: the exact sum of two bf16 values rounded once. */
+int oracle_self_conditioning(int32_t T, int32_t H, int32_t I, int32_t g, float eps, const uint16_t* embeds,
+                             const uint16_t* signal, const uint16_t* pre_norm_w, const oracle_qlinear* gate,
+                             const oracle_qlinear* up, const oracle_qlinear* down, uint16_t* out, int nthreads) {
+    const size_t n = (size_t)T * (H > 0 ? H : 0);
+    uint16_t* sn = (uint16_t*)malloc(sizeof(uint16_t) * (n ? n : 1));
+    uint16_t* sv = (uint16_t*)malloc(sizeof(uint16_t) * (n ? n : 1));
+    int rc = oracle_rms_norm(T, H, eps, signal, pre_norm_w, sn);
+    if (!rc) rc = oracle_dense_mlp(T, H, I, g, sn, gate, up, down, sv, NULL, NULL, NULL, nthreads);
+#if ORACLE_MUTANT == 12
+    /* planted: the embeddings are added after the post norm */
+    if (!rc) rc = oracle_rms_norm(T, H, eps, sv, NULL, sn);
+    for (size_t i = 0; !rc && i < n; ++i) out[i] = bf16_from_double((double)bf(embeds[i]) + (double)bf(sn[i]));
+#else
+    for (size_t i = 0; !rc && i < n; ++i) sn[i] = bf16_from_double((double)bf(embeds[i]) + (double)bf(sv[i]));
+    if (!rc) rc = oracle_rms_norm(T, H, eps, sn, NULL, out);
+#endif
+    free(sn);
+    free(sv);
     return rc;
 }
 

@@ -442,6 +442,77 @@ def check_route_q4(lib):
         assert np.array_equal(a[key], b[key]), f"4-bit router != dense router on the dequantised weight: {key}"
 
 
+def _dense_small(T=6, H=256, I=192, seed=25):
+    return ms.make_dense(T, H=H, I=I, seed=seed)
+
+
+def check_dense_mlp_brute_force(lib):
+    """gate, up, m and out of every token against a dense float64 computation
+    (library matmul, mpmath GeGLU, torch bf16 rounding of the dequantised
+    weights): each is the nearest bf16 to its exact value."""
+    dn = _dense_small()
+    out, g, u, m = oracle.dense_mlp(dn.x, dn.gate, dn.up, dn.down, taps=True, lib=lib)
+    wg = dense_dequant(dn.gate[0], dn.gate[1], dn.gate[2], dn.H, dn.group)
+    wu = dense_dequant(dn.up[0], dn.up[1], dn.up[2], dn.H, dn.group)
+    wd = dense_dequant(dn.down[0], dn.down[1], dn.down[2], dn.I, dn.group)
+    x = f64(dn.x)
+    assert_nearest_bf16(g, x @ wg.T, "dense gate_proj")
+    assert_nearest_bf16(u, x @ wu.T, "dense up_proj")
+    for t in range(dn.T):
+        assert_nearest_bf16(m[t], geglu_exact(f64(g[t]), f64(u[t])), f"dense GeGLU, token {t}")
+    assert_nearest_bf16(out, f64(m) @ wd.T, "dense down_proj")
+
+
+def check_dense_mlp_is_single_expert(lib):
+    """The dense MLP is the routed layer's one-expert, top-1 case with weight 1
+    and the expert's gate_up rows = gate_proj rows then up_proj rows (the
+    split at the intermediate size): bit for bit the same output."""
+    dn = _dense_small(T=9, seed=26)
+    d = small_dims(T=dn.T, H=dn.H, E=1, k=1, inter=dn.I)
+    gu = tuple(np.concatenate([a, b])[None] for a, b in zip(dn.gate, dn.up))
+    dw = tuple(a[None] for a in dn.down)
+    idx = np.zeros((dn.T, 1), np.int32)
+    w = np.full((dn.T, 1), 0x3F80, np.uint16)
+    want = oracle.experts(d, dn.x, idx, w, gu, dw, lib=lib)
+    assert np.array_equal(oracle.dense_mlp(dn.x, dn.gate, dn.up, dn.down, lib=lib), want), "dense MLP != one expert"
+
+
+def check_dense_branch_wiring(lib):
+    """The dense branch is RMSNorm(mlp(RMSNorm(h, pre)), post), composed
+    from the parts pinned above (and not with the norms' weights exchanged)."""
+    dn = _dense_small(T=7, seed=27)
+    out = oracle.dense_branch(dn.x, dn.pre_w, dn.post_w, dn.gate, dn.up, dn.down, dn.eps, lib=lib)
+    y = oracle.dense_mlp(oracle.rms_norm(dn.x, dn.pre_w, dn.eps, lib=lib), dn.gate, dn.up, dn.down, lib=lib)
+    assert np.array_equal(out, oracle.rms_norm(y, dn.post_w, dn.eps, lib=lib)), "dense branch wiring"
+
+
+def check_self_conditioning_exact_math(lib):
+    """out = c / sqrt(mean(c^2) + eps) within its fp32 steps and one bf16
+    rounding, for c = bf16(embeds + s) (torch's rounding of the exact sum)
+    and s the pinned dense MLP of RMSNorm(signal, pre)."""
+    dn = _dense_small(T=8, seed=28)
+    out = f64(oracle.self_conditioning(dn.embeds, dn.x, dn.pre_w, dn.gate, dn.up, dn.down, dn.eps, lib=lib))
+    s_ = oracle.dense_mlp(oracle.rms_norm(dn.x, dn.pre_w, dn.eps, lib=lib), dn.gate, dn.up, dn.down, lib=lib)
+    exact_sum = f64(dn.embeds) + f64(s_)
+    assert np.array_equal(exact_sum.astype(np.float32).astype(np.float64), exact_sum), "sum not exact in float32"
+    c = f64(torch_bf16_bits(exact_sum.astype(np.float32)))
+    exact = c / np.sqrt(np.mean(c * c, axis=1, keepdims=True) + dn.eps)
+    assert np.all(np.abs(out - exact) <= 2.0 ** -8 * np.abs(exact) + 1e-30), "self-conditioning far from c / rms(c)"
+
+
+def check_self_conditioning_zero_mlp(lib):
+    """With an all-zero down_proj (codes, scales and biases 0) the MLP adds
+    nothing, and RMSNormNoScale of a constant row c (eps = 0) is sign(c)."""
+    dn = _dense_small(T=3, seed=29)
+    zero = (np.zeros_like(dn.down[0]), np.zeros_like(dn.down[1]), np.zeros_like(dn.down[2]))
+    emb = np.zeros((3, dn.H), np.uint16)
+    for t, c in enumerate((0x3F80, 0xC0A0, 0x3C23)):  # 1, -5, ~0.00995
+        emb[t] = c
+    out = oracle.self_conditioning(emb, dn.x, dn.pre_w, dn.gate, dn.up, zero, 0.0, lib=lib)
+    want = np.where(emb & 0x8000, 0xBF80, 0x3F80).astype(np.uint16)
+    assert np.array_equal(out, want), "RMSNormNoScale of a constant row"
+
+
 ALL_CHECKS = [
     check_bf16_from_float, check_bf16_from_double,
     check_router_constant_row, check_router_zero_row, check_router_scale_invariance,
@@ -451,4 +522,6 @@ ALL_CHECKS = [
     check_expert_relabel, check_token_permutation,
     check_rms_norm_exact_math, check_rms_norm_invariances, check_rms_norm_constant_row, check_moe_branch_wiring,
     check_route_q4,
+    check_dense_mlp_brute_force, check_dense_mlp_is_single_expert, check_dense_branch_wiring,
+    check_self_conditioning_exact_math, check_self_conditioning_zero_mlp,
 ]

@@ -22,6 +22,9 @@ MUTANTS = {
     8: "RMS norm with a weight drops the weight",
     9: "MoE branch routes on the normalised expert input",
     10: "4-bit router drops the biases",
+    11: "dense MLP swaps the gate and up linears",
+    12: "self-conditioning adds the embeddings after the post norm",
+    13: "dense branch's post norm takes the pre norm's weight",
 }
 
 
