@@ -29,7 +29,7 @@ STATUS = {0: "ok", 1: "null pointer", 2: "bad shape", 3: "pointer not 16-byte al
 # Every function the public header declares.
 EXPORTS = ("moe_status_str", "moe_workspace_bytes", "moe_route", "moe_dispatch", "moe_experts",
            "moe_experts_noalloc", "moe_forward", "moe_forward_branch", "moe_forward_hostio", "moe_route_q4",
-           "moe_forward_q4router", "moe_timing_enable",
+           "moe_forward_q4router", "moe_dense_mlp", "moe_dense_branch", "moe_self_conditioning", "moe_timing_enable",
            "moe_timing_read",
            "moe_launches_per_forward", "moe_device_error")
 
@@ -77,12 +77,16 @@ def load(path: str = LIB_PATH):
     lib.moe_forward_branch.argtypes = [D, P, P, P, P, P, P, Q, Q, P, P, P, P, P, Z, P]
     lib.moe_route_q4.argtypes = [D, P, Q, P, P, P, P, P]
     lib.moe_forward_q4router.argtypes = [D, P, Q, P, P, Q, Q, P, P, P, P, Z, P]
+    lib.moe_dense_mlp.argtypes = [D, P, Q, Q, P, P, Z, P]
+    lib.moe_dense_branch.argtypes = [D, P, P, P, Q, Q, P, P, Z, P]
+    lib.moe_self_conditioning.argtypes = [D, P, P, P, Q, Q, P, P, Z, P]
     lib.moe_timing_enable.argtypes = [I]
     lib.moe_timing_read.argtypes = [ctypes.POINTER(ctypes.c_float), I, ctypes.POINTER(I)]
     lib.moe_launches_per_forward.argtypes = [ctypes.c_void_p]
     lib.moe_device_error.argtypes = []
     for fn in ("moe_route", "moe_dispatch", "moe_experts", "moe_experts_noalloc", "moe_forward", "moe_forward_branch",
-               "moe_forward_hostio", "moe_route_q4", "moe_forward_q4router",
+               "moe_forward_hostio", "moe_route_q4", "moe_forward_q4router", "moe_dense_mlp", "moe_dense_branch",
+               "moe_self_conditioning",
                "moe_timing_enable", "moe_timing_read", "moe_launches_per_forward", "moe_device_error"):
         getattr(lib, fn).restype = I
     _lib = lib
@@ -184,6 +188,31 @@ def moe_forward_branch(d: Dims, residual, router_w, router_scale, per_expert_sca
         ctypes.byref(d), _ptr(residual), _ptr(router_w), _ptr(router_scale), _ptr(per_expert_scale),
         _ptr(pre_norm_w), _ptr(post_norm_w), ctypes.byref(gate_up), ctypes.byref(down), _ptr(out),
         _ptr(idx_out), _ptr(w_out), _ptr(expert_in_out), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def moe_dense_mlp(d: Dims, x, gate_up: QWeight, down: QWeight, out, workspace=None, ws_bytes: int = 0,
+                  stream=None):
+    """The dense 4-bit GeGLU MLP over all rows (d.E = d.k = 1, d.inter = its
+    intermediate size); gate_up rows are gate_proj then up_proj."""
+    _check("moe_dense_mlp", load().moe_dense_mlp(ctypes.byref(d), _ptr(x), ctypes.byref(gate_up),
+                                                 ctypes.byref(down), _ptr(out), _ptr(workspace), ws_bytes,
+                                                 _stream(stream)))
+
+
+def moe_dense_branch(d: Dims, h, pre_norm_w, post_norm_w, gate_up: QWeight, down: QWeight, out, workspace=None,
+                     ws_bytes: int = 0, stream=None):
+    """The decoder layer's dense branch: RMSNorm(mlp(RMSNorm(h, pre)), post)."""
+    _check("moe_dense_branch", load().moe_dense_branch(
+        ctypes.byref(d), _ptr(h), _ptr(pre_norm_w), _ptr(post_norm_w), ctypes.byref(gate_up), ctypes.byref(down),
+        _ptr(out), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def moe_self_conditioning(d: Dims, inputs_embeds, signal, pre_norm_w, gate_up: QWeight, down: QWeight, out,
+                          workspace=None, ws_bytes: int = 0, stream=None):
+    """SelfConditioning.forward: RMSNormNoScale(inputs_embeds + mlp(RMSNorm(signal, pre)))."""
+    _check("moe_self_conditioning", load().moe_self_conditioning(
+        ctypes.byref(d), _ptr(inputs_embeds), _ptr(signal), _ptr(pre_norm_w), ctypes.byref(gate_up),
+        ctypes.byref(down), _ptr(out), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def moe_forward_hostio(d: Dims, x_host, router_w, router_scale, per_expert_scale, gate_up: QWeight,

@@ -330,8 +330,6 @@ __device__ __forceinline__ uint32_t elect_one() {
     return pred;
 }
 
-// Cluster-wide barrier (all threads of all CTAs of the cluster). Non-aligned
-// form; callers still reconverge their warp first (__syncwarp).
 // Programmatic dependent launch: let the next kernel of the stream be
 // scheduled now (it still waits for this grid before touching memory), and
 // wait for the previous kernel's grid to complete and its memory to be
@@ -339,8 +337,82 @@ __device__ __forceinline__ uint32_t elect_one() {
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Cluster-wide barrier (all threads of all CTAs of the cluster). Non-aligned
+// form; callers still reconverge their warp first (__syncwarp).
 __device__ __forceinline__ void cluster_barrier() {
     asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// ------------------------------------------------------------ row norms --
+// 8 bf16 (one 16-byte chunk) -> positions holding elements (0,4,1,5,2,6,3,7):
+// the K order in which the grouped GEMM's dequantised weights come out.
+__device__ __forceinline__ uint4 interleave8(uint4 v) {
+    uint4 o;
+    o.x = __byte_perm(v.x, v.z, 0x5410);
+    o.y = __byte_perm(v.x, v.z, 0x7632);
+    o.z = __byte_perm(v.y, v.w, 0x5410);
+    o.w = __byte_perm(v.y, v.w, 0x7632);
+    return o;
+}
+
+// Error-free sum a + b = s + e (Knuth's two-sum).
+__device__ __forceinline__ void two_sum_f(float a, float b, float& s, float& e) {
+    s = __fadd_rn(a, b);
+    const float bp = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
+}
+
+// Adds the squares of both bf16 halves of `b` (exact in fp32) to the
+// two-float sum (hi, lo).
+__device__ __forceinline__ void sumsq_bf16x2(uint32_t b, float& hi, float& lo) {
+    const float l = __uint_as_float(b << 16), h = __uint_as_float(b & 0xFFFF0000u);
+    float s1, e1;
+    two_sum_f(hi, __fmul_rn(l, l), s1, e1);
+    hi = s1;
+    lo = __fadd_rn(lo, e1);
+    two_sum_f(hi, __fmul_rn(h, h), s1, e1);
+    hi = s1;
+    lo = __fadd_rn(lo, e1);
+}
+
+// rsqrt(mean + eps) of one row whose sum of squares the NT threads of the
+// block hold as two-float partials (hi, lo): warp, then block reduction in a
+// fixed order (the same result every call), the fp32 mean being the exact
+// mean rounded once (unless within ~2^-40 of a rounding boundary), and a
+// correctly rounded rsqrt. Every thread of the block calls it, once a kernel.
+template <int NT>
+__device__ __forceinline__ float block_rsqrt_mean(float hi, float lo, int H, float eps) {
+    __shared__ float2 part[NT / 32];
+    __shared__ float rs_s;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float h2 = __shfl_xor_sync(0xffffffffu, hi, o), l2 = __shfl_xor_sync(0xffffffffu, lo, o);
+        float s1, e1;
+        two_sum_f(hi, h2, s1, e1);
+        hi = s1;
+        lo = __fadd_rn(__fadd_rn(lo, l2), e1);
+    }
+    if (lane == 0) part[warp] = make_float2(hi, lo);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float hs = 0.f, ls = 0.f;
+        for (int i = 0; i < NT / 32; ++i) {
+            float s1, e1;
+            two_sum_f(hs, part[i].x, s1, e1);
+            hs = s1;
+            ls = __fadd_rn(__fadd_rn(ls, part[i].y), e1);
+        }
+        // mean = (hs + ls) / H rounded once: q0 = RN(hs / H), the residual
+        // hs - q0 H is exact (fma), the correction moves q0 by under half an ulp
+        const float Hf = (float)H;
+        const float q0 = __fdiv_rn(hs, Hf);
+        const float rsd = __fadd_rn(__fmaf_rn(-q0, Hf, hs), ls);
+        const float mean = __fadd_rn(q0, __fdiv_rn(rsd, Hf));
+        rs_s = __frsqrt_rn(__fadd_rn(mean, eps));
+    }
+    __syncthreads();
+    return rs_s;
 }
 
 }  // namespace moe

@@ -150,16 +150,6 @@ __device__ __forceinline__ void zero_warp_counts(DispatchSmem& sm, int tid) {
     for (int i = tid; i < kW * (kMaxE + 1); i += kDispatchThreads) (&sm.wh[0][0])[i] = 0;
 }
 
-// 8 bf16 (one 16-byte chunk) -> positions holding elements (0,4,1,5,2,6,3,7).
-__device__ __forceinline__ uint4 interleave8(uint4 v) {
-    uint4 o;
-    o.x = __byte_perm(v.x, v.z, 0x5410);
-    o.y = __byte_perm(v.x, v.z, 0x7632);
-    o.z = __byte_perm(v.y, v.w, 0x5410);
-    o.w = __byte_perm(v.y, v.w, 0x7632);
-    return o;
-}
-
 // Slot chunk of CTA c in the three-kernel path.
 __host__ __device__ inline int chunk_slots(int S) {
     const int c = (S + kDispatchMaxChunks - 1) / kDispatchMaxChunks;
@@ -451,13 +441,6 @@ __global__ void __launch_bounds__(128) combine_kernel(const uint16_t* __restrict
                    pack_bf16x2(acc[6], acc[7]));
 }
 
-// Error-free sum a + b = s + e (Knuth's two-sum).
-__device__ __forceinline__ void two_sum_f(float a, float b, float& s, float& e) {
-    s = __fadd_rn(a, b);
-    const float bp = __fsub_rn(s, a);
-    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
-}
-
 // Combine followed by the MoE branch's post norm (postFfNorm2), one CTA a
 // token: c = the combined row (bf16, as combine_kernel), then
 // out = bf16((c * rsqrt(mean(c^2) + eps)) * post_w) with fp32 steps; the sum of
@@ -470,11 +453,9 @@ __global__ void __launch_bounds__(kNormThreads) combine_norm_kernel(const uint16
                                                                     const uint16_t* __restrict__ post_w,
                                                                     uint16_t* __restrict__ out, int k, int H,
                                                                     float eps) {
-    __shared__ float2 part[kNormThreads / 32];
-    __shared__ float rs_s;
     pdl_trigger();
     pdl_wait();
-    const int chunks = H / 8, t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int chunks = H / 8, t = blockIdx.x, tid = threadIdx.x;
     const uint4* yt = reinterpret_cast<const uint4*>(y + (size_t)t * k * H);
     const uint16_t* wt = w + (size_t)t * k;
     uint4 cv[kNormChunks];
@@ -499,47 +480,12 @@ __global__ void __launch_bounds__(kNormThreads) combine_norm_kernel(const uint16
         const uint32_t b0 = pack_bf16x2(acc[0], acc[1]), b1 = pack_bf16x2(acc[2], acc[3]),
                        b2 = pack_bf16x2(acc[4], acc[5]), b3 = pack_bf16x2(acc[6], acc[7]);
         cv[q] = make_uint4(b0, b1, b2, b3);
-        const uint32_t bb[4] = {b0, b1, b2, b3};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {  // squares of bf16 values are exact in fp32
-            const float l = __uint_as_float(bb[e] << 16), h = __uint_as_float(bb[e] & 0xFFFF0000u);
-            float s1, e1;
-            two_sum_f(hi, __fmul_rn(l, l), s1, e1);
-            hi = s1;
-            lo = __fadd_rn(lo, e1);
-            two_sum_f(hi, __fmul_rn(h, h), s1, e1);
-            hi = s1;
-            lo = __fadd_rn(lo, e1);
-        }
+        sumsq_bf16x2(b0, hi, lo);
+        sumsq_bf16x2(b1, hi, lo);
+        sumsq_bf16x2(b2, hi, lo);
+        sumsq_bf16x2(b3, hi, lo);
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float h2 = __shfl_xor_sync(0xffffffffu, hi, o), l2 = __shfl_xor_sync(0xffffffffu, lo, o);
-        float s1, e1;
-        two_sum_f(hi, h2, s1, e1);
-        hi = s1;
-        lo = __fadd_rn(__fadd_rn(lo, l2), e1);
-    }
-    if (lane == 0) part[warp] = make_float2(hi, lo);
-    __syncthreads();
-    if (tid == 0) {
-        float hs = 0.f, ls = 0.f;
-        for (int i = 0; i < kNormThreads / 32; ++i) {  // warp order: the same result every call
-            float s1, e1;
-            two_sum_f(hs, part[i].x, s1, e1);
-            hs = s1;
-            ls = __fadd_rn(__fadd_rn(ls, part[i].y), e1);
-        }
-        // mean = (hs + ls) / H rounded once: q0 = RN(hs / H), the residual
-        // hs - q0 H is exact (fma), the correction moves q0 by under half an ulp
-        const float Hf = (float)H;
-        const float q0 = __fdiv_rn(hs, Hf);
-        const float rsd = __fadd_rn(__fmaf_rn(-q0, Hf, hs), ls);
-        const float mean = __fadd_rn(q0, __fdiv_rn(rsd, Hf));
-        rs_s = __frsqrt_rn(__fadd_rn(mean, eps));
-    }
-    __syncthreads();
-    const float rs = rs_s;
+    const float rs = block_rsqrt_mean<kNormThreads>(hi, lo, H, eps);
 #pragma unroll
     for (int q = 0; q < kNormChunks; ++q) {
         const int c = tid + q * kNormThreads;

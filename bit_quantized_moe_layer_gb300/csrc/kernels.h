@@ -101,6 +101,17 @@ cudaError_t launch_combine_norm(const uint16_t* y, const uint16_t* w, const uint
                                 int k, int H, float eps, cudaStream_t stream);
 int dispatch_error_word();
 
+// Dense MLP input: xs[t] = row t of x, or RMSNorm(x, pre_w) with fp32 steps
+// (pre_w non-null), each 8-element block of K interleaved as the gather's;
+// perm[t] = t; and the tile list of one expert whose token tiles of nmax
+// rows cover all T rows (num_tiles: count, rows of the largest). H <= 8192.
+cudaError_t launch_dense_prep(const uint16_t* x, const uint16_t* pre_w, float eps, uint16_t* xs, int32_t* perm,
+                              Tile* tiles, int32_t* num_tiles, int T, int H, int nmax, cudaStream_t stream);
+// out[t] = bf16((c * rsqrt(mean(c^2) + eps)) [* w]) of c = s[t], or of
+// c = bf16(embeds[t] + s[t]) (embeds non-null); w null: no weight. H <= 8192.
+cudaError_t launch_add_norm(const uint16_t* embeds, const uint16_t* s, const uint16_t* w, float eps, uint16_t* out,
+                            int T, int H, cudaStream_t stream);
+
 // Grouped dequant-GEMM on tcgen05 (one expert per token tile).
 enum GemmMode { kGateUp = 0, kDown = 1 };
 struct GemmArgs {

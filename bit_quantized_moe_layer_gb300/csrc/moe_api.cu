@@ -291,6 +291,86 @@ int run_experts(const moe_dims* d, const uint16_t* x, const int32_t* idx, const 
     return MOE_OK;
 }
 
+// The dense 4-bit GeGLU MLP on the grouped GEMMs: one expert (E = 1, k = 1)
+// whose token tiles cover all T rows. x -> [pre norm] -> gate_up + GeGLU ->
+// down -> [post norm, after adding `embeds` when given] -> out.
+int run_dense(const moe_dims* d, const uint16_t* x, const uint16_t* pre_norm_w, const uint16_t* embeds,
+              const uint16_t* post_norm_w, bool post_norm, const moe_qweight* gu, const moe_qweight* dn, uint16_t* out,
+              uint8_t* ws, const Layout& L, const DeviceInfo& di, cudaStream_t s) {
+    const int T = d->T, H = d->H, I = d->inter;
+    int32_t* perm = reinterpret_cast<int32_t*>(ws + L.perm);
+    Tile* tiles = reinterpret_cast<Tile*>(ws + L.tiles);
+    int32_t* ntiles = reinterpret_cast<int32_t*>(ws + L.ntiles);
+    uint16_t* xs = reinterpret_cast<uint16_t*>(ws + L.xs);
+    uint16_t* mid = reinterpret_cast<uint16_t*>(ws + L.mid);
+    uint16_t* y = reinterpret_cast<uint16_t*>(ws + L.y);
+    // 128-row token tiles once they alone give every SM a gate_up item,
+    // else 64-row tiles (twice the items, half the MMA width each)
+    const int gu_tiles = I / 64;
+    const int nmax = ((long)((T + 127) / 128) * gu_tiles >= di.sms) ? 128 : 64;
+    const int ntok = (T + nmax - 1) / nmax;
+
+    CUtensorMap m_gu, m_dn, m_xs, m_mid;
+    if (!make_map_2d(&m_gu, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, gu->w, H / 8, (uint64_t)2 * I, 32, 64) ||
+        !make_map_2d(&m_dn, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, dn->w, I / 8, (uint64_t)H, 32, 128) ||
+        !make_map_2d(&m_xs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, xs, H, T, 64, 16) ||
+        !make_map_2d(&m_mid, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, mid, I, T, 64, 16))
+        return MOE_ERR_CUDA;
+
+    CallTimer tm(s);
+    tm.mark(0);
+    tm.mark(1);
+    tm.mark(2);
+    int rc = fail(launch_dense_prep(x, pre_norm_w, d->eps, xs, perm, tiles, ntiles, T, H, nmax, s));
+    if (rc) return rc;
+    tm.mark(3);
+
+    GemmArgs ga{};
+    ga.scales = gu->scales;
+    ga.biases = gu->biases;
+    ga.tiles = tiles;
+    ga.num_tiles = ntiles;
+    ga.perm = perm;
+    ga.out = mid;
+    ga.K = H;
+    ga.N = 2 * I;
+    ga.inter = I;
+    ga.out_ld = I;
+    ga.nmax = nmax;
+    ga.E = 1;
+    ga.n_tiles = gu_tiles;
+    ga.w = reinterpret_cast<const uint8_t*>(gu->w);
+    ga.prefetch_items = 2;
+    ga.tiles_per_expert = ntok;  // every item is expert 0's
+    gemm_stages(H, nmax, &ga.wstages, &ga.bregion);
+    int grid = di.sms < ntok * ga.n_tiles ? di.sms : ntok * ga.n_tiles;
+    if ((rc = fail(launch_gemm(kGateUp, m_gu, m_xs, ga, grid, s)))) return rc;
+    tm.mark(4);
+
+    GemmArgs gd = ga;
+    gd.scales = dn->scales;
+    gd.biases = dn->biases;
+    gd.w = reinterpret_cast<const uint8_t*>(dn->w);
+    gd.out = post_norm ? y : out;
+    gd.K = I;
+    gd.N = H;
+    gd.out_ld = H;
+    gd.n_tiles = H / 128;
+    gemm_stages(I, nmax, &gd.wstages, &gd.bregion);
+    grid = di.sms < ntok * gd.n_tiles ? di.sms : ntok * gd.n_tiles;
+    if ((rc = fail(launch_gemm(kDown, m_dn, m_mid, gd, grid, s)))) return rc;
+    tm.mark(5);
+    if (post_norm && (rc = fail(launch_add_norm(embeds, y, post_norm_w, d->eps, out, T, H, s)))) return rc;
+    tm.mark(6);
+    return MOE_OK;
+}
+
+int check_dense(const moe_dims* d) {
+    int rc = check_dims(d);
+    if (rc) return rc;
+    return (d->E == 1 && d->k == 1) ? MOE_OK : MOE_ERR_SHAPE;
+}
+
 int route_impl(const moe_dims* d, const uint16_t* x, const uint16_t* rw, const uint16_t* rs, const uint16_t* pes,
                int32_t* idx, uint16_t* w, cudaStream_t s, const uint16_t* pre_norm_w = nullptr,
                uint16_t* xe = nullptr, const moe_qweight* rq = nullptr) {
@@ -550,6 +630,56 @@ int moe_forward_branch(const moe_dims* d, const uint16_t* residual, const uint16
         return rc;
     tm.mark(1);
     return run_experts(d, xe, idx, w, gate_up, down, out, ws, L, di, s, tm, post_norm_w);
+}
+
+int moe_dense_mlp(const moe_dims* d, const uint16_t* x, const moe_qweight* gate_up, const moe_qweight* down,
+                  uint16_t* out, void* workspace, size_t ws_bytes, void* stream) {
+    int rc = check_dense(d);
+    if (rc) return rc;
+    if ((rc = check_ptrs({x, out}))) return rc;
+    if ((rc = check_qweight(gate_up)) || (rc = check_qweight(down))) return rc;
+    if (d->T == 0) return MOE_OK;
+    DeviceInfo di;
+    if ((rc = device_info(&di))) return rc;
+    const Layout L = layout(d);
+    uint8_t* ws = nullptr;
+    if ((rc = get_workspace(d, workspace, ws_bytes, L, &ws))) return rc;
+    return run_dense(d, x, nullptr, nullptr, nullptr, false, gate_up, down, out, ws, L, di,
+                     static_cast<cudaStream_t>(stream));
+}
+
+int moe_dense_branch(const moe_dims* d, const uint16_t* h, const uint16_t* pre_norm_w, const uint16_t* post_norm_w,
+                     const moe_qweight* gate_up, const moe_qweight* down, uint16_t* out, void* workspace,
+                     size_t ws_bytes, void* stream) {
+    int rc = check_dense(d);
+    if (rc) return rc;
+    if ((rc = check_ptrs({h, pre_norm_w, post_norm_w, out}))) return rc;
+    if ((rc = check_qweight(gate_up)) || (rc = check_qweight(down))) return rc;
+    if (d->T == 0) return MOE_OK;
+    DeviceInfo di;
+    if ((rc = device_info(&di))) return rc;
+    const Layout L = layout(d);
+    uint8_t* ws = nullptr;
+    if ((rc = get_workspace(d, workspace, ws_bytes, L, &ws))) return rc;
+    return run_dense(d, h, pre_norm_w, nullptr, post_norm_w, true, gate_up, down, out, ws, L, di,
+                     static_cast<cudaStream_t>(stream));
+}
+
+int moe_self_conditioning(const moe_dims* d, const uint16_t* inputs_embeds, const uint16_t* signal,
+                          const uint16_t* pre_norm_w, const moe_qweight* gate_up, const moe_qweight* down,
+                          uint16_t* out, void* workspace, size_t ws_bytes, void* stream) {
+    int rc = check_dense(d);
+    if (rc) return rc;
+    if ((rc = check_ptrs({inputs_embeds, signal, pre_norm_w, out}))) return rc;
+    if ((rc = check_qweight(gate_up)) || (rc = check_qweight(down))) return rc;
+    if (d->T == 0) return MOE_OK;
+    DeviceInfo di;
+    if ((rc = device_info(&di))) return rc;
+    const Layout L = layout(d);
+    uint8_t* ws = nullptr;
+    if ((rc = get_workspace(d, workspace, ws_bytes, L, &ws))) return rc;
+    return run_dense(d, signal, pre_norm_w, inputs_embeds, nullptr, true, gate_up, down, out, ws, L, di,
+                     static_cast<cudaStream_t>(stream));
 }
 
 int moe_forward_hostio(const moe_dims* d, const uint16_t* x_host, const uint16_t* router_w,

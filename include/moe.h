@@ -205,6 +205,53 @@ int moe_forward_branch(const moe_dims* d, const uint16_t* residual, const uint16
                        void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * The dense 4-bit GeGLU MLP: SelfConditioning's gate_proj, up_proj and
+ * down_proj QuantizedLinears with the compiled geglu between them
+ * (SelfConditioning.forward in "diffusion-gemma/model.ts"), which is also
+ * how the decoder layer's GegluMLP is read (its file is not on the pages).
+ * Row by row over all T rows:
+ *   gate = bf16(x . W_gate^T), up = bf16(x . W_up^T)       [I] each
+ *   m    = bf16(gelu_approx(gate) * up)
+ *   out  = bf16(m . W_down^T)                               [H]
+ * It is the routed layer's one-expert, top-1 case and runs on the same
+ * grouped GEMMs: d->E and d->k must be 1 (MOE_ERR_SHAPE otherwise) and
+ * d->inter is the MLP's intermediate size I (a multiple of 64).
+ *   gate_up  the [2I, H] weight in the affine layout above: rows [0, I) are
+ *            gate_proj, rows [I, 2I) up_proj (a checkpoint's two linears
+ *            concatenated along the output dimension, with their scales and
+ *            biases likewise);
+ *   down     the [H, I] down_proj weight.
+ * x and out [T,H] bf16. Workspace as moe_experts (moe_workspace_bytes of
+ * the same dims). 3 kernel launches: input staging, gate_up + GeGLU, down.
+ */
+int moe_dense_mlp(const moe_dims* d, const uint16_t* x, const moe_qweight* gate_up,
+                  const moe_qweight* down, uint16_t* out, void* workspace, size_t ws_bytes,
+                  void* stream);
+
+/*
+ * The decoder layer's dense branch (DiffusionGemmaDecoderLayer.forwardWith):
+ *   out = norm(moe_dense_mlp(norm(h, pre_norm_w)), post_norm_w)
+ * with the norm of moe_forward_branch (pre_feedforward_layernorm and
+ * post_feedforward_layernorm_1). The pre norm runs in the input-staging
+ * kernel; the post norm adds a fourth launch (one CTA a token).
+ */
+int moe_dense_branch(const moe_dims* d, const uint16_t* h, const uint16_t* pre_norm_w,
+                     const uint16_t* post_norm_w, const moe_qweight* gate_up,
+                     const moe_qweight* down, uint16_t* out, void* workspace, size_t ws_bytes,
+                     void* stream);
+
+/*
+ * SelfConditioning.forward: with s = moe_dense_mlp(norm(signal, pre_norm_w)),
+ *   c   = bf16(inputs_embeds + s)                 (a bf16 add)
+ *   out = bf16(c * rsqrt(mean(c^2) + eps))        (RMSNormNoScale, fp32 steps)
+ * inputs_embeds, signal, out [T,H] bf16; pre_norm_w [H]. 4 launches.
+ */
+int moe_self_conditioning(const moe_dims* d, const uint16_t* inputs_embeds, const uint16_t* signal,
+                          const uint16_t* pre_norm_w, const moe_qweight* gate_up,
+                          const moe_qweight* down, uint16_t* out, void* workspace,
+                          size_t ws_bytes, void* stream);
+
+/*
  * The whole layer with HOST activations: copies x_host [T,H] to the device,
  * runs moe_forward and copies out [T,H] back to out_host, then synchronises
  * the stream. Weights and router parameters are device pointers. Host
@@ -222,7 +269,9 @@ int moe_forward_hostio(const moe_dims* d, const uint16_t* x_host, const uint16_t
  * stream (at most 1024 calls are kept). moe_timing_read synchronises the
  * recorded events and writes, for each stage, the summed milliseconds into
  * ms[0..n) in the order: route, dispatch, gather, gate_up, down, combine,
- * and the number of calls into *calls; it then clears the record.
+ * and the number of calls into *calls; it then clears the record. The
+ * dense calls record their input staging as "gather" and their post norm
+ * as "combine".
  * Returns the number of stages written.
  */
 int moe_timing_enable(int enable);

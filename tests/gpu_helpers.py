@@ -206,3 +206,26 @@ def oracle_experts_rows(inp: ms.LayerInputs, idx: np.ndarray, w: np.ndarray, row
         d = dataclasses.replace(d, T=len(rows))
         x, idx, w = x[rows], idx[rows], w[rows]
     return oracle.experts(d, x, idx, w, (inp.gu_w, inp.gu_s, inp.gu_b), (inp.dn_w, inp.dn_s, inp.dn_b))
+
+
+def compare_normed_out(got, want, c, w, eps, what, c_err=None):
+    """Output of a post norm out = bf16((c * rs_t) [* w]), rs_t =
+    rsqrt(mean(c^2) + eps), against the oracle's, for the oracle's input row
+    c. A GPU input within c_err of c (default: the layer bound 2e-2 RMS(c)
+    plus a one-ulp rounding difference of c) is carried by that scaling, and
+    the output rounds once more: |out - ref| <= c_err rs_t |w[h]| + ulp(ref).
+    The RMS error stays below 1e-3 of the RMS."""
+    g, o, cc = f64(got), f64(want), f64(c)
+    wv = np.ones((1, cc.shape[1])) if w is None else np.abs(f64(w))[None, :]
+    rs = 1.0 / np.sqrt(np.mean(cc * cc, axis=1, keepdims=True) + eps)
+    if c_err is None:
+        c_err = 2e-2 * float(np.sqrt(np.mean(cc * cc))) + bf16_ulp(cc)
+    err = np.abs(g - o)
+    tol = c_err * rs * wv + bf16_ulp(o)
+    bad = np.flatnonzero((err > tol).ravel())
+    stats = dict(max_err_over_tol=float((err / tol).max()) if err.size else 0.0,
+                 rms_err_over_rms=float(np.sqrt(np.mean(err ** 2)) / np.sqrt(np.mean(o ** 2))) if err.size else 0.0)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite GPU output"
+    assert bad.size == 0, f"{what}: {bad.size} elements beyond tolerance {stats}"
+    assert stats["rms_err_over_rms"] <= 1e-3, f"{what}: RMS error too large {stats}"
+    return stats

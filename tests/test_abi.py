@@ -90,3 +90,25 @@ def test_zero_tokens_is_a_no_op(lib):
     buf = ctypes.create_string_buffer(64)
     p = (ctypes.addressof(buf) + 15) & ~15
     assert lib.moe_route(ctypes.byref(d), p, p, p, p, p, p, None) == 0
+
+
+def test_dense_calls_check_arguments(lib):
+    """The dense MLP calls are the one-expert, top-1 case: other E or k is a
+    shape error; null and misaligned pointers and T = 0 as for the layer."""
+    import bit_quantized_moe_layer_gb300 as moe
+    buf = ctypes.create_string_buffer(64)
+    p = (ctypes.addressof(buf) + 15) & ~15
+    q = moe.qweight(p, p, p)
+    Q = ctypes.byref(q)
+    for E, k, status in ((8, 2, 2), (2, 1, 2), (1, 2, 4)):  # k > E fails the layer's own check first
+        d = moe.dims(8, 256, E, k, 192)
+        assert lib.moe_dense_mlp(ctypes.byref(d), p, Q, Q, p, None, 0, None) == status
+        assert lib.moe_dense_branch(ctypes.byref(d), p, p, p, Q, Q, p, None, 0, None) == status
+        assert lib.moe_self_conditioning(ctypes.byref(d), p, p, p, Q, Q, p, None, 0, None) == status
+    d = moe.dims(8, 256, 1, 1, 192)
+    assert lib.moe_dense_mlp(ctypes.byref(d), None, Q, Q, p, None, 0, None) == 1
+    assert lib.moe_dense_branch(ctypes.byref(d), p, None, p, Q, Q, p, None, 0, None) == 1
+    assert lib.moe_self_conditioning(ctypes.byref(d), p + 2, p, p, Q, Q, p, None, 0, None) == 3
+    assert lib.moe_dense_mlp(ctypes.byref(moe.dims(8, 256, 1, 1, 100)), p, Q, Q, p, None, 0, None) == 4
+    d0 = moe.dims(0, 256, 1, 1, 192)
+    assert lib.moe_self_conditioning(ctypes.byref(d0), p, p, p, Q, Q, p, None, 0, None) == 0

@@ -53,28 +53,6 @@ def check_expert_input(got, want, what):
         assert rows.size <= max(1, got.shape[0] // 1000), f"{what}: expert input differs on {rows.size} tokens"
 
 
-def compare_branch_out(got, want, post, combined, eps, what):
-    """The post norm maps the combined bf16 row c of token t to
-    bf16(c rs_t post[h]), rs_t = rsqrt(mean(c^2) + eps). The layer's own bound
-    on c (2e-2 of its RMS) plus a one-ulp difference of c (fp32 sum in slot
-    order against the exact sum, each rounded once) is carried by that
-    scaling, and the output rounds once more:
-    |out - ref| <= (2e-2 RMS(c) + ulp(c)) rs_t post[h] + ulp(ref).
-    The RMS error stays below 1e-3 of the RMS."""
-    g, o, w, c = gh.f64(got), gh.f64(want), gh.f64(post)[None, :], gh.f64(combined)
-    rs = 1.0 / np.sqrt(np.mean(c * c, axis=1, keepdims=True) + eps)
-    rms_c = float(np.sqrt(np.mean(c * c)))
-    err = np.abs(g - o)
-    tol = (2e-2 * rms_c + gh.bf16_ulp(c)) * rs * w + gh.bf16_ulp(o)
-    bad = np.flatnonzero((err > tol).ravel())
-    stats = dict(max_err_over_tol=float((err / tol).max()),
-                 rms_err_over_rms=float(np.sqrt(np.mean(err ** 2)) / np.sqrt(np.mean(o ** 2))))
-    assert np.all(np.isfinite(g)), f"{what}: non-finite GPU output"
-    assert bad.size == 0, f"{what}: {bad.size} elements beyond tolerance {stats}"
-    assert stats["rms_err_over_rms"] <= 1e-3, f"{what}: RMS error too large {stats}"
-    return stats
-
-
 def run_case(inp, rows=None, seed=0):
     d = inp.dims
     pre, post = ms.make_branch_norms(d, seed)
@@ -91,7 +69,7 @@ def run_case(inp, rows=None, seed=0):
     y = oracle.experts(dr, xe_ref[rows], ref["idx"][rows], ref["w"][rows], (inp.gu_w, inp.gu_s, inp.gu_b),
                        (inp.dn_w, inp.dn_s, inp.dn_b))
     want = oracle.rms_norm(y, post, d.eps)
-    return compare_branch_out(out[rows], want, post, y, d.eps, f"branch T={d.T}")
+    return gh.compare_normed_out(out[rows], want, y, post, d.eps, f"branch T={d.T}")
 
 
 @pytest.mark.parametrize("name", FULL)
@@ -125,4 +103,4 @@ def test_branch_matches_composition():
     assert np.array_equal(idx, idx2) and np.array_equal(w, w2), "branch routing != moe_route(residual)"
     g2 = dataclasses.replace(g, x=gh.dev16(xe))
     y = gh.gpu_experts(g2, idx, w)
-    compare_branch_out(out, oracle.rms_norm(y, post, d.eps), post, y, d.eps, "branch vs composition")
+    gh.compare_normed_out(out, oracle.rms_norm(y, post, d.eps), y, post, d.eps, "branch vs composition")
