@@ -67,6 +67,33 @@ def roofline_model(d: ms.Dims, touched: int, peaks):
     return dict(bytes=bytes_alg, flops=flops, t_roof_s=max(t_hbm, t_tc), bound="hbm" if t_hbm >= t_tc else "tensor")
 
 
+def dense_model(dn):
+    """Algorithmic bytes (packed weights, scales, biases, x in, out) and
+    flops of one dense MLP call over T rows."""
+    g = dn.group
+    w = 3 * dn.I * dn.H // 2 + 3 * 2 * (dn.I * dn.H // g) * 2
+    return dict(bytes=w + 2 * dn.T * dn.H * 2, flops=2 * dn.T * dn.H * 3 * dn.I,
+                gate_up_flops=2 * dn.T * dn.H * 2 * dn.I)
+
+
+def dense_report(dn, dense_ms, stage_ms, calls, peaks, world):
+    m = dense_model(dn)
+    t_hbm, t_tc = m["bytes"] / (peaks["hbm"] * 1e9), m["flops"] / (peaks["tc"] * 1e12)
+    t_roof = max(t_hbm, t_tc)
+    gu_ms = stage_ms["gate_up"] / max(1, calls)
+    gu_tflops = m["gate_up_flops"] / (gu_ms * 1e-3) / 1e12
+    return dict(
+        workload=f"dense 4-bit GeGLU MLP: T={dn.T} H={dn.H} I={dn.I} group={dn.group} (I not on the pages)",
+        ms_per_step={k: v for k, v in dense_ms.items()},
+        value={k: whole_job_rate(dn.T, world, v * 1e-3) for k, v in dense_ms.items()}, unit="tokens/s",
+        roofline=dict(bound="tensor" if t_tc >= t_hbm else "hbm", t_roof_us=t_roof * 1e6,
+                      t_mlp_us=dense_ms["mlp"] * 1e3, frac=t_roof / (dense_ms["mlp"] * 1e-3), bytes=m["bytes"],
+                      flops=m["flops"], peak_source=f"{peaks['source']} bf16_tflops and hbm_gbs"),
+        gate_up_kernel=dict(ms_per_launch=gu_ms, achieved_tflops=gu_tflops, peak=peaks["tc"],
+                            frac=gu_tflops / peaks["tc"]),
+        stages_ms_per_call={k: v / max(1, calls) for k, v in stage_ms.items() if v > 0})
+
+
 class ClockSampler:
     """SM clock, power and clock-event reasons of one GPU, read through NVML
     (ctypes, read-only queries) every 2 ms while the timed region runs, plus
@@ -334,29 +361,67 @@ def run_ours(args, wl):
             e2e_ms.append(1e3 * (time.perf_counter() - t0))
     e2e_step = max_over_ranks(statistics.mean(e2e_ms), world, "cuda")
 
+    def timed(call):
+        """Mean ms of `call` over the timed steps, like region 1 (L2 flushed
+        between steps, events around each call on its stream)."""
+        for _ in range(args.warmup):
+            flush.zero_()
+            call()
+        st = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        en = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()
+            st[i].record(stream)
+            call()
+            en[i].record(stream)
+        torch.cuda.synchronize()
+        return max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in zip(st, en)), world, "cuda")
+
     # The decoder layer's MoE branch (moe_forward_branch: the router on the
     # residual, the experts on preFfNorm2(residual), postFfNorm2 of their
-    # output), timed like region 1.
+    # output).
     pre_w, post_w = (torch.from_numpy(a.view(np.int16).copy()).cuda()
                      for a in ms.make_branch_norms(inp.dims, wl.seed))
     out_b = torch.empty_like(out)
+    branch_ms = timed(lambda: moe.moe_forward_branch(
+        d, x, layer.router_w, layer.router_scale, layer.pes, pre_w, post_w, layer.gate_up, layer.down, out_b, idx,
+        wts, None, ws, ws.numel(), stream))
 
-    def branch_step():
-        moe.moe_forward_branch(d, x, layer.router_w, layer.router_scale, layer.pes, pre_w, post_w, layer.gate_up,
-                               layer.down, out_b, idx, wts, None, ws, ws.numel(), stream)
+    # The layer with the 4-bit group-64 router projection (moe_forward_q4router).
+    rq = [torch.from_numpy(a.view(np.int32 if a.dtype == np.uint32 else np.int16).copy()).cuda()
+          for a in ms.make_router_q4(inp.dims, wl.seed)]
+    q4_ms = timed(lambda: moe.moe_forward_q4router(
+        d, x, moe.qweight(*rq), layer.router_scale, layer.pes, layer.gate_up, layer.down, out_b, idx, wts, ws,
+        ws.numel(), stream))
 
-    for _ in range(args.warmup):
+    # The dense 4-bit GeGLU MLP at the same T (H as the layer, I = 2112):
+    # moe_dense_mlp, the decoder layer's dense branch and SelfConditioning.
+    dn = ms.make_dense(d.T, H=d.H, I=ms.DENSE_INTER, seed=wl.seed + rank)
+    dd = moe.dims(dn.T, dn.H, 1, 1, dn.I, eps=dn.eps)
+    t16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16).copy()).cuda()
+    t32 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int32).copy()).cuda()
+    dgu = (t32(np.concatenate([dn.gate[0], dn.up[0]])), t16(np.concatenate([dn.gate[1], dn.up[1]])),
+           t16(np.concatenate([dn.gate[2], dn.up[2]])))
+    ddn = (t32(dn.down[0]), t16(dn.down[1]), t16(dn.down[2]))
+    dx, demb, dpre, dpost = t16(dn.x), t16(dn.embeds), t16(dn.pre_w), t16(dn.post_w)
+    dws = torch.empty(moe.workspace_bytes(dd), dtype=torch.uint8, device="cuda")
+    dout = torch.empty((dn.T, dn.H), dtype=torch.int16, device="cuda")
+    qg, qd = moe.qweight(*dgu), moe.qweight(*ddn)
+    dense_calls = {
+        "mlp": lambda: moe.moe_dense_mlp(dd, dx, qg, qd, dout, dws, dws.numel(), stream),
+        "branch": lambda: moe.moe_dense_branch(dd, dx, dpre, dpost, qg, qd, dout, dws, dws.numel(), stream),
+        "self_conditioning": lambda: moe.moe_self_conditioning(dd, demb, dx, dpre, qg, qd, dout, dws, dws.numel(),
+                                                               stream),
+    }
+    dense_ms = {k_: timed(f_) for k_, f_ in dense_calls.items()}
+    moe.timing_enable(True)
+    for _ in range(args.steps):
         flush.zero_()
-        branch_step()
-    bstarts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    bends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    for i in range(args.steps):
-        flush.zero_()
-        bstarts[i].record(stream)
-        branch_step()
-        bends[i].record(stream)
+        dense_calls["mlp"]()
     torch.cuda.synchronize()
-    branch_ms = max_over_ranks(statistics.mean(s_.elapsed_time(e_) for s_, e_ in zip(bstarts, bends)), world, "cuda")
+    dense_stage_ms, dense_calls_n = moe.timing_read()
+    moe.timing_enable(False)
+    err |= moe.device_error()
 
     if rank != 0:
         if world > 1:
@@ -397,6 +462,9 @@ def run_ours(args, wl):
         gpu_launches=moe.launches_per_forward(d) * args.steps,
         branch=dict(call="moe_forward_branch (router on the residual, experts on preFfNorm2, postFfNorm2)",
                     ms_per_step=branch_ms, value=whole_job_rate(d.T, world, branch_ms * 1e-3), unit="tokens/s"),
+        q4router=dict(call="moe_forward_q4router (the layer with the 4-bit group-64 router projection)",
+                      ms_per_step=q4_ms, value=whole_job_rate(d.T, world, q4_ms * 1e-3), unit="tokens/s"),
+        dense=dense_report(dn, dense_ms, dense_stage_ms, dense_calls_n, peaks, world),
         clocks=clk.summary(),
         device_error=err,
     )

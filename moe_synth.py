@@ -215,6 +215,20 @@ def make_dense(T: int, H: int = 2816, I: int = DENSE_INTER, seed: int = 0, group
     return DenseInputs(T, H, I, group, eps, x, embeds, gate, up, down, pre_w, post_w)
 
 
+# The vocabulary size is not on the pages; the image token id 258880 bounds
+# it from below, and the head workloads take 2^18 = 262144.
+VOCAB = 262144
+
+
+def make_head(T: int, H: int = 2816, V: int = VOCAB, seed: int = 0, group: int = 64, h_scale: float = 1.0):
+    """Inputs of the tied 4-bit head: h [T,H] bf16 bits ~ N(0, h_scale^2) (a
+    final-normed hidden state), the embedding table [V,H] as a 4-bit group-g
+    weight with the experts' code, scale and bias recipe."""
+    h = bf16_bits(_rng(seed, f"head-h:{T}x{H}").standard_normal((T, H)) * h_scale)
+    w, s, b = make_qweight(1, V, H, group, seed, "embed")
+    return h, (w[0], s[0], b[0])
+
+
 def make_custom(d: Dims, seed: int = 0, **skew) -> LayerInputs:
     """Inputs for an arbitrary layer shape with the standard distributions."""
     return make_layer(Workload("custom", d, seed=seed, **skew))

@@ -81,6 +81,8 @@ def _declare(lib):
     lib.oracle_self_conditioning.argtypes = [ctypes.c_int32] * 4 + [ctypes.c_float, P, P, P, Q, Q, Q, P,
                                                                     ctypes.c_int]
     lib.oracle_self_conditioning.restype = ctypes.c_int
+    lib.oracle_lm_head.argtypes = [ctypes.c_int32] * 4 + [ctypes.c_float, P, Q, P, P, ctypes.c_int]
+    lib.oracle_lm_head.restype = ctypes.c_int
     return lib
 
 
@@ -301,3 +303,20 @@ def self_conditioning(embeds, signal, pre_norm_w, gate, up, down, eps: float, gr
     if rc != 0:
         raise ValueError(f"oracle_self_conditioning rejected the inputs ({rc})")
     return out
+
+
+def lm_head(h, embed, cap: float = 30.0, group: int = 64, taps: bool = False, nthreads: int = 0, lib=None):
+    """The tied 4-bit head and its fp32 softcap: h [T,H] bf16 bits, embed =
+    (w uint32 [V, H/8], scales [V, H/g], biases [V, H/g]). Returns out
+    [T,V] float32, or (out, logits bf16 bits [T,V])."""
+    lib = lib or load()
+    h = _c(h, np.uint16)
+    T, H = h.shape
+    V = np.asarray(embed[0]).shape[0]
+    out = np.zeros((T, V), np.float32)
+    lg = np.zeros((T, V), np.uint16) if taps else None
+    q, keep = _qlinear(embed)
+    rc = lib.oracle_lm_head(T, H, V, group, ctypes.c_float(cap), _p(h), ctypes.byref(q), _p(out), _p(lg), nthreads)
+    if rc != 0:
+        raise ValueError(f"oracle_lm_head rejected the inputs ({rc})")
+    return (out, lg) if taps else out

@@ -8,7 +8,8 @@
  * Source: the DiffusionGemma language-model page ("diffusion-gemma/model.ts"),
  * classes DiffRouter (router forward), DiffExperts (experts forward),
  * DiffusionGemmaDecoderLayer (the MoE and dense branches' norms) and
- * SelfConditioning (the dense 4-bit GeGLU MLP), and
+ * SelfConditioning (the dense 4-bit GeGLU MLP), logitsFromHidden (the tied
+ * 4-bit head and its softcap), and
  * the vision page ("diffusion-gemma/vision.ts", manualRms) for the fp32
  * semantics of the no-scale RMS norm.
  *
@@ -610,6 +611,60 @@ int oracle_self_conditioning(int32_t T, int32_t H, int32_t I, int32_t g, float e
     free(sn);
     free(sv);
     return rc;
+}
+
+/* ------------------------------------------------------------ LM head --- */
+
+/*
+ * The tied 4-bit head with the final-logit softcap
+ * (DiffusionGemmaModel.logitsFromHidden, "diffusion-gemma/model.ts"):
+ *   logits = embed.asLinear(h)                bf16 [T, V]: h . W^T with the
+ *                                             embedding table [V, H] as a
+ *                                             4-bit group-g QuantizedLinear
+ *   out    = softcap(float32(logits))         fp32 [T, V]
+ * The softcap's formula is in a file the pages do not print; it is read as
+ * the usual final-logit softcapping cap * tanh(x / cap), in fp32 steps (x /
+ * cap rounded, tanh rounded once, the product rounded). cap <= 0: no cap.
+ * The table is dequantised one vocabulary row at a time. Optional tap:
+ * logits [T, V] bf16. Returns 0, or -1 on bad sizes.
+ */
+int oracle_lm_head(int32_t T, int32_t H, int32_t V, int32_t g, float cap, const uint16_t* h,
+                   const oracle_qlinear* embed, float* out, uint16_t* logits_tap, int nthreads) {
+    if (T < 0 || H <= 0 || V <= 0 || g <= 0 || H % 8 || H % g) return -1;
+    set_threads(nthreads);
+#pragma omp parallel
+    {
+        float* wr = (float*)malloc(sizeof(float) * (size_t)H);
+#pragma omp for schedule(dynamic, 64)
+        for (int v = 0; v < V; ++v) {
+            dequant_expert(embed->w + (size_t)v * (H / 8), embed->s + (size_t)v * (H / g),
+                           embed->b + (size_t)v * (H / g), 1, H, g, wr);
+            for (int t = 0; t < T; ++t) {
+                const uint16_t* ht = h + (size_t)t * H;
+                double acc = 0.0;
+                for (int k = 0; k < H; ++k) acc += (double)bf(ht[k]) * (double)wr[k];
+                const uint16_t lb = bf16_from_double(acc);
+                if (logits_tap) logits_tap[(size_t)t * V + v] = lb;
+#if ORACLE_MUTANT == 15
+                const float x = (float)acc; /* planted: the logit is not rounded to bf16 */
+#else
+                const float x = bf(lb);
+#endif
+                float o = x;
+                if (cap > 0.0f) {
+#if ORACLE_MUTANT == 14
+                    o = (float)tanh((double)x) * cap; /* planted: tanh(x) * cap */
+#else
+                    const float q = x / cap;
+                    o = (float)tanh((double)q) * cap;
+#endif
+                }
+                out[(size_t)t * V + v] = o;
+            }
+        }
+        free(wr);
+    }
+    return 0;
 }
 
 /* Router then experts on the same x: the layer as one call. */

@@ -513,6 +513,34 @@ def check_self_conditioning_zero_mlp(lib):
     assert np.array_equal(out, want), "RMSNormNoScale of a constant row"
 
 
+def check_lm_head_brute_force(lib):
+    """The head's bf16 logits are the nearest bf16 to h . W^T (the table
+    dequantised here, float64 matmul), and its output is cap * tanh(x / cap)
+    of those logits within three fp32 ulps (three fp32 roundings; float64
+    numpy tanh). h is scaled so the logits reach the softcap's saturation."""
+    h, emb = ms.make_head(T=5, H=256, V=384, seed=50, h_scale=40.0)
+    out, lg = oracle.lm_head(h, emb, cap=30.0, taps=True, lib=lib)
+    w = dense_dequant(emb[0], emb[1], emb[2], 256, 64)
+    assert_nearest_bf16(lg, f64(h) @ w.T, "head logits")
+    x = f64(lg)
+    assert np.abs(x).max() > 60.0, "test logits do not reach saturation"
+    exact = 30.0 * np.tanh(x / 30.0)
+    assert np.all(np.abs(out.astype(np.float64) - exact) <= 3 * 2.0 ** -24 * np.abs(exact) + 1e-30), \
+        "head softcap far from cap * tanh(x / cap)"
+
+
+def check_lm_head_symmetry_and_no_cap(lib):
+    """Negating h negates the output bit for bit (every step is odd); the
+    output stays within the cap; cap 0 returns the bf16 logits widened."""
+    h, emb = ms.make_head(T=4, H=256, V=256, seed=51, h_scale=8.0)
+    a = oracle.lm_head(h, emb, cap=30.0, lib=lib)
+    b = oracle.lm_head(h ^ np.uint16(0x8000), emb, cap=30.0, lib=lib)
+    assert np.array_equal(a, -b), "head(-h) != -head(h)"
+    assert np.all(np.abs(a) <= 30.0), "softcapped logit beyond the cap"
+    out, lg = oracle.lm_head(h, emb, cap=0.0, taps=True, lib=lib)
+    assert np.array_equal(out, ms.bits_to_f32(lg)), "cap 0: output != float32(bf16 logits)"
+
+
 ALL_CHECKS = [
     check_bf16_from_float, check_bf16_from_double,
     check_router_constant_row, check_router_zero_row, check_router_scale_invariance,
@@ -524,4 +552,5 @@ ALL_CHECKS = [
     check_route_q4,
     check_dense_mlp_brute_force, check_dense_mlp_is_single_expert, check_dense_branch_wiring,
     check_self_conditioning_exact_math, check_self_conditioning_zero_mlp,
+    check_lm_head_brute_force, check_lm_head_symmetry_and_no_cap,
 ]

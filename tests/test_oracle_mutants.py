@@ -25,6 +25,8 @@ MUTANTS = {
     11: "dense MLP swaps the gate and up linears",
     12: "self-conditioning adds the embeddings after the post norm",
     13: "dense branch's post norm takes the pre norm's weight",
+    14: "head softcap is tanh(x) * cap",
+    15: "head softcap reads the unrounded logit",
 }
 
 
