@@ -29,7 +29,8 @@ STATUS = {0: "ok", 1: "null pointer", 2: "bad shape", 3: "pointer not 16-byte al
 # Every function the public header declares.
 EXPORTS = ("moe_status_str", "moe_workspace_bytes", "moe_route", "moe_dispatch", "moe_experts",
            "moe_experts_noalloc", "moe_forward", "moe_forward_branch", "moe_forward_hostio", "moe_route_q4",
-           "moe_forward_q4router", "moe_dense_mlp", "moe_dense_branch", "moe_self_conditioning", "moe_timing_enable",
+           "moe_forward_q4router", "moe_dense_mlp", "moe_dense_branch", "moe_self_conditioning", "moe_lm_head",
+           "moe_timing_enable",
            "moe_timing_read",
            "moe_launches_per_forward", "moe_device_error")
 
@@ -80,13 +81,14 @@ def load(path: str = LIB_PATH):
     lib.moe_dense_mlp.argtypes = [D, P, Q, Q, P, P, Z, P]
     lib.moe_dense_branch.argtypes = [D, P, P, P, Q, Q, P, P, Z, P]
     lib.moe_self_conditioning.argtypes = [D, P, P, P, Q, Q, P, P, Z, P]
+    lib.moe_lm_head.argtypes = [D, ctypes.c_int32, ctypes.c_float, P, Q, P, P, Z, P]
     lib.moe_timing_enable.argtypes = [I]
     lib.moe_timing_read.argtypes = [ctypes.POINTER(ctypes.c_float), I, ctypes.POINTER(I)]
     lib.moe_launches_per_forward.argtypes = [ctypes.c_void_p]
     lib.moe_device_error.argtypes = []
     for fn in ("moe_route", "moe_dispatch", "moe_experts", "moe_experts_noalloc", "moe_forward", "moe_forward_branch",
                "moe_forward_hostio", "moe_route_q4", "moe_forward_q4router", "moe_dense_mlp", "moe_dense_branch",
-               "moe_self_conditioning",
+               "moe_self_conditioning", "moe_lm_head",
                "moe_timing_enable", "moe_timing_read", "moe_launches_per_forward", "moe_device_error"):
         getattr(lib, fn).restype = I
     _lib = lib
@@ -213,6 +215,14 @@ def moe_self_conditioning(d: Dims, inputs_embeds, signal, pre_norm_w, gate_up: Q
     _check("moe_self_conditioning", load().moe_self_conditioning(
         ctypes.byref(d), _ptr(inputs_embeds), _ptr(signal), _ptr(pre_norm_w), ctypes.byref(gate_up),
         ctypes.byref(down), _ptr(out), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def moe_lm_head(d: Dims, vocab: int, softcap: float, h, embed: QWeight, logits, workspace=None, ws_bytes: int = 0,
+                stream=None):
+    """The tied 4-bit head: logits [T, vocab] float32 = softcap * tanh(bf16(h . W^T) / softcap)."""
+    _check("moe_lm_head", load().moe_lm_head(ctypes.byref(d), vocab, ctypes.c_float(softcap), _ptr(h),
+                                             ctypes.byref(embed), _ptr(logits), _ptr(workspace), ws_bytes,
+                                             _stream(stream)))
 
 
 def moe_forward_hostio(d: Dims, x_host, router_w, router_scale, per_expert_scale, gate_up: QWeight,

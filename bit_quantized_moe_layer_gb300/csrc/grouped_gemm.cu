@@ -1,7 +1,9 @@
 // Grouped 4-bit dequant-GEMM on the 5th-generation tensor cores (tcgen05):
 // the two QuantizedSwitchLinear calls of DiffExperts.forward
 // ("diffusion-gemma/model.ts"), gate_up with the split + GeGLU fused into its
-// epilogue, and down.
+// epilogue, and down; with one expert, the dense MLP's linears and the tied
+// head (DiffusionGemmaModel.logitsFromHidden), whose epilogue applies the
+// final-logit softcap.
 //
 // The product is computed transposed (D^T = W . X^T) so the weight rows fill
 // the 128-row M side of the MMA and the few tokens an expert receives fill
@@ -484,6 +486,18 @@ __global__ void __launch_bounds__((3 + 16 / APW + 4 * EPW) * 32, 1)
                         if (tok < tl.rows)
                             a.out[(size_t)(tl.p0 + tok) * a.out_ld + pos] = (uint16_t)geglu_bf16(gb, ub);
                     }
+                } else if (MODE == kHead) {
+                    // logits bf16 (the head's output dtype), widened to fp32, then
+                    // cap * tanh(x / cap) in fp32 steps; 32 lanes store 128 B of a row
+                    const int vrow = 128 * j + 32 * q + lane;
+                    const float cap = a.softcap;
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int tok = c0 + jj;
+                        const float x = bf16_bits_to_f32(f32_to_bf16_bits(v[jj]));
+                        const float o = cap > 0.f ? __fmul_rn(tanhf(__fdiv_rn(x, cap)), cap) : x;
+                        if (tok < tl.rows) a.out_f32[(size_t)(tl.p0 + tok) * a.out_ld + vrow] = o;
+                    }
                 } else {
                     const int hrow = 128 * j + 32 * q + lane;
 #pragma unroll
@@ -562,8 +576,12 @@ static cudaError_t launch_mode(const CUtensorMap& wmap, const CUtensorMap& bmap,
 cudaError_t launch_gemm(int mode, const CUtensorMap& wmap, const CUtensorMap& bmap, const GemmArgs& a, int grid,
                         cudaStream_t stream) {
     const size_t smem = gemm_smem_bytes(a.K, a.wstages, a.bregion);
-    return mode == kGateUp ? launch_mode<kGateUp>(wmap, bmap, a, grid, smem, stream)
-                           : launch_mode<kDown>(wmap, bmap, a, grid, smem, stream);
+    switch (mode) {
+        case kGateUp: return launch_mode<kGateUp>(wmap, bmap, a, grid, smem, stream);
+        case kDown: return launch_mode<kDown>(wmap, bmap, a, grid, smem, stream);
+        case kHead: return launch_mode<kHead>(wmap, bmap, a, grid, smem, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 int gemm_error_word() {

@@ -113,7 +113,9 @@ cudaError_t launch_add_norm(const uint16_t* embeds, const uint16_t* s, const uin
                             int T, int H, cudaStream_t stream);
 
 // Grouped dequant-GEMM on tcgen05 (one expert per token tile).
-enum GemmMode { kGateUp = 0, kDown = 1 };
+// kHead: the tied head, as kDown but the epilogue writes row (p0 + token)
+// of out_f32 directly (no permutation): softcap(bf16 logit) in fp32.
+enum GemmMode { kGateUp = 0, kDown = 1, kHead = 2 };
 struct GemmArgs {
     const uint16_t* scales;   // [E, N, K/64]
     const uint16_t* biases;   // [E, N, K/64]
@@ -138,6 +140,10 @@ struct GemmArgs {
     const uint8_t* w;
     int prefetch_items;
     int tiles_per_expert;
+    // kHead: logits [rows, out_ld] fp32 and the final-logit softcap
+    // (cap * tanh(x / cap) of the bf16 logit x; cap <= 0: x itself).
+    float* out_f32;
+    float softcap;
 };
 // wmap: packed weights as uint32 [E*N rows, K/8], box {32, 64 or 128}, 128B swizzle.
 // bmap: B operand (xs or mid) as bf16 [S rows, K], box {64, 16}, 128B swizzle.

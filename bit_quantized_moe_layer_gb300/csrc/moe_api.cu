@@ -365,6 +365,60 @@ int run_dense(const moe_dims* d, const uint16_t* x, const uint16_t* pre_norm_w, 
     return MOE_OK;
 }
 
+// The tied head: h -> interleaved staging -> one-expert GEMM over the vocab
+// rows of the 4-bit table with the softcap epilogue (fp32 logits).
+int run_head(const moe_dims* d, int vocab, float softcap, const uint16_t* h, const moe_qweight* embed, float* logits,
+             uint8_t* ws, const Layout& L, const DeviceInfo& di, cudaStream_t s) {
+    const int T = d->T, H = d->H;
+    int32_t* perm = reinterpret_cast<int32_t*>(ws + L.perm);
+    Tile* tiles = reinterpret_cast<Tile*>(ws + L.tiles);
+    int32_t* ntiles = reinterpret_cast<int32_t*>(ws + L.ntiles);
+    uint16_t* xs = reinterpret_cast<uint16_t*>(ws + L.xs);
+    // a vocab-sized weight gives every SM many items: 128-row token tiles
+    // (twice the MMA work per dequantised stage) unless T fits one 64-row tile
+    const int nmax = T > 64 ? 128 : 64;
+    const int ntok = (T + nmax - 1) / nmax;
+    const int n_tiles = vocab / 128;
+
+    CUtensorMap m_w, m_xs;
+    if (!make_map_2d(&m_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, embed->w, H / 8, (uint64_t)vocab, 32, 128) ||
+        !make_map_2d(&m_xs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, xs, H, T, 64, 16))
+        return MOE_ERR_CUDA;
+    CallTimer tm(s);
+    tm.mark(0);
+    tm.mark(1);
+    tm.mark(2);
+    int rc = fail(launch_dense_prep(h, nullptr, 0.f, xs, perm, tiles, ntiles, T, H, nmax, s));
+    if (rc) return rc;
+    tm.mark(3);
+    GemmArgs ga{};
+    ga.scales = embed->scales;
+    ga.biases = embed->biases;
+    ga.tiles = tiles;
+    ga.num_tiles = ntiles;
+    ga.perm = perm;
+    ga.out_f32 = logits;
+    ga.softcap = softcap;
+    ga.K = H;
+    ga.N = vocab;
+    ga.inter = 0;
+    ga.out_ld = vocab;
+    ga.nmax = nmax;
+    ga.E = 1;
+    ga.n_tiles = n_tiles;
+    ga.w = reinterpret_cast<const uint8_t*>(embed->w);
+    ga.prefetch_items = 2;
+    ga.tiles_per_expert = ntok;
+    gemm_stages(H, nmax, &ga.wstages, &ga.bregion);
+    const long items = (long)ntok * n_tiles;
+    const int grid = items < di.sms ? (int)items : di.sms;
+    if ((rc = fail(launch_gemm(kHead, m_w, m_xs, ga, grid, s)))) return rc;
+    tm.mark(4);
+    tm.mark(5);
+    tm.mark(6);
+    return MOE_OK;
+}
+
 int check_dense(const moe_dims* d) {
     int rc = check_dims(d);
     if (rc) return rc;
@@ -680,6 +734,24 @@ int moe_self_conditioning(const moe_dims* d, const uint16_t* inputs_embeds, cons
     if ((rc = get_workspace(d, workspace, ws_bytes, L, &ws))) return rc;
     return run_dense(d, signal, pre_norm_w, inputs_embeds, nullptr, true, gate_up, down, out, ws, L, di,
                      static_cast<cudaStream_t>(stream));
+}
+
+int moe_lm_head(const moe_dims* d, int32_t vocab, float softcap, const uint16_t* h, const moe_qweight* embed,
+                float* logits, void* workspace, size_t ws_bytes, void* stream) {
+    int rc = check_dense(d);
+    if (rc) return rc;
+    if (vocab <= 0) return MOE_ERR_SHAPE;
+    if (vocab % 128 != 0) return MOE_ERR_UNSUPPORTED;  // 128-row weight tiles
+    if (!(softcap >= 0.0f) || isinf(softcap)) return MOE_ERR_SHAPE;
+    if ((rc = check_ptrs({h, logits}))) return rc;
+    if ((rc = check_qweight(embed))) return rc;
+    if (d->T == 0) return MOE_OK;
+    DeviceInfo di;
+    if ((rc = device_info(&di))) return rc;
+    const Layout L = layout(d);
+    uint8_t* ws = nullptr;
+    if ((rc = get_workspace(d, workspace, ws_bytes, L, &ws))) return rc;
+    return run_head(d, vocab, softcap, h, embed, logits, ws, L, di, static_cast<cudaStream_t>(stream));
 }
 
 int moe_forward_hostio(const moe_dims* d, const uint16_t* x_host, const uint16_t* router_w,

@@ -252,6 +252,30 @@ int moe_self_conditioning(const moe_dims* d, const uint16_t* inputs_embeds, cons
                           size_t ws_bytes, void* stream);
 
 /*
+ * The tied 4-bit head with the final-logit softcap
+ * (DiffusionGemmaModel.logitsFromHidden in "diffusion-gemma/model.ts"):
+ *   x      = bf16(h . W^T)                  the embedding table W [vocab, H]
+ *                                           as a 4-bit group-64 QuantizedLinear
+ *   logits = softcap * tanh(x / softcap)    fp32 steps on the widened bf16 x
+ *                                           (softcap 0: logits = x)
+ * The softcap's formula is read as the usual final-logit softcapping (its
+ * file is not on the pages); the model's cap is 30.
+ *   d       T, H as for the layer; E = k = 1 (MOE_ERR_SHAPE otherwise);
+ *           inter any valid value (it only sizes unused workspace)
+ *   vocab   rows of the table, a multiple of 128 (MOE_ERR_UNSUPPORTED
+ *           otherwise)
+ *   h       [T,H] bf16; embed the table in the affine layout above
+ *           (w uint32 [vocab, H/8], scales and biases bf16 [vocab, H/64])
+ *   logits  [T, vocab] float32, written whole
+ * Workspace as moe_dense_mlp. 2 launches: input staging, then the grouped
+ * GEMM with one expert and the softcap in its epilogue. Timing records
+ * them as "gather" and "gate_up".
+ */
+int moe_lm_head(const moe_dims* d, int32_t vocab, float softcap, const uint16_t* h,
+                const moe_qweight* embed, float* logits, void* workspace, size_t ws_bytes,
+                void* stream);
+
+/*
  * The whole layer with HOST activations: copies x_host [T,H] to the device,
  * runs moe_forward and copies out [T,H] back to out_host, then synchronises
  * the stream. Weights and router parameters are device pointers. Host

@@ -112,3 +112,23 @@ def test_dense_calls_check_arguments(lib):
     assert lib.moe_dense_mlp(ctypes.byref(moe.dims(8, 256, 1, 1, 100)), p, Q, Q, p, None, 0, None) == 4
     d0 = moe.dims(0, 256, 1, 1, 192)
     assert lib.moe_self_conditioning(ctypes.byref(d0), p, p, p, Q, Q, p, None, 0, None) == 0
+
+
+def test_lm_head_checks_arguments(lib):
+    """moe_lm_head: E = k = 1, vocab a positive multiple of 128, a finite
+    non-negative softcap, non-null aligned pointers; T = 0 is a no-op."""
+    import bit_quantized_moe_layer_gb300 as moe
+    buf = ctypes.create_string_buffer(64)
+    p = (ctypes.addressof(buf) + 15) & ~15
+    q = moe.qweight(p, p, p)
+    Q = ctypes.byref(q)
+    cap = ctypes.c_float(30.0)
+    d = moe.dims(8, 256, 1, 1, 64)
+    assert lib.moe_lm_head(ctypes.byref(moe.dims(8, 256, 8, 2, 64)), 1024, cap, p, Q, p, None, 0, None) == 2
+    assert lib.moe_lm_head(ctypes.byref(d), 0, cap, p, Q, p, None, 0, None) == 2
+    assert lib.moe_lm_head(ctypes.byref(d), 1000, cap, p, Q, p, None, 0, None) == 4
+    assert lib.moe_lm_head(ctypes.byref(d), 1024, ctypes.c_float(float("nan")), p, Q, p, None, 0, None) == 2
+    assert lib.moe_lm_head(ctypes.byref(d), 1024, ctypes.c_float(-1.0), p, Q, p, None, 0, None) == 2
+    assert lib.moe_lm_head(ctypes.byref(d), 1024, cap, None, Q, p, None, 0, None) == 1
+    assert lib.moe_lm_head(ctypes.byref(d), 1024, cap, p, Q, p + 4, None, 0, None) == 3
+    assert lib.moe_lm_head(ctypes.byref(moe.dims(0, 256, 1, 1, 64)), 1024, cap, p, Q, p, None, 0, None) == 0
