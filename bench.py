@@ -94,6 +94,24 @@ def dense_report(dn, dense_ms, stage_ms, calls, peaks, world):
         stages_ms_per_call={k: v / max(1, calls) for k, v in stage_ms.items() if v > 0})
 
 
+def head_report(T, H, V, head_ms, stage_ms, calls, peaks, world, group=64):
+    """The tied head: algorithmic bytes = packed table + scales + biases +
+    h in + fp32 logits out; flops = 2 T H V."""
+    bytes_ = V * H // 2 + 2 * (V * H // group) * 2 + T * H * 2 + T * V * 4
+    flops = 2 * T * H * V
+    t_hbm, t_tc = bytes_ / (peaks["hbm"] * 1e9), flops / (peaks["tc"] * 1e12)
+    gemm_ms = stage_ms["gate_up"] / max(1, calls)
+    return dict(workload=f"tied 4-bit head + fp32 softcap 30: T={T} H={H} vocab={V} group={group} (vocab not on the "
+                         f"pages)",
+                ms_per_step=head_ms, value=whole_job_rate(T, world, head_ms * 1e-3), unit="tokens/s",
+                roofline=dict(bound="tensor" if t_tc >= t_hbm else "hbm", t_roof_us=max(t_hbm, t_tc) * 1e6,
+                              t_head_us=head_ms * 1e3, frac=max(t_hbm, t_tc) / (head_ms * 1e-3), bytes=bytes_,
+                              flops=flops),
+                gemm_kernel=dict(ms_per_launch=gemm_ms, achieved_tflops=flops / (gemm_ms * 1e-3) / 1e12,
+                                 achieved_gbs=bytes_ / (gemm_ms * 1e-3) / 1e9),
+                stages_ms_per_call={k: v / max(1, calls) for k, v in stage_ms.items() if v > 0})
+
+
 class ClockSampler:
     """SM clock, power and clock-event reasons of one GPU, read through NVML
     (ctypes, read-only queries) every 2 ms while the timed region runs, plus
@@ -414,6 +432,24 @@ def run_ours(args, wl):
                                                                stream),
     }
     dense_ms = {k_: timed(f_) for k_, f_ in dense_calls.items()}
+
+    # The tied 4-bit head with the fp32 softcap at the same T, vocabulary 2^18.
+    hh, hemb = ms.make_head(d.T, H=d.H, V=ms.VOCAB, seed=wl.seed + rank)
+    hd = moe.dims(d.T, d.H, 1, 1, 64)
+    h_h, h_emb = t16(hh), (t32(hemb[0]), t16(hemb[1]), t16(hemb[2]))
+    h_out = torch.empty((d.T, ms.VOCAB), dtype=torch.float32, device="cuda")
+    h_ws = torch.empty(moe.workspace_bytes(hd), dtype=torch.uint8, device="cuda")
+    qh = moe.qweight(*h_emb)
+    head_call = lambda: moe.moe_lm_head(hd, ms.VOCAB, 30.0, h_h, qh, h_out, h_ws, h_ws.numel(), stream)
+    head_ms = timed(head_call)
+    moe.timing_enable(True)
+    for _ in range(args.steps):
+        flush.zero_()
+        head_call()
+    torch.cuda.synchronize()
+    head_stage_ms, head_calls_n = moe.timing_read()
+    moe.timing_enable(False)
+    del h_out, h_emb, qh
     moe.timing_enable(True)
     for _ in range(args.steps):
         flush.zero_()
@@ -465,6 +501,7 @@ def run_ours(args, wl):
         q4router=dict(call="moe_forward_q4router (the layer with the 4-bit group-64 router projection)",
                       ms_per_step=q4_ms, value=whole_job_rate(d.T, world, q4_ms * 1e-3), unit="tokens/s"),
         dense=dense_report(dn, dense_ms, dense_stage_ms, dense_calls_n, peaks, world),
+        lm_head=head_report(d.T, d.H, ms.VOCAB, head_ms, head_stage_ms, head_calls_n, peaks, world),
         clocks=clk.summary(),
         device_error=err,
     )
