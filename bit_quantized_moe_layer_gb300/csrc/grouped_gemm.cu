@@ -18,10 +18,14 @@
 //   warp 1        TMEM owner and MMA issuer (one elected thread): per stage
 //                 it waits for the A slot and the B slot, at an item's first
 //                 stage for a free accumulator buffer;
-//   warp 2        TMA producer of the B operand (the token tile, 16-row boxes)
-//                 into a ring that the MMA's completion releases; its slots
-//                 are sized at run time for the largest token tile of the
-//                 call, so small tiles get a deep ring;
+//   warp 2        TMA producer of the B operand into a ring that the MMA's
+//                 completion releases. Token tiles of up to 64 rows load as
+//                 16-row, 64-wide blocks, the atoms (brows) x 128 B apart;
+//                 tiles of up to 128 rows as one 3-D copy a stage of its
+//                 four 64-wide atoms (a box of 16 to 128 rows, the smallest
+//                 that holds the tile), the atoms (box rows) x 128 B apart.
+//                 The slots are sized at run time for the largest token
+//                 tile of the call, so small tiles get a deep ring;
 //   dequant warps 8 warps, thread = weight row = TMEM lane; warp (q, p)
 //                 dequantises atoms 2p and 2p + 1 (64 K each) of lane
 //                 quarter q of every stage into the next slot of a ring of A
@@ -96,6 +100,13 @@ __device__ __forceinline__ uint32_t geglu_bf16(float g, float up) {
     return f32_to_bf16_bits(m);
 }
 
+// Rows of the B box that holds a tile of `rows` token rows: 16 << index.
+__device__ __forceinline__ int bbox_index(int rows) {
+    int i = 0;
+    while ((16 << i) < rows && i < 3) ++i;
+    return i;
+}
+
 // Position of element n inside its 8-block in the interleaved K order.
 __device__ __forceinline__ int interleaved_pos(int n) {
     const int r = n & 7;
@@ -128,7 +139,7 @@ __device__ __forceinline__ void dequant_atom(const uint4 c0, const uint4 c1, uin
 // warps per TMEM lane quarter.
 template <int MODE, int NMAX, int NA, int APW, int EPW>
 __global__ void __launch_bounds__((3 + 16 / APW + 4 * EPW) * 32, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap bmap,
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ BMaps bmaps,
                         GemmArgs a) {
     constexpr int kDqWarps = 16 / APW;
     constexpr int kEpiWarp0 = 3 + kDqWarps;
@@ -275,23 +286,35 @@ __global__ void __launch_bounds__((3 + 16 / APW + 4 * EPW) * 32, 1)
         for (int l = (li > 2 ? li - 2 : 0); l < li; ++l) mbar_drain(&sh.sfull[l & 1], (l >> 1) & 1);
     } else if (warp == 2) {
         // ---------------------------------------------------- B operand --
-        if (elect_one()) prefetch_tensormap(&bmap);
+        if (elect_one()) {
+            for (int i = 0; i < 4; ++i) prefetch_tensormap(&bmaps.m[i]);
+            prefetch_tensormap(&bmaps.m2);
+        }
+        const uint32_t box_atoms = (uint32_t)min(4, K / 64);
         int slot = 0;
         uint32_t ph = 0, issued = 0;
         bool ok = true;
         for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x) {
             const Tile tl = a.tiles[it / a.n_tiles];
+            const int bi = bbox_index(tl.rows);
             const int nrows16 = (tl.rows + 15) & ~15;
+            // the whole box counts, rows and atoms past the tensor (zero-filled) included
+            const uint32_t box_bytes = box_atoms * (16u << bi) * 128u;
             for (int s = 0; s < nstages; ++s) {
                 if (!(ok = mbar_wait(&sh.bempty[slot], ph ^ 1, abort_flag, kSleepRing, 3))) break;
                 uint8_t* bst = bring + (size_t)slot * bslot_bytes;
-                const int atoms = min(kStageK, K - s * kStageK) / 64;
                 if (elect_one()) {
-                    mbar_arrive_expect_tx(&sh.bfull[slot], atoms * nrows16 * 128);
-                    for (int at = 0; at < atoms; ++at)
-                        for (int r = 0; r < nrows16; r += 16)
-                            tma_load_2d(bst + at * brows * 128 + r * 128, &bmap, &sh.bfull[slot],
-                                        s * kStageK + at * 64, tl.p0 + r);
+                    if constexpr (NMAX > 64) {
+                        mbar_arrive_expect_tx(&sh.bfull[slot], box_bytes);
+                        tma_load_3d(bst, &bmaps.m[bi], &sh.bfull[slot], 0, tl.p0, s * (kStageK / 64));
+                    } else {
+                        const int atoms = min(kStageK, K - s * kStageK) / 64;
+                        mbar_arrive_expect_tx(&sh.bfull[slot], atoms * nrows16 * 128);
+                        for (int at = 0; at < atoms; ++at)
+                            for (int r = 0; r < nrows16; r += 16)
+                                tma_load_2d(bst + at * brows * 128 + r * 128, &bmaps.m2, &sh.bfull[slot],
+                                            s * kStageK + at * 64, tl.p0 + r);
+                    }
                 }
                 __syncwarp();
                 ++issued;
@@ -313,12 +336,14 @@ __global__ void __launch_bounds__((3 + 16 / APW + 4 * EPW) * 32, 1)
         bool ok = true;
         Tile tl_next = {};
         if (blockIdx.x < num_items) tl_next = a.tiles[blockIdx.x / a.n_tiles];
-        const uint32_t atom_step = (uint32_t)(brows * 128) >> 4;  // descriptor units (16 B)
         for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x, ++li) {
             const Tile tl = tl_next;
             if (it + (int)gridDim.x < num_items) tl_next = a.tiles[(it + gridDim.x) / a.n_tiles];
             const uint32_t nrows16 = (uint32_t)((tl.rows + 15) & ~15);
             const uint32_t idesc = idesc_bf16_m128(nrows16);
+            // distance of the B slot's atoms in descriptor units (16 B)
+            const uint32_t atom_step =
+                (uint32_t)(((NMAX > 64) ? (16 << bbox_index(tl.rows)) : brows) * 128) >> 4;
             const int db = li & 1;
             const uint32_t dcol = tmem + kD0 + (uint32_t)(db * NMAX);
             // the accumulator buffer's previous item (li - 2) has been read out
@@ -544,7 +569,7 @@ void gemm_stages(int K, int nmax, int* wstages, int* bregion) {
 }
 
 template <int MODE, int NMAX, int NA, int APW, int EPW>
-static cudaError_t launch_one(const CUtensorMap& wmap, const CUtensorMap& bmap, const GemmArgs& a, int grid,
+static cudaError_t launch_one(const CUtensorMap& wmap, const BMaps& bmaps, const GemmArgs& a, int grid,
                               size_t smem, cudaStream_t stream) {
     static bool attr_set[64] = {};
     int dev = 0;
@@ -557,29 +582,29 @@ static cudaError_t launch_one(const CUtensorMap& wmap, const CUtensorMap& bmap, 
         attr_set[dev] = true;
     }
     return launch_pdl(grouped_gemm_kernel<MODE, NMAX, NA, APW, EPW>, dim3(grid), dim3((3 + 16 / APW + 4 * EPW) * 32),
-                      smem, stream, wmap, bmap, a);
+                      smem, stream, wmap, bmaps, a);
 }
 
 template <int MODE>
-static cudaError_t launch_mode(const CUtensorMap& wmap, const CUtensorMap& bmap, const GemmArgs& a, int grid,
+static cudaError_t launch_mode(const CUtensorMap& wmap, const BMaps& bmaps, const GemmArgs& a, int grid,
                                size_t smem, cudaStream_t stream) {
     // Eight dequant warps of two atoms each (fewer warps than one atom each:
     // less barrier traffic per byte, measured faster). Token tiles of up to
     // 64: three A slots and 4 epilogue warps (15 warps); up to 128: two A
     // slots (TMEM holds 2 x 128 accumulator columns) and 8 epilogue warps, as
     // a 128-token tile's GeGLU needs the wider epilogue (19 warps).
-    if (a.nmax == 64) return launch_one<MODE, 64, 3, 2, 1>(wmap, bmap, a, grid, smem, stream);
-    if (a.nmax == 128) return launch_one<MODE, 128, 2, 2, 2>(wmap, bmap, a, grid, smem, stream);
+    if (a.nmax == 64) return launch_one<MODE, 64, 3, 2, 1>(wmap, bmaps, a, grid, smem, stream);
+    if (a.nmax == 128) return launch_one<MODE, 128, 2, 2, 2>(wmap, bmaps, a, grid, smem, stream);
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_gemm(int mode, const CUtensorMap& wmap, const CUtensorMap& bmap, const GemmArgs& a, int grid,
+cudaError_t launch_gemm(int mode, const CUtensorMap& wmap, const BMaps& bmaps, const GemmArgs& a, int grid,
                         cudaStream_t stream) {
     const size_t smem = gemm_smem_bytes(a.K, a.wstages, a.bregion);
     switch (mode) {
-        case kGateUp: return launch_mode<kGateUp>(wmap, bmap, a, grid, smem, stream);
-        case kDown: return launch_mode<kDown>(wmap, bmap, a, grid, smem, stream);
-        case kHead: return launch_mode<kHead>(wmap, bmap, a, grid, smem, stream);
+        case kGateUp: return launch_mode<kGateUp>(wmap, bmaps, a, grid, smem, stream);
+        case kDown: return launch_mode<kDown>(wmap, bmaps, a, grid, smem, stream);
+        case kHead: return launch_mode<kHead>(wmap, bmaps, a, grid, smem, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -145,12 +145,23 @@ struct GemmArgs {
     float* out_f32;
     float softcap;
 };
+// Maps of the B operand (xs or mid, bf16 [S rows, K]), 128B swizzle:
+//   m[i]  S rows of K/64 atoms of 64: dims {64, S, K/64}, byte strides
+//         {2K, 128}, box {64, R, min(4, K/64)} for R = 16 << i. One copy
+//         loads a stage's atoms of R token rows, atom after atom;
+//   m2    [S rows, K] with box {64, 16}: one copy a 16-row, 64-wide block.
+// The kernels for token tiles of up to 64 rows load 16-row blocks (m2),
+// those for up to 128 rows one box of the smallest R that holds the tile
+// (m[i]): each measured the faster for its tile sizes.
+struct BMaps {
+    CUtensorMap m[4];
+    CUtensorMap m2;
+};
 // wmap: packed weights as uint32 [E*N rows, K/8], box {32, 64 or 128}, 128B swizzle.
-// bmap: B operand (xs or mid) as bf16 [S rows, K], box {64, 16}, 128B swizzle.
 size_t gemm_smem_bytes(int K, int wstages, int bregion);
 void gemm_stages(int K, int nmax, int* wstages, int* bregion);
-cudaError_t launch_gemm(int mode, const CUtensorMap& wmap, const CUtensorMap& bmap, const GemmArgs& a,
-                        int grid, cudaStream_t stream);
+cudaError_t launch_gemm(int mode, const CUtensorMap& wmap, const BMaps& bmaps, const GemmArgs& a, int grid,
+                        cudaStream_t stream);
 int gemm_error_word();
 
 }  // namespace moe

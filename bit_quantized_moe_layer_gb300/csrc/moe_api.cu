@@ -105,6 +105,25 @@ bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const voi
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The grouped GEMM's token-operand maps over a bf16 [rows, K] buffer (see
+// BMaps): 3-D boxes of 16, 32, 64 and 128 rows by min(4, K/64) atoms, and the
+// 2-D 16-row box.
+bool make_bmaps(BMaps* b, const void* ptr, uint64_t K, uint64_t rows) {
+    auto fn = encode_fn();
+    if (!fn || !make_map_2d(&b->m2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, K, rows, 64, 16)) return false;
+    for (int i = 0; i < 4; ++i) {
+        cuuint64_t dims[3] = {64, rows, K / 64};
+        cuuint64_t strides[2] = {K * 2, 128};
+        cuuint32_t box[3] = {64, (cuuint32_t)(16 << i), (cuuint32_t)(K / 64 < 4 ? K / 64 : 4)};
+        cuuint32_t estr[3] = {1, 1, 1};
+        if (fn(&b->m[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    }
+    return true;
+}
+
 // bf16(x) of a double, one rounding to nearest even (x > 0, normal range).
 float bf16_round(double x) {
     int e;
@@ -217,11 +236,11 @@ int run_experts(const moe_dims* d, const uint16_t* x, const int32_t* idx, const 
     uint16_t* y = reinterpret_cast<uint16_t*>(ws + L.y);
     const int nmax = (S / E > 40) ? 128 : 64;
 
-    CUtensorMap m_gu, m_dn, m_xs, m_mid;
+    CUtensorMap m_gu, m_dn;
+    BMaps m_xs, m_mid;
     if (!make_map_2d(&m_gu, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, gu->w, H / 8, (uint64_t)E * 2 * I, 32, 64) ||
         !make_map_2d(&m_dn, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, dn->w, I / 8, (uint64_t)E * H, 32, 128) ||
-        !make_map_2d(&m_xs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, xs, H, S, 64, 16) ||
-        !make_map_2d(&m_mid, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, mid, I, S, 64, 16))
+        !make_bmaps(&m_xs, xs, H, S) || !make_bmaps(&m_mid, mid, I, S))
         return MOE_ERR_CUDA;
 
     DispatchArgs da{idx, perm, offsets, inv, tiles, ntiles, S, E, nmax, reinterpret_cast<int32_t*>(ws + L.dhist)};
@@ -310,11 +329,11 @@ int run_dense(const moe_dims* d, const uint16_t* x, const uint16_t* pre_norm_w, 
     const int nmax = ((long)((T + 127) / 128) * gu_tiles >= di.sms) ? 128 : 64;
     const int ntok = (T + nmax - 1) / nmax;
 
-    CUtensorMap m_gu, m_dn, m_xs, m_mid;
+    CUtensorMap m_gu, m_dn;
+    BMaps m_xs, m_mid;
     if (!make_map_2d(&m_gu, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, gu->w, H / 8, (uint64_t)2 * I, 32, 64) ||
         !make_map_2d(&m_dn, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, dn->w, I / 8, (uint64_t)H, 32, 128) ||
-        !make_map_2d(&m_xs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, xs, H, T, 64, 16) ||
-        !make_map_2d(&m_mid, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, mid, I, T, 64, 16))
+        !make_bmaps(&m_xs, xs, H, T) || !make_bmaps(&m_mid, mid, I, T))
         return MOE_ERR_CUDA;
 
     CallTimer tm(s);
@@ -380,9 +399,10 @@ int run_head(const moe_dims* d, int vocab, float softcap, const uint16_t* h, con
     const int ntok = (T + nmax - 1) / nmax;
     const int n_tiles = vocab / 128;
 
-    CUtensorMap m_w, m_xs;
+    CUtensorMap m_w;
+    BMaps m_xs;
     if (!make_map_2d(&m_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, embed->w, H / 8, (uint64_t)vocab, 32, 128) ||
-        !make_map_2d(&m_xs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, xs, H, T, 64, 16))
+        !make_bmaps(&m_xs, xs, H, T))
         return MOE_ERR_CUDA;
     CallTimer tm(s);
     tm.mark(0);
