@@ -80,23 +80,19 @@ __host__ __device__ inline int scale_buf_bytes(int K) {
 // 0.5 g (1 + tanh(s)), s = sqrt(2/pi) (g + 0.044715 g^3). 0.5 (1 + tanh s) is
 // the logistic of 2s, evaluated in that form so it keeps its relative
 // accuracy where 1 + tanh(s) cancels (s << 0). p = g*up is exact in fp32.
-// For s >= 0 the value is p - p*t with t = 1 - logistic(2s) > 0, formed by a
-// fused multiply-add rounded toward zero: the exact value lies strictly
-// between 0 and p, so an exact bf16 tie of p (large g, where t is below
-// fp32's resolution of 1) rounds toward zero as the exact value does.
+// r = e / (1 + e) with e = exp(-2|s|): for s < 0 it is the logistic of 2s
+// and the value is p r; for s >= 0 it is 1 - logistic(2s) > 0 and the value
+// is p - p r, formed by a fused multiply-add rounded toward zero: the exact
+// value lies strictly between 0 and p, so an exact bf16 tie of p (large g,
+// where r is below fp32's resolution of 1) rounds toward zero as the exact
+// value does. One exp and one divide serve both signs.
 __device__ __forceinline__ uint32_t geglu_bf16(float g, float up) {
     const float c = 0.7978845608028654f;  // sqrt(2/pi)
     const float s = __fmul_rn(c, __fadd_rn(g, __fmul_rn(0.044715f, __fmul_rn(g, __fmul_rn(g, g)))));
     const float p = __fmul_rn(g, up);
-    float m;
-    if (s < 0.f) {
-        const float e = expf(__fmul_rn(2.0f, s));
-        m = __fmul_rn(p, __fdiv_rn(e, __fadd_rn(1.0f, e)));
-    } else {
-        const float e = expf(__fmul_rn(-2.0f, s));
-        const float t = fmaxf(__fdiv_rn(e, __fadd_rn(1.0f, e)), 1e-30f);
-        m = __fmaf_rz(-p, t, p);
-    }
+    const float e = expf(__fmul_rn(-2.0f, fabsf(s)));
+    const float r = __fdiv_rn(e, __fadd_rn(1.0f, e));
+    const float m = (s < 0.f) ? __fmul_rn(p, r) : __fmaf_rz(-p, fmaxf(r, 1e-30f), p);
     return f32_to_bf16_bits(m);
 }
 
