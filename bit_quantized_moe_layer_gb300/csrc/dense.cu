@@ -37,14 +37,14 @@ __device__ __forceinline__ uint4 scale_chunk(uint4 v, float rs, const uint16_t* 
 // Input of the dense MLP's gate_up product. Row t: xs[t] = the row, or
 // RMSNorm(row, pre_w) = bf16((x * rsqrt(mean(x^2) + eps)) * pre_w) with
 // fp32 steps, stored with each 8-element block of K in the interleaved
-// order; perm[t] = t (the down product writes row t of its output). CTA 0
-// also writes the tile list: token tiles of nmax rows, all of expert 0.
+// order (the down product then writes row t of its output). CTA 0 also
+// writes the tile list: token tiles of nmax rows, all of expert 0.
 __global__ void __launch_bounds__(kRowThreads)
     dense_prep_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ pre_w, float eps,
-                      uint16_t* __restrict__ xs, int32_t* __restrict__ perm, Tile* __restrict__ tiles,
-                      int32_t* __restrict__ num_tiles, int T, int H, int nmax) {
+                      uint16_t* __restrict__ xs, Tile* __restrict__ tiles, int32_t* __restrict__ num_tiles, int T,
+                      int H, int nmax) {
     pdl_trigger();
-    pdl_wait();  // the previous call's GEMMs may still read xs, perm and the tiles
+    pdl_wait();  // the previous call's GEMMs may still read xs and the tiles
     const int t = blockIdx.x, tid = threadIdx.x, chunks = H / 8;
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
     uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)t * H);
@@ -76,7 +76,6 @@ __global__ void __launch_bounds__(kRowThreads)
         const int c = tid + q * kRowThreads;
         if (c < chunks) dst[c] = interleave8(v[q]);
     }
-    if (tid == 0) perm[t] = t;
     if (t == 0) {
         const int ntiles = (T + nmax - 1) / nmax;
         for (int i = tid; i < ntiles; i += kRowThreads) tiles[i] = Tile{0, i * nmax, min(nmax, T - i * nmax), 0};
@@ -134,11 +133,11 @@ __global__ void __launch_bounds__(kRowThreads)
 
 }  // namespace
 
-cudaError_t launch_dense_prep(const uint16_t* x, const uint16_t* pre_w, float eps, uint16_t* xs, int32_t* perm,
-                              Tile* tiles, int32_t* num_tiles, int T, int H, int nmax, cudaStream_t stream) {
+cudaError_t launch_dense_prep(const uint16_t* x, const uint16_t* pre_w, float eps, uint16_t* xs, Tile* tiles,
+                              int32_t* num_tiles, int T, int H, int nmax, cudaStream_t stream) {
     if (T <= 0 || H % 8 != 0 || H / 8 > kRowThreads * kRowChunks || nmax <= 0) return cudaErrorInvalidValue;
-    return launch_pdl(dense_prep_kernel, dim3((unsigned)T), dim3(kRowThreads), 0, stream, x, pre_w, eps, xs, perm,
-                      tiles, num_tiles, T, H, nmax);
+    return launch_pdl(dense_prep_kernel, dim3((unsigned)T), dim3(kRowThreads), 0, stream, x, pre_w, eps, xs, tiles,
+                      num_tiles, T, H, nmax);
 }
 
 cudaError_t launch_add_norm(const uint16_t* embeds, const uint16_t* s, const uint16_t* w, float eps, uint16_t* out,

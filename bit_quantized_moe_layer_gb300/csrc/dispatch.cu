@@ -410,10 +410,11 @@ cudaError_t launch_gather(const uint16_t* x, const int32_t* perm, const int32_t*
 }
 
 // One thread per (token t = blockIdx.x, 16-byte chunk c of H):
-// out[t] = bf16(sum_j bf16(y[t k + j] * w[t k + j])), the products rounded to
-// bf16 (the product of two bf16 arrays is a bf16 array) and summed in fp32
-// in j order.
+// out[t] = bf16(sum_j bf16(y_j * w[t k + j])), y_j = row inv[t k + j] of the
+// down product (stored by sorted row), the products rounded to bf16 (the
+// product of two bf16 arrays is a bf16 array) and summed in fp32 in j order.
 __global__ void __launch_bounds__(128) combine_kernel(const uint16_t* __restrict__ y,
+                                                      const int32_t* __restrict__ inv,
                                                       const uint16_t* __restrict__ w,
                                                       uint16_t* __restrict__ out, int k, int H) {
     pdl_trigger();
@@ -421,13 +422,14 @@ __global__ void __launch_bounds__(128) combine_kernel(const uint16_t* __restrict
     const int chunks = H / 8;
     const int t = blockIdx.x, c = blockIdx.y * 128 + threadIdx.x;
     if (c >= chunks) return;
-    const uint4* yt = reinterpret_cast<const uint4*>(y + (size_t)t * k * H) + c;
+    const uint4* yc = reinterpret_cast<const uint4*>(y) + c;
     const uint16_t* wt = w + (size_t)t * k;
+    const int32_t* it = inv + (size_t)t * k;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
     for (int j = 0; j < k; ++j) {
         const uint32_t wb = __ldg(wt + j), w2 = wb | (wb << 16);
-        const uint4 v = __ldg(yt + (size_t)j * chunks);
+        const uint4 v = __ldg(yc + (size_t)__ldg(it + j) * chunks);
         const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -449,6 +451,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const uint16_t* __restrict
 constexpr int kNormThreads = 256;
 constexpr int kNormChunks = 4;  // 16-byte chunks a thread: H <= 8192
 __global__ void __launch_bounds__(kNormThreads) combine_norm_kernel(const uint16_t* __restrict__ y,
+                                                                    const int32_t* __restrict__ inv,
                                                                     const uint16_t* __restrict__ w,
                                                                     const uint16_t* __restrict__ post_w,
                                                                     uint16_t* __restrict__ out, int k, int H,
@@ -456,8 +459,9 @@ __global__ void __launch_bounds__(kNormThreads) combine_norm_kernel(const uint16
     pdl_trigger();
     pdl_wait();
     const int chunks = H / 8, t = blockIdx.x, tid = threadIdx.x;
-    const uint4* yt = reinterpret_cast<const uint4*>(y + (size_t)t * k * H);
+    const uint4* y4 = reinterpret_cast<const uint4*>(y);
     const uint16_t* wt = w + (size_t)t * k;
+    const int32_t* it = inv + (size_t)t * k;
     uint4 cv[kNormChunks];
     float hi = 0.f, lo = 0.f;
 #pragma unroll
@@ -468,7 +472,7 @@ __global__ void __launch_bounds__(kNormThreads) combine_norm_kernel(const uint16
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         for (int j = 0; j < k; ++j) {
             const uint32_t wb = __ldg(wt + j), w2 = wb | (wb << 16);
-            const uint4 v = __ldg(yt + (size_t)j * chunks + c);
+            const uint4 v = __ldg(y4 + (size_t)__ldg(it + j) * chunks + c);
             const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -502,19 +506,19 @@ __global__ void __launch_bounds__(kNormThreads) combine_norm_kernel(const uint16
     }
 }
 
-cudaError_t launch_combine_norm(const uint16_t* y, const uint16_t* w, const uint16_t* post_w, uint16_t* out, int T,
-                                int k, int H, float eps, cudaStream_t stream) {
+cudaError_t launch_combine_norm(const uint16_t* y, const int32_t* inv, const uint16_t* w, const uint16_t* post_w,
+                                uint16_t* out, int T, int k, int H, float eps, cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
     if (H / 8 > kNormThreads * kNormChunks) return cudaErrorInvalidValue;
-    return launch_pdl(combine_norm_kernel, dim3((unsigned)T), dim3(kNormThreads), 0, stream, y, w, post_w, out, k, H,
-                      eps);
+    return launch_pdl(combine_norm_kernel, dim3((unsigned)T), dim3(kNormThreads), 0, stream, y, inv, w, post_w, out,
+                      k, H, eps);
 }
 
-cudaError_t launch_combine(const uint16_t* y, const uint16_t* w, uint16_t* out, int T, int k, int H,
-                           cudaStream_t stream) {
+cudaError_t launch_combine(const uint16_t* y, const int32_t* inv, const uint16_t* w, uint16_t* out, int T, int k,
+                           int H, cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
     const dim3 grid((unsigned)T, (unsigned)((H / 8 + 127) / 128));
-    return launch_pdl(combine_kernel, grid, dim3(128), 0, stream, y, w, out, k, H);
+    return launch_pdl(combine_kernel, grid, dim3(128), 0, stream, y, inv, w, out, k, H);
 }
 
 int dispatch_error_word() {

@@ -38,7 +38,7 @@
 //                 TMEM and B from shared memory;
 //   epilogue      an item accumulates its whole K in one of two TMEM
 //     warps       accumulator buffers (fp32); once per item these warps read
-//                 it and apply GeGLU (gate_up) or scatter y to flat slots
+//                 it and apply GeGLU (gate_up) or store y by sorted row
 //                 (down) while the next item accumulates in the other buffer.
 // The dequantised pair order inside each 8-element K block is (0,4),(1,5),
 // (2,6),(3,7); the B operands (gathered x, GeGLU output) are stored in that
@@ -470,11 +470,6 @@ __global__ void __launch_bounds__((3 + 16 / APW + 4 * EPW) * 32, 1)
             const Tile tl = a.tiles[it / a.n_tiles];
             const int j = it % a.n_tiles;
             const int nrows16 = (tl.rows + 15) & ~15;
-            int pf[NMAX / 32];  // down: flat slot of sorted row 32 i + lane
-            if (MODE == kDown) {
-#pragma unroll
-                for (int i = 0; i < NMAX / 32; ++i) pf[i] = (32 * i + lane < tl.rows) ? a.perm[tl.p0 + 32 * i + lane] : 0;
-            }
             // The item's accumulator (buffer li & 1) holds the whole K: this
             // warp reads its 16-column chunks one at a time, then hands the
             // buffer back (it is not needed again before item li + 2).
@@ -524,15 +519,13 @@ __global__ void __launch_bounds__((3 + 16 / APW + 4 * EPW) * 32, 1)
                         if (tok < tl.rows) a.out_f32[(size_t)(tl.p0 + tok) * a.out_ld + vrow] = o;
                     }
                 } else {
+                    // y by sorted row: 32 lanes store 64 B of a row
                     const int hrow = 128 * j + 32 * q + lane;
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) {
                         const int tok = c0 + jj;
-                        int src = pf[0];  // select, not an indexed load: pf stays in registers
-#pragma unroll
-                        for (int i = 1; i < NMAX / 32; ++i) src = ((tok >> 5) == i) ? pf[i] : src;
-                        const int f = __shfl_sync(0xffffffffu, src, tok & 31);
-                        if (tok < tl.rows) a.out[(size_t)f * a.out_ld + hrow] = (uint16_t)f32_to_bf16_bits(v[jj]);
+                        if (tok < tl.rows)
+                            a.out[(size_t)(tl.p0 + tok) * a.out_ld + hrow] = (uint16_t)f32_to_bf16_bits(v[jj]);
                     }
                 }
             }

@@ -92,21 +92,22 @@ cudaError_t launch_dispatch_gather(const DispatchArgs& a, const uint16_t* x, uin
 cudaError_t launch_gather(const uint16_t* x, const int32_t* perm, const int32_t* offsets, uint16_t* xs,
                           int S, int k, int H, int E, cudaStream_t stream);
 
-// Combine: out[t] = bf16(sum_j bf16(y[t*k+j] * w[t*k+j])), fp32 sum in j order.
-cudaError_t launch_combine(const uint16_t* y, const uint16_t* w, uint16_t* out, int T, int k, int H,
-                           cudaStream_t stream);
+// Combine: out[t] = bf16(sum_j bf16(y[inv[t*k+j]] * w[t*k+j])), fp32 sum in
+// j order; y by sorted row, inv the sorted row of each flat slot.
+cudaError_t launch_combine(const uint16_t* y, const int32_t* inv, const uint16_t* w, uint16_t* out, int T, int k,
+                           int H, cudaStream_t stream);
 // Combine, then the MoE branch's post norm: out[t] = bf16((c * rsqrt(mean(c^2)
 // + eps)) * post_w) of the combined bf16 row c (fp32 steps). H <= 8192.
-cudaError_t launch_combine_norm(const uint16_t* y, const uint16_t* w, const uint16_t* post_w, uint16_t* out, int T,
-                                int k, int H, float eps, cudaStream_t stream);
+cudaError_t launch_combine_norm(const uint16_t* y, const int32_t* inv, const uint16_t* w, const uint16_t* post_w,
+                                uint16_t* out, int T, int k, int H, float eps, cudaStream_t stream);
 int dispatch_error_word();
 
 // Dense MLP input: xs[t] = row t of x, or RMSNorm(x, pre_w) with fp32 steps
 // (pre_w non-null), each 8-element block of K interleaved as the gather's;
-// perm[t] = t; and the tile list of one expert whose token tiles of nmax
-// rows cover all T rows (num_tiles: count, rows of the largest). H <= 8192.
-cudaError_t launch_dense_prep(const uint16_t* x, const uint16_t* pre_w, float eps, uint16_t* xs, int32_t* perm,
-                              Tile* tiles, int32_t* num_tiles, int T, int H, int nmax, cudaStream_t stream);
+// and the tile list of one expert whose token tiles of nmax rows cover all
+// T rows (num_tiles: count, rows of the largest). H <= 8192.
+cudaError_t launch_dense_prep(const uint16_t* x, const uint16_t* pre_w, float eps, uint16_t* xs, Tile* tiles,
+                              int32_t* num_tiles, int T, int H, int nmax, cudaStream_t stream);
 // out[t] = bf16((c * rsqrt(mean(c^2) + eps)) [* w]) of c = s[t], or of
 // c = bf16(embeds[t] + s[t]) (embeds non-null); w null: no weight. H <= 8192.
 cudaError_t launch_add_norm(const uint16_t* embeds, const uint16_t* s, const uint16_t* w, float eps, uint16_t* out,
@@ -121,8 +122,7 @@ struct GemmArgs {
     const uint16_t* biases;   // [E, N, K/64]
     const Tile* tiles;
     const int32_t* num_tiles; // [0] tile count, [1] rows of the largest tile
-    const int32_t* perm;      // down: flat slot of each sorted row
-    uint16_t* out;            // gate_up: mid [S, inter]; down: y [S, H] by flat slot
+    uint16_t* out;            // gate_up: mid [S, inter]; down: y [S, H]; both by sorted row
     int K;                    // reduction length (H or inter)
     int N;                    // rows of the weight (2*inter or H)
     int inter;                // gate_up: split point

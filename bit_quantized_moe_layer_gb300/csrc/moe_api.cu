@@ -264,7 +264,6 @@ int run_experts(const moe_dims* d, const uint16_t* x, const int32_t* idx, const 
     ga.biases = gu->biases;
     ga.tiles = tiles;
     ga.num_tiles = ntiles;
-    ga.perm = perm;
     ga.out = mid;
     ga.K = H;
     ga.N = 2 * I;
@@ -303,8 +302,8 @@ int run_experts(const moe_dims* d, const uint16_t* x, const int32_t* idx, const 
     if (rc) return rc;
     tm.mark(5);
 
-    rc = fail(post_norm_w ? launch_combine_norm(y, w, post_norm_w, out, d->T, d->k, H, d->eps, s)
-                          : launch_combine(y, w, out, d->T, d->k, H, s));
+    rc = fail(post_norm_w ? launch_combine_norm(y, inv, w, post_norm_w, out, d->T, d->k, H, d->eps, s)
+                          : launch_combine(y, inv, w, out, d->T, d->k, H, s));
     if (rc) return rc;
     tm.mark(6);
     return MOE_OK;
@@ -317,7 +316,6 @@ int run_dense(const moe_dims* d, const uint16_t* x, const uint16_t* pre_norm_w, 
               const uint16_t* post_norm_w, bool post_norm, const moe_qweight* gu, const moe_qweight* dn, uint16_t* out,
               uint8_t* ws, const Layout& L, const DeviceInfo& di, cudaStream_t s) {
     const int T = d->T, H = d->H, I = d->inter;
-    int32_t* perm = reinterpret_cast<int32_t*>(ws + L.perm);
     Tile* tiles = reinterpret_cast<Tile*>(ws + L.tiles);
     int32_t* ntiles = reinterpret_cast<int32_t*>(ws + L.ntiles);
     uint16_t* xs = reinterpret_cast<uint16_t*>(ws + L.xs);
@@ -340,7 +338,7 @@ int run_dense(const moe_dims* d, const uint16_t* x, const uint16_t* pre_norm_w, 
     tm.mark(0);
     tm.mark(1);
     tm.mark(2);
-    int rc = fail(launch_dense_prep(x, pre_norm_w, d->eps, xs, perm, tiles, ntiles, T, H, nmax, s));
+    int rc = fail(launch_dense_prep(x, pre_norm_w, d->eps, xs, tiles, ntiles, T, H, nmax, s));
     if (rc) return rc;
     tm.mark(3);
 
@@ -349,7 +347,6 @@ int run_dense(const moe_dims* d, const uint16_t* x, const uint16_t* pre_norm_w, 
     ga.biases = gu->biases;
     ga.tiles = tiles;
     ga.num_tiles = ntiles;
-    ga.perm = perm;
     ga.out = mid;
     ga.K = H;
     ga.N = 2 * I;
@@ -389,7 +386,6 @@ int run_dense(const moe_dims* d, const uint16_t* x, const uint16_t* pre_norm_w, 
 int run_head(const moe_dims* d, int vocab, float softcap, const uint16_t* h, const moe_qweight* embed, float* logits,
              uint8_t* ws, const Layout& L, const DeviceInfo& di, cudaStream_t s) {
     const int T = d->T, H = d->H;
-    int32_t* perm = reinterpret_cast<int32_t*>(ws + L.perm);
     Tile* tiles = reinterpret_cast<Tile*>(ws + L.tiles);
     int32_t* ntiles = reinterpret_cast<int32_t*>(ws + L.ntiles);
     uint16_t* xs = reinterpret_cast<uint16_t*>(ws + L.xs);
@@ -408,7 +404,7 @@ int run_head(const moe_dims* d, int vocab, float softcap, const uint16_t* h, con
     tm.mark(0);
     tm.mark(1);
     tm.mark(2);
-    int rc = fail(launch_dense_prep(h, nullptr, 0.f, xs, perm, tiles, ntiles, T, H, nmax, s));
+    int rc = fail(launch_dense_prep(h, nullptr, 0.f, xs, tiles, ntiles, T, H, nmax, s));
     if (rc) return rc;
     tm.mark(3);
     GemmArgs ga{};
@@ -416,7 +412,6 @@ int run_head(const moe_dims* d, int vocab, float softcap, const uint16_t* h, con
     ga.biases = embed->biases;
     ga.tiles = tiles;
     ga.num_tiles = ntiles;
-    ga.perm = perm;
     ga.out_f32 = logits;
     ga.softcap = softcap;
     ga.K = H;
