@@ -85,13 +85,15 @@ __host__ __device__ inline int scale_buf_bytes(int K) {
 // is p - p r, formed by a fused multiply-add rounded toward zero: the exact
 // value lies strictly between 0 and p, so an exact bf16 tie of p (large g,
 // where r is below fp32's resolution of 1) rounds toward zero as the exact
-// value does. One exp and one divide serve both signs.
+// value does. One exp and one divide serve both signs. For e <= 2^-25,
+// 1 + e rounds to 1 and the quotient is e itself: taking e skips the
+// divide's slow path for subnormal e (far tails of s), with the same result.
 __device__ __forceinline__ uint32_t geglu_bf16(float g, float up) {
     const float c = 0.7978845608028654f;  // sqrt(2/pi)
     const float s = __fmul_rn(c, __fadd_rn(g, __fmul_rn(0.044715f, __fmul_rn(g, __fmul_rn(g, g)))));
     const float p = __fmul_rn(g, up);
     const float e = expf(__fmul_rn(-2.0f, fabsf(s)));
-    const float r = __fdiv_rn(e, __fadd_rn(1.0f, e));
+    const float r = (e <= 0x1p-25f) ? e : __fdiv_rn(e, __fadd_rn(1.0f, e));
     const float m = (s < 0.f) ? __fmul_rn(p, r) : __fmaf_rz(-p, fmaxf(r, 1e-30f), p);
     return f32_to_bf16_bits(m);
 }
