@@ -105,6 +105,17 @@ __device__ __forceinline__ int bbox_index(int rows) {
     return i;
 }
 
+// Token tile and weight tile of work item `it` (ntok token tiles).
+__device__ __forceinline__ void item_coords(const GemmArgs& a, int ntok, int it, int& ti, int& j) {
+    if (a.weight_major) {
+        ti = it % ntok;
+        j = it / ntok;
+    } else {
+        ti = it / a.n_tiles;
+        j = it % a.n_tiles;
+    }
+}
+
 // Position of element n inside its 8-block in the interleaved K order.
 __device__ __forceinline__ int interleaved_pos(int n) {
     const int r = n & 7;
@@ -156,8 +167,11 @@ __global__ void __launch_bounds__((3 + 16 / APW + 4 * EPW) * 32, 1)
         const uint32_t row_bytes = (uint32_t)a.K / 2, G = (uint32_t)a.K / 64;
         for (int i = 0; i < a.prefetch_items; ++i) {
             const int it = blockIdx.x + i * gridDim.x;
-            const int e = (it / a.n_tiles) / a.tiles_per_expert, j = it % a.n_tiles;
-            if (e >= a.E) break;
+            // before the wait the token-tile count is the host's (tiles_per_expert)
+            int ti, j;
+            item_coords(a, a.tiles_per_expert, it, ti, j);
+            const int e = ti / a.tiles_per_expert;
+            if (e >= a.E || j >= a.n_tiles) break;  // past the last item
             const int nblk = (MODE == kGateUp) ? 2 : 1;  // gate and up halves, or one 128-row block
             for (int h = 0; h < nblk; ++h) {
                 const size_t r0 = (MODE == kGateUp) ? (size_t)e * a.N + (size_t)h * a.inter + 64 * j
@@ -224,7 +238,8 @@ __global__ void __launch_bounds__((3 + 16 / APW + 4 * EPW) * 32, 1)
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
 
-    const int num_items = a.num_tiles[0] * a.n_tiles;
+    const int ntok = a.num_tiles[0];
+    const int num_items = ntok * a.n_tiles;
     const int K = a.K;
     const int nstages = (K + kStageK - 1) / kStageK;
     if (warp == 0) {
@@ -236,8 +251,9 @@ __global__ void __launch_bounds__((3 + 16 / APW + 4 * EPW) * 32, 1)
         int li = 0;
         bool ok = true;
         for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x, ++li) {
-            const Tile tl = a.tiles[it / a.n_tiles];
-            const int j = it % a.n_tiles;
+            int ti, j;
+            item_coords(a, ntok, it, ti, j);
+            const Tile tl = a.tiles[ti];
             const int sb = li & 1;
             if (!(ok = mbar_wait(&sh.sempty[sb], ((li >> 1) & 1) ^ 1, abort_flag, kSleepRing, 1))) break;
             uint8_t* sbuf = scale_base + sb * sbuf_bytes;
@@ -293,7 +309,9 @@ __global__ void __launch_bounds__((3 + 16 / APW + 4 * EPW) * 32, 1)
         uint32_t ph = 0, issued = 0;
         bool ok = true;
         for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x) {
-            const Tile tl = a.tiles[it / a.n_tiles];
+            int ti, j;
+            item_coords(a, ntok, it, ti, j);
+            const Tile tl = a.tiles[ti];
             const int bi = bbox_index(tl.rows);
             const int nrows16 = (tl.rows + 15) & ~15;
             // the whole box counts, rows and atoms past the tensor (zero-filled) included
@@ -333,10 +351,17 @@ __global__ void __launch_bounds__((3 + 16 / APW + 4 * EPW) * 32, 1)
         uint32_t bph = 0, aph = 0;  // phases of the B slot's and the A slot's barriers
         bool ok = true;
         Tile tl_next = {};
-        if (blockIdx.x < num_items) tl_next = a.tiles[blockIdx.x / a.n_tiles];
+        int ti, jn;
+        if (blockIdx.x < num_items) {
+            item_coords(a, ntok, blockIdx.x, ti, jn);
+            tl_next = a.tiles[ti];
+        }
         for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x, ++li) {
             const Tile tl = tl_next;
-            if (it + (int)gridDim.x < num_items) tl_next = a.tiles[(it + gridDim.x) / a.n_tiles];
+            if (it + (int)gridDim.x < num_items) {
+                item_coords(a, ntok, it + gridDim.x, ti, jn);
+                tl_next = a.tiles[ti];
+            }
             const uint32_t nrows16 = (uint32_t)((tl.rows + 15) & ~15);
             const uint32_t idesc = idesc_bf16_m128(nrows16);
             // distance of the B slot's atoms in descriptor units (16 B)
@@ -469,8 +494,9 @@ __global__ void __launch_bounds__((3 + 16 / APW + 4 * EPW) * 32, 1)
         bool ok = true;
         int li = 0;
         for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x, ++li) {
-            const Tile tl = a.tiles[it / a.n_tiles];
-            const int j = it % a.n_tiles;
+            int ti, j;
+            item_coords(a, ntok, it, ti, j);
+            const Tile tl = a.tiles[ti];
             const int nrows16 = (tl.rows + 15) & ~15;
             // The item's accumulator (buffer li & 1) holds the whole K: this
             // warp reads its 16-column chunks one at a time, then hands the

@@ -140,6 +140,11 @@ struct GemmArgs {
     const uint8_t* w;
     int prefetch_items;
     int tiles_per_expert;
+    // Item order. 0: token-tile-major (it = tile * n_tiles + j). 1 (one
+    // expert, several token tiles): weight-tile-major (it = j * tiles +
+    // tile), so the token tiles of a weight tile run together and share its
+    // copy in L2 instead of streaming the weights once per token tile.
+    int weight_major;
     // kHead: logits [rows, out_ld] fp32 and the final-logit softcap
     // (cap * tanh(x / cap) of the bf16 logit x; cap <= 0: x itself).
     float* out_f32;

@@ -358,6 +358,7 @@ int run_dense(const moe_dims* d, const uint16_t* x, const uint16_t* pre_norm_w, 
     ga.w = reinterpret_cast<const uint8_t*>(gu->w);
     ga.prefetch_items = 2;
     ga.tiles_per_expert = ntok;  // every item is expert 0's
+    ga.weight_major = 1;
     gemm_stages(H, nmax, &ga.wstages, &ga.bregion);
     int grid = di.sms < ntok * ga.n_tiles ? di.sms : ntok * ga.n_tiles;
     if ((rc = fail(launch_gemm(kGateUp, m_gu, m_xs, ga, grid, s)))) return rc;
@@ -424,6 +425,7 @@ int run_head(const moe_dims* d, int vocab, float softcap, const uint16_t* h, con
     ga.w = reinterpret_cast<const uint8_t*>(embed->w);
     ga.prefetch_items = 2;
     ga.tiles_per_expert = ntok;
+    ga.weight_major = 1;
     gemm_stages(H, nmax, &ga.wstages, &ga.bregion);
     const long items = (long)ntok * n_tiles;
     const int grid = items < di.sms ? (int)items : di.sms;
