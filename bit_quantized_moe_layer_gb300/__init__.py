@@ -24,10 +24,10 @@ LIB_PATH = os.path.join(_HERE, "libmoe.so")
 STAGES = ("route", "dispatch", "gather", "gate_up", "down", "combine")
 STATUS = {0: "ok", 1: "null pointer", 2: "bad shape", 3: "pointer not 16-byte aligned",
           4: "unsupported configuration", 5: "workspace too small", 6: "CUDA error",
-          7: "kernel wait timed out", 8: "no usable sm_100-family GPU"}
+          7: "kernel wait timed out", 8: "no usable GPU (needs compute capability 10.3, sm_103a)"}
 
 # Every function the public header declares.
-EXPORTS = ("moe_status_str", "moe_workspace_bytes", "moe_route", "moe_dispatch", "moe_experts",
+EXPORTS = ("moe_status_str", "moe_workspace_bytes", "moe_workspace_map_of", "moe_route", "moe_dispatch", "moe_experts",
            "moe_experts_noalloc", "moe_forward", "moe_forward_branch", "moe_forward_hostio", "moe_route_q4",
            "moe_forward_q4router", "moe_dense_mlp", "moe_dense_branch", "moe_self_conditioning", "moe_lm_head",
            "moe_timing_enable",
@@ -45,6 +45,11 @@ class Dims(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("E", ctypes.c_int32),
                 ("k", ctypes.c_int32), ("inter", ctypes.c_int32), ("group", ctypes.c_int32),
                 ("bits", ctypes.c_int32), ("eps", ctypes.c_float)]
+
+
+class WorkspaceMap(ctypes.Structure):
+    _fields_ = [("idx", ctypes.c_size_t), ("w", ctypes.c_size_t), ("perm", ctypes.c_size_t),
+                ("inv", ctypes.c_size_t), ("offsets", ctypes.c_size_t)]
 
 
 class QWeight(ctypes.Structure):
@@ -69,6 +74,8 @@ def load(path: str = LIB_PATH):
     lib.moe_status_str.restype = ctypes.c_char_p
     lib.moe_workspace_bytes.argtypes = [D]
     lib.moe_workspace_bytes.restype = Z
+    lib.moe_workspace_map_of.argtypes = [D, ctypes.POINTER(WorkspaceMap)]
+    lib.moe_workspace_map_of.restype = I
     lib.moe_route.argtypes = [D, P, P, P, P, P, P, P]
     lib.moe_dispatch.argtypes = [D, P, P, P, P, P]
     lib.moe_experts.argtypes = [D, P, P, P, Q, Q, P, P, Z, P]
@@ -131,6 +138,13 @@ def qweight(w, scales, biases) -> QWeight:
 
 def workspace_bytes(d: Dims) -> int:
     return int(load().moe_workspace_bytes(ctypes.byref(d)))
+
+
+def workspace_map(d: Dims) -> WorkspaceMap:
+    """Byte offsets of idx, w, perm, inv and offsets inside a caller workspace."""
+    m = WorkspaceMap()
+    _check("moe_workspace_map_of", load().moe_workspace_map_of(ctypes.byref(d), ctypes.byref(m)))
+    return m
 
 
 def moe_route(d: Dims, x, router_w, router_scale, per_expert_scale, idx_out, w_out, stream=None):

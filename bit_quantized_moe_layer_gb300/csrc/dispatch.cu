@@ -132,13 +132,15 @@ __device__ __forceinline__ void warp_scatter(const DispatchArgs& a, int c0, int 
     for (int b = c0; b < c1; b += 32) {
         const int f = b + lane;
         int e = (f < c1) ? a.idx[f] : -1;
-        if (e >= a.E) e = -1;
+        if (e >= a.E || e < 0) e = -1;
         const unsigned peers = __match_any_sync(0xffffffffu, e);
         const int rank = __popc(peers & lt_mask);
         if (e >= 0) {
             const int p = wh_row[e] + rank;
             a.perm[p] = f;
             a.inv[f] = p;
+        } else if (f < c1) {
+            a.inv[f] = -1;  // a dropped slot: the combine skips it
         }
         __syncwarp();
         if (e >= 0 && rank == 0) wh_row[e] += __popc(peers);
@@ -207,6 +209,8 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
             const int p = wh[e] + rank;
             a.perm[p] = f;
             a.inv[f] = p;
+        } else if (f < c1) {
+            a.inv[f] = -1;  // a dropped slot: the combine skips it
         }
         __syncwarp();
         if (e >= 0 && rank == 0) wh[e] += __popc(peers);
@@ -274,6 +278,8 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_gather_kernel(Dispa
                 a.inv[f] = p;
                 src_tok[p - r0] = f / k;
             }
+        } else if (f < c1 && blockIdx.x == 0) {
+            a.inv[f] = -1;  // a dropped slot: the combine skips it
         }
         __syncwarp();
         if (e >= 0 && rank == 0) wh[e] += __popc(peers);
@@ -428,8 +434,10 @@ __global__ void __launch_bounds__(128) combine_kernel(const uint16_t* __restrict
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
     for (int j = 0; j < k; ++j) {
+        const int p = __ldg(it + j);
+        if (p < 0) continue;  // slot dropped by the dispatch (expert id out of range)
         const uint32_t wb = __ldg(wt + j), w2 = wb | (wb << 16);
-        const uint4 v = __ldg(yc + (size_t)__ldg(it + j) * chunks);
+        const uint4 v = __ldg(yc + (size_t)p * chunks);
         const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -471,8 +479,10 @@ __global__ void __launch_bounds__(kNormThreads) combine_norm_kernel(const uint16
         if (c >= chunks) continue;
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         for (int j = 0; j < k; ++j) {
+            const int p = __ldg(it + j);
+            if (p < 0) continue;  // slot dropped by the dispatch
             const uint32_t wb = __ldg(wt + j), w2 = wb | (wb << 16);
-            const uint4 v = __ldg(y4 + (size_t)__ldg(it + j) * chunks + c);
+            const uint4 v = __ldg(y4 + (size_t)p * chunks + c);
             const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {

@@ -66,11 +66,14 @@ int device_info(DeviceInfo* out) {
     std::lock_guard<std::mutex> lock(mu);
     if ((int)cache.size() <= dev) cache.resize(dev + 1);
     if (!cache[dev].ok) {
-        int major = 0, sms = 0;
-        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
             return MOE_ERR_DEVICE;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ERR_DEVICE;
-        if (major != 10) return MOE_ERR_DEVICE;  // tcgen05 needs the sm_100 family
+        // The library is built for sm_103a only (arch-specific code runs on
+        // compute capability 10.3 and nothing else): refuse other GPUs here.
+        if (major != 10 || minor != 3) return MOE_ERR_DEVICE;
         cache[dev].sms = sms;
         cache[dev].ok = true;
     }
@@ -529,9 +532,22 @@ const char* moe_status_str(int status) {
         case MOE_ERR_WORKSPACE: return "workspace too small";
         case MOE_ERR_CUDA: return "CUDA error";
         case MOE_ERR_TIMEOUT: return "kernel wait timed out";
-        case MOE_ERR_DEVICE: return "no usable sm_100-family GPU";
+        case MOE_ERR_DEVICE: return "no usable GPU (needs compute capability 10.3, sm_103a)";
         default: return "unknown status";
     }
+}
+
+int moe_workspace_map_of(const moe_dims* d, moe_workspace_map* map) {
+    int rc = check_dims(d);
+    if (rc) return rc;
+    if (!map) return MOE_ERR_NULL;
+    const Layout L = layout(d);
+    map->idx = L.idx;
+    map->w = L.w;
+    map->perm = L.perm;
+    map->inv = L.inv;
+    map->offsets = L.offsets;
+    return MOE_OK;
 }
 
 size_t moe_workspace_bytes(const moe_dims* d) {

@@ -65,7 +65,7 @@ typedef enum moe_status {
     MOE_ERR_WORKSPACE = 5,    /* workspace too small                       */
     MOE_ERR_CUDA = 6,         /* a CUDA call or launch failed              */
     MOE_ERR_TIMEOUT = 7,      /* a kernel gave up waiting (see moe_device_error) */
-    MOE_ERR_DEVICE = 8        /* no usable sm_100-family GPU               */
+    MOE_ERR_DEVICE = 8        /* no usable GPU: needs compute capability 10.3 */
 } moe_status;
 
 /* Human-readable name of a status code. Never NULL. */
@@ -99,8 +99,8 @@ int moe_route(const moe_dims* d, const uint16_t* x, const uint16_t* router_w,
  *   offsets[e] .. offsets[e+1]   slot range of expert e (offsets int32 [E+1])
  *   perm[p] = f                  p-th slot in expert order (int32 [T*k])
  *   inv[f]  = p                  inverse of perm (int32 [T*k])
- * idx int32 [T,k] must hold ids in [0,E); a bad id is dropped and raised in
- * moe_device_error. Bit-exact and deterministic. For T*k > 8192 the sort runs
+ * idx int32 [T,k] must hold ids in [0,E); a slot with a bad id is dropped
+ * (inv = -1, no row in perm or offsets) and raised in moe_device_error. Bit-exact and deterministic. For T*k > 8192 the sort runs
  * as three kernels that need 64 KB of device scratch: this call allocates it
  * once per device on first use and holds it until the process exits.
  */
@@ -115,7 +115,9 @@ int moe_dispatch(const moe_dims* d, const int32_t* idx, int32_t* perm, int32_t* 
  *   y = bf16(m . Wdn[e]^T)             [H]
  * out[t] = bf16( sum_j bf16(y_{t,j} * w[t,j]) ), fp32 sum in j order.
  * x may differ from the router's input (the layer routes on the residual
- * and feeds the experts its pre-feed-forward-norm-2 output).
+ * and feeds the experts its pre-feed-forward-norm-2 output). A slot whose
+ * expert id lies outside [0,E) is dropped (it adds nothing to out) and
+ * raised in moe_device_error.
  * workspace: moe_workspace_bytes(d) bytes of device memory, or NULL to use
  * a grow-only buffer the library owns per device (not safe for concurrent
  * calls from several host threads). out may not alias x.
@@ -123,6 +125,22 @@ int moe_dispatch(const moe_dims* d, const int32_t* idx, int32_t* perm, int32_t* 
 int moe_experts(const moe_dims* d, const uint16_t* x, const int32_t* idx, const uint16_t* w,
                 const moe_qweight* gate_up, const moe_qweight* down, uint16_t* out,
                 void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Where the routed calls that take a workspace (moe_experts, moe_forward,
+ * moe_forward_q4router, moe_forward_branch, moe_forward_hostio) leave the
+ * dispatch of their last call inside a caller-provided workspace, as byte
+ * offsets from its start: perm and inv (int32 [T*k]) and offsets (int32
+ * [E+1]) exactly as moe_dispatch defines them, computed by the kernels the
+ * call itself runs; idx (int32 [T,k]) and w (bf16 [T,k]) hold the routing
+ * when the call was given no idx_out / w_out. For inspection and bit-exact
+ * tests of the in-call dispatch; the layout depends only on the dims.
+ * Returns MOE_OK, or an error for invalid dims (the map is then untouched).
+ */
+typedef struct moe_workspace_map {
+    size_t idx, w, perm, inv, offsets;
+} moe_workspace_map;
+int moe_workspace_map_of(const moe_dims* d, moe_workspace_map* map);
 
 /*
  * moe_experts without any allocation. (The pages have no counterpart: this

@@ -145,7 +145,11 @@ int oracle_route(const oracle_dims* d, const uint16_t* x, const uint16_t* router
     if (T < 0 || H <= 0 || E <= 0 || k <= 0 || k > E || k > 64) return -1;
     set_threads(nthreads);
     /* hidden^-0.5 enters as a scalar in the array dtype (bf16). */
+#if ORACLE_MUTANT == 16
+    const float root = (float)pow((double)H, -0.5); /* planted: the scalar kept in fp32 */
+#else
     const float root = bf(bf16_from_double(pow((double)H, -0.5)));
+#endif
 
 #pragma omp parallel
     {
@@ -172,7 +176,11 @@ int oracle_route(const oracle_dims* d, const uint16_t* x, const uint16_t* router
             float denom = mean + d->eps;
             float r = (float)(1.0 / sqrt((double)denom)); /* rsqrt, rounded to fp32 */
             for (int h = 0; h < H; ++h) {
+#if ORACLE_MUTANT == 17
+                float nv = bf(xt[h]) * r;                                   /* planted: not cast to bf16 */
+#else
                 float nv = bf(bf16_from_float(bf(xt[h]) * r));             /* cast to bf16 */
+#endif
                 float n2 = bf(bf16_from_float(nv * bf(router_scale[h])));  /* * scale */
                 n3[h] = bf16_from_float(n2 * root);                         /* * H^-0.5 */
             }
@@ -454,7 +462,11 @@ int oracle_rms_norm(int32_t T, int32_t H, float eps, const uint16_t* x, const ui
         float mean = (float)(ss / (double)H);
         float r = (float)(1.0 / sqrt((double)(mean + eps)));
         for (int h = 0; h < H; ++h) {
+#if ORACLE_MUTANT == 18
+            float nv = bf(bf16_from_float(bf(xt[h]) * r)); /* planted: x*r rounded before the weight */
+#else
             float nv = bf(xt[h]) * r;
+#endif
 #if ORACLE_MUTANT == 8
             out[(size_t)t * H + h] = bf16_from_float(nv); /* planted: weight dropped */
 #else

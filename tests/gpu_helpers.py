@@ -107,21 +107,47 @@ def gpu_forward(g: GpuLayer, workspace=None):
     return host16(out), idx.cpu().numpy(), host16(w)
 
 
-def near_tie_rows(logits: np.ndarray, scores: np.ndarray, k: int) -> np.ndarray:
+def near_tie_rows(logits: np.ndarray, scores: np.ndarray, k: int):
     """Tokens whose oracle k-th and (k+1)-th experts (in the canonical order)
-    have exact logits within NEAR_TIE_REL of each other, or equal bf16 scores
-    (a tie at the scores' own precision, decided by the lower id, which a
-    sub-ulp accumulation-order difference in one score can turn over)."""
+    are a near tie. Returns two masks:
+      band       the exact logits are within NEAR_TIE_REL of each other (the
+                 stated exemption);
+      score_tie  outside the band, but the two bf16 scores are equal: the
+                 tie is decided by the lower id on both sides, so a GPU
+                 difference there needs a GPU score that rounded the other
+                 way, which check_routing only accepts next to a bf16
+                 rounding midpoint (midpoint_logit)."""
     T, E = scores.shape
     if k >= E:
-        return np.zeros(T, bool)
+        z = np.zeros(T, bool)
+        return z, z
     s = f64(scores)
     order = np.lexsort((np.broadcast_to(np.arange(E), (T, E)), -s), axis=1)
     lk = np.take_along_axis(logits, order[:, k - 1:k], 1)[:, 0]
     lk1 = np.take_along_axis(logits, order[:, k:k + 1], 1)[:, 0]
     sk = np.take_along_axis(s, order[:, k - 1:k], 1)[:, 0]
     sk1 = np.take_along_axis(s, order[:, k:k + 1], 1)[:, 0]
-    return (np.abs(lk - lk1) <= NEAR_TIE_REL * np.maximum(np.abs(lk), np.abs(lk1))) | (sk == sk1)
+    band = np.abs(lk - lk1) <= NEAR_TIE_REL * np.maximum(np.abs(lk), np.abs(lk1))
+    return band, (sk == sk1) & ~band
+
+
+MIDPOINT_REL = 2.0 ** -20
+# fp32 accumulation bound of one GPU router logit, in units of 2^-24 times the
+# sum of |products|: each of the 8 CTAs of a router cluster accumulates its
+# H/8 products in the tensor core's fp32 accumulator (16 products a step),
+# then the 8 partials are added; (H/8)/16 + 16 + 8 <= 64 steps for H <= 5504.
+ACCUM_STEPS = 64
+
+
+def midpoint_logit(v: float, abs_dot: float | None = None) -> bool:
+    """Whether the exact logit v lies close enough to a bf16 rounding midpoint
+    that an fp32-accumulated score may round the other way: within
+    ACCUM_STEPS * 2^-24 * sum|products| (abs_dot) of it, or within
+    MIDPOINT_REL of |v| when the products are not known."""
+    u = float(bf16_ulp(np.array([v]))[0])
+    mid = np.floor(abs(v) / u) * u + u / 2
+    window = ACCUM_STEPS * 2.0 ** -24 * abs_dot if abs_dot is not None else MIDPOINT_REL * abs(v)
+    return abs(abs(v) - mid) <= window
 
 
 def softmax_near_midpoint(scores: np.ndarray) -> np.ndarray:
@@ -137,28 +163,44 @@ def softmax_near_midpoint(scores: np.ndarray) -> np.ndarray:
     return np.abs(p - mid) <= 4 * 2.0 ** -24 * np.abs(p)
 
 
-def check_routing(d, ref, idx, w):
+def check_routing(d, ref, idx, w, router_w=None):
     """Compare GPU routing with the oracle's. The pages' top-k (argpartition)
     is an unordered set, so sets are compared per token and the weights per
     (token, expert); the emitted order must be descending in the oracle's
     scores except between experts whose exact logits are within the near-tie
-    band. Returns (near-tie tokens, tokens whose set differs)."""
-    ties = near_tie_rows(ref["logits"], ref["scores"], d.k)
+    band. A token whose set differs must be a near tie (one swap, between its
+    k-th and (k+1)-th experts): inside the band, or an equal-score tie whose
+    two exact logits include one next to a bf16 rounding midpoint (the
+    window is the GPU's fp32 accumulation bound when the router weight
+    router_w [E,H] bf16 bits is given, with the oracle's normed input).
+    Returns the counts {band, score_tie, differ, differ_score_tie}."""
+    band, score_tie = near_tie_rows(ref["logits"], ref["scores"], d.k)
     T, k = idx.shape
     lg = ref["logits"]
-    band = lambda a, b: abs(a - b) <= NEAR_TIE_REL * max(abs(a), abs(b)) + 1e-12
-    differ = 0
+    in_band = lambda a, b: abs(a - b) <= NEAR_TIE_REL * max(abs(a), abs(b)) + 1e-12
+    differ = differ_score_tie = 0
     for t in range(T):
         gs, os_ = set(idx[t].tolist()), set(ref["idx"][t].tolist())
         assert len(gs) == k and all(0 <= e < d.E for e in gs), f"token {t}: invalid expert ids {idx[t]}"
         if gs != os_:
             differ += 1
-            assert ties[t], (f"routing differs on non-tie token {t}: gpu {sorted(gs)} oracle {sorted(os_)}")
+            assert band[t] or score_tie[t], \
+                f"routing differs on non-tie token {t}: gpu {sorted(gs)} oracle {sorted(os_)}"
             extra, missing = gs - os_, os_ - gs
             assert len(extra) == 1 and len(missing) == 1, f"near-tie token {t}: more than one swap"
             ex_, mi_ = extra.pop(), missing.pop()
+            if in_band(lg[t, ex_], lg[t, mi_]):
+                continue
             sc_ = f64(ref["scores"][t])
-            assert band(lg[t, ex_], lg[t, mi_]) or sc_[ex_] == sc_[mi_], f"near-tie token {t}: swap outside the band"
+            assert sc_[ex_] == sc_[mi_], f"near-tie token {t}: swap outside the band"
+            ad = [None, None]
+            if router_w is not None and "normed" in ref:
+                nt = np.abs(f64(ref["normed"][t]))
+                ad = [float(nt @ np.abs(f64(router_w[e]))) for e in (ex_, mi_)]
+            assert midpoint_logit(lg[t, ex_], ad[0]) or midpoint_logit(lg[t, mi_], ad[1]), \
+                (f"token {t}: equal-score swap ({ex_} for {mi_}) with neither exact logit near a bf16 "
+                 f"rounding midpoint: {lg[t, ex_]!r}, {lg[t, mi_]!r}")
+            differ_score_tie += 1
             continue
         sc = f64(ref["scores"][t])
         for j in range(k - 1):  # emitted order: score descending, ties to the lower id
@@ -174,7 +216,18 @@ def check_routing(d, ref, idx, w):
             ulps = 2 if p_mid[j] else 1
             assert abs(gw[e] - o) <= ulps * float(bf16_ulp(np.array([o]))[0]) + 1e-30, \
                 f"token {t} expert {e}: weight {gw[e]} vs oracle {o}"
-    return int(ties.sum()), differ
+    return dict(band=int(band.sum()), score_tie=int(score_tie.sum()), differ=differ,
+                differ_score_tie=differ_score_tie)
+
+
+def workspace_dispatch(d, ws: torch.Tensor):
+    """perm, offsets and inv that the last routed call left in the caller
+    workspace `ws` (uint8 tensor), at the library's own workspace map."""
+    m = moe.workspace_map(d)
+    S = d.T * d.k
+    host = ws.cpu().numpy()
+    take = lambda off, n: host[off:off + 4 * n].view(np.int32).copy()
+    return take(m.perm, S), take(m.offsets, d.E + 1), take(m.inv, S)
 
 
 def compare_out(gpu_bits: np.ndarray, ref_bits: np.ndarray, what: str = "out") -> dict:

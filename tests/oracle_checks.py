@@ -154,6 +154,30 @@ def check_router_constant_row(lib):
         assert np.all(r["normed"] == want), f"constant row, H={H}: normed != {want:#06x}"
 
 
+
+def _golden_row(g) -> np.ndarray:
+    """The hand-built row of the norm-rounding goldens: x[0] = 64, else 1."""
+    x = np.full(g["H"], 0x3F80, np.uint16)
+    x[0] = 0x4280
+    return x
+
+
+def check_router_norm_rounding_golden(lib):
+    """Hand-derived bits of n3 = bf16(bf16(bf16(x r) scale) bf16(H^-0.5)) on
+    a row where the bf16 scalar and the fp32 scalar, and a rounded and an
+    unrounded n, give different results (golden: router_norm_rounding.json)."""
+    g = load_golden("router_norm_rounding.json")
+    H = g["H"]
+    d = dataclasses.replace(small_dims(T=2, H=H, E=4, k=2), eps=g["eps"])
+    x = np.tile(_golden_row(g), (d.T, 1))
+    sc = np.full(H, 0x3F80, np.uint16)
+    sc[1], sc[2] = 0x3F10, 0x3F04
+    wr, _, pes = ms.make_router(d)
+    r = _route(lib, d, x, wr, sc, pes)
+    for h, want in g["normed_bits"].items():
+        got = r["normed"][:, int(h)]
+        assert np.all(got == int(want, 16)), f"normed[{h}] = {got[0]:#06x}, golden {want}"
+
 def check_router_zero_row(lib):
     """x = 0: every score is 0, the tie goes to the lowest ids and the
     softmax is uniform: w_j = bf16(bf16(1/k) * pes[j])."""
@@ -411,6 +435,18 @@ def check_rms_norm_constant_row(lib):
         assert np.array_equal(f64(got), sign * np.tile(f64(w), (2, 1))), f"constant row {c:#06x}, weight"
 
 
+
+def check_rms_norm_rounding_golden(lib):
+    """Hand-derived bits of bf16((x r) w) with x r kept in fp32 before the
+    weight (golden: rms_norm_rounding.json); rounding x r to bf16 first
+    gives different bits on this row."""
+    g = load_golden("rms_norm_rounding.json")
+    x = np.tile(_golden_row(g), (2, 1))
+    w = np.full(g["H"], 0x3FC0, np.uint16)
+    out = oracle.rms_norm(x, w, g["eps"], lib=lib)
+    for h, want in g["out_bits"].items():
+        assert np.all(out[:, int(h)] == int(want, 16)), f"rms_norm out[{h}] = {out[0, int(h)]:#06x}, golden {want}"
+
 def check_moe_branch_wiring(lib):
     """The branch is route(residual), experts(RMSNorm(residual, pre)) and
     RMSNorm(., post) of their output, composed from the parts pinned above:
@@ -543,12 +579,13 @@ def check_lm_head_symmetry_and_no_cap(lib):
 
 ALL_CHECKS = [
     check_bf16_from_float, check_bf16_from_double,
-    check_router_constant_row, check_router_zero_row, check_router_scale_invariance,
+    check_router_constant_row, check_router_norm_rounding_golden, check_router_zero_row, check_router_scale_invariance,
     check_router_exact_math, check_router_logits_topk, check_router_weights,
     check_dispatch,
     check_experts_brute_force, check_experts_one_hot, check_geglu_ties, check_single_expert_identity,
     check_expert_relabel, check_token_permutation,
-    check_rms_norm_exact_math, check_rms_norm_invariances, check_rms_norm_constant_row, check_moe_branch_wiring,
+    check_rms_norm_exact_math, check_rms_norm_invariances, check_rms_norm_constant_row, check_rms_norm_rounding_golden,
+    check_moe_branch_wiring,
     check_route_q4,
     check_dense_mlp_brute_force, check_dense_mlp_is_single_expert, check_dense_branch_wiring,
     check_self_conditioning_exact_math, check_self_conditioning_zero_mlp,

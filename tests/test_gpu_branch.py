@@ -59,7 +59,7 @@ def run_case(inp, rows=None, seed=0):
     g = gh.upload(inp)
     out, idx, w, xe = gpu_branch(g, pre, post)
     ref = gh.oracle_route(inp)
-    gh.check_routing(d, ref, idx, w)
+    gh.check_routing(d, ref, idx, w, inp.router_w)
     xe_ref = oracle.rms_norm(inp.x, pre, d.eps)
     check_expert_input(xe, xe_ref, f"T={d.T}")
     rows = np.arange(d.T) if rows is None else rows

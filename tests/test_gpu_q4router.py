@@ -25,6 +25,11 @@ def _built():
     oracle.build()
 
 
+def dequantised(rq, d):
+    """The 4-bit router weight dequantised independently (bf16 bits [E, H])."""
+    return oc.torch_bf16_bits(oc.dense_dequant(rq[0][None], rq[1][None], rq[2][None], d.H, d.group)[0])
+
+
 def upload_rq(rq):
     ts = (gh.dev32(rq[0]), gh.dev16(rq[1]), gh.dev16(rq[2]))
     return ts, moe.qweight(*ts)
@@ -48,8 +53,8 @@ def test_route_q4(name):
     _, rq_q = upload_rq(rq)
     idx, w = gpu_route_q4(g, rq_q)
     ref = oracle.route_q4(d, inp.x, rq, inp.router_scale, inp.pes, taps=True)
-    ties, differ = gh.check_routing(d, ref, idx, w)
-    print(f"{name} q4 router: near-tie tokens {ties}, differing {differ} of {d.T}")
+    c = gh.check_routing(d, ref, idx, w, dequantised(rq, d))
+    print(f"{name} q4 router: routing {c} of {d.T} tokens")
 
 
 def test_route_q4_equals_dense_on_dequantised_weight():
@@ -80,7 +85,7 @@ def test_forward_q4router():
     torch.cuda.synchronize()
     idx, w, out = idx.cpu().numpy(), gh.host16(w), gh.host16(out)
     ref = oracle.route_q4(d, inp.x, rq, inp.router_scale, inp.pes, taps=True)
-    gh.check_routing(d, ref, idx, w)
+    gh.check_routing(d, ref, idx, w, dequantised(rq, d))
     same = np.array([set(idx[t]) == set(ref["idx"][t]) for t in range(d.T)])
     want = gh.oracle_experts_rows(inp, ref["idx"], ref["w"], np.flatnonzero(same))
     print(f"canvas q4router forward: {gh.compare_out(out[same], want, 'q4router forward')}")

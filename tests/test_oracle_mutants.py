@@ -27,6 +27,9 @@ MUTANTS = {
     13: "dense branch's post norm takes the pre norm's weight",
     14: "head softcap is tanh(x) * cap",
     15: "head softcap reads the unrounded logit",
+    16: "router hidden**-0.5 scalar kept in fp32, not rounded to bf16",
+    17: "router norm output not rounded to bf16 before the scale multiply",
+    18: "RMSNorm with a weight rounds x*r to bf16 before the weight",
 }
 
 

@@ -3,10 +3,13 @@ library allocate (their device memory belongs to their own pool, or a
 cudaMalloc's device synchronisation is not affordable in their loop). It uses
 a fixed scratch array inside the library instead of a workspace.
 
-Checked through the C ABI against moe_experts, the allocating entry point,
-within the same tolerance as the other parity tests, on two calls in a row
-with different sizes (the second call reuses the scratch the first one left
-behind), and for the rejection of sizes beyond the fixed scratch. This file
+Checked through the C ABI against moe_experts, the allocating entry point:
+the two run the same kernels on the same inputs, so their outputs must be
+equal bit for bit (the statistics of the usual layer tolerance are printed
+too), on two calls in a row with different sizes (the second call reuses
+the scratch the first one left behind); a call with an out-of-range expert
+id after a large call (a stale inverse index left in the scratch must not
+be read); and the rejection of sizes beyond the fixed scratch. This file
 is collected last so that a run stopping at the first failure has already
 run every other test; it also passes alone in a fresh process.
 """
@@ -55,8 +58,30 @@ def test_noalloc_matches_allocating_call_twice(moe):
         idx, w = _routing(inp)
         got = _noalloc(moe, g, idx, w)
         want = gh.gpu_experts(g, idx, w)
-        gh.compare_out(got, want, f"noalloc {name}")
+        print(f"noalloc {name}: {gh.compare_out(got, want, f'noalloc {name}')}")
+        assert np.array_equal(got, want), f"noalloc {name}: output differs from moe_experts"
     assert moe.device_error() == 0
+
+
+def test_noalloc_bad_expert_after_large_call(moe):
+    """A canvas-sized call leaves its inverse permutation in the scratch; a
+    small call with an out-of-range id must drop that slot (adding nothing),
+    raise the error word and stay finite, equal to moe_experts with the slot
+    moved to a valid expert with weight 0."""
+    big = ms.make_layer("canvas", seed=22)
+    gb = gh.upload(big)
+    _noalloc(moe, gb, *_routing(big))
+    inp = ms.make_layer("canvas", T=8, seed=23)
+    g = gh.upload(inp)
+    idx, w = _routing(inp)
+    bad, zero_w = idx.copy(), w.copy()
+    bad[5, 2] = 300
+    zero_w[5, 2] = 0
+    moe.device_error()
+    got = _noalloc(moe, g, bad, w)
+    assert moe.device_error() & 2
+    assert np.all(np.isfinite(gh.f64(got)))
+    assert np.array_equal(got, gh.gpu_experts(g, idx, zero_w))
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(moe):
