@@ -10,7 +10,10 @@ its own batch (weak scaling, no collective on the data path).
 
 Prints ONE JSON line (rank 0). `value` is tokens/s with the inputs resident
 in HBM, timed with CUDA events around each layer call on its stream; L2 is
-flushed (256 MB memset) between steps, outside the timed events. `e2e` is the
+flushed between steps, outside the timed events (a 256 MB memset, then a
+256 MB read so that no dirty line of the flush is written back inside the
+timed region; --flush write keeps the memset alone). `workloads` times the
+layer's other workloads (decode, prefill, skew, tiny) the same way. `e2e` is the
 same metric through moe_forward_hostio (pinned host x in, host out, copies
 inside the timed call). `roofline` is for the dominant kernel (gate_up),
 timed with the library's own CUDA events on the launching stream.
@@ -190,6 +193,29 @@ class ClockSampler:
                     source="NVML every 2 ms during the timed region")
 
 
+class L2Flush:
+    """Between timed steps (outside the CUDA events): write a 256 MB buffer,
+    which evicts the 129 MB L2; with mode "write+read" (default) then read a
+    second 256 MB buffer, so the L2 holds clean lines of that buffer and the
+    flush's own dirty lines are written back before the timed region instead
+    of inside it."""
+
+    def __init__(self, mode: str = "write+read"):
+        import torch
+        self.mode = mode
+        self.wbuf = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        self.rbuf = torch.ones((256 << 20) // 8, dtype=torch.int64, device="cuda") if mode == "write+read" else None
+
+    def __call__(self):
+        self.wbuf.zero_()
+        if self.rbuf is not None:
+            self.rbuf.max()
+
+    def describe(self) -> str:
+        return ("flushed between steps outside the timed events: 256 MB memset"
+                + (", then a 256 MB read (clean L2)" if self.rbuf is not None else ""))
+
+
 def cores_available() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -292,6 +318,70 @@ def whole_job_rate(tokens_per_rank: int, world: int, seconds: float) -> float:
     return world * tokens_per_rank / seconds
 
 
+def time_workload(wl, rank, world, layer, head_inp, args, flush, stream, peaks, local, uuid):
+    """One moe_forward per step on workload `wl`, timed like the headline:
+    L2 flushed between steps outside the events, CUDA events around each
+    step on the launching stream, clocks sampled meanwhile. The expert
+    weights of the headline layer are reused when the layer is the same
+    (same sizes and seed: the generator gives the same bytes)."""
+    import torch
+    import bit_quantized_moe_layer_gb300 as moe
+    seed = wl.seed + rank
+    d0 = wl.dims
+    same = all(getattr(d0, f) == getattr(head_inp.dims, f) for f in ("H", "E", "inter", "group"))
+    if same:
+        x_h = ms.make_x(d0, seed, mu=wl.skew_mu)
+        wr, sc, pes = ms.make_router(d0, seed, kappa=wl.skew_kappa, zipf_s=wl.zipf_s)
+        t16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16).copy()).cuda()
+        lay = moe.DeviceLayer(t16(wr), t16(sc), t16(pes), layer.gu, layer.dn)
+    else:
+        full = ms.make_layer(wl, seed=seed)
+        x_h, lay = full.x, moe.to_device_layer(full)
+    d = moe.dims_of(d0)
+    x = torch.from_numpy(x_h.view(np.int16).copy()).cuda()
+    out = torch.empty((d.T, d.H), dtype=torch.int16, device="cuda")
+    idx = torch.empty((d.T, d.k), dtype=torch.int32, device="cuda")
+    wts = torch.empty((d.T, d.k), dtype=torch.int16, device="cuda")
+    ws = torch.empty(moe.workspace_bytes(d), dtype=torch.uint8, device="cuda")
+    step = lambda: moe.moe_forward(d, x, lay.router_w, lay.router_scale, lay.pes, lay.gate_up, lay.down, out, idx,
+                                   wts, ws, ws.numel(), stream)
+    steps = max(20, min(args.steps, 100))
+    for _ in range(args.warmup):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    touched = int(np.unique(idx.cpu().numpy()).size)
+    st = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    en = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    with ClockSampler(local, uuid) as clk:
+        for i in range(steps):
+            flush()
+            st[i].record(stream)
+            step()
+            en[i].record(stream)
+        torch.cuda.synchronize()
+    ms_step = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in zip(st, en)), world, "cuda")
+    moe.timing_enable(True)
+    for _ in range(steps):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    stage_ms, calls = moe.timing_read()
+    moe.timing_enable(False)
+    model = roofline_model(d0, touched, peaks)
+    gu_bytes, _ = layer_bytes(d0)
+    gu_ms = stage_ms["gate_up"] / max(1, calls)
+    return dict(workload=wl_desc(wl), steps=steps, ms_per_step=ms_step, value=whole_job_rate(d.T, world, ms_step * 1e-3),
+                unit="tokens/s", experts_touched=touched,
+                layer_roofline=dict(bound=model["bound"], t_roof_us=model["t_roof_s"] * 1e6,
+                                    frac=model["t_roof_s"] / (ms_step * 1e-3), bytes=model["bytes"],
+                                    flops=model["flops"]),
+                gate_up=dict(ms_per_launch=gu_ms, achieved_gbs=touched * gu_bytes / (gu_ms * 1e-3) / 1e9,
+                             achieved_tflops=(d.T * d.k * 2 * d.H * 2 * d.inter) / (gu_ms * 1e-3) / 1e12),
+                stages_ms_per_call={k: v / max(1, calls) for k, v in stage_ms.items()},
+                clocks=clk.summary(), gpu_launches=moe.launches_per_forward(d) * steps)
+
+
 def run_ours(args, wl):
     import torch
     import torch.distributed as dist
@@ -317,7 +407,7 @@ def run_ours(args, wl):
     idx = torch.empty((d.T, d.k), dtype=torch.int32, device="cuda")
     wts = torch.empty((d.T, d.k), dtype=torch.int16, device="cuda")
     ws = torch.empty(moe.workspace_bytes(d), dtype=torch.uint8, device="cuda")
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    flush = L2Flush(args.flush)
     stream = torch.cuda.current_stream()
 
     def step():
@@ -325,7 +415,7 @@ def run_ours(args, wl):
                         idx, wts, ws, ws.numel(), stream)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize()
     touched = int(np.unique(idx.cpu().numpy()).size)
@@ -344,7 +434,7 @@ def run_ours(args, wl):
     torch.cuda.synchronize()
     with ClockSampler(local, uuid) as clk:
         for i in range(args.steps):
-            flush.zero_()
+            flush()
             starts[i].record(stream)
             step()
             ends[i].record(stream)
@@ -356,7 +446,7 @@ def run_ours(args, wl):
     # and the per-launch roofline of the dominant kernel).
     moe.timing_enable(True)
     for i in range(args.steps):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize()
     stage_ms, calls = moe.timing_read()
@@ -370,7 +460,7 @@ def run_ours(args, wl):
     out_host = torch.empty((d.T, d.H), dtype=torch.int16).pin_memory()
     e2e_ms = []
     for i in range(args.warmup + args.steps):
-        flush.zero_()
+        flush()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         moe.moe_forward_hostio(d, x_host, layer.router_w, layer.router_scale, layer.pes, layer.gate_up,
@@ -383,17 +473,28 @@ def run_ours(args, wl):
         """Mean ms of `call` over the timed steps, like region 1 (L2 flushed
         between steps, events around each call on its stream)."""
         for _ in range(args.warmup):
-            flush.zero_()
+            flush()
             call()
         st = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         en = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         for i in range(args.steps):
-            flush.zero_()
+            flush()
             st[i].record(stream)
             call()
             en[i].record(stream)
         torch.cuda.synchronize()
         return max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in zip(st, en)), world, "cuda")
+
+    # The other workloads of the layer, each timed like the headline (L2
+    # flushed, events around each moe_forward on its stream, clocks sampled).
+    workloads = {}
+    if not args.no_workloads:
+        for name in ("decode", "prefill", "skew", "tiny"):
+            if name == wl.name:
+                continue
+            workloads[name] = time_workload(ms.WORKLOADS[name], rank, world, layer, inp, args, flush, stream,
+                                            peaks, local, uuid)
+        torch.cuda.synchronize()
 
     # The decoder layer's MoE branch (moe_forward_branch: the router on the
     # residual, the experts on preFfNorm2(residual), postFfNorm2 of their
@@ -444,7 +545,7 @@ def run_ours(args, wl):
     head_ms = timed(head_call)
     moe.timing_enable(True)
     for _ in range(args.steps):
-        flush.zero_()
+        flush()
         head_call()
     torch.cuda.synchronize()
     head_stage_ms, head_calls_n = moe.timing_read()
@@ -452,7 +553,7 @@ def run_ours(args, wl):
     del h_out, h_emb, qh
     moe.timing_enable(True)
     for _ in range(args.steps):
-        flush.zero_()
+        flush()
         dense_calls["mlp"]()
     torch.cuda.synchronize()
     dense_stage_ms, dense_calls_n = moe.timing_read()
@@ -482,7 +583,7 @@ def run_ours(args, wl):
         ms_per_step=ms_step, higher_is_better=True, scaling="weak", vs_baseline=None, dtype="bf16",
         data="synthetic (seeded; no checkpoint on the pages)",
         config=dict(workload=wl_desc(wl), global_batch=world * d.T, tokens_per_gpu=d.T, parallelism=f"replicas x{world}",
-                    l2="flushed between steps: 256 MB memset outside the timed events",
+                    l2=flush.describe(),
                     experts_touched=touched),
         roofline=dict(bound="hbm", achieved=achieved, peak=peaks["hbm"], unit="GB/s", frac=achieved / peaks["hbm"],
                       traffic=traffic_from_profile(f"gate_up:{wl.name}", src_hash), kernel="grouped_gemm gate_up",
@@ -503,6 +604,7 @@ def run_ours(args, wl):
         dense=dense_report(dn, dense_ms, dense_stage_ms, dense_calls_n, peaks, world),
         lm_head=head_report(d.T, d.H, ms.VOCAB, head_ms, head_stage_ms, head_calls_n, peaks, world),
         clocks=clk.summary(),
+        workloads=workloads,
         device_error=err,
     )
     print(json.dumps(line), flush=True)
@@ -519,6 +621,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=8.0)
+    ap.add_argument("--flush", default="write+read", choices=["write+read", "write"])
+    ap.add_argument("--no-workloads", action="store_true", help="skip the other workloads' lines")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -19,18 +19,24 @@
 //                 it waits for the A slot and the B slot, at an item's first
 //                 stage for a free accumulator buffer;
 //   warp 2        TMA producer of the B operand into a ring that the MMA's
-//                 completion releases. Token tiles of up to 64 rows load as
-//                 16-row, 64-wide blocks, the atoms (brows) x 128 B apart;
-//                 tiles of up to 128 rows as one 3-D copy a stage of its
-//                 four 64-wide atoms (a box of 16 to 128 rows, the smallest
-//                 that holds the tile), the atoms (box rows) x 128 B apart.
+//                 completion releases: one 3-D copy a stage of its four
+//                 64-wide atoms (a box of 16 to 128 rows, the smallest that
+//                 holds the tile), the atoms (box rows) x 128 B apart. (The
+//                 lockstep kernel for token tiles of up to 64 rows, used
+//                 when the weight ring is too shallow for the groups, loads
+//                 16-row, 64-wide blocks instead, the atoms brows x 128 B
+//                 apart.)
 //                 The slots are sized at run time for the largest token
 //                 tile of the call, so small tiles get a deep ring;
-//   dequant warps 8 warps, thread = weight row = TMEM lane; warp (q, p)
-//                 dequantises atoms 2p and 2p + 1 (64 K each) of lane
-//                 quarter q of every stage into the next slot of a ring of A
-//                 slots in TMEM (tcgen05.st), so the dequantisation runs up
-//                 to a few stages ahead of the MMA. A packed word holds 8
+//   dequant warps thread = weight row = TMEM lane. Token tiles of up to 64
+//                 rows: 3 groups of 4 warps (one per TMEM lane quarter);
+//                 group r takes every stage g with g % 3 == r, all four
+//                 atoms of its quarter, into A slot r, so the two or three
+//                 dequant warps sharing a scheduler work on different stages
+//                 and one covers the other's barrier waits. Tiles of up to
+//                 128 rows: 8 warps in lockstep, warp (q, p) dequantises
+//                 atoms 2p and 2p + 1 (64 K each) of lane quarter q of every
+//                 stage into the next of 2 A slots. A packed word holds 8
 //                 codes; the 0x4300 magic
 //                 gives 128+q per bf16 half, minus 128 gives q exactly, and
 //                 one fma.rn.bf16x2 with the group's scale and bias gives
@@ -143,14 +149,24 @@ __device__ __forceinline__ void dequant_atom(const uint4 c0, const uint4 c1, uin
 
 }  // namespace
 
-// NA A slots in TMEM (a ring the dequant warps fill ahead of the MMA), APW
-// atoms of a stage per dequant warp (16 / APW dequant warps), EPW epilogue
-// warps per TMEM lane quarter.
-template <int MODE, int NMAX, int NA, int APW, int EPW>
-__global__ void __launch_bounds__((3 + 16 / APW + 4 * EPW) * 32, 1)
+// NA A slots in TMEM (a ring the dequant warps fill ahead of the MMA), EPW
+// epilogue warps per TMEM lane quarter. GROUPS: NA groups of 4 dequant
+// warps, group r taking the stages g with g % NA == r into A slot r (each
+// warp all four atoms of its lane quarter); otherwise 16 / APW dequant
+// warps in lockstep, APW atoms of every stage each.
+template <int NA, int APW, bool GROUPS>
+__host__ __device__ constexpr int dequant_warps() {
+    return GROUPS ? 4 * NA : 16 / APW;
+}
+
+template <int MODE, int NMAX, int NA, int APW, int EPW, bool GROUPS>
+__global__ void __launch_bounds__((3 + dequant_warps<NA, APW, GROUPS>() + 4 * EPW) * 32, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ BMaps bmaps,
                         GemmArgs a) {
-    constexpr int kDqWarps = 16 / APW;
+    constexpr int kDqWarps = dequant_warps<NA, APW, GROUPS>();
+    // one 3-D box a token stage (the lockstep kernel for tiles of up to 64
+    // rows loads 16-row blocks)
+    constexpr bool kBox3 = NMAX > 64 || GROUPS;
     constexpr int kEpiWarp0 = 3 + kDqWarps;
     constexpr int kEpiWarps = 4 * EPW;
     constexpr int kAccChunks = NMAX / 16 / EPW;  // 16-column chunks of one epilogue warp
@@ -207,14 +223,14 @@ __global__ void __launch_bounds__((3 + 16 / APW + 4 * EPW) * 32, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < NP; ++s) {
             mbar_init(&sh.wfull[s], 1);
-            mbar_init(&sh.wempty[s], kDqWarps);  // every dequant warp reads every stage
+            mbar_init(&sh.wempty[s], GROUPS ? 4 : kDqWarps);  // the warps that read the stage
         }
         for (int s = 0; s < NB; ++s) {
             mbar_init(&sh.bfull[s], 1);
             mbar_init(&sh.bempty[s], 1);
         }
         for (int i = 0; i < NA; ++i) {
-            mbar_init(&sh.afull[i], kDqWarps);
+            mbar_init(&sh.afull[i], GROUPS ? 4 : kDqWarps);  // the warps that write the slot
             mbar_init(&sh.aempty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -320,7 +336,7 @@ __global__ void __launch_bounds__((3 + 16 / APW + 4 * EPW) * 32, 1)
                 if (!(ok = mbar_wait(&sh.bempty[slot], ph ^ 1, abort_flag, kSleepRing, 3))) break;
                 uint8_t* bst = bring + (size_t)slot * bslot_bytes;
                 if (elect_one()) {
-                    if constexpr (NMAX > 64) {
+                    if constexpr (kBox3) {
                         mbar_arrive_expect_tx(&sh.bfull[slot], box_bytes);
                         tma_load_3d(bst, &bmaps.m[bi], &sh.bfull[slot], 0, tl.p0, s * (kStageK / 64));
                     } else {
@@ -366,7 +382,7 @@ __global__ void __launch_bounds__((3 + 16 / APW + 4 * EPW) * 32, 1)
             const uint32_t idesc = idesc_bf16_m128(nrows16);
             // distance of the B slot's atoms in descriptor units (16 B)
             const uint32_t atom_step =
-                (uint32_t)(((NMAX > 64) ? (16 << bbox_index(tl.rows)) : brows) * 128) >> 4;
+                (uint32_t)((kBox3 ? (16 << bbox_index(tl.rows)) : brows) * 128) >> 4;
             const int db = li & 1;
             const uint32_t dcol = tmem + kD0 + (uint32_t)(db * NMAX);
             // the accumulator buffer's previous item (li - 2) has been read out
@@ -405,7 +421,82 @@ __global__ void __launch_bounds__((3 + 16 / APW + 4 * EPW) * 32, 1)
         if (elect_one()) umma_commit(&sh.mdrain);
         __syncwarp();
         mbar_drain(&sh.mdrain, 0);
-    } else if (warp >= 3 && warp < kEpiWarp0) {
+    } else if (GROUPS && warp >= 3 && warp < kEpiWarp0) {
+        // ------------------------------------------- dequant, stage groups --
+        // Warp (q, r): TMEM lanes 32q..32q+31 (q = warp % 4, the lane quarter
+        // a warp may access), every stage g (counted over this CTA's items)
+        // with g % NA == r, all four atoms, into A slot r. Phase safety: a
+        // group waits for stage g's weights only after the MMA of stage
+        // g - 2 NA has completed (its previous stage waited for that A slot),
+        // so every stage up to g - 2 NA has landed; the host launches this
+        // kernel only with at least 2 NA weight stages, so the slot of stage
+        // g is at most one phase behind when the group waits on it.
+        const int q = warp & 3;
+        const int grp = (warp - 3) >> 2;
+        int row;  // row in the packed stage and the scale buffer
+        if (MODE == kGateUp)
+            row = (lane < 16) ? (16 * q + lane) : (64 + 16 * q + (lane - 16));
+        else
+            row = 32 * q + lane;
+        const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
+        // this thread's 128-byte row in ring slot 0, its 8 chunks swizzled
+        uint32_t wo[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            wo[i] = smem_u32(wring) + (uint32_t)row * 128u + ((uint32_t)(i ^ (row & 7)) << 4);
+        const uint32_t srow = smem_u32(scale_base) + (uint32_t)(row * G) * 2u;
+        const uint32_t bias_off = (uint32_t)(128 * G * 2);
+        const uint32_t acol = tmem + lane_addr + (uint32_t)grp * 128u;
+        bool ok = true;
+        int li = 0;
+        uint32_t gbase = 0;  // stages of this CTA's earlier items
+        for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x, ++li, gbase += (uint32_t)nstages) {
+            const int sb = li & 1;
+            if (!(ok = mbar_wait(&sh.sfull[sb], (li >> 1) & 1, abort_flag, 0, 8))) break;
+            const uint32_t sS = srow + (uint32_t)(sb * sbuf_bytes);
+            const int s0 = (grp - (int)(gbase % NA) + NA) % NA;  // first stage of the item that is ours
+            if (s0 >= nstages) mbar_arrive_lane0(&sh.sempty[sb]);  // none: release the scales at once
+            for (int s = s0; s < nstages; s += NA) {
+                const uint32_t g = gbase + (uint32_t)s;
+                const int atoms = min(kStageK, K - s * kStageK) / 64;
+                const uint32_t wslot = g % (uint32_t)NP;
+                if (!(ok = mbar_wait(&sh.wfull[wslot], (g / NP) & 1, abort_flag, 0, 9))) break;
+                uint4 c[8];
+                uint32_t S1[4], B1[4];
+                const uint32_t so = wslot * (uint32_t)kPackedStageBytes;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if (i < atoms) {  // warp-uniform
+                        c[2 * i] = lds128(wo[2 * i] + so);
+                        c[2 * i + 1] = lds128(wo[2 * i + 1] + so);
+                        S1[i] = lds_u16(sS + (uint32_t)(8 * s + 2 * i));
+                        B1[i] = lds_u16(sS + bias_off + (uint32_t)(8 * s + 2 * i));
+                    }
+                }
+                // The arrive releases the loads above: the slot (and, after
+                // this warp's last stage of the item, the scale buffer) may
+                // be refilled.
+                __syncwarp();
+                mbar_arrive_lane0(&sh.wempty[wslot]);
+                if (s + NA >= nstages) mbar_arrive_lane0(&sh.sempty[sb]);
+                if (!(ok = mbar_wait(&sh.aempty[grp], ((g / NA) & 1) ^ 1, abort_flag, 0, 10))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if (i < atoms) {
+                        uint32_t r[32];
+                        dequant_atom(c[2 * i], c[2 * i + 1], S1[i], B1[i], r);
+                        tmem_st32(acol + i * 32, r);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                mbar_arrive_lane0(&sh.afull[grp]);
+            }
+        }
+        tmem_wait_st();
+    } else if (!GROUPS && warp >= 3 && warp < kEpiWarp0) {
         // ------------------------------------------------------- dequant --
         // 16 / APW warps; warp (q, p) covers TMEM lanes 32q..32q+31 (q =
         // warp % 4, the lane quarter a warp may access) and atoms p APW ..
@@ -589,33 +680,41 @@ void gemm_stages(int K, int nmax, int* wstages, int* bregion) {
     *bregion = (int)((limit - gemm_smem_bytes(K, nw, 0)) & ~size_t(1023));
 }
 
-template <int MODE, int NMAX, int NA, int APW, int EPW>
+template <int MODE, int NMAX, int NA, int APW, int EPW, bool GROUPS>
 static cudaError_t launch_one(const CUtensorMap& wmap, const BMaps& bmaps, const GemmArgs& a, int grid,
                               size_t smem, cudaStream_t stream) {
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    auto kernel = grouped_gemm_kernel<MODE, NMAX, NA, APW, EPW, GROUPS>;
     if (!attr_set[dev]) {
-        cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, NMAX, NA, APW, EPW>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, 232448 - 2048);
+        cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448 - 2048);
         if (err != cudaSuccess) return err;
         attr_set[dev] = true;
     }
-    return launch_pdl(grouped_gemm_kernel<MODE, NMAX, NA, APW, EPW>, dim3(grid), dim3((3 + 16 / APW + 4 * EPW) * 32),
-                      smem, stream, wmap, bmaps, a);
+    constexpr int warps = 3 + dequant_warps<NA, APW, GROUPS>() + 4 * EPW;
+    return launch_pdl(kernel, dim3(grid), dim3(warps * 32), smem, stream, wmap, bmaps, a);
 }
 
 template <int MODE>
 static cudaError_t launch_mode(const CUtensorMap& wmap, const BMaps& bmaps, const GemmArgs& a, int grid,
                                size_t smem, cudaStream_t stream) {
-    // Eight dequant warps of two atoms each (fewer warps than one atom each:
-    // less barrier traffic per byte, measured faster). Token tiles of up to
-    // 64: three A slots and 4 epilogue warps (15 warps); up to 128: two A
-    // slots (TMEM holds 2 x 128 accumulator columns) and 8 epilogue warps, as
-    // a 128-token tile's GeGLU needs the wider epilogue (19 warps).
-    if (a.nmax == 64) return launch_one<MODE, 64, 3, 2, 1>(wmap, bmaps, a, grid, smem, stream);
-    if (a.nmax == 128) return launch_one<MODE, 128, 2, 2, 2>(wmap, bmaps, a, grid, smem, stream);
+    // Token tiles of up to 128 rows: two A slots (TMEM holds 2 x 128
+    // accumulator columns), eight lockstep dequant warps of two atoms each
+    // and 8 epilogue warps, as a 128-token tile's GeGLU needs the wider
+    // epilogue (19 warps; stage groups measured no faster here).
+    //
+    // Token tiles of up to 64 rows: three stage groups of four dequant warps
+    // (12), one 3-D token box a stage (canvas gate_up 90 -> 76 us, down 51
+    // -> 47, decode gate_up 43 -> 37, measured standalone), when the weight
+    // ring holds at least 6 stages (the groups' phase-safety condition);
+    // otherwise the lockstep kernel.
+    if (a.nmax == 64) {
+        if (a.wstages >= 2 * 3) return launch_one<MODE, 64, 3, 2, 1, true>(wmap, bmaps, a, grid, smem, stream);
+        return launch_one<MODE, 64, 3, 2, 1, false>(wmap, bmaps, a, grid, smem, stream);
+    }
+    if (a.nmax == 128) return launch_one<MODE, 128, 2, 2, 2, false>(wmap, bmaps, a, grid, smem, stream);
     return cudaErrorInvalidValue;
 }
 

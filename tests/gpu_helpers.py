@@ -230,20 +230,66 @@ def workspace_dispatch(d, ws: torch.Tensor):
     return take(m.perm, S), take(m.offsets, d.E + 1), take(m.inv, S)
 
 
-def compare_out(gpu_bits: np.ndarray, ref_bits: np.ndarray, what: str = "out") -> dict:
+def bf16_round(v) -> np.ndarray:
+    """float32-exact values -> nearest bf16 (torch's rounding), as float64."""
+    t = torch.from_numpy(np.ascontiguousarray(v, dtype=np.float32)).to(torch.bfloat16)
+    return t.to(torch.float64).numpy()
+
+
+def compare_out(gpu_bits: np.ndarray, ref_bits: np.ndarray, what: str = "out", explain=None) -> dict:
+    """Layer output against the oracle's. Tier 1, per element:
+    |gpu - oracle| <= max(2e-2 RMS, 1 bf16 ulp of the oracle value). An
+    element beyond tier 1 must be explained by the accumulation order alone
+    (tier 2): out = bf16(sum_j bf16(y_j w_j)), and each bf16 y_j that the GPU
+    accumulates in fp32 may round one ulp away from the oracle's exactly
+    rounded y_j, so |gpu - oracle| <= ulp(out) + sum_j (w_j ulp(y_j) +
+    ulp(bf16(y_j w_j)) + |y_j| dw_j), dw_j the routing-weight difference.
+    `explain(rows)` returns the oracle's y [rows, k, H], w [rows, k] and the
+    weight differences dw [rows, k] of those token rows; without it tier 1
+    is final. The RMS error stays <= 1e-3 RMS."""
     g, o = f64(gpu_bits), f64(ref_bits)
     rms = float(np.sqrt(np.mean(o * o)))
     err = np.abs(g - o)
     tol = np.maximum(2e-2 * rms, bf16_ulp(o))
-    bad = np.flatnonzero((err > tol).ravel())
+    bad = np.argwhere(err > tol)
     stats = dict(rms=rms, max_err_over_rms=float(err.max() / rms) if err.size else 0.0,
                  rms_err_over_rms=float(np.sqrt(np.mean(err ** 2)) / rms) if err.size else 0.0,
-                 n_strict=int((err > 2e-2 * rms).sum()), n_diff=int((err > 0).sum()), n=int(err.size))
+                 n_strict=int((err > 2e-2 * rms).sum()), n_diff=int((err > 0).sum()), n=int(err.size),
+                 n_tier2=int(len(bad)))
     assert np.all(np.isfinite(g)), f"{what}: non-finite GPU output"
-    assert bad.size == 0, (f"{what}: {bad.size} elements beyond tolerance; first flat index {bad[0]}: "
-                           f"gpu {g.ravel()[bad[0]]} oracle {o.ravel()[bad[0]]} (rms {rms}) {stats}")
+    if len(bad):
+        first = tuple(bad[0])
+        msg = (f"{what}: {len(bad)} elements beyond max(2e-2 RMS, 1 ulp); first {first}: gpu {g[first]} "
+               f"oracle {o[first]} (rms {rms}) {stats}")
+        assert explain is not None, msg
+        rows = np.unique(bad[:, 0])
+        y, w, dw = explain(rows)
+        at = {r: i for i, r in enumerate(rows)}
+        for r, h in bad:
+            i = at[r]
+            yj, wj = y[i, :, h], w[i]
+            p = bf16_round(yj * wj)
+            bound = float(bf16_ulp(np.array([o[r, h]]))[0] + np.sum(wj * bf16_ulp(yj) + bf16_ulp(p) +
+                                                                   np.abs(yj) * dw[i]))
+            assert err[r, h] <= bound, f"{msg}; element ({r}, {h}) error {err[r, h]} > tier-2 bound {bound}"
     assert stats["rms_err_over_rms"] <= 1e-3, f"{what}: RMS error too large {stats}"
     return stats
+
+
+def explainer(inp: ms.LayerInputs, idx: np.ndarray, w: np.ndarray, w_gpu: np.ndarray | None = None):
+    """The oracle's per-slot expert outputs y and routing weights for given
+    token rows (and the GPU's routing-weight differences), for compare_out's
+    tier-2 check."""
+    d = inp.dims
+
+    def f(rows):
+        sub = dataclasses.replace(d, T=len(rows))
+        _, _, _, y = oracle.experts(sub, inp.x[rows], idx[rows], w[rows], (inp.gu_w, inp.gu_s, inp.gu_b),
+                                    (inp.dn_w, inp.dn_s, inp.dn_b), taps=True)
+        wf = f64(w[rows])
+        dw = np.zeros_like(wf) if w_gpu is None else np.abs(f64(w_gpu[rows]) - wf)
+        return f64(y).reshape(len(rows), d.k, d.H), wf, dw
+    return f
 
 
 def oracle_route(inp: ms.LayerInputs):

@@ -52,6 +52,21 @@ def oracle_out(name):
     return _oracle_out[name]
 
 
+def gpu_weights_in_oracle_order(idx, w, ref_idx, rows):
+    """The GPU's routing weights rearranged into the oracle's expert order,
+    for tokens whose expert sets agree (all others zero)."""
+    out = np.zeros(ref_idx.shape, np.uint16)
+    for t in rows:
+        pos = {e: j for j, e in enumerate(idx[t].tolist())}
+        out[t] = [w[t, pos[e]] for e in ref_idx[t].tolist()]
+    return out
+
+
+def sub_explainer(explain, rows):
+    """An explainer for a comparison restricted to `rows` (indices into it)."""
+    return lambda r: explain(rows[r])
+
+
 def sample_rows(T, n=48, seed=0):
     if T <= n:
         return np.arange(T)
@@ -104,7 +119,7 @@ def test_experts(name):
     """The experts path alone, fed the oracle's routing; every token."""
     inp, g, ref = layer(name)
     out = gh.gpu_experts(g, ref["idx"], ref["w"])
-    stats = gh.compare_out(out, oracle_out(name), f"{name} experts")
+    stats = gh.compare_out(out, oracle_out(name), f"{name} experts", gh.explainer(inp, ref["idx"], ref["w"]))
     print(f"{name} experts: {stats}")
 
 
@@ -116,7 +131,10 @@ def test_forward(name):
     out, idx, w = gh.gpu_forward(g)
     c = gh.check_routing(inp.dims, ref, idx, w, inp.router_w)
     same = np.array([set(idx[t]) == set(ref["idx"][t]) for t in range(inp.dims.T)])
-    stats = gh.compare_out(out[same], oracle_out(name)[same], f"{name} forward")
+    rows = np.flatnonzero(same)
+    w_gpu = gpu_weights_in_oracle_order(idx, w, ref["idx"], rows)
+    stats = gh.compare_out(out[rows], oracle_out(name)[rows], f"{name} forward",
+                           sub_explainer(gh.explainer(inp, ref["idx"], ref["w"], w_gpu), rows))
     print(f"{name} forward: routing {c}, output {stats}")
 
 
@@ -165,7 +183,8 @@ def test_experts_dispatch_edges_bit_exact(case):
     operm, ooff, oinv = oracle.dispatch(d.T, d.k, d.E, idx)
     assert np.array_equal(off, ooff) and np.array_equal(perm, operm) and np.array_equal(inv, oinv)
     rows = sample_rows(d.T, 64, seed=3)
-    gh.compare_out(out[rows], gh.oracle_experts_rows(inp, idx, w, rows), f"edge {case}")
+    gh.compare_out(out[rows], gh.oracle_experts_rows(inp, idx, w, rows), f"edge {case}",
+                   sub_explainer(gh.explainer(inp, idx, w), rows))
 
 
 @pytest.mark.parametrize("T", [1, 17, 33, 130])
@@ -177,8 +196,10 @@ def test_ragged_token_counts(T):
     out, idx, w = gh.gpu_forward(g)
     gh.check_routing(inp.dims, ref, idx, w, inp.router_w)
     same = np.array([set(idx[t]) == set(ref["idx"][t]) for t in range(T)])
-    want = gh.oracle_experts_rows(inp, ref["idx"], ref["w"], np.flatnonzero(same))
-    gh.compare_out(out[same], want, f"T={T}")
+    rows = np.flatnonzero(same)
+    want = gh.oracle_experts_rows(inp, ref["idx"], ref["w"], rows)
+    w_gpu = gpu_weights_in_oracle_order(idx, w, ref["idx"], rows)
+    gh.compare_out(out[rows], want, f"T={T}", sub_explainer(gh.explainer(inp, ref["idx"], ref["w"], w_gpu), rows))
 
 
 def test_tiny_layer_ragged():
@@ -186,7 +207,8 @@ def test_tiny_layer_ragged():
     g = gh.upload(inp)
     ref = gh.oracle_route(inp)
     out = gh.gpu_experts(g, ref["idx"], ref["w"])
-    gh.compare_out(out, gh.oracle_experts_rows(inp, ref["idx"], ref["w"]), "tiny T=37")
+    gh.compare_out(out, gh.oracle_experts_rows(inp, ref["idx"], ref["w"]), "tiny T=37",
+                   gh.explainer(inp, ref["idx"], ref["w"]))
 
 
 def test_many_rows_one_expert():
@@ -200,7 +222,8 @@ def test_many_rows_one_expert():
     w = ms.bf16_bits(rng.uniform(0.05, 0.3, (300, 8)))
     out = gh.gpu_experts(g, idx, w)
     rows = sample_rows(300, 40, seed=2)
-    gh.compare_out(out[rows], gh.oracle_experts_rows(inp, idx, w, rows), "many rows one expert")
+    gh.compare_out(out[rows], gh.oracle_experts_rows(inp, idx, w, rows), "many rows one expert",
+                   sub_explainer(gh.explainer(inp, idx, w), rows))
 
 
 def test_single_expert_identity():
