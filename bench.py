@@ -494,7 +494,22 @@ def run_ours(args, wl):
                 continue
             workloads[name] = time_workload(ms.WORKLOADS[name], rank, world, layer, inp, args, flush, stream,
                                             peaks, local, uuid)
+        # the decode step through the small-token dequant-GEMV path instead
+        # of the tensor-core grouped GEMM (moe_set_small_t_path(1))
+        prev = moe.set_small_t_path(1)
+        try:
+            workloads["decode_gemv_path"] = time_workload(ms.WORKLOADS["decode"], rank, world, layer, inp, args,
+                                                          flush, stream, peaks, local, uuid)
+        finally:
+            moe.set_small_t_path(prev)
         torch.cuda.synchronize()
+
+    if args.layer_only:
+        emit_line(args, wl, inp, d, world, rank, peaks, touched, ms_step, stage_ms, calls, clk, e2e_step, workloads,
+                  err, flush, None)
+        if world > 1:
+            dist.destroy_process_group()
+        return
 
     # The decoder layer's MoE branch (moe_forward_branch: the router on the
     # residual, the experts on preFfNorm2(residual), postFfNorm2 of their
@@ -560,11 +575,25 @@ def run_ours(args, wl):
     moe.timing_enable(False)
     err |= moe.device_error()
 
-    if rank != 0:
-        if world > 1:
-            dist.destroy_process_group()
-        return
+    extras = dict(
+        branch=dict(call="moe_forward_branch (router on the residual, experts on preFfNorm2, postFfNorm2)",
+                    ms_per_step=branch_ms, value=whole_job_rate(d.T, world, branch_ms * 1e-3), unit="tokens/s"),
+        q4router=dict(call="moe_forward_q4router (the layer with the 4-bit group-64 router projection)",
+                      ms_per_step=q4_ms, value=whole_job_rate(d.T, world, q4_ms * 1e-3), unit="tokens/s"),
+        dense=dense_report(dn, dense_ms, dense_stage_ms, dense_calls_n, peaks, world),
+        lm_head=head_report(d.T, d.H, ms.VOCAB, head_ms, head_stage_ms, head_calls_n, peaks, world))
+    emit_line(args, wl, inp, d, world, rank, peaks, touched, ms_step, stage_ms, calls, clk, e2e_step, workloads,
+              err, flush, extras)
+    if world > 1:
+        dist.destroy_process_group()
 
+
+def emit_line(args, wl, inp, d, world, rank, peaks, touched, ms_step, stage_ms, calls, clk, e2e_step, workloads,
+              err, flush, extras):
+    """Rank 0 prints the one JSON line."""
+    import bit_quantized_moe_layer_gb300 as moe
+    if rank != 0:
+        return
     gu_bytes, dn_bytes = layer_bytes(inp.dims)
     gu_ms = stage_ms["gate_up"] / max(1, calls)
     achieved = touched * gu_bytes / (gu_ms * 1e-3) / 1e9
@@ -597,19 +626,12 @@ def run_ours(args, wl):
         e2e=dict(value=whole_job_rate(d.T, world, e2e_step * 1e-3), unit="tokens/s", h2d_bytes_per_step=d.T * d.H * 2,
                  d2h_bytes_per_step=d.T * d.H * 2, ms_per_step=e2e_step),
         gpu_launches=moe.launches_per_forward(d) * args.steps,
-        branch=dict(call="moe_forward_branch (router on the residual, experts on preFfNorm2, postFfNorm2)",
-                    ms_per_step=branch_ms, value=whole_job_rate(d.T, world, branch_ms * 1e-3), unit="tokens/s"),
-        q4router=dict(call="moe_forward_q4router (the layer with the 4-bit group-64 router projection)",
-                      ms_per_step=q4_ms, value=whole_job_rate(d.T, world, q4_ms * 1e-3), unit="tokens/s"),
-        dense=dense_report(dn, dense_ms, dense_stage_ms, dense_calls_n, peaks, world),
-        lm_head=head_report(d.T, d.H, ms.VOCAB, head_ms, head_stage_ms, head_calls_n, peaks, world),
+        **(extras or {}),
         clocks=clk.summary(),
         workloads=workloads,
         device_error=err,
     )
     print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
 
 
 def main():
@@ -623,6 +645,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=8.0)
     ap.add_argument("--flush", default="write+read", choices=["write+read", "write"])
     ap.add_argument("--no-workloads", action="store_true", help="skip the other workloads' lines")
+    ap.add_argument("--layer-only", action="store_true",
+                    help="time the layer alone (no MoE branch, 4-bit router, dense MLP or head lines)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

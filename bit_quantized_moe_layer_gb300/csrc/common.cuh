@@ -352,6 +352,55 @@ __device__ __forceinline__ void cluster_barrier() {
     asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
+// ------------------------------------------------------ GeGLU, K order --
+// bf16(gelu_approx(g) * up) for bf16 g, up, where gelu_approx(g) =
+// 0.5 g (1 + tanh(s)), s = sqrt(2/pi) (g + 0.044715 g^3). 0.5 (1 + tanh s) is
+// the logistic of 2s, evaluated in that form so it keeps its relative
+// accuracy where 1 + tanh(s) cancels (s << 0). p = g*up is exact in fp32.
+// r = e / (1 + e) with e = exp(-2|s|): for s < 0 it is the logistic of 2s
+// and the value is p r; for s >= 0 it is 1 - logistic(2s) > 0 and the value
+// is p - p r, formed by a fused multiply-add rounded toward zero: the exact
+// value lies strictly between 0 and p, so an exact bf16 tie of p (large g,
+// where r is below fp32's resolution of 1) rounds toward zero as the exact
+// value does. One exp and one divide serve both signs. For e <= 2^-25,
+// 1 + e rounds to 1 and the quotient is e itself: taking e skips the
+// divide's slow path for subnormal e (far tails of s), with the same result.
+__device__ __forceinline__ uint32_t geglu_bf16(float g, float up) {
+    const float c = 0.7978845608028654f;  // sqrt(2/pi)
+    const float s = __fmul_rn(c, __fadd_rn(g, __fmul_rn(0.044715f, __fmul_rn(g, __fmul_rn(g, g)))));
+    const float p = __fmul_rn(g, up);
+    const float e = expf(__fmul_rn(-2.0f, fabsf(s)));
+    const float r = (e <= 0x1p-25f) ? e : __fdiv_rn(e, __fadd_rn(1.0f, e));
+    const float m = (s < 0.f) ? __fmul_rn(p, r) : __fmaf_rz(-p, fmaxf(r, 1e-30f), p);
+    return f32_to_bf16_bits(m);
+}
+
+// Position of element n inside its 8-block in the interleaved K order.
+__device__ __forceinline__ int interleaved_pos(int n) {
+    const int r = n & 7;
+    return (n & ~7) | (r < 4 ? 2 * r : 2 * r - 7);
+}
+
+// ------------------------------------------------------------- dequant --
+// Dequantise one 64-wide K atom (8 packed words) of a weight row with its
+// group's scale and bias (bf16 bits) into 32 bf16x2 TMEM columns.
+__device__ __forceinline__ void dequant_atom(const uint4 c0, const uint4 c1, uint32_t S1, uint32_t B1,
+                                             uint32_t (&r)[32]) {
+    const uint32_t S2 = S1 | (S1 << 16), B2 = B1 | (B1 << 16);
+    const uint32_t wd[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t w = wd[i];
+        const uint32_t sh4[4] = {w, w >> 4, w >> 8, w >> 12};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t t = lop3_and_or(sh4[c], 0x000F000Fu, 0x43004300u);  // 128+q
+            const uint32_t qv = fma_bf16x2(t, 0x3F803F80u, 0xC300C300u);       // q exactly
+            r[4 * i + c] = fma_bf16x2(qv, S2, B2);                            // bf16(S q + B)
+        }
+    }
+}
+
 // ------------------------------------------------------------ row norms --
 // 8 bf16 (one 16-byte chunk) -> positions holding elements (0,4,1,5,2,6,3,7):
 // the K order in which the grouped GEMM's dequantised weights come out.

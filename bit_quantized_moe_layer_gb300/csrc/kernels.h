@@ -169,4 +169,17 @@ cudaError_t launch_gemm(int mode, const CUtensorMap& wmap, const BMaps& bmaps, c
                         cudaStream_t stream);
 int gemm_error_word();
 
+// Small-token dequant-GEMV (a few rows per expert): the same work items as
+// the grouped GEMM with token tiles of up to kGemvRows rows, the products
+// taken group-factored in fp32 on the CUDA cores, x = xs (gate_up, GeGLU
+// epilogue into mid) or mid (down, y by sorted row). a.w serves only the L2
+// warm-up, a.bregion is unused; a.wstages from gemv_stages(K); a.nmax must
+// be kGemvRows.
+constexpr int kGemvRows = 4;
+size_t gemv_smem_bytes(int K, int wstages);
+int gemv_stages(int K);  // weight-ring depth that fits (0: K too large)
+cudaError_t launch_gemv(int mode, const CUtensorMap& wmap, const GemmArgs& a, const uint16_t* xsrc, int grid,
+                        cudaStream_t stream);
+int gemv_error_word();
+
 }  // namespace moe

@@ -12,6 +12,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -152,7 +153,7 @@ Layout layout(const moe_dims* d) {
         o = up256(o + (bytes ? bytes : 1));
         return at;
     };
-    L.max_tiles = d->E + (int)((S + 15) / 16);
+    L.max_tiles = d->E + (int)((S + kGemvRows - 1) / kGemvRows);  // token tiles of >= kGemvRows rows
     L.idx = take(S * 4);
     L.w = take(S * 2);
     L.perm = take(S * 4);
@@ -224,6 +225,18 @@ struct CallTimer {
 int fail(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 // ------------------------------------------------------------- pipeline --
+// Small-token path (moe_set_small_t_path): 0 = the tcgen05 grouped GEMM for
+// every call; 1 = the dequant-GEMV for calls with at most two slots per
+// expert on average, when its buffers fit the shared memory at both K (H
+// for gate_up, inter for down).
+std::atomic<int> g_small_t_path{0};
+
+bool use_gemv(const moe_dims* d) {
+    const long S = (long)d->T * d->k;
+    return g_small_t_path.load(std::memory_order_relaxed) == 1 && S <= 2L * d->E && gemv_stages(d->H) >= 2 &&
+           gemv_stages(d->inter) >= 2;
+}
+
 int run_experts(const moe_dims* d, const uint16_t* x, const int32_t* idx, const uint16_t* w,
                 const moe_qweight* gu, const moe_qweight* dn, uint16_t* out, uint8_t* ws, const Layout& L,
                 const DeviceInfo& di, cudaStream_t s, CallTimer& tm, const uint16_t* post_norm_w = nullptr) {
@@ -237,13 +250,17 @@ int run_experts(const moe_dims* d, const uint16_t* x, const int32_t* idx, const 
     uint16_t* xs = reinterpret_cast<uint16_t*>(ws + L.xs);
     uint16_t* mid = reinterpret_cast<uint16_t*>(ws + L.mid);
     uint16_t* y = reinterpret_cast<uint16_t*>(ws + L.y);
-    const int nmax = (S / E > 40) ? 128 : 64;
+    // A few rows per expert (a decode step): the dequant-GEMV path, which
+    // streams the weights without padding the tokens to a tensor-core tile;
+    // otherwise the tcgen05 grouped GEMM with token tiles of 64 or 128 rows.
+    const bool gemv = use_gemv(d);
+    const int nmax = gemv ? kGemvRows : (S / E > 40) ? 128 : 64;
 
     CUtensorMap m_gu, m_dn;
     BMaps m_xs, m_mid;
     if (!make_map_2d(&m_gu, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, gu->w, H / 8, (uint64_t)E * 2 * I, 32, 64) ||
         !make_map_2d(&m_dn, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, dn->w, I / 8, (uint64_t)E * H, 32, 128) ||
-        !make_bmaps(&m_xs, xs, H, S) || !make_bmaps(&m_mid, mid, I, S))
+        (!gemv && (!make_bmaps(&m_xs, xs, H, S) || !make_bmaps(&m_mid, mid, I, S))))
         return MOE_ERR_CUDA;
 
     DispatchArgs da{idx, perm, offsets, inv, tiles, ntiles, S, E, nmax, reinterpret_cast<int32_t*>(ws + L.dhist)};
@@ -279,12 +296,16 @@ int run_experts(const moe_dims* d, const uint16_t* x, const int32_t* idx, const 
     // CTA's first two items while the router, dispatch and gather run
     // (guess: one tile per expert, as when every expert has up to nmax rows).
     ga.w = reinterpret_cast<const uint8_t*>(gu->w);
-    ga.prefetch_items = (nmax == 64) ? 2 : 0;
+    ga.prefetch_items = (nmax <= 64) ? 2 : 0;
     ga.tiles_per_expert = 1;
-    gemm_stages(H, nmax, &ga.wstages, &ga.bregion);
+    if (gemv) {
+        ga.wstages = gemv_stages(H);
+    } else {
+        gemm_stages(H, nmax, &ga.wstages, &ga.bregion);
+    }
     int grid = di.sms;
     if ((long)L.max_tiles * ga.n_tiles < grid) grid = L.max_tiles * ga.n_tiles;
-    rc = fail(launch_gemm(kGateUp, m_gu, m_xs, ga, grid, s));
+    rc = fail(gemv ? launch_gemv(kGateUp, m_gu, ga, xs, grid, s) : launch_gemm(kGateUp, m_gu, m_xs, ga, grid, s));
     if (rc) return rc;
     tm.mark(4);
 
@@ -298,10 +319,14 @@ int run_experts(const moe_dims* d, const uint16_t* x, const int32_t* idx, const 
     gd.inter = I;
     gd.out_ld = H;
     gd.n_tiles = H / 128;
-    gemm_stages(I, nmax, &gd.wstages, &gd.bregion);
+    if (gemv) {
+        gd.wstages = gemv_stages(I);
+    } else {
+        gemm_stages(I, nmax, &gd.wstages, &gd.bregion);
+    }
     grid = di.sms;
     if ((long)L.max_tiles * gd.n_tiles < grid) grid = L.max_tiles * gd.n_tiles;
-    rc = fail(launch_gemm(kDown, m_dn, m_mid, gd, grid, s));
+    rc = fail(gemv ? launch_gemv(kDown, m_dn, gd, mid, grid, s) : launch_gemm(kDown, m_dn, m_mid, gd, grid, s));
     if (rc) return rc;
     tm.mark(5);
 
@@ -814,6 +839,11 @@ int moe_forward_hostio(const moe_dims* d, const uint16_t* x_host, const uint16_t
     return fail(cudaStreamSynchronize(s));
 }
 
+int moe_set_small_t_path(int mode) {
+    if (mode != 0 && mode != 1) return -MOE_ERR_SHAPE;
+    return g_small_t_path.exchange(mode);
+}
+
 int moe_timing_enable(int enable) {
     Timing& t = timing();
     std::lock_guard<std::mutex> lock(t.mu);
@@ -854,7 +884,7 @@ int moe_launches_per_forward(const moe_dims* d) {
 
 int moe_device_error(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return -MOE_ERR_CUDA;
-    return router_error_word() | dispatch_error_word() | gemm_error_word();
+    return router_error_word() | dispatch_error_word() | gemm_error_word() | gemv_error_word();
 }
 
 }  // extern "C"

@@ -306,6 +306,24 @@ int moe_forward_hostio(const moe_dims* d, const uint16_t* x_host, const uint16_t
                        void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * Which kernels the experts part of the routed calls (moe_experts,
+ * moe_experts_noalloc, moe_forward and the calls built on it) runs when
+ * tokens are few. mode 0 (the default): the tcgen05 grouped dequant-GEMM for
+ * every call. mode 1: a dequant-GEMV on the CUDA cores (no tensor-core
+ * padding of the few rows an expert gets) for calls with T*k <= 2*E, i.e.
+ * at most two rows per expert on average, token tiles of up to 4 rows. Both
+ * dequantise each weight to bf16(S*q + B) and accumulate in fp32; their
+ * outputs differ only by the order of the fp32 sums. On GB300 the GEMV
+ * measured about half as fast as the tensor-core path at the decode size
+ * (T = 8, H = 2816, E = 128, k = 8): the exact bf16 dequantisation already
+ * takes most of the issue slots, and the CUDA-core products add to them,
+ * while the tensor core's products cost no issue slots. The setting is
+ * process-wide; change it only between calls. Returns the previous mode, or
+ * -MOE_ERR_SHAPE for a mode other than 0 or 1.
+ */
+int moe_set_small_t_path(int mode);
+
+/*
  * Per-kernel timing. After moe_timing_enable(1), each moe_forward /
  * moe_experts call records CUDA events around each of its kernels on its
  * stream (at most 1024 calls are kept). moe_timing_read synchronises the
