@@ -294,9 +294,11 @@ int run_experts(const moe_dims* d, const uint16_t* x, const int32_t* idx, const 
     ga.n_tiles = I / 64;
     // With small token tiles the kernels stream weights: warm L2 with each
     // CTA's first two items while the router, dispatch and gather run
-    // (guess: one tile per expert, as when every expert has up to nmax rows).
+    // (guess: token tile t is expert t's, as when every expert has between
+    // one and nmax rows). With fewer slots than experts most experts get
+    // none and the guess would fetch weights nobody reads: no warm-up.
     ga.w = reinterpret_cast<const uint8_t*>(gu->w);
-    ga.prefetch_items = (nmax <= 64) ? 2 : 0;
+    ga.prefetch_items = (nmax <= 64 && S >= E) ? 2 : 0;
     ga.tiles_per_expert = 1;
     if (gemv) {
         ga.wstages = gemv_stages(H);
