@@ -319,23 +319,38 @@ __global__ void __launch_bounds__((3 + dequant_warps<NA, APW, GROUPS>() + 4 * EP
         int bslot = 0, li = 0, as = 0;
         uint32_t bph = 0, aph = 0;  // phases of the B slot's and the A slot's barriers
         bool ok = true;
-        Tile tl_next = {};
-        int ti, jn;
-        if (blockIdx.x < num_items) {
-            item_coords(a, ntok, blockIdx.x, ti, jn);
-            tl_next = a.tiles[ti];
+        // Token rows of this CTA's items li and li + 32 in lane li % 32,
+        // loaded once: the issuer paces the whole pipeline, and a global load
+        // at each item boundary cost it ~500 cycles an item (measured with a
+        // per-stage clock trace). Items from the 64th on (long weight-major
+        // calls) load their rows one item ahead instead.
+        int rows_lo = 0, rows_hi = 0, rows_next = 0;
+        {
+            int ti, jn;
+            const int i0 = blockIdx.x + lane * (int)gridDim.x, i1 = i0 + 32 * (int)gridDim.x;
+            if (i0 < num_items) {
+                item_coords(a, ntok, i0, ti, jn);
+                rows_lo = a.tiles[ti].rows;
+            }
+            if (i1 < num_items) {
+                item_coords(a, ntok, i1, ti, jn);
+                rows_hi = a.tiles[ti].rows;
+            }
         }
         for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x, ++li) {
-            const Tile tl = tl_next;
-            if (it + (int)gridDim.x < num_items) {
+            const int r_lo = __shfl_sync(0xffffffffu, rows_lo, li & 31);
+            const int r_hi = __shfl_sync(0xffffffffu, rows_hi, li & 31);
+            const int rows = li < 32 ? r_lo : (li < 64 ? r_hi : rows_next);
+            if (li >= 63 && it + (int)gridDim.x < num_items) {
+                int ti, jn;
                 item_coords(a, ntok, it + gridDim.x, ti, jn);
-                tl_next = a.tiles[ti];
+                rows_next = a.tiles[ti].rows;
             }
-            const uint32_t nrows16 = (uint32_t)((tl.rows + 15) & ~15);
+            const uint32_t nrows16 = (uint32_t)((rows + 15) & ~15);
             const uint32_t idesc = idesc_bf16_m128(nrows16);
             // distance of the B slot's atoms in descriptor units (16 B)
             const uint32_t atom_step =
-                (uint32_t)((kBox3 ? (16 << bbox_index(tl.rows)) : brows) * 128) >> 4;
+                (uint32_t)((kBox3 ? (16 << bbox_index(rows)) : brows) * 128) >> 4;
             const int db = li & 1;
             const uint32_t dcol = tmem + kD0 + (uint32_t)(db * NMAX);
             // the accumulator buffer's previous item (li - 2) has been read out
@@ -348,11 +363,33 @@ __global__ void __launch_bounds__((3 + dequant_warps<NA, APW, GROUPS>() + 4 * EP
                 const uint64_t bdesc0 = sw128_kmajor_desc(smem_u32(bring + (size_t)bslot * bslot_bytes));
                 const uint32_t acol = tmem + as * 128;
                 if (elect_one()) {
+                    if (nk == 16) {
+                        // a full stage: 16 MMAs without a per-MMA test (the
+                        // tests slowed the issuer, which paces the pipeline)
+                        const uint64_t b1 = bdesc0 + atom_step, b2 = b1 + atom_step, b3 = b2 + atom_step;
+                        umma_ts(dcol, acol + 0, bdesc0 + 0, idesc, s > 0 ? 1u : 0u);
+                        umma_ts(dcol, acol + 8, bdesc0 + 2, idesc, 1u);
+                        umma_ts(dcol, acol + 16, bdesc0 + 4, idesc, 1u);
+                        umma_ts(dcol, acol + 24, bdesc0 + 6, idesc, 1u);
+                        umma_ts(dcol, acol + 32, b1 + 0, idesc, 1u);
+                        umma_ts(dcol, acol + 40, b1 + 2, idesc, 1u);
+                        umma_ts(dcol, acol + 48, b1 + 4, idesc, 1u);
+                        umma_ts(dcol, acol + 56, b1 + 6, idesc, 1u);
+                        umma_ts(dcol, acol + 64, b2 + 0, idesc, 1u);
+                        umma_ts(dcol, acol + 72, b2 + 2, idesc, 1u);
+                        umma_ts(dcol, acol + 80, b2 + 4, idesc, 1u);
+                        umma_ts(dcol, acol + 88, b2 + 6, idesc, 1u);
+                        umma_ts(dcol, acol + 96, b3 + 0, idesc, 1u);
+                        umma_ts(dcol, acol + 104, b3 + 2, idesc, 1u);
+                        umma_ts(dcol, acol + 112, b3 + 4, idesc, 1u);
+                        umma_ts(dcol, acol + 120, b3 + 6, idesc, 1u);
+                    } else {
 #pragma unroll
-                    for (int k16 = 0; k16 < 16; ++k16) {
-                        if (k16 < nk) {
-                            const uint64_t bdesc = bdesc0 + (uint64_t)((k16 >> 2) * atom_step + (k16 & 3) * 2);
-                            umma_ts(dcol, acol + k16 * 8, bdesc, idesc, (s > 0 || k16 > 0) ? 1u : 0u);
+                        for (int k16 = 0; k16 < 16; ++k16) {
+                            if (k16 < nk) {
+                                const uint64_t bdesc = bdesc0 + (uint64_t)((k16 >> 2) * atom_step + (k16 & 3) * 2);
+                                umma_ts(dcol, acol + k16 * 8, bdesc, idesc, (s > 0 || k16 > 0) ? 1u : 0u);
+                            }
                         }
                     }
                     umma_commit(&sh.bempty[bslot]);
