@@ -127,6 +127,7 @@ __global__ void __launch_bounds__(kWarps * 32) router_kernel(const __grid_consta
     __shared__ uint64_t full, wfull, mdone;
     __shared__ uint32_t tmem_base;
     __shared__ uint16_t pes_s[kMaxRouterE];  // per_expert_scale
+    __shared__ float rs_s[64];               // 1 / rms of each token of the tile
     __shared__ int abort_flag_s;
     pdl_trigger();
     pdl_wait();
@@ -221,35 +222,54 @@ __global__ void __launch_bounds__(kWarps * 32) router_kernel(const __grid_consta
         const bool have = mbar_wait(&full, (uint32_t)it & 1, abort_flag);
 
         // ---- 1. partial sums of squares of this slice, to every CTA ----
-        for (int t = warp; t < TT; t += kWarps) {
-            float hi = 0.f, lo = 0.f;
-            for (int i = lane; have && i < cnt * 8; i += 32) {
+        // 512 / TT threads a token (8, 16 or 32 adjacent lanes of a warp),
+        // thread `sub` summing chunks sub, sub + tpt, ... of the token's
+        // slice in two independent two-float accumulators (alternate chunks),
+        // so no thread runs one long dependent chain. The merge and the
+        // butterfly over the token's threads are error-free two-sums, whose
+        // results do not depend on operand order, so every thread of the
+        // token ends with the same value.
+        {
+            const int tpt = (kWarps * 32) / TT;
+            const int t = (int)threadIdx.x / tpt, sub = (int)threadIdx.x % tpt;
+            const int nchunk = have ? cnt * 8 : 0;
+            float h0 = 0.f, l0 = 0.f, h1 = 0.f, l1 = 0.f;
+            for (int i = sub; i < nchunk; i += 2 * tpt) {
                 const uint4 v = *reinterpret_cast<const uint4*>(sm.xt + (i >> 3) * TT * 128 + sw128(t, i & 7));
                 const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                const int i2 = i + tpt;
+                uint4 v2 = make_uint4(0u, 0u, 0u, 0u);
+                if (i2 < nchunk) v2 = *reinterpret_cast<const uint4*>(sm.xt + (i2 >> 3) * TT * 128 + sw128(t, i2 & 7));
+                const uint32_t w2[4] = {v2.x, v2.y, v2.z, v2.w};
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
+                    // squares of bf16 values are exact in fp32 (zero chunks add nothing)
                     const float x0 = bf16_bits_to_f32(w[j] & 0xFFFFu), x1 = bf16_bits_to_f32(w[j] >> 16);
-                    acc2(hi, lo, __fmul_rn(x0, x0));  // squares of bf16 values are exact in fp32
-                    acc2(hi, lo, __fmul_rn(x1, x1));
+                    const float y0 = bf16_bits_to_f32(w2[j] & 0xFFFFu), y1 = bf16_bits_to_f32(w2[j] >> 16);
+                    acc2(h0, l0, __fmul_rn(x0, x0));
+                    acc2(h1, l1, __fmul_rn(y0, y0));
+                    acc2(h0, l0, __fmul_rn(x1, x1));
+                    acc2(h1, l1, __fmul_rn(y1, y1));
                 }
             }
-            // Butterfly: both lanes of a pair form the same (exact) two-sum,
-            // so every lane ends with the same value.
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
+            float hi, lo, se;
+            two_sum(h0, h1, hi, se);
+            lo = __fadd_rn(__fadd_rn(l0, l1), se);
+            for (int o = tpt / 2; o > 0; o >>= 1) {
                 const float h2 = __shfl_xor_sync(0xffffffffu, hi, o), l2 = __shfl_xor_sync(0xffffffffu, lo, o);
-                float s, e;
-                two_sum(hi, h2, s, e);
-                hi = s;
-                lo = __fadd_rn(__fadd_rn(lo, l2), e);
+                float s2, e2;
+                two_sum(hi, h2, s2, e2);
+                hi = s2;
+                lo = __fadd_rn(__fadd_rn(lo, l2), e2);
             }
-            if (lane < kCS) cluster.map_shared_rank(sm.pss, lane)[rank * TT + t] = make_float2(hi, lo);
+            if (sub < kCS) cluster.map_shared_rank(sm.pss, sub)[rank * TT + t] = make_float2(hi, lo);
         }
         __syncwarp();
         cluster_barrier();  // A: all partial sums of squares delivered
 
-        // ---- 2. rsqrt of the fp32 mean, normalise this slice in place ----
-        for (int t = warp; t < TT; t += kWarps) {
+        // ---- 2. rsqrt of the fp32 mean (a thread a token), normalise this slice in place ----
+        if ((int)threadIdx.x < TT) {
+            const int t = threadIdx.x;
             float hs = 0.f, ls = 0.f;
             for (int src = 0; src < kCS; ++src) {  // CTA order: the same result in every CTA
                 const float2 p = sm.pss[src * TT + t];
@@ -265,16 +285,23 @@ __global__ void __launch_bounds__(kWarps * 32) router_kernel(const __grid_consta
             const float q0 = __fdiv_rn(hs, Hf);
             const float rsd = __fadd_rn(__fmaf_rn(-q0, Hf, hs), ls);
             const float mean = __fadd_rn(q0, __fdiv_rn(rsd, Hf));
-            const float rs = __frsqrt_rn(__fadd_rn(mean, a.eps));
-            // bf16 after each op: x*rs in fp32 rounded once (cvt.rn), then the
-            // two bf16 x bf16 products, each exact in fp32 and rounded once
-            // (mul.rn.bf16x2), two elements an instruction.
-            const bool xe_row = a.xe && t0 + t < a.T;
-            for (int i = lane; have && i < cnt * 8; i += 32) {
-                uint4* p = reinterpret_cast<uint4*>(sm.xt + (i >> 3) * TT * 128 + sw128(t, i & 7));
+            rs_s[t] = __frsqrt_rn(__fadd_rn(mean, a.eps));
+        }
+        __syncthreads();
+        // bf16 after each op: x*rs in fp32 rounded once (cvt.rn), then the
+        // two bf16 x bf16 products, each exact in fp32 and rounded once
+        // (mul.rn.bf16x2), two elements an instruction. Element i of the
+        // loop is token i % TT, chunk i / TT of the slice.
+        {
+            const int nchunk = cnt * 8;
+            const int tshift = 31 - __clz(TT);
+            for (int i = threadIdx.x; have && i < TT * nchunk; i += kWarps * 32) {
+                const int t = i & (TT - 1), c = i >> tshift;
+                const float rs = rs_s[t];
+                uint4* p = reinterpret_cast<uint4*>(sm.xt + (c >> 3) * TT * 128 + sw128(t, c & 7));
                 const uint4 v = *p;
-                if (xe_row) {  // the expert input: bf16((x * rs) * pre_w), one rounding
-                    const uint4 pw = reinterpret_cast<const uint4*>(sm.psl)[i];
+                if (a.xe && t0 + t < a.T) {  // the expert input: bf16((x * rs) * pre_w), one rounding
+                    const uint4 pw = reinterpret_cast<const uint4*>(sm.psl)[c];
                     const uint32_t xv[4] = {v.x, v.y, v.z, v.w}, wv[4] = {pw.x, pw.y, pw.z, pw.w};
                     uint32_t e[4];
 #pragma unroll
@@ -283,11 +310,11 @@ __global__ void __launch_bounds__(kWarps * 32) router_kernel(const __grid_consta
                             __fmul_rn(__fmul_rn(__uint_as_float(xv[j] << 16), rs), __uint_as_float(wv[j] << 16)),
                             __fmul_rn(__fmul_rn(__uint_as_float(xv[j] & 0xFFFF0000u), rs),
                                       __uint_as_float(wv[j] & 0xFFFF0000u)));
-                    const size_t h = (size_t)(kb0 + (i >> 3)) * 64 + (i & 7) * 8;
+                    const size_t h = (size_t)(kb0 + (c >> 3)) * 64 + (c & 7) * 8;
                     *reinterpret_cast<uint4*>(a.xe + (size_t)(t0 + t) * H + h) = make_uint4(e[0], e[1], e[2], e[3]);
                 }
-                const uint4 s = reinterpret_cast<const uint4*>(sm.rsl)[i];  // router_scale of the same 8 columns
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w}, sc[4] = {s.x, s.y, s.z, s.w};
+                const uint4 sv = reinterpret_cast<const uint4*>(sm.rsl)[c];  // router_scale of the same 8 columns
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w}, sc[4] = {sv.x, sv.y, sv.z, sv.w};
                 uint32_t o[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
