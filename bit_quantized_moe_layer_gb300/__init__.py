@@ -30,7 +30,7 @@ STATUS = {0: "ok", 1: "null pointer", 2: "bad shape", 3: "pointer not 16-byte al
 EXPORTS = ("moe_status_str", "moe_workspace_bytes", "moe_workspace_map_of", "moe_route", "moe_dispatch", "moe_experts",
            "moe_experts_noalloc", "moe_forward", "moe_forward_branch", "moe_forward_hostio", "moe_route_q4",
            "moe_forward_q4router", "moe_dense_mlp", "moe_dense_branch", "moe_self_conditioning", "moe_lm_head",
-           "moe_set_small_t_path", "moe_timing_enable",
+           "moe_set_small_t_path", "moe_set_router_path", "moe_timing_enable",
            "moe_timing_read",
            "moe_launches_per_forward", "moe_device_error")
 
@@ -91,6 +91,8 @@ def load(path: str = LIB_PATH):
     lib.moe_lm_head.argtypes = [D, ctypes.c_int32, ctypes.c_float, P, Q, P, P, Z, P]
     lib.moe_set_small_t_path.argtypes = [I]
     lib.moe_set_small_t_path.restype = I
+    lib.moe_set_router_path.argtypes = [I]
+    lib.moe_set_router_path.restype = I
     lib.moe_timing_enable.argtypes = [I]
     lib.moe_timing_read.argtypes = [ctypes.POINTER(ctypes.c_float), I, ctypes.POINTER(I)]
     lib.moe_launches_per_forward.argtypes = [ctypes.c_void_p]
@@ -255,6 +257,17 @@ def set_small_t_path(mode: int) -> int:
     rc = load().moe_set_small_t_path(int(mode))
     if rc < 0:
         raise MoeError("moe_set_small_t_path", -rc)
+    return rc
+
+
+def set_router_path(mode: int) -> int:
+    """0 (default): the row router where it fits and the cluster router would
+    walk three or more waves of tiles, else the cluster router; 1: always
+    the cluster router; 2: the row router wherever it fits. Returns the
+    previous mode."""
+    rc = load().moe_set_router_path(int(mode))
+    if rc < 0:
+        raise MoeError("moe_set_router_path", -rc)
     return rc
 
 

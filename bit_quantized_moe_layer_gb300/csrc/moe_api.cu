@@ -231,6 +231,11 @@ int fail(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 // for gate_up, inter for down).
 std::atomic<int> g_small_t_path{0};
 
+// Router kernel (moe_set_router_path): 0 = the row router where it fits and
+// the clusters would walk three or more waves, 1 = the cluster router always,
+// 2 = the row router wherever it fits.
+std::atomic<int> g_router_path{0};
+
 bool use_gemv(const moe_dims* d) {
     const long S = (long)d->T * d->k;
     return g_small_t_path.load(std::memory_order_relaxed) == 1 && S <= 2L * d->E && gemv_stages(d->H) >= 2 &&
@@ -475,7 +480,13 @@ int check_dense(const moe_dims* d) {
 int route_impl(const moe_dims* d, const uint16_t* x, const uint16_t* rw, const uint16_t* rs, const uint16_t* pes,
                int32_t* idx, uint16_t* w, cudaStream_t s, const uint16_t* pre_norm_w = nullptr,
                uint16_t* xe = nullptr, const moe_qweight* rq = nullptr) {
-    const int tt = router_tokens_per_cluster(d->T, d->H, d->E);
+    // The row router (one CTA per 16 tokens over the whole row, no cross-CTA
+    // exchange) when the cluster router would walk three or more waves of
+    // tiles; the cluster router otherwise and for the 4-bit projection.
+    const int rpath = g_router_path.load(std::memory_order_relaxed);
+    const bool rows = rq == nullptr && ((rpath == 0 && router_prefer_rows(d->T, d->H, d->E)) ||
+                                        (rpath == 2 && router_rows_fits(d->H, d->E, false)));
+    const int tt = rows ? 16 : router_tokens_per_cluster(d->T, d->H, d->E);
     RouterArgs ra{x,    rw,   rs,   pes,  idx,    w,
                   d->T, d->H, d->E, d->k, d->eps, bf16_round(pow((double)d->H, -0.5)),
                   tt,   pre_norm_w, xe, rq ? rq->w : nullptr, rq ? rq->scales : nullptr,
@@ -486,7 +497,7 @@ int route_impl(const moe_dims* d, const uint16_t* x, const uint16_t* rw, const u
         m_rw = m_x;  // not read: the 4-bit projection is dequantised in the kernel
     else if (!make_map_2d(&m_rw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rw, d->H, d->E, 64, d->E < 128 ? d->E : 128))
         return MOE_ERR_CUDA;
-    return fail(launch_router(m_rw, m_x, ra, s));
+    return fail(rows ? launch_router_rows(m_rw, m_x, ra, s) : launch_router(m_rw, m_x, ra, s));
 }
 
 int get_workspace(const moe_dims* d, void* workspace, size_t ws_bytes, const Layout& L, uint8_t** out) {
@@ -839,6 +850,11 @@ int moe_forward_hostio(const moe_dims* d, const uint16_t* x_host, const uint16_t
     if (rc) return rc;
     if (cudaMemcpyAsync(out_host, odev, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
     return fail(cudaStreamSynchronize(s));
+}
+
+int moe_set_router_path(int mode) {
+    if (mode < 0 || mode > 2) return -MOE_ERR_SHAPE;
+    return g_router_path.exchange(mode);
 }
 
 int moe_set_small_t_path(int mode) {

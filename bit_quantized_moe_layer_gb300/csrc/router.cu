@@ -461,6 +461,294 @@ __global__ void __launch_bounds__(kWarps * 32) router_kernel(const __grid_consta
     }
 }
 
+// ------------------------------------------------------------------------
+// Row router: the same computation as router_kernel, one CTA per 16 tokens
+// over the whole hidden dimension, no cluster. The CTA keeps its 16 x rows
+// in shared memory (H / 64 boxes of 16 rows x 128 B, the MMA's K-major
+// layout), sums each token's squares itself (warp w <-> token w: lanes take
+// alternate 16-byte chunks into two two-float accumulators, merged by
+// error-free two-sums, so the mean is the exactly rounded one as above),
+// normalises in place with the same three bf16 roundings, and streams the
+// router weight through a ring of 64-wide K blocks (128 experts x 128 B,
+// TMA) into one accumulator: D[e][t] in 16 TMEM columns. The scores leave
+// TMEM by lane quarter, are rounded to bf16 and staged as [token][expert];
+// warp w then takes token w's top k, softmax and per-expert scale as the
+// cluster router does. No cross-CTA exchange or barrier: the tile's latency
+// is its x copy, two passes over shared memory and the weight stream.
+namespace {
+constexpr int kRowTT = 16;                 // tokens a CTA (one warp each)
+constexpr int kRowWarps = 16;
+constexpr int kRowWStages = 8;             // most router-weight ring stages (one 64-wide K block each)
+static_assert(kRowTT == kRowWarps, "warp w owns token w");
+}  // namespace
+
+// Router-weight ring stages that fit beside the x tile (0 if fewer than 4).
+__host__ __device__ inline int row_wstages(int H) {
+    const long fixed = 1024 + (long)(H / 64) * kRowTT * 128 + (long)kRowTT * kChunkE * 2;
+    const long n = ((long)(232448 - 1024) - fixed) / kWBlockBytes;
+    return n < 4 ? 0 : (n > kRowWStages ? kRowWStages : (int)n);
+}
+
+size_t router_rows_smem_bytes(int H) {
+    const size_t nkb = (size_t)H / 64;
+    return 1024 + nkb * kRowTT * 128 + (size_t)row_wstages(H) * kWBlockBytes + (size_t)kRowTT * kChunkE * 2;
+}
+
+__global__ void __launch_bounds__(kRowWarps * 32, 1) router_rows_kernel(const __grid_constant__ CUtensorMap wmap,
+                                                                        const __grid_constant__ CUtensorMap xmap,
+                                                                        RouterArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ uint64_t xfull, mdone, wfull[kRowWStages], wempty[kRowWStages];
+    __shared__ uint32_t tmem_base;
+    __shared__ uint16_t pes_s[kChunkE];
+    __shared__ float rs_s[kRowTT];
+    __shared__ int abort_flag_s, have_s, got_s;
+    pdl_trigger();
+    pdl_wait();
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int H = a.H, E = a.E, k = a.k;
+    const int nkb = H / 64;
+    uint8_t* xt = base;                                             // nkb boxes of 16 rows x 128 B
+    const int NW = row_wstages(H);                                  // weight ring stages
+    uint8_t* wring = xt + (size_t)nkb * kRowTT * 128;               // NW blocks of 128 rows x 128 B
+    uint16_t* sc = reinterpret_cast<uint16_t*>(wring + (size_t)NW * kWBlockBytes);  // [16][E]
+    volatile int* abort_flag = &abort_flag_s;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t0 = blockIdx.x * kRowTT;
+    const uint32_t wbytes = (uint32_t)E * 128u;                     // one K block of the weight (E <= 128 rows)
+    const int nw0 = nkb < NW ? nkb : NW;
+
+    for (int e = threadIdx.x; e < E; e += blockDim.x) pes_s[e] = a.per_expert_scale[e];
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&xmap);
+        prefetch_tensormap(&wmap);
+        mbar_init(&xfull, 1);
+        mbar_init(&mdone, 1);
+        for (int s = 0; s < kRowWStages; ++s) {
+            mbar_init(&wfull[s], 1);
+            mbar_init(&wempty[s], 1);
+        }
+        abort_flag_s = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {  // scores accumulator: 128 lanes (experts) x 16 columns (tokens)
+        tmem_alloc(&tmem_base, 32);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+    if (threadIdx.x == 0) {
+        // the tile's rows (rows past T read as zero) and the first weight blocks
+        mbar_arrive_expect_tx(&xfull, (uint32_t)nkb * kRowTT * 128u);
+        for (int kb = 0; kb < nkb; ++kb) tma_load_2d(xt + (size_t)kb * kRowTT * 128, &xmap, &xfull, kb * 64, t0);
+        for (int s = 0; s < nw0; ++s) {
+            mbar_arrive_expect_tx(&wfull[s], wbytes);
+            tma_load_2d(wring + (size_t)s * kWBlockBytes, &wmap, &wfull[s], s * 64, 0);
+        }
+    }
+    if (warp == 0) {
+        const bool h = mbar_wait(&xfull, 0, abort_flag);
+        if (lane == 0) have_s = h;
+    }
+    __syncthreads();
+    const bool have = have_s != 0;
+
+    // ---- 1. sums of squares and 1/rms: warp w <-> token w ----
+    {
+        const int t = warp;
+        const int nchunk = have ? nkb * 8 : 0;
+        float h0 = 0.f, l0 = 0.f, h1 = 0.f, l1 = 0.f;
+        for (int i = lane; i < nchunk; i += 64) {
+            const uint4 v = *reinterpret_cast<const uint4*>(xt + (size_t)(i >> 3) * kRowTT * 128 + sw128(t, i & 7));
+            const int i2 = i + 32;
+            uint4 v2 = make_uint4(0u, 0u, 0u, 0u);
+            if (i2 < nchunk) v2 = *reinterpret_cast<const uint4*>(xt + (size_t)(i2 >> 3) * kRowTT * 128 + sw128(t, i2 & 7));
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w}, w2[4] = {v2.x, v2.y, v2.z, v2.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                // squares of bf16 values are exact in fp32 (zero chunks add nothing)
+                const float x0 = bf16_bits_to_f32(w[j] & 0xFFFFu), x1 = bf16_bits_to_f32(w[j] >> 16);
+                const float y0 = bf16_bits_to_f32(w2[j] & 0xFFFFu), y1 = bf16_bits_to_f32(w2[j] >> 16);
+                acc2(h0, l0, __fmul_rn(x0, x0));
+                acc2(h1, l1, __fmul_rn(y0, y0));
+                acc2(h0, l0, __fmul_rn(x1, x1));
+                acc2(h1, l1, __fmul_rn(y1, y1));
+            }
+        }
+        float hs, ls, se;
+        two_sum(h0, h1, hs, se);
+        ls = __fadd_rn(__fadd_rn(l0, l1), se);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float h2 = __shfl_xor_sync(0xffffffffu, hs, o), l2 = __shfl_xor_sync(0xffffffffu, ls, o);
+            float s2, e2;
+            two_sum(hs, h2, s2, e2);
+            hs = s2;
+            ls = __fadd_rn(__fadd_rn(ls, l2), e2);
+        }
+        if (lane == 0) {
+            // mean = (hs + ls) / H rounded once to fp32, as in router_kernel
+            const float Hf = (float)H;
+            const float q0 = __fdiv_rn(hs, Hf);
+            const float rsd = __fadd_rn(__fmaf_rn(-q0, Hf, hs), ls);
+            const float mean = __fadd_rn(q0, __fdiv_rn(rsd, Hf));
+            rs_s[t] = __frsqrt_rn(__fadd_rn(mean, a.eps));
+        }
+    }
+    __syncthreads();
+
+    // ---- 2. normalise in place: element i is token i % 16, chunk i / 16 ----
+    const uint32_t rootb = f32_to_bf16_bits(a.root), root2 = rootb | (rootb << 16);
+    for (int i = threadIdx.x; have && i < kRowTT * nkb * 8; i += kRowWarps * 32) {
+        const int t = i & (kRowTT - 1), c = i >> 4;
+        const float rs = rs_s[t];
+        uint4* p = reinterpret_cast<uint4*>(xt + (size_t)(c >> 3) * kRowTT * 128 + sw128(t, c & 7));
+        const uint4 v = *p;
+        const size_t h = (size_t)c * 8;  // first of the chunk's 8 hidden columns
+        if (a.xe && t0 + t < a.T) {  // the expert input: bf16((x * rs) * pre_w), one rounding
+            const uint4 pw = __ldg(reinterpret_cast<const uint4*>(a.pre_w + h));
+            const uint32_t xv[4] = {v.x, v.y, v.z, v.w}, wv[4] = {pw.x, pw.y, pw.z, pw.w};
+            uint32_t e[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                e[j] = pack_bf16x2(
+                    __fmul_rn(__fmul_rn(__uint_as_float(xv[j] << 16), rs), __uint_as_float(wv[j] << 16)),
+                    __fmul_rn(__fmul_rn(__uint_as_float(xv[j] & 0xFFFF0000u), rs), __uint_as_float(wv[j] & 0xFFFF0000u)));
+            *reinterpret_cast<uint4*>(a.xe + (size_t)(t0 + t) * H + h) = make_uint4(e[0], e[1], e[2], e[3]);
+        }
+        const uint4 sv = __ldg(reinterpret_cast<const uint4*>(a.router_scale + h));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w}, scl[4] = {sv.x, sv.y, sv.z, sv.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t n = pack_bf16x2(__fmul_rn(__uint_as_float(w[j] << 16), rs),
+                                           __fmul_rn(__uint_as_float(w[j] & 0xFFFF0000u), rs));
+            o[j] = mul_bf16x2(mul_bf16x2(n, scl[j]), root2);
+        }
+        *p = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    // The normalised tile was written by ordinary stores; the tensor core
+    // reads it through the async proxy.
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+
+    // ---- 3. scores: D[e][t] += W[e][kb] . n[t][kb] over the K blocks ----
+    // Warp 1's elected thread waits for each weight block and issues its 4
+    // MMAs, whose commit frees the slot; warp 2's refills each freed slot
+    // with the block NW further on, so NW - 1 or NW copies stay in flight.
+    if (warp == 1) {
+        tc_fence_after();
+        if (elect_one()) {
+            const uint32_t idesc = idesc_bf16_m128((uint32_t)kRowTT);
+            bool ok = have;
+            for (int kb = 0; ok && kb < nkb; ++kb) {
+                const int slot = kb % NW;
+                if (!(ok = mbar_wait(&wfull[slot], (uint32_t)(kb / NW) & 1u, abort_flag))) break;
+                tc_fence_after();
+                const uint64_t ad = sw128_kmajor_desc(smem_u32(wring + (size_t)slot * kWBlockBytes));
+                const uint64_t bd = sw128_kmajor_desc(smem_u32(xt + (size_t)kb * kRowTT * 128));
+#pragma unroll
+                for (int k16 = 0; k16 < 4; ++k16)
+                    umma_ss(tmem, ad + (uint64_t)(k16 * 2), bd + (uint64_t)(k16 * 2), idesc,
+                            (kb > 0 || k16 > 0) ? 1u : 0u);
+                umma_commit(&wempty[slot]);
+            }
+            umma_commit(&mdone);  // every MMA above (none if the tile was not loaded)
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        if (elect_one()) {
+            int issued = nw0;  // weight blocks whose copy has been issued
+            for (int b = nw0; have && b < nkb; ++b) {
+                const int slot = b % NW;
+                if (!mbar_wait(&wempty[slot], (uint32_t)((b - NW) / NW) & 1u, abort_flag)) break;
+                mbar_arrive_expect_tx(&wfull[slot], wbytes);
+                tma_load_2d(wring + (size_t)slot * kWBlockBytes, &wmap, &wfull[slot], b * 64, 0);
+                issued = b + 1;
+            }
+            // The last copy issued into each slot lands before the CTA exits
+            // (earlier ones were consumed by the MMAs before the slot was
+            // refilled).
+            for (int b = issued - 1; b >= 0 && b >= issued - NW; --b) mbar_drain(&wfull[b % NW], (uint32_t)(b / NW) & 1u);
+        }
+        __syncwarp();
+    }
+    if (warp == 0) {
+        const bool g = mbar_wait(&mdone, 0, abort_flag);
+        if (lane == 0) got_s = g && have;
+    }
+    __syncthreads();
+    tc_fence_after();
+    const bool got = got_s != 0;
+
+    // ---- 4. scores to shared memory as [token][expert] bf16 ----
+    if (warp < 4) {
+        uint32_t v[16];
+        if (got) {
+            tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16), v);
+            tmem_wait_ld();
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = 0u;
+        }
+        const int e = 32 * warp + lane;
+        if (e < E) {
+#pragma unroll
+            for (int j = 0; j < kRowTT; ++j) sc[j * E + e] = (uint16_t)f32_to_bf16_bits(__uint_as_float(v[j]));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- 5. token warp: top k, precise softmax, per-expert scale ----
+    const int t = t0 + warp;
+    if (got && t < a.T) {
+        const uint16_t* sr = sc + warp * E;
+        uint32_t cand[4];  // keys of this lane's experts e = lane + 32 i (E <= 128)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int e = lane + 32 * i;
+            cand[i] = (e < E) ? ((order_key16(sr[e]) << 16) | (0xFFFFu - (uint32_t)e)) : 0u;
+        }
+        int my_idx = 0;
+        float my_s = 0.f, top_s = 0.f;
+        for (int j = 0; j < k; ++j) {
+            uint32_t best = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) best = max(best, cand[i]);
+            const uint32_t win = __reduce_max_sync(0xffffffffu, best);
+            const int e = (int)(0xFFFFu - (win & 0xFFFFu));
+            const float sv = bf16_bits_to_f32(key16_to_bits(win >> 16));
+            if (j == 0) top_s = sv;
+            if (lane == j) {
+                my_idx = e;
+                my_s = sv;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (cand[i] == win) cand[i] = 0u;
+        }
+        const float ex = (lane < k) ? expf(__fsub_rn(my_s, top_s)) : 0.f;
+        float sum = 0.f;
+        for (int j = 0; j < k; ++j) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, ex, j));
+        if (lane < k) {
+            const float pr = bf16_bits_to_f32(f32_to_bf16_bits(__fdiv_rn(ex, sum)));
+            const float pes = bf16_bits_to_f32(pes_s[my_idx]);
+            a.idx[(size_t)t * k + lane] = my_idx;
+            a.w[(size_t)t * k + lane] = (uint16_t)f32_to_bf16_bits(__fmul_rn(pr, pes));
+        }
+    }
+    if (!have && threadIdx.x == 0) mbar_drain(&xfull, 0);  // the tile's copies land before exit
+    __syncwarp();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 32);
+    }
+}
+
 int router_error_word() {
     int v = 0, z = 0;
     if (cudaMemcpyFromSymbol(&v, g_error_word, sizeof(int)) != cudaSuccess) return 0;
@@ -553,6 +841,54 @@ cudaError_t launch_router(const CUtensorMap& wmap, const CUtensorMap& xmap, cons
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = router_config(clusters, smem, stream, attr);
     return cudaLaunchKernelEx(&cfg, router_kernel, wmap, xmap, a);
+}
+
+namespace {
+cudaError_t ensure_router_rows_attr() {
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        cudaError_t err = cudaFuncSetAttribute(router_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)kRouterSmemLimit);
+        if (err != cudaSuccess) return err;
+        attr_set[dev] = true;
+    }
+    return cudaSuccess;
+}
+}  // namespace
+
+bool router_rows_fits(int H, int E, bool q4) {
+    return !q4 && E >= 1 && E <= kChunkE && H % 64 == 0 && H >= 64 && row_wstages(H) >= 4 &&
+           router_rows_smem_bytes(H) <= kRouterSmemLimit;
+}
+
+// The row router where it fits and the cluster router would walk three or
+// more waves of tiles. Measured at H = 2816, E = 128 (us, launch included):
+// one CTA of the row router streams the whole router weight in ~23 us
+// whatever T, while a cluster takes ~6 us a tile after ~3 us of setup:
+// T = 8: cluster 13.0, row 27.3; T = 256: 15.0 / 27.3; T = 1024 (two
+// waves): 25.2 / 27.3; T = 2048 (three): 33.4 / 29.3; T = 4096 (five):
+// 48.8 / 47.7.
+bool router_prefer_rows(int T, int H, int E) {
+    if (!router_rows_fits(H, E, false)) return false;
+    const int tt = router_tokens_per_cluster(T, H, E);
+    const size_t smem = router_smem_bytes(H, E, tt);
+    if (smem > kRouterSmemLimit) return true;
+    const int waves = ((T + tt - 1) / tt + router_resident_clusters(smem) - 1) / router_resident_clusters(smem);
+    return waves >= 3;
+}
+
+cudaError_t launch_router_rows(const CUtensorMap& wmap, const CUtensorMap& xmap, const RouterArgs& a,
+                               cudaStream_t stream) {
+    if (a.T == 0) return cudaSuccess;
+    if (!router_rows_fits(a.H, a.E, a.rq_w != nullptr) || a.k < 1 || a.k > 32 || a.k > a.E) return cudaErrorInvalidValue;
+    cudaError_t err = ensure_router_rows_attr();
+    if (err != cudaSuccess) return err;
+    const int ctas = (a.T + kRowTT - 1) / kRowTT;
+    return launch_pdl(router_rows_kernel, dim3((unsigned)ctas), dim3(kRowWarps * 32), router_rows_smem_bytes(a.H),
+                      stream, wmap, xmap, a);
 }
 
 }  // namespace moe

@@ -324,6 +324,26 @@ int moe_forward_hostio(const moe_dims* d, const uint16_t* x_host, const uint16_t
 int moe_set_small_t_path(int mode);
 
 /*
+ * Which router kernel moe_route, moe_forward, moe_forward_branch and
+ * moe_forward_q4router run (process-wide, change only between calls).
+ * mode 0 (the default): one CTA per 16 tokens over the whole hidden row
+ * (dense router weight, E <= 128, H a multiple of 64 up to 4992) when the
+ * cluster router would walk three or more waves of tiles (large T), the
+ * cluster router otherwise; mode 1: always the cluster
+ * router (8-CTA thread-block clusters splitting the hidden dimension); mode
+ * 2: the row router wherever it fits. Both
+ * compute the same roundings (DiffRouter.forward of "diffusion-gemma/
+ * model.ts": RMSNormNoScale in fp32 with the exactly rounded mean, bf16
+ * after each of the three multiplies, fp32-accumulated scores rounded to
+ * bf16, top k, softmax, per-expert scale); the scores' fp32 sums run in a
+ * different order, so a score can round to the neighbouring bf16 value and
+ * a near-tie can pick the other expert. The 4-bit projection (moe_route_q4)
+ * always runs on the cluster router. Returns the previous mode, or
+ * -MOE_ERR_SHAPE for a mode other than 0, 1 or 2.
+ */
+int moe_set_router_path(int mode);
+
+/*
  * Per-kernel timing. After moe_timing_enable(1), each moe_forward /
  * moe_experts call records CUDA events around each of its kernels on its
  * stream (at most 1024 calls are kept). moe_timing_read synchronises the

@@ -132,21 +132,26 @@ def near_tie_rows(logits: np.ndarray, scores: np.ndarray, k: int):
 
 
 MIDPOINT_REL = 2.0 ** -20
-# fp32 accumulation bound of one GPU router logit, in units of 2^-24 times the
-# sum of |products|: each of the 8 CTAs of a router cluster accumulates its
-# H/8 products in the tensor core's fp32 accumulator (16 products a step),
-# then the 8 partials are added; (H/8)/16 + 16 + 8 <= 64 steps for H <= 5504.
-ACCUM_STEPS = 64
 
 
-def midpoint_logit(v: float, abs_dot: float | None = None) -> bool:
+def accum_steps(H: int) -> int:
+    """fp32 accumulation bound of one GPU router logit, in units of 2^-24
+    times the sum of |products|. The row router accumulates all H products in
+    the tensor core's fp32 accumulator, 16 products a step: H/16 steps plus 16
+    inside a step. The cluster router's bound is smaller (each of 8 CTAs
+    accumulates H/8 products, then the 8 partials are added: H/128 + 24), so
+    this one covers both kernels."""
+    return H // 16 + 16
+
+
+def midpoint_logit(v: float, abs_dot: float | None = None, steps: int = 64) -> bool:
     """Whether the exact logit v lies close enough to a bf16 rounding midpoint
     that an fp32-accumulated score may round the other way: within
-    ACCUM_STEPS * 2^-24 * sum|products| (abs_dot) of it, or within
-    MIDPOINT_REL of |v| when the products are not known."""
+    steps * 2^-24 * sum|products| (abs_dot) of it, or within MIDPOINT_REL of
+    |v| when the products are not known."""
     u = float(bf16_ulp(np.array([v]))[0])
     mid = np.floor(abs(v) / u) * u + u / 2
-    window = ACCUM_STEPS * 2.0 ** -24 * abs_dot if abs_dot is not None else MIDPOINT_REL * abs(v)
+    window = steps * 2.0 ** -24 * abs_dot if abs_dot is not None else MIDPOINT_REL * abs(v)
     return abs(abs(v) - mid) <= window
 
 
@@ -197,7 +202,8 @@ def check_routing(d, ref, idx, w, router_w=None):
             if router_w is not None and "normed" in ref:
                 nt = np.abs(f64(ref["normed"][t]))
                 ad = [float(nt @ np.abs(f64(router_w[e]))) for e in (ex_, mi_)]
-            assert midpoint_logit(lg[t, ex_], ad[0]) or midpoint_logit(lg[t, mi_], ad[1]), \
+            steps = accum_steps(d.H)
+            assert midpoint_logit(lg[t, ex_], ad[0], steps) or midpoint_logit(lg[t, mi_], ad[1], steps), \
                 (f"token {t}: equal-score swap ({ex_} for {mi_}) with neither exact logit near a bf16 "
                  f"rounding midpoint: {lg[t, ex_]!r}, {lg[t, mi_]!r}")
             differ_score_tie += 1

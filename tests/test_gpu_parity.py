@@ -82,6 +82,51 @@ def test_route(name):
     print(f"{name}: routing {c} of {inp.dims.T} tokens")
 
 
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("name", ALL)
+def test_route_each_kernel(name, mode):
+    """Both router kernels against the oracle on every workload, whichever
+    the default picks there: the cluster router (moe_set_router_path(1)),
+    which the 4-bit projection and small T use, and the row router
+    (moe_set_router_path(2)), which large T uses. The two sum the scores in
+    different fp32 orders, so each is held to the oracle (check_routing), not
+    to the other."""
+    import bit_quantized_moe_layer_gb300 as moe
+    inp, g, ref = layer(name)
+    prev = moe.set_router_path(mode)
+    try:
+        idx, w = gh.gpu_route(g)
+    finally:
+        moe.set_router_path(prev)
+    c = gh.check_routing(inp.dims, ref, idx, w, inp.router_w)
+    print(f"{name}: {'cluster' if mode == 1 else 'row'} router {c} of {inp.dims.T} tokens")
+
+
+@pytest.mark.parametrize("T", [1, 15, 17, 100, 257])
+def test_row_router_ragged(T):
+    """The row router on token counts that leave a partial 16-token tile."""
+    import bit_quantized_moe_layer_gb300 as moe
+    inp = ms.make_layer("canvas", T=T, seed=5)
+    g = gh.upload(inp)
+    ref = gh.oracle_route(inp)
+    prev = moe.set_router_path(2)
+    try:
+        idx, w = gh.gpu_route(g)
+    finally:
+        moe.set_router_path(prev)
+    gh.check_routing(inp.dims, ref, idx, w, inp.router_w)
+
+
+def test_router_path_switch():
+    import bit_quantized_moe_layer_gb300 as moe
+    assert moe.set_router_path(0) == 0
+    assert moe.set_router_path(1) == 0
+    assert moe.set_router_path(2) == 1
+    assert moe.set_router_path(0) == 2
+    with pytest.raises(moe.MoeError):
+        moe.set_router_path(3)
+
+
 @pytest.mark.parametrize("name", ALL)
 def test_dispatch(name):
     inp, g, ref = layer(name)

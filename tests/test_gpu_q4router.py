@@ -67,7 +67,11 @@ def test_route_q4_equals_dense_on_dequantised_weight():
     g = gh.upload(dataclasses.replace(inp, router_w=dense))
     _, rq_q = upload_rq(rq)
     idx_q, w_q = gpu_route_q4(g, rq_q)
-    idx_d, w_d = gh.gpu_route(g)
+    prev = moe.set_router_path(1)  # the dense weight through the same (cluster) kernel
+    try:
+        idx_d, w_d = gh.gpu_route(g)
+    finally:
+        moe.set_router_path(prev)
     assert np.array_equal(idx_q, idx_d) and np.array_equal(w_q, w_d), "4-bit router != dense router on its weight"
 
 
