@@ -419,6 +419,49 @@ cudaError_t launch_gather(const uint16_t* x, const int32_t* perm, const int32_t*
 // out[t] = bf16(sum_j bf16(y_j * w[t k + j])), y_j = row inv[t k + j] of the
 // down product (stored by sorted row), the products rounded to bf16 (the
 // product of two bf16 arrays is a bf16 array) and summed in fp32 in j order.
+// fp32 sums, in slot order j, of bf16(y[inv[j]] * w[j]) over the 8 elements
+// of one 16-byte chunk (yc: the chunk in row 0 of y; rows are `chunks`
+// chunks apart). For k <= 8 every row's load is issued before the sums, so
+// the k reads are in flight together (the combine measured ~10% faster at
+// T = 256 and T = 4096 than with one row a step); dropped slots (inv < 0)
+// add nothing.
+__device__ __forceinline__ void combine_chunk(const uint4* __restrict__ yc, int chunks, const int32_t* __restrict__ it,
+                                              const uint16_t* __restrict__ wt, int k, float (&acc)[8]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    auto add = [&](const uint4& v, uint32_t wb) {
+        const uint32_t w2 = wb | (wb << 16);
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t pr = mul_bf16x2(u[q], w2);  // bf16(y * w), both halves
+            acc[2 * q] = __fadd_rn(acc[2 * q], __uint_as_float(pr << 16));
+            acc[2 * q + 1] = __fadd_rn(acc[2 * q + 1], __uint_as_float(pr & 0xFFFF0000u));
+        }
+    };
+    if (k <= 8) {
+        int p[8];
+        uint32_t wv[8];
+        uint4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            p[j] = j < k ? __ldg(it + j) : -1;
+            wv[j] = j < k ? (uint32_t)__ldg(wt + j) : 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = p[j] >= 0 ? __ldg(yc + (size_t)p[j] * chunks) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (p[j] >= 0) add(v[j], wv[j]);
+    } else {
+        for (int j = 0; j < k; ++j) {
+            const int p = __ldg(it + j);
+            if (p < 0) continue;  // slot dropped by the dispatch (expert id out of range)
+            add(__ldg(yc + (size_t)p * chunks), __ldg(wt + j));
+        }
+    }
+}
+
 __global__ void __launch_bounds__(128) combine_kernel(const uint16_t* __restrict__ y,
                                                       const int32_t* __restrict__ inv,
                                                       const uint16_t* __restrict__ w,
@@ -428,24 +471,8 @@ __global__ void __launch_bounds__(128) combine_kernel(const uint16_t* __restrict
     const int chunks = H / 8;
     const int t = blockIdx.x, c = blockIdx.y * 128 + threadIdx.x;
     if (c >= chunks) return;
-    const uint4* yc = reinterpret_cast<const uint4*>(y) + c;
-    const uint16_t* wt = w + (size_t)t * k;
-    const int32_t* it = inv + (size_t)t * k;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-    for (int j = 0; j < k; ++j) {
-        const int p = __ldg(it + j);
-        if (p < 0) continue;  // slot dropped by the dispatch (expert id out of range)
-        const uint32_t wb = __ldg(wt + j), w2 = wb | (wb << 16);
-        const uint4 v = __ldg(yc + (size_t)p * chunks);
-        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const uint32_t p = mul_bf16x2(u[q], w2);  // bf16(y * w), both halves
-            acc[2 * q] = __fadd_rn(acc[2 * q], __uint_as_float(p << 16));
-            acc[2 * q + 1] = __fadd_rn(acc[2 * q + 1], __uint_as_float(p & 0xFFFF0000u));
-        }
-    }
+    float acc[8];
+    combine_chunk(reinterpret_cast<const uint4*>(y) + c, chunks, inv + (size_t)t * k, w + (size_t)t * k, k, acc);
     reinterpret_cast<uint4*>(out + (size_t)t * H)[c] =
         make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
                    pack_bf16x2(acc[6], acc[7]));
@@ -477,20 +504,8 @@ __global__ void __launch_bounds__(kNormThreads) combine_norm_kernel(const uint16
         const int c = tid + q * kNormThreads;
         cv[q] = make_uint4(0, 0, 0, 0);
         if (c >= chunks) continue;
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int j = 0; j < k; ++j) {
-            const int p = __ldg(it + j);
-            if (p < 0) continue;  // slot dropped by the dispatch
-            const uint32_t wb = __ldg(wt + j), w2 = wb | (wb << 16);
-            const uint4 v = __ldg(y4 + (size_t)p * chunks + c);
-            const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const uint32_t p = mul_bf16x2(u[e], w2);
-                acc[2 * e] = __fadd_rn(acc[2 * e], __uint_as_float(p << 16));
-                acc[2 * e + 1] = __fadd_rn(acc[2 * e + 1], __uint_as_float(p & 0xFFFF0000u));
-            }
-        }
+        float acc[8];
+        combine_chunk(y4 + c, chunks, it, wt, k, acc);
         const uint32_t b0 = pack_bf16x2(acc[0], acc[1]), b1 = pack_bf16x2(acc[2], acc[3]),
                        b2 = pack_bf16x2(acc[4], acc[5]), b3 = pack_bf16x2(acc[6], acc[7]);
         cv[q] = make_uint4(b0, b1, b2, b3);

@@ -61,6 +61,7 @@ constexpr int kPackedStageBytes = 128 * 128;  // 128 rows x 32 words
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxPackedStages = 8;
 constexpr int kMaxBStages = 8;
+constexpr int kEpiStageBytes = 8 * 1024;  // down epilogue: [16 tokens][32 rows] bf16 per epilogue warp (<= 8)
 constexpr int kMaxASlots = 3;  // A-operand ring in TMEM (128 columns a slot)
 // Sleep between tests for waits with slack (producers, epilogue).
 constexpr uint32_t kSleepRing = 200;  // ns: the TMA producers
@@ -169,6 +170,9 @@ __global__ void __launch_bounds__((3 + dequant_warps<NA, APW, GROUPS>() + 4 * EP
     uint8_t* scale_base = bring + (size_t)a.bregion;
     const int G = a.K / 64;  // groups per weight row
     const int sbuf_bytes = scale_buf_bytes(a.K);
+    // down: the epilogue's staging tiles after the scale buffers
+    uint8_t* epi_stage =
+        reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(scale_base + 2 * sbuf_bytes) + 127) & ~uintptr_t(127));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int* abort_flag = &sh.abort_flag;
@@ -628,14 +632,26 @@ __global__ void __launch_bounds__((3 + dequant_warps<NA, APW, GROUPS>() + 4 * EP
                         if (tok < tl.rows) a.out_f32[(size_t)(tl.p0 + tok) * a.out_ld + vrow] = o;
                     }
                 } else {
-                    // y by sorted row: 32 lanes store 64 B of a row
-                    const int hrow = 128 * j + 32 * q + lane;
+                    // y by sorted row, through this warp's [16 tokens][32 rows]
+                    // staging tile: the lanes write their row's 16 tokens, then
+                    // each lane stores 8 consecutive rows of one token (16
+                    // bytes). With one 2-byte store a lane per token the
+                    // stores paced the down kernel at T = 4096 (149.5 -> 129.0
+                    // us measured; canvas 47.1 -> 45.1).
+                    uint16_t* stg = reinterpret_cast<uint16_t*>(epi_stage + (size_t)(warp - kEpiWarp0) * 1024);
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        const int tok = c0 + jj;
+                    for (int jj = 0; jj < 16; ++jj) stg[jj * 32 + lane] = (uint16_t)f32_to_bf16_bits(v[jj]);
+                    __syncwarp();
+                    const int hbase = 128 * j + 32 * q;
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int tokl = (lane >> 2) + 8 * u, seg = lane & 3;
+                        const uint4 val = *reinterpret_cast<const uint4*>(stg + tokl * 32 + seg * 8);
+                        const int tok = c0 + tokl;
                         if (tok < tl.rows)
-                            a.out[(size_t)(tl.p0 + tok) * a.out_ld + hrow] = (uint16_t)f32_to_bf16_bits(v[jj]);
+                            *reinterpret_cast<uint4*>(a.out + (size_t)(tl.p0 + tok) * a.out_ld + hbase + seg * 8) = val;
                     }
+                    __syncwarp();
                 }
             }
             tc_fence_before();
@@ -653,21 +669,21 @@ __global__ void __launch_bounds__((3 + dequant_warps<NA, APW, GROUPS>() + 4 * EP
     }
 }
 
-size_t gemm_smem_bytes(int K, int wstages, int bregion) {
+size_t gemm_smem_bytes(int mode, int K, int wstages, int bregion) {
     return 1024 /* alignment slack */ + (size_t)wstages * kPackedStageBytes + (size_t)bregion +
-           2 * (size_t)scale_buf_bytes(K);
+           2 * (size_t)scale_buf_bytes(K) + (mode == kDown ? kEpiStageBytes + 128 : 0);
 }
 
 // Shared-memory split: the deepest packed-weight ring (up to 8 stages) that
 // leaves the B ring at least two slots of the largest possible token tile;
 // the rest goes to the B ring.
-void gemm_stages(int K, int nmax, int* wstages, int* bregion) {
+void gemm_stages(int mode, int K, int nmax, int* wstages, int* bregion) {
     const size_t limit = 232448 - 2048;  // 227 KB per CTA minus the static part
     const int min_b = 2 * 4 * nmax * 128;
     int nw = kMaxPackedStages;
-    while (nw > 2 && gemm_smem_bytes(K, nw, min_b) > limit) --nw;
+    while (nw > 2 && gemm_smem_bytes(mode, K, nw, min_b) > limit) --nw;
     *wstages = nw;
-    *bregion = (int)((limit - gemm_smem_bytes(K, nw, 0)) & ~size_t(1023));
+    *bregion = (int)((limit - gemm_smem_bytes(mode, K, nw, 0)) & ~size_t(1023));
 }
 
 template <int MODE, int NMAX, int NA, int APW, int EPW, bool GROUPS>
@@ -710,7 +726,7 @@ static cudaError_t launch_mode(const CUtensorMap& wmap, const BMaps& bmaps, cons
 
 cudaError_t launch_gemm(int mode, const CUtensorMap& wmap, const BMaps& bmaps, const GemmArgs& a, int grid,
                         cudaStream_t stream) {
-    const size_t smem = gemm_smem_bytes(a.K, a.wstages, a.bregion);
+    const size_t smem = gemm_smem_bytes(mode, a.K, a.wstages, a.bregion);
     switch (mode) {
         case kGateUp: return launch_mode<kGateUp>(wmap, bmaps, a, grid, smem, stream);
         case kDown: return launch_mode<kDown>(wmap, bmaps, a, grid, smem, stream);

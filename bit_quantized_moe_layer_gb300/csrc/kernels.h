@@ -173,8 +173,9 @@ struct BMaps {
     CUtensorMap m2;
 };
 // wmap: packed weights as uint32 [E*N rows, K/8], box {32, 64 or 128}, 128B swizzle.
-size_t gemm_smem_bytes(int K, int wstages, int bregion);
-void gemm_stages(int K, int nmax, int* wstages, int* bregion);
+// mode: the GemmMode (the down kernel also holds its epilogue's staging tiles).
+size_t gemm_smem_bytes(int mode, int K, int wstages, int bregion);
+void gemm_stages(int mode, int K, int nmax, int* wstages, int* bregion);
 cudaError_t launch_gemm(int mode, const CUtensorMap& wmap, const BMaps& bmaps, const GemmArgs& a, int grid,
                         cudaStream_t stream);
 int gemm_error_word();

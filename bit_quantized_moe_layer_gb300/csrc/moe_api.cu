@@ -308,7 +308,7 @@ int run_experts(const moe_dims* d, const uint16_t* x, const int32_t* idx, const 
     if (gemv) {
         ga.wstages = gemv_stages(H);
     } else {
-        gemm_stages(H, nmax, &ga.wstages, &ga.bregion);
+        gemm_stages(kGateUp, H, nmax, &ga.wstages, &ga.bregion);
     }
     int grid = di.sms;
     if ((long)L.max_tiles * ga.n_tiles < grid) grid = L.max_tiles * ga.n_tiles;
@@ -329,7 +329,7 @@ int run_experts(const moe_dims* d, const uint16_t* x, const int32_t* idx, const 
     if (gemv) {
         gd.wstages = gemv_stages(I);
     } else {
-        gemm_stages(I, nmax, &gd.wstages, &gd.bregion);
+        gemm_stages(kDown, I, nmax, &gd.wstages, &gd.bregion);
     }
     grid = di.sms;
     if ((long)L.max_tiles * gd.n_tiles < grid) grid = L.max_tiles * gd.n_tiles;
@@ -394,7 +394,7 @@ int run_dense(const moe_dims* d, const uint16_t* x, const uint16_t* pre_norm_w, 
     ga.prefetch_items = 2;
     ga.tiles_per_expert = ntok;  // every item is expert 0's
     ga.weight_major = 1;
-    gemm_stages(H, nmax, &ga.wstages, &ga.bregion);
+    gemm_stages(kGateUp, H, nmax, &ga.wstages, &ga.bregion);
     int grid = di.sms < ntok * ga.n_tiles ? di.sms : ntok * ga.n_tiles;
     if ((rc = fail(launch_gemm(kGateUp, m_gu, m_xs, ga, grid, s)))) return rc;
     tm.mark(4);
@@ -408,7 +408,7 @@ int run_dense(const moe_dims* d, const uint16_t* x, const uint16_t* pre_norm_w, 
     gd.N = H;
     gd.out_ld = H;
     gd.n_tiles = H / 128;
-    gemm_stages(I, nmax, &gd.wstages, &gd.bregion);
+    gemm_stages(kDown, I, nmax, &gd.wstages, &gd.bregion);
     grid = di.sms < ntok * gd.n_tiles ? di.sms : ntok * gd.n_tiles;
     if ((rc = fail(launch_gemm(kDown, m_dn, m_mid, gd, grid, s)))) return rc;
     tm.mark(5);
@@ -461,7 +461,7 @@ int run_head(const moe_dims* d, int vocab, float softcap, const uint16_t* h, con
     ga.prefetch_items = 2;
     ga.tiles_per_expert = ntok;
     ga.weight_major = 1;
-    gemm_stages(H, nmax, &ga.wstages, &ga.bregion);
+    gemm_stages(kHead, H, nmax, &ga.wstages, &ga.bregion);
     const long items = (long)ntok * n_tiles;
     const int grid = items < di.sms ? (int)items : di.sms;
     if ((rc = fail(launch_gemm(kHead, m_w, m_xs, ga, grid, s)))) return rc;
