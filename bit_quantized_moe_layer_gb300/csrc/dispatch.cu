@@ -546,6 +546,28 @@ cudaError_t launch_combine(const uint16_t* y, const int32_t* inv, const uint16_t
     return launch_pdl(combine_kernel, grid, dim3(128), 0, stream, y, inv, w, out, k, H);
 }
 
+// dst[i] = src[i] for `bytes` bytes (a multiple of 16, both 16-byte
+// aligned), grid-stride, 16 bytes a thread a step. src may be pinned host
+// memory mapped into the device's address space: the copy then reads it
+// over the host link from every SM at once.
+__global__ void __launch_bounds__(256) copy16_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src,
+                                                     size_t n) {
+    pdl_trigger();
+    pdl_wait();
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+        dst[i] = src[i];
+}
+
+cudaError_t launch_copy16(void* dst, const void* src, size_t bytes, int sms, cudaStream_t stream) {
+    if (bytes == 0) return cudaSuccess;
+    if (bytes % 16 != 0) return cudaErrorInvalidValue;
+    const size_t n = bytes / 16;
+    const size_t blocks = (n + 255) / 256;
+    const unsigned grid = (unsigned)(blocks < (size_t)sms * 4 ? blocks : (size_t)sms * 4);
+    return launch_pdl(copy16_kernel, dim3(grid), dim3(256), 0, stream, static_cast<uint4*>(dst),
+                      static_cast<const uint4*>(src), n);
+}
+
 int dispatch_error_word() {
     int v = 0, z = 0;
     if (cudaMemcpyFromSymbol(&v, g_error_word, sizeof(int)) != cudaSuccess) return 0;

@@ -111,6 +111,9 @@ cudaError_t launch_combine(const uint16_t* y, const int32_t* inv, const uint16_t
 cudaError_t launch_combine_norm(const uint16_t* y, const int32_t* inv, const uint16_t* w, const uint16_t* post_w,
                                 uint16_t* out, int T, int k, int H, float eps, cudaStream_t stream);
 int dispatch_error_word();
+// dst = src, `bytes` a multiple of 16, both 16-byte aligned; src may be
+// mapped pinned host memory.
+cudaError_t launch_copy16(void* dst, const void* src, size_t bytes, int sms, cudaStream_t stream);
 
 // Dense MLP input: xs[t] = row t of x, or RMSNorm(x, pre_w) with fp32 steps
 // (pre_w non-null), each 8-element block of K interleaved as the gather's;

@@ -294,11 +294,14 @@ int moe_lm_head(const moe_dims* d, int32_t vocab, float softcap, const uint16_t*
                 void* stream);
 
 /*
- * The whole layer with HOST activations: copies x_host [T,H] to the device,
- * runs moe_forward and copies out [T,H] back to out_host, then synchronises
- * the stream. Weights and router parameters are device pointers. Host
- * buffers should be pinned (cudaHostAlloc) for full copy speed. The device
- * copies of x and out live in the workspace.
+ * The whole layer with HOST activations: brings x_host [T,H] to the device,
+ * runs moe_forward and delivers out [T,H] to out_host, then synchronises
+ * the stream. Weights and router parameters are device pointers. Pinned
+ * host buffers (cudaHostAlloc, cudaHostRegister) are used through their
+ * device mapping: a copy kernel reads x_host into the workspace and the
+ * combine writes out_host directly. Other host buffers go through
+ * cudaMemcpyAsync to and from workspace copies (slower). The stream must not
+ * carry other work on these host buffers meanwhile.
  */
 int moe_forward_hostio(const moe_dims* d, const uint16_t* x_host, const uint16_t* router_w,
                        const uint16_t* router_scale, const uint16_t* per_expert_scale,
