@@ -85,6 +85,19 @@ def test_branch_prefill_sampled():
     print(f"prefill branch: {run_case(inp, rows, seed=1)}")
 
 
+@pytest.mark.parametrize("T", [17, 256])
+def test_branch_row_router(T):
+    """The branch with the row router forced (moe_set_router_path(2)), which
+    the default picks only at large T: its expert input and routing against
+    the oracle at small T."""
+    prev = moe.set_router_path(2)
+    try:
+        stats = run_case(ms.make_layer("canvas", T=T, seed=8), seed=3)
+    finally:
+        moe.set_router_path(prev)
+    print(f"T={T} branch, row router: {stats}")
+
+
 @pytest.mark.parametrize("T", [1, 17, 130])
 def test_branch_ragged(T):
     run_case(ms.make_layer("canvas", T=T, seed=6), seed=2)
