@@ -45,7 +45,9 @@
 //   epilogue      an item accumulates its whole K in one of two TMEM
 //     warps       accumulator buffers (fp32); once per item these warps read
 //                 it and apply GeGLU (gate_up) or store y by sorted row
-//                 (down) while the next item accumulates in the other buffer.
+//                 (down, through a shared-memory staging tile as 16-byte
+//                 pieces of rows) while the next item accumulates in the
+//                 other buffer.
 // The dequantised pair order inside each 8-element K block is (0,4),(1,5),
 // (2,6),(3,7); the B operands (gathered x, GeGLU output) are stored in that
 // same K order, so the MMA sums the same products.
