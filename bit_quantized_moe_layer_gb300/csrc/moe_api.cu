@@ -96,34 +96,90 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void* ptr, uint64_t inner,
-                 uint64_t rows, uint32_t box_inner, uint32_t box_rows) {
+// A tensor map is a pure function of its encode arguments (address, type,
+// sizes, strides, box; the rest is fixed here), so encoded maps are kept in
+// a small least-recently-used table: repeated calls on the same buffers (a
+// decode or serving loop) skip the ~14 host-side encodes a forward needs.
+struct MapKey {
+    const void* ptr;
+    int dt, rank;
+    uint64_t dims[3], strides[2];
+    uint32_t box[3];
+    bool operator==(const MapKey& o) const {
+        if (ptr != o.ptr || dt != o.dt || rank != o.rank) return false;
+        for (int i = 0; i < rank; ++i)
+            if (dims[i] != o.dims[i] || box[i] != o.box[i]) return false;
+        for (int i = 0; i + 1 < rank; ++i)
+            if (strides[i] != o.strides[i]) return false;
+        return true;
+    }
+};
+
+bool encode_cached(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ptr, const uint64_t* dims,
+                   const uint64_t* strides, const uint32_t* box) {
+    constexpr int kSlots = 64;
+    struct Entry {
+        MapKey key;
+        CUtensorMap map;
+        uint64_t used;
+    };
+    static Entry table[kSlots];
+    static uint64_t tick = 0;
+    static std::mutex mu;
+    MapKey key{ptr, (int)dt, rank, {0, 0, 0}, {0, 0}, {0, 0, 0}};
+    for (int i = 0; i < rank; ++i) {
+        key.dims[i] = dims[i];
+        key.box[i] = box[i];
+    }
+    for (int i = 0; i + 1 < rank; ++i) key.strides[i] = strides[i];
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (Entry& e : table)
+            if (e.used && e.key == key) {
+                e.used = ++tick;
+                *m = e.map;
+                return true;
+            }
+    }
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[2] = {inner, rows};
-    cuuint64_t strides[1] = {inner * esize};
-    cuuint32_t box[2] = {box_inner, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    cuuint64_t d[3], st[2];
+    cuuint32_t b[3], estr[3] = {1, 1, 1};
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+    }
+    for (int i = 0; i + 1 < rank; ++i) st[i] = strides[i];
+    if (fn(m, dt, (cuuint32_t)rank, const_cast<void*>(ptr), d, st, b, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    std::lock_guard<std::mutex> lock(mu);
+    Entry* victim = &table[0];
+    for (Entry& e : table)
+        if (e.used < victim->used) victim = &e;
+    victim->key = key;
+    victim->map = *m;
+    victim->used = ++tick;
+    return true;
+}
+
+bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void* ptr, uint64_t inner,
+                 uint64_t rows, uint32_t box_inner, uint32_t box_rows) {
+    const uint64_t dims[2] = {inner, rows}, strides[1] = {inner * esize};
+    const uint32_t box[2] = {box_inner, box_rows};
+    return encode_cached(m, dt, 2, ptr, dims, strides, box);
 }
 
 // The grouped GEMM's token-operand maps over a bf16 [rows, K] buffer (see
 // BMaps): 3-D boxes of 16, 32, 64 and 128 rows by min(4, K/64) atoms, and the
 // 2-D 16-row box.
 bool make_bmaps(BMaps* b, const void* ptr, uint64_t K, uint64_t rows) {
-    auto fn = encode_fn();
-    if (!fn || !make_map_2d(&b->m2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, K, rows, 64, 16)) return false;
+    if (!make_map_2d(&b->m2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, K, rows, 64, 16)) return false;
     for (int i = 0; i < 4; ++i) {
-        cuuint64_t dims[3] = {64, rows, K / 64};
-        cuuint64_t strides[2] = {K * 2, 128};
-        cuuint32_t box[3] = {64, (cuuint32_t)(16 << i), (cuuint32_t)(K / 64 < 4 ? K / 64 : 4)};
-        cuuint32_t estr[3] = {1, 1, 1};
-        if (fn(&b->m[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return false;
+        const uint64_t dims[3] = {64, rows, K / 64}, strides[2] = {K * 2, 128};
+        const uint32_t box[3] = {64, (uint32_t)(16 << i), (uint32_t)(K / 64 < 4 ? K / 64 : 4)};
+        if (!encode_cached(&b->m[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides, box)) return false;
     }
     return true;
 }
