@@ -24,7 +24,22 @@ struct DispatchSmem {
     int cnt[kMaxE], off[kMaxE + 1], tbase[kMaxE + 1];
 };
 
-// Counts of the slots [c0, c1) by expert into wh_row (warp match-any: one add
+// The lanes of the warp whose expert id equals this lane's (e < 0 for a
+// dropped or absent slot, which all match one another): the mask
+// __match_any_sync would give, built from one ballot per bit of e + 1
+// (bits = the bits of E), far cheaper than the match instruction here.
+__device__ __forceinline__ unsigned same_expert_lanes(int e, int bits) {
+    const unsigned v = (unsigned)(e + 1);
+    unsigned peers = 0xffffffffu;
+    for (int b = 0; b < bits; ++b) {
+        const unsigned bit = (v >> b) & 1u;
+        const unsigned m = __ballot_sync(0xffffffffu, bit != 0u);
+        peers &= bit ? m : ~m;
+    }
+    return peers;
+}
+
+// Counts of the slots [c0, c1) by expert into wh_row (lanes of equal id: one add
 // per group of equal ids). Out-of-range ids are dropped (and flagged once).
 __device__ __forceinline__ void warp_histogram(const int32_t* idx, int c0, int c1, int E, int* wh_row, int lane,
                                                bool flag) {
@@ -36,7 +51,7 @@ __device__ __forceinline__ void warp_histogram(const int32_t* idx, int c0, int c
             if (flag) atomicOr(&g_error_word, kErrBadExpert);
             e = -1;
         }
-        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const unsigned peers = same_expert_lanes(e, 32 - __clz(E));
         if (e >= 0 && (peers & lt_mask) == 0) wh_row[e] += __popc(peers);
     }
 }
@@ -133,7 +148,7 @@ __device__ __forceinline__ void warp_scatter(const DispatchArgs& a, int c0, int 
         const int f = b + lane;
         int e = (f < c1) ? a.idx[f] : -1;
         if (e >= a.E || e < 0) e = -1;
-        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const unsigned peers = same_expert_lanes(e, 32 - __clz(a.E));
         const int rank = __popc(peers & lt_mask);
         if (e >= 0) {
             const int p = wh_row[e] + rank;
@@ -186,11 +201,18 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
     __syncthreads();
     const unsigned lt_mask = (1u << lane) - 1u;
     int* wh = sm.wh[warp];
+    // the lanes with the same expert in each 32-slot group, found once and
+    // used by both passes: by ballots when the warps' groups are full (the
+    // match instruction is the costly one there: canvas histogram 2.1 -> 1.2
+    // us), by the match when they hold a few ids (decode: 0.2 against 0.7 us)
+    const bool full_groups = a.S >= 32 * kW;
+    unsigned pm[kPerLane];
 #pragma unroll
     for (int i = 0; i < kPerLane; ++i) {
+        pm[i] = 0u;
         if (c0 + 32 * i >= c1) break;  // warp-uniform
-        const unsigned peers = __match_any_sync(0xffffffffu, ev[i]);
-        if (ev[i] >= 0 && (peers & lt_mask) == 0) wh[ev[i]] += __popc(peers);
+        pm[i] = full_groups ? same_expert_lanes(ev[i], 32 - __clz(a.E)) : __match_any_sync(0xffffffffu, ev[i]);
+        if (ev[i] >= 0 && (pm[i] & lt_mask) == 0) wh[ev[i]] += __popc(pm[i]);
     }
     __syncthreads();
     scan_over_warps(sm, sm.cnt, a.E, warp, lane);
@@ -203,7 +225,7 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
     for (int i = 0; i < kPerLane; ++i) {
         if (c0 + 32 * i >= c1) break;  // warp-uniform
         const int f = c0 + 32 * i + lane, e = ev[i];
-        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const unsigned peers = pm[i];
         const int rank = __popc(peers & lt_mask);
         if (e >= 0) {
             const int p = wh[e] + rank;
@@ -253,11 +275,18 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_gather_kernel(Dispa
     __syncthreads();
     const unsigned lt_mask = (1u << lane) - 1u;
     int* wh = sm.wh[warp];
+    // the lanes with the same expert in each 32-slot group, found once and
+    // used by both passes: by ballots when the warps' groups are full (the
+    // match instruction is the costly one there: canvas histogram 2.1 -> 1.2
+    // us), by the match when they hold a few ids (decode: 0.2 against 0.7 us)
+    const bool full_groups = a.S >= 32 * kW;
+    unsigned pm[kPerLane];
 #pragma unroll
     for (int i = 0; i < kPerLane; ++i) {
+        pm[i] = 0u;
         if (c0 + 32 * i >= c1) break;  // warp-uniform
-        const unsigned peers = __match_any_sync(0xffffffffu, ev[i]);
-        if (ev[i] >= 0 && (peers & lt_mask) == 0) wh[ev[i]] += __popc(peers);
+        pm[i] = full_groups ? same_expert_lanes(ev[i], 32 - __clz(a.E)) : __match_any_sync(0xffffffffu, ev[i]);
+        if (ev[i] >= 0 && (pm[i] & lt_mask) == 0) wh[ev[i]] += __popc(pm[i]);
     }
     __syncthreads();
     scan_over_warps(sm, sm.cnt, a.E, warp, lane);
@@ -269,7 +298,7 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_gather_kernel(Dispa
     for (int i = 0; i < kPerLane; ++i) {
         if (c0 + 32 * i >= c1) break;  // warp-uniform
         const int f = c0 + 32 * i + lane, e = ev[i];
-        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const unsigned peers = pm[i];
         const int rank = __popc(peers & lt_mask);
         if (e >= 0) {
             const int p = wh[e] + rank;
