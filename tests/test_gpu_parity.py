@@ -271,6 +271,42 @@ def test_many_rows_one_expert():
                    sub_explainer(gh.explainer(inp, idx, w), rows))
 
 
+def test_ragged_tiles_many_rows():
+    """~100 rows an expert (the 128-row token tiles): experts with 1, 16,
+    127..130, 255..257 and 513 rows, one with 600 (several full tiles and a
+    tail), the rest ~89 rows each. The sampled tokens include each special
+    expert's rows at the tile boundaries."""
+    T = 1600
+    inp = ms.make_layer("canvas", T=T, seed=12)
+    d = inp.dims
+    special = {0: 600, 1: 257, 2: 129, 3: 128, 4: 1, 5: 255, 6: 256, 7: 513, 8: 16, 9: 130, 10: 127}
+    rest = [e for e in range(d.E) if e not in special]
+    left = T * d.k - sum(special.values())
+    counts = dict(special)
+    for i, e in enumerate(rest):
+        counts[e] = left // len(rest) + (1 if i < left % len(rest) else 0)
+    assert sum(counts.values()) == T * d.k and max(counts.values()) <= T
+    # Expert e fills a run of consecutive positions of the column-major
+    # [k, T] slot grid, so no token meets an expert twice.
+    order = np.repeat(np.arange(d.E), [counts[e] for e in range(d.E)])
+    rng = np.random.default_rng(12)
+    order = np.concatenate([order[order == e] for e in rng.permutation(d.E)])
+    idx = order.reshape(d.k, T).T.astype(np.int32).copy()
+    assert all(len(set(r)) == d.k for r in idx.tolist())
+    w = ms.bf16_bits(rng.uniform(0.05, 0.3, idx.shape))
+    g = gh.upload(inp)
+    out = gh.gpu_experts(g, idx, w)
+    pick = set(sample_rows(T, 32, seed=5).tolist())
+    for e, c in special.items():
+        toks = np.flatnonzero((idx == e).any(axis=1))  # the expert's rows in sorted order
+        for r in (0, 126, 127, 128, 129, 254, 255, 256, 257, 383, 384, 511, 512, 513, c - 1):
+            if 0 <= r < c:
+                pick.add(int(toks[r]))
+    rows = np.array(sorted(pick))
+    gh.compare_out(out[rows], gh.oracle_experts_rows(inp, idx, w, rows), "ragged tiles",
+                   sub_explainer(gh.explainer(inp, idx, w), rows))
+
+
 def test_single_expert_identity():
     """E = 1, k = 1, per_expert_scale = 1: the layer is one dense 4-bit GeGLU MLP."""
     d = ms.Dims(T=40, H=256, E=1, k=1, inter=128)
