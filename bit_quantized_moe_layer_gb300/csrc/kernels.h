@@ -61,8 +61,9 @@ cudaError_t launch_router(const CUtensorMap& wmap, const CUtensorMap& xmap, cons
 int router_error_word();
 // Row router: the same results as launch_router, one CTA per 16 tokens over
 // the whole hidden dimension (no cluster); dense router weight only, E <=
-// 128, H a multiple of 64 whose 16-row tile fits in shared memory beside a
-// ring of at least 4 weight blocks (H <= 4992). xmap: x as bf16 [T rows, H], box {64, 16}, 128B swizzle; wmap as
+// 128, H a multiple of 64 whose 16-row tile fits in shared memory beside
+// the router_scale and pre_w rows and a ring of at least 2 weight stages of
+// two K blocks (H <= 4416). xmap: x as bf16 [T rows, H], box {64, 16}, 128B swizzle; wmap as
 // for launch_router. a.tt is unused.
 bool router_rows_fits(int H, int E, bool q4);
 bool router_prefer_rows(int T, int H, int E);  // fits, and the clusters would walk three or more waves

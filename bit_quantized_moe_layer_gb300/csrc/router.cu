@@ -465,12 +465,13 @@ __global__ void __launch_bounds__(kWarps * 32) router_kernel(const __grid_consta
 // Row router: the same computation as router_kernel, one CTA per 16 tokens
 // over the whole hidden dimension, no cluster. The CTA keeps its 16 x rows
 // in shared memory (H / 64 boxes of 16 rows x 128 B, the MMA's K-major
-// layout), sums each token's squares itself (warp w <-> token w: lanes take
-// alternate 16-byte chunks into two two-float accumulators, merged by
-// error-free two-sums, so the mean is the exactly rounded one as above),
-// normalises in place with the same three bf16 roundings, and streams the
-// router weight through a ring of 64-wide K blocks (128 experts x 128 B,
-// TMA) into one accumulator: D[e][t] in 16 TMEM columns. The scores leave
+// layout) with the router_scale (and pre_w) row, sums each token's squares
+// itself (warp w <-> token w: each lane takes every 32nd 16-byte chunk, four
+// at a time into four two-float accumulators, merged by error-free
+// two-sums, so the mean is the exactly rounded one as above), normalises in
+// place with the same three bf16 roundings, and streams the router weight
+// through a ring of stages of two 64-wide K blocks (128 experts x 128 B
+// each, TMA) into one accumulator: D[e][t] in 16 TMEM columns. The scores leave
 // TMEM by lane quarter, are rounded to bf16 and staged as [token][expert];
 // warp w then takes token w's top k, softmax and per-expert scale as the
 // cluster router does. No cross-CTA exchange or barrier: the tile's latency
@@ -478,20 +479,23 @@ __global__ void __launch_bounds__(kWarps * 32) router_kernel(const __grid_consta
 namespace {
 constexpr int kRowTT = 16;                 // tokens a CTA (one warp each)
 constexpr int kRowWarps = 16;
-constexpr int kRowWStages = 8;             // most router-weight ring stages (one 64-wide K block each)
+constexpr int kRowWStages = 4;             // most router-weight ring stages (two 64-wide K blocks each)
+constexpr int kRowStageBytes = 2 * kWBlockBytes;
 static_assert(kRowTT == kRowWarps, "warp w owns token w");
 }  // namespace
 
-// Router-weight ring stages that fit beside the x tile (0 if fewer than 4).
+// Router-weight ring stages that fit beside the x tile, the scores and the
+// router_scale and pre_w rows (0 if fewer than 2).
 __host__ __device__ inline int row_wstages(int H) {
-    const long fixed = 1024 + (long)(H / 64) * kRowTT * 128 + (long)kRowTT * kChunkE * 2;
-    const long n = ((long)(232448 - 1024) - fixed) / kWBlockBytes;
-    return n < 4 ? 0 : (n > kRowWStages ? kRowWStages : (int)n);
+    const long fixed = 1024 + (long)(H / 64) * kRowTT * 128 + (long)kRowTT * kChunkE * 2 + 4L * H;
+    const long n = ((long)(232448 - 1024) - fixed) / kRowStageBytes;
+    return n < 2 ? 0 : (n > kRowWStages ? kRowWStages : (int)n);
 }
 
 size_t router_rows_smem_bytes(int H) {
     const size_t nkb = (size_t)H / 64;
-    return 1024 + nkb * kRowTT * 128 + (size_t)row_wstages(H) * kWBlockBytes + (size_t)kRowTT * kChunkE * 2;
+    return 1024 + nkb * kRowTT * 128 + (size_t)row_wstages(H) * kRowStageBytes + (size_t)kRowTT * kChunkE * 2 +
+           4 * (size_t)H;
 }
 
 __global__ void __launch_bounds__(kRowWarps * 32, 1) router_rows_kernel(const __grid_constant__ CUtensorMap wmap,
@@ -510,13 +514,16 @@ __global__ void __launch_bounds__(kRowWarps * 32, 1) router_rows_kernel(const __
     const int nkb = H / 64;
     uint8_t* xt = base;                                             // nkb boxes of 16 rows x 128 B
     const int NW = row_wstages(H);                                  // weight ring stages
-    uint8_t* wring = xt + (size_t)nkb * kRowTT * 128;               // NW blocks of 128 rows x 128 B
-    uint16_t* sc = reinterpret_cast<uint16_t*>(wring + (size_t)NW * kWBlockBytes);  // [16][E]
+    const int nst = (nkb + 1) / 2;                                  // weight stages: K blocks 2s, 2s + 1
+    uint8_t* wring = xt + (size_t)nkb * kRowTT * 128;               // NW stages of two 128-row x 128 B blocks
+    uint16_t* sc = reinterpret_cast<uint16_t*>(wring + (size_t)NW * kRowStageBytes);  // [16][E]
+    uint16_t* scl = sc + kRowTT * E;                                // router_scale [H]
+    uint16_t* pwl = scl + H;                                        // pre_w [H] (expert input only)
     volatile int* abort_flag = &abort_flag_s;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t0 = blockIdx.x * kRowTT;
     const uint32_t wbytes = (uint32_t)E * 128u;                     // one K block of the weight (E <= 128 rows)
-    const int nw0 = nkb < NW ? nkb : NW;
+    const int nw0 = nst < NW ? nst : NW;
 
     for (int e = threadIdx.x; e < E; e += blockDim.x) pes_s[e] = a.per_expert_scale[e];
     if (threadIdx.x == 0) {
@@ -540,12 +547,19 @@ __global__ void __launch_bounds__(kRowWarps * 32, 1) router_rows_kernel(const __
     tc_fence_after();
     const uint32_t tmem = tmem_base;
     if (threadIdx.x == 0) {
-        // the tile's rows (rows past T read as zero) and the first weight blocks
-        mbar_arrive_expect_tx(&xfull, (uint32_t)nkb * kRowTT * 128u);
+        // the tile's rows (rows past T read as zero), the router_scale (and
+        // pre_w) row, and the first weight stages
+        const uint32_t vbytes = (uint32_t)H * 2u;
+        mbar_arrive_expect_tx(&xfull, (uint32_t)nkb * kRowTT * 128u + (a.xe ? 2u : 1u) * vbytes);
         for (int kb = 0; kb < nkb; ++kb) tma_load_2d(xt + (size_t)kb * kRowTT * 128, &xmap, &xfull, kb * 64, t0);
+        bulk_load(scl, a.router_scale, vbytes, &xfull);
+        if (a.xe) bulk_load(pwl, a.pre_w, vbytes, &xfull);
         for (int s = 0; s < nw0; ++s) {
-            mbar_arrive_expect_tx(&wfull[s], wbytes);
-            tma_load_2d(wring + (size_t)s * kWBlockBytes, &wmap, &wfull[s], s * 64, 0);
+            const int nb = min(2, nkb - 2 * s);
+            mbar_arrive_expect_tx(&wfull[s], (uint32_t)nb * wbytes);
+            for (int b = 0; b < nb; ++b)
+                tma_load_2d(wring + (size_t)s * kRowStageBytes + (size_t)b * kWBlockBytes, &wmap, &wfull[s],
+                            (2 * s + b) * 64, 0);
         }
     }
     if (warp == 0) {
@@ -559,27 +573,39 @@ __global__ void __launch_bounds__(kRowWarps * 32, 1) router_rows_kernel(const __
     {
         const int t = warp;
         const int nchunk = have ? nkb * 8 : 0;
-        float h0 = 0.f, l0 = 0.f, h1 = 0.f, l1 = 0.f;
-        for (int i = lane; i < nchunk; i += 64) {
-            const uint4 v = *reinterpret_cast<const uint4*>(xt + (size_t)(i >> 3) * kRowTT * 128 + sw128(t, i & 7));
-            const int i2 = i + 32;
-            uint4 v2 = make_uint4(0u, 0u, 0u, 0u);
-            if (i2 < nchunk) v2 = *reinterpret_cast<const uint4*>(xt + (size_t)(i2 >> 3) * kRowTT * 128 + sw128(t, i2 & 7));
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w}, w2[4] = {v2.x, v2.y, v2.z, v2.w};
+        // four chunks a lane at a time into four two-float accumulators
+        // (four independent chains), merged by two-sums at the end
+        float hh[4] = {0.f, 0.f, 0.f, 0.f}, ll[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int i0 = lane; i0 < nchunk; i0 += 128) {
+            uint32_t w[4][4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + 32 * u;
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (i < nchunk) v = *reinterpret_cast<const uint4*>(xt + (size_t)(i >> 3) * kRowTT * 128 + sw128(t, i & 7));
+                w[u][0] = v.x;
+                w[u][1] = v.y;
+                w[u][2] = v.z;
+                w[u][3] = v.w;
+            }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                // squares of bf16 values are exact in fp32 (zero chunks add nothing)
-                const float x0 = bf16_bits_to_f32(w[j] & 0xFFFFu), x1 = bf16_bits_to_f32(w[j] >> 16);
-                const float y0 = bf16_bits_to_f32(w2[j] & 0xFFFFu), y1 = bf16_bits_to_f32(w2[j] >> 16);
-                acc2(h0, l0, __fmul_rn(x0, x0));
-                acc2(h1, l1, __fmul_rn(y0, y0));
-                acc2(h0, l0, __fmul_rn(x1, x1));
-                acc2(h1, l1, __fmul_rn(y1, y1));
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    // squares of bf16 values are exact in fp32 (zero chunks add nothing)
+                    const float x0 = bf16_bits_to_f32(w[u][j] & 0xFFFFu), x1 = bf16_bits_to_f32(w[u][j] >> 16);
+                    acc2(hh[u], ll[u], __fmul_rn(x0, x0));
+                    acc2(hh[u], ll[u], __fmul_rn(x1, x1));
+                }
             }
         }
-        float hs, ls, se;
-        two_sum(h0, h1, hs, se);
-        ls = __fadd_rn(__fadd_rn(l0, l1), se);
+        float hs, ls, se, ha, la, hb, lb;
+        two_sum(hh[0], hh[1], ha, se);
+        la = __fadd_rn(__fadd_rn(ll[0], ll[1]), se);
+        two_sum(hh[2], hh[3], hb, se);
+        lb = __fadd_rn(__fadd_rn(ll[2], ll[3]), se);
+        two_sum(ha, hb, hs, se);
+        ls = __fadd_rn(__fadd_rn(la, lb), se);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             const float h2 = __shfl_xor_sync(0xffffffffu, hs, o), l2 = __shfl_xor_sync(0xffffffffu, ls, o);
@@ -608,7 +634,7 @@ __global__ void __launch_bounds__(kRowWarps * 32, 1) router_rows_kernel(const __
         const uint4 v = *p;
         const size_t h = (size_t)c * 8;  // first of the chunk's 8 hidden columns
         if (a.xe && t0 + t < a.T) {  // the expert input: bf16((x * rs) * pre_w), one rounding
-            const uint4 pw = __ldg(reinterpret_cast<const uint4*>(a.pre_w + h));
+            const uint4 pw = *reinterpret_cast<const uint4*>(pwl + h);
             const uint32_t xv[4] = {v.x, v.y, v.z, v.w}, wv[4] = {pw.x, pw.y, pw.z, pw.w};
             uint32_t e[4];
 #pragma unroll
@@ -618,14 +644,14 @@ __global__ void __launch_bounds__(kRowWarps * 32, 1) router_rows_kernel(const __
                     __fmul_rn(__fmul_rn(__uint_as_float(xv[j] & 0xFFFF0000u), rs), __uint_as_float(wv[j] & 0xFFFF0000u)));
             *reinterpret_cast<uint4*>(a.xe + (size_t)(t0 + t) * H + h) = make_uint4(e[0], e[1], e[2], e[3]);
         }
-        const uint4 sv = __ldg(reinterpret_cast<const uint4*>(a.router_scale + h));
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w}, scl[4] = {sv.x, sv.y, sv.z, sv.w};
+        const uint4 sv = *reinterpret_cast<const uint4*>(scl + h);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w}, sw[4] = {sv.x, sv.y, sv.z, sv.w};
         uint32_t o[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const uint32_t n = pack_bf16x2(__fmul_rn(__uint_as_float(w[j] << 16), rs),
                                            __fmul_rn(__uint_as_float(w[j] & 0xFFFF0000u), rs));
-            o[j] = mul_bf16x2(mul_bf16x2(n, scl[j]), root2);
+            o[j] = mul_bf16x2(mul_bf16x2(n, sw[j]), root2);
         }
         *p = make_uint4(o[0], o[1], o[2], o[3]);
     }
@@ -635,24 +661,29 @@ __global__ void __launch_bounds__(kRowWarps * 32, 1) router_rows_kernel(const __
     __syncthreads();
 
     // ---- 3. scores: D[e][t] += W[e][kb] . n[t][kb] over the K blocks ----
-    // Warp 1's elected thread waits for each weight block and issues its 4
-    // MMAs, whose commit frees the slot; warp 2's refills each freed slot
-    // with the block NW further on, so NW - 1 or NW copies stay in flight.
+    // Warp 1's elected thread waits for each weight stage (two K blocks)
+    // and issues its 8 MMAs in K order, whose commit frees the slot; warp 2
+    // refills each freed slot with the stage NW further on, so NW - 1 or NW
+    // stages stay in flight.
     if (warp == 1) {
         tc_fence_after();
         if (elect_one()) {
             const uint32_t idesc = idesc_bf16_m128((uint32_t)kRowTT);
             bool ok = have;
-            for (int kb = 0; ok && kb < nkb; ++kb) {
-                const int slot = kb % NW;
-                if (!(ok = mbar_wait(&wfull[slot], (uint32_t)(kb / NW) & 1u, abort_flag))) break;
+            for (int st = 0; ok && st < nst; ++st) {
+                const int slot = st % NW;
+                if (!(ok = mbar_wait(&wfull[slot], (uint32_t)(st / NW) & 1u, abort_flag))) break;
                 tc_fence_after();
-                const uint64_t ad = sw128_kmajor_desc(smem_u32(wring + (size_t)slot * kWBlockBytes));
-                const uint64_t bd = sw128_kmajor_desc(smem_u32(xt + (size_t)kb * kRowTT * 128));
+                for (int b = 0; b < 2 && 2 * st + b < nkb; ++b) {
+                    const int kb = 2 * st + b;
+                    const uint64_t ad = sw128_kmajor_desc(
+                        smem_u32(wring + (size_t)slot * kRowStageBytes + (size_t)b * kWBlockBytes));
+                    const uint64_t bd = sw128_kmajor_desc(smem_u32(xt + (size_t)kb * kRowTT * 128));
 #pragma unroll
-                for (int k16 = 0; k16 < 4; ++k16)
-                    umma_ss(tmem, ad + (uint64_t)(k16 * 2), bd + (uint64_t)(k16 * 2), idesc,
-                            (kb > 0 || k16 > 0) ? 1u : 0u);
+                    for (int k16 = 0; k16 < 4; ++k16)
+                        umma_ss(tmem, ad + (uint64_t)(k16 * 2), bd + (uint64_t)(k16 * 2), idesc,
+                                (kb > 0 || k16 > 0) ? 1u : 0u);
+                }
                 umma_commit(&wempty[slot]);
             }
             umma_commit(&mdone);  // every MMA above (none if the tile was not loaded)
@@ -660,18 +691,22 @@ __global__ void __launch_bounds__(kRowWarps * 32, 1) router_rows_kernel(const __
         __syncwarp();
     } else if (warp == 2) {
         if (elect_one()) {
-            int issued = nw0;  // weight blocks whose copy has been issued
-            for (int b = nw0; have && b < nkb; ++b) {
-                const int slot = b % NW;
-                if (!mbar_wait(&wempty[slot], (uint32_t)((b - NW) / NW) & 1u, abort_flag)) break;
-                mbar_arrive_expect_tx(&wfull[slot], wbytes);
-                tma_load_2d(wring + (size_t)slot * kWBlockBytes, &wmap, &wfull[slot], b * 64, 0);
-                issued = b + 1;
+            int issued = nw0;  // weight stages whose copies have been issued
+            for (int st = nw0; have && st < nst; ++st) {
+                const int slot = st % NW;
+                if (!mbar_wait(&wempty[slot], (uint32_t)((st - NW) / NW) & 1u, abort_flag)) break;
+                const int nb = min(2, nkb - 2 * st);
+                mbar_arrive_expect_tx(&wfull[slot], (uint32_t)nb * wbytes);
+                for (int b = 0; b < nb; ++b)
+                    tma_load_2d(wring + (size_t)slot * kRowStageBytes + (size_t)b * kWBlockBytes, &wmap, &wfull[slot],
+                                (2 * st + b) * 64, 0);
+                issued = st + 1;
             }
-            // The last copy issued into each slot lands before the CTA exits
-            // (earlier ones were consumed by the MMAs before the slot was
-            // refilled).
-            for (int b = issued - 1; b >= 0 && b >= issued - NW; --b) mbar_drain(&wfull[b % NW], (uint32_t)(b / NW) & 1u);
+            // The last copies issued into each slot land before the CTA
+            // exits (earlier ones were consumed by the MMAs before the slot
+            // was refilled).
+            for (int st = issued - 1; st >= 0 && st >= issued - NW; --st)
+                mbar_drain(&wfull[st % NW], (uint32_t)(st / NW) & 1u);
         }
         __syncwarp();
     }
@@ -860,7 +895,7 @@ cudaError_t ensure_router_rows_attr() {
 }  // namespace
 
 bool router_rows_fits(int H, int E, bool q4) {
-    return !q4 && E >= 1 && E <= kChunkE && H % 64 == 0 && H >= 64 && row_wstages(H) >= 4 &&
+    return !q4 && E >= 1 && E <= kChunkE && H % 64 == 0 && H >= 64 && row_wstages(H) >= 2 &&
            router_rows_smem_bytes(H) <= kRouterSmemLimit;
 }
 
