@@ -17,7 +17,9 @@
 //                 the item's scales and biases (bulk copies, double-buffered);
 //   warp 1        TMEM owner and MMA issuer (one elected thread): per stage
 //                 it waits for the A slot and the B slot, at an item's first
-//                 stage for a free accumulator buffer;
+//                 stage for a free accumulator buffer (the 128-row kernel's
+//                 token copy completes on the A slot's barrier and one
+//                 commit frees both slots: one wait and one commit a stage);
 //   warp 2        TMA producer of the B operand into a ring that the MMA's
 //                 completion releases: one 3-D copy a stage of its four
 //                 64-wide atoms (a box of 16 to 128 rows, the smallest that
@@ -129,6 +131,11 @@ __global__ void __launch_bounds__((3 + dequant_warps<NA, APW, GROUPS>() + 4 * EP
     constexpr uint32_t kD0 = NA * 128;           // accumulator buffers after the A slots
     static_assert(kD0 + 2 * NMAX <= kTmemCols, "TMEM columns");
     static_assert(NA <= kMaxASlots, "A slots");
+    // 128-row lockstep kernel: the token operand's ring is the A ring (one
+    // slot a stage): its copy completes on the stage's A barrier, and one
+    // MMA commit frees both, so the MMA issuer, whose barrier operations
+    // delay its MMAs, waits on one barrier and commits once a stage.
+    constexpr bool kMerged = !GROUPS && NMAX == 128;
     extern __shared__ __align__(1024) uint8_t dsmem[];
     __shared__ Smem sh;
     pdl_trigger();
@@ -166,7 +173,7 @@ __global__ void __launch_bounds__((3 + dequant_warps<NA, APW, GROUPS>() + 4 * EP
     int brows = 16;
     while (brows < maxrows && brows < NMAX) brows <<= 1;
     const int bslot_bytes = 4 * brows * 128;
-    const int NB = min(kMaxBStages, a.bregion / bslot_bytes);
+    const int NB = kMerged ? NA : min(kMaxBStages, a.bregion / bslot_bytes);
     uint8_t* wring = base;
     uint8_t* bring = base + (size_t)NP * kPackedStageBytes;
     uint8_t* scale_base = bring + (size_t)a.bregion;
@@ -189,7 +196,8 @@ __global__ void __launch_bounds__((3 + dequant_warps<NA, APW, GROUPS>() + 4 * EP
             mbar_init(&sh.bempty[s], 1);
         }
         for (int i = 0; i < NA; ++i) {
-            mbar_init(&sh.afull[i], GROUPS ? 4 : kDqWarps);  // the warps that write the slot
+            // the warps that write the slot (and the token copy's arrival)
+            mbar_init(&sh.afull[i], GROUPS ? 4 : kDqWarps + (kMerged ? 1 : 0));
             mbar_init(&sh.aempty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -280,6 +288,8 @@ __global__ void __launch_bounds__((3 + dequant_warps<NA, APW, GROUPS>() + 4 * EP
             prefetch_tensormap(&bmaps.m2);
         }
         const uint32_t box_atoms = (uint32_t)min(4, K / 64);
+        uint64_t* const bF = kMerged ? sh.afull : sh.bfull;    // the copy completes here
+        uint64_t* const bE = kMerged ? sh.aempty : sh.bempty;  // the slot is free
         int slot = 0;
         uint32_t ph = 0, issued = 0;
         bool ok = true;
@@ -292,18 +302,18 @@ __global__ void __launch_bounds__((3 + dequant_warps<NA, APW, GROUPS>() + 4 * EP
             // the whole box counts, rows and atoms past the tensor (zero-filled) included
             const uint32_t box_bytes = box_atoms * (16u << bi) * 128u;
             for (int s = 0; s < nstages; ++s) {
-                if (!(ok = mbar_wait(&sh.bempty[slot], ph ^ 1, abort_flag, kSleepRing, 3))) break;
+                if (!(ok = mbar_wait(&bE[slot], ph ^ 1, abort_flag, kSleepRing, 3))) break;
                 uint8_t* bst = bring + (size_t)slot * bslot_bytes;
                 if (elect_one()) {
                     if constexpr (kBox3) {
-                        mbar_arrive_expect_tx(&sh.bfull[slot], box_bytes);
-                        tma_load_3d(bst, &bmaps.m[bi], &sh.bfull[slot], 0, tl.p0, s * (kStageK / 64));
+                        mbar_arrive_expect_tx(&bF[slot], box_bytes);
+                        tma_load_3d(bst, &bmaps.m[bi], &bF[slot], 0, tl.p0, s * (kStageK / 64));
                     } else {
                         const int atoms = min(kStageK, K - s * kStageK) / 64;
-                        mbar_arrive_expect_tx(&sh.bfull[slot], atoms * nrows16 * 128);
+                        mbar_arrive_expect_tx(&bF[slot], atoms * nrows16 * 128);
                         for (int at = 0; at < atoms; ++at)
                             for (int r = 0; r < nrows16; r += 16)
-                                tma_load_2d(bst + at * brows * 128 + r * 128, &bmaps.m2, &sh.bfull[slot],
+                                tma_load_2d(bst + at * brows * 128 + r * 128, &bmaps.m2, &bF[slot],
                                             s * kStageK + at * 64, tl.p0 + r);
                     }
                 }
@@ -316,7 +326,7 @@ __global__ void __launch_bounds__((3 + dequant_warps<NA, APW, GROUPS>() + 4 * EP
             }
         }
         for (uint32_t g = (issued > (uint32_t)NB ? issued - NB : 0); g < issued; ++g)
-            mbar_drain(&sh.bfull[g % NB], (g / NB) & 1);
+            mbar_drain(&bF[g % NB], (g / NB) & 1);
     } else if (warp == 1) {
         // ---------------------------------------------------- MMA issuer --
         // The whole warp runs the loop; one elected lane issues the MMAs of a
@@ -363,7 +373,7 @@ __global__ void __launch_bounds__((3 + dequant_warps<NA, APW, GROUPS>() + 4 * EP
             if (li >= 2 && !(ok = mbar_wait(&sh.dempty[db], ((li >> 1) - 1) & 1, abort_flag, 0, 6))) break;
             for (int s = 0; s < nstages; ++s) {
                 if (!(ok = mbar_wait(&sh.afull[as], aph, abort_flag, 0, 7))) break;
-                if (!(ok = mbar_wait(&sh.bfull[bslot], bph, abort_flag, 0, 5))) break;
+                if (!kMerged && !(ok = mbar_wait(&sh.bfull[bslot], bph, abort_flag, 0, 5))) break;
                 tc_fence_after();
                 const int nk = min(kStageK, K - s * kStageK) / 16;
                 const uint64_t bdesc0 = sw128_kmajor_desc(smem_u32(bring + (size_t)bslot * bslot_bytes));
@@ -398,7 +408,7 @@ __global__ void __launch_bounds__((3 + dequant_warps<NA, APW, GROUPS>() + 4 * EP
                             }
                         }
                     }
-                    umma_commit(&sh.bempty[bslot]);
+                    if (!kMerged) umma_commit(&sh.bempty[bslot]);
                     umma_commit(&sh.aempty[as]);
                     if (s == nstages - 1) umma_commit(&sh.dfull[db]);
                 }
