@@ -262,7 +262,7 @@ def set_small_t_path(mode: int) -> int:
 
 def set_router_path(mode: int) -> int:
     """0 (default): the row router where it fits and the cluster router would
-    walk three or more waves of tiles, else the cluster router; 1: always
+    walk two or more waves of tiles, else the cluster router; 1: always
     the cluster router; 2: the row router wherever it fits. Returns the
     previous mode."""
     rc = load().moe_set_router_path(int(mode))

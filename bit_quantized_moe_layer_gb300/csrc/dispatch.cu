@@ -218,8 +218,9 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
     scan_over_warps(sm, sm.cnt, a.E, warp, lane);
     __syncthreads();
     finish_experts(a, sm, tid, warp, lane);
-    for (int i = tid; i < kW * a.E; i += kDispatchThreads) sm.wh[i / a.E][i % a.E] += sm.off[i % a.E];
-    __syncthreads();
+    // the warp's own bases (the scatter reads no other warp's row)
+    for (int e = lane; e < a.E; e += 32) wh[e] += sm.off[e];
+    __syncwarp();
     // stable scatter in slot order from the warp's running bases
 #pragma unroll
     for (int i = 0; i < kPerLane; ++i) {
@@ -292,8 +293,9 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_gather_kernel(Dispa
     scan_over_warps(sm, sm.cnt, a.E, warp, lane);
     __syncthreads();
     finish_experts(a, sm, tid, warp, lane, blockIdx.x == 0);
-    for (int i = tid; i < kW * a.E; i += kDispatchThreads) sm.wh[i / a.E][i % a.E] += sm.off[i % a.E];
-    __syncthreads();
+    // the warp's own bases (the scatter reads no other warp's row)
+    for (int e = lane; e < a.E; e += 32) wh[e] += sm.off[e];
+    __syncwarp();
 #pragma unroll
     for (int i = 0; i < kPerLane; ++i) {
         if (c0 + 32 * i >= c1) break;  // warp-uniform

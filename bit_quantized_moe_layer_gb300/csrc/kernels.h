@@ -66,7 +66,7 @@ int router_error_word();
 // two K blocks (H <= 4416). xmap: x as bf16 [T rows, H], box {64, 16}, 128B swizzle; wmap as
 // for launch_router. a.tt is unused.
 bool router_rows_fits(int H, int E, bool q4);
-bool router_prefer_rows(int T, int H, int E);  // fits, and the clusters would walk three or more waves
+bool router_prefer_rows(int T, int H, int E);  // fits, and the clusters would walk two or more waves
 size_t router_rows_smem_bytes(int H);
 cudaError_t launch_router_rows(const CUtensorMap& wmap, const CUtensorMap& xmap, const RouterArgs& a,
                                cudaStream_t stream);

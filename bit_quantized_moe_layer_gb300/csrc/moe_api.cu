@@ -288,7 +288,7 @@ int fail(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 std::atomic<int> g_small_t_path{0};
 
 // Router kernel (moe_set_router_path): 0 = the row router where it fits and
-// the clusters would walk three or more waves, 1 = the cluster router always,
+// the clusters would walk two or more waves, 1 = the cluster router always,
 // 2 = the row router wherever it fits.
 std::atomic<int> g_router_path{0};
 
@@ -537,7 +537,7 @@ int route_impl(const moe_dims* d, const uint16_t* x, const uint16_t* rw, const u
                int32_t* idx, uint16_t* w, cudaStream_t s, const uint16_t* pre_norm_w = nullptr,
                uint16_t* xe = nullptr, const moe_qweight* rq = nullptr) {
     // The row router (one CTA per 16 tokens over the whole row, no cross-CTA
-    // exchange) when the cluster router would walk three or more waves of
+    // exchange) when the cluster router would walk two or more waves of
     // tiles; the cluster router otherwise and for the 4-bit projection.
     const int rpath = g_router_path.load(std::memory_order_relaxed);
     const bool rows = rq == nullptr && ((rpath == 0 && router_prefer_rows(d->T, d->H, d->E)) ||

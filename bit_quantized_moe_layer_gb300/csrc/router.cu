@@ -899,20 +899,20 @@ bool router_rows_fits(int H, int E, bool q4) {
            router_rows_smem_bytes(H) <= kRouterSmemLimit;
 }
 
-// The row router where it fits and the cluster router would walk three or
-// more waves of tiles. Measured at H = 2816, E = 128 (us, launch included):
-// one CTA of the row router streams the whole router weight in ~23 us
-// whatever T, while a cluster takes ~6 us a tile after ~3 us of setup:
-// T = 8: cluster 13.0, row 27.3; T = 256: 15.0 / 27.3; T = 1024 (two
-// waves): 25.2 / 27.3; T = 2048 (three): 33.4 / 29.3; T = 4096 (five):
-// 48.8 / 47.7.
+// The row router where it fits and the cluster router would walk two or
+// more waves of tiles. Measured at H = 2816, E = 128 (us, launch included,
+// L2 flushed): one wave of row-router CTAs takes ~23 us whatever T, while a
+// cluster takes ~6 us a tile after ~3 us of setup: T = 256: cluster 15.0,
+// row 23.1; T = 512 and 768 (one wave): 17.0 / 23.2; T = 1024 and 1536 (two
+// waves): 25.2 / 23.2; T = 2048 (three): 33.4 / 23.7; T = 4096 (five):
+// 47.7 / 41.6.
 bool router_prefer_rows(int T, int H, int E) {
     if (!router_rows_fits(H, E, false)) return false;
     const int tt = router_tokens_per_cluster(T, H, E);
     const size_t smem = router_smem_bytes(H, E, tt);
     if (smem > kRouterSmemLimit) return true;
     const int waves = ((T + tt - 1) / tt + router_resident_clusters(smem) - 1) / router_resident_clusters(smem);
-    return waves >= 3;
+    return waves >= 2;
 }
 
 cudaError_t launch_router_rows(const CUtensorMap& wmap, const CUtensorMap& xmap, const RouterArgs& a,

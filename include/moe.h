@@ -331,7 +331,7 @@ int moe_set_small_t_path(int mode);
  * moe_forward_q4router run (process-wide, change only between calls).
  * mode 0 (the default): one CTA per 16 tokens over the whole hidden row
  * (dense router weight, E <= 128, H a multiple of 64 up to 4416) when the
- * cluster router would walk three or more waves of tiles (large T), the
+ * cluster router would walk two or more waves of tiles (large T), the
  * cluster router otherwise; mode 1: always the cluster
  * router (8-CTA thread-block clusters splitting the hidden dimension); mode
  * 2: the row router wherever it fits. Both
