@@ -351,26 +351,48 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_count_kernel(Dispat
 }
 
 // 2: one CTA: per-expert totals and chunk prefixes, offsets, tiles; the
-// chunk histogram becomes each chunk's base position per expert.
+// chunk histogram becomes each chunk's base position per expert. G adjacent
+// threads share an expert, each loading a run of consecutive chunks at once,
+// then a scan over the G runs by shuffles, and each writes its chunks'
+// final bases once (offset included).
 __global__ void __launch_bounds__(kDispatchThreads) dispatch_scan_kernel(DispatchArgs a) {
     __shared__ DispatchSmem sm;
+    constexpr int kMaxRun = (kDispatchMaxChunks + 3) / 4;  // chunks a thread (G >= 4)
+    static_assert(kDispatchThreads / 4 >= kMaxE, "G >= 4 threads an expert");
     pdl_trigger();
     pdl_wait();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nch = (a.S + chunk_slots(a.S) - 1) / chunk_slots(a.S);
-    for (int e = tid; e < a.E; e += kDispatchThreads) {
-        int run = 0;
-        for (int c = 0; c < nch; ++c) {
-            const int v = a.chunk_hist[c * a.E + e];
-            a.chunk_hist[c * a.E + e] = run;
-            run += v;
-        }
-        sm.cnt[e] = run;
+    const int nch = (a.S + chunk_slots(a.S) - 1) / chunk_slots(a.S);  // <= kDispatchMaxChunks
+    const int G = a.E <= kDispatchThreads / 8 ? 8 : 4;                 // threads an expert (divides 32)
+    const int e = tid / G, m = tid % G;
+    const int run = (nch + G - 1) / G;  // <= kMaxRun
+    const int cb = m * run;             // this thread's first chunk
+    int v[kMaxRun];
+    int sum = 0;
+#pragma unroll
+    for (int j = 0; j < kMaxRun; ++j) {
+        v[j] = (e < a.E && j < run && cb + j < nch) ? a.chunk_hist[(cb + j) * a.E + e] : 0;
+        sum += v[j];
     }
+    // inclusive scan of the runs' sums over the expert's G threads
+    int inc = sum;
+    for (int o = 1; o < G; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, inc, o, G);
+        if (m >= o) inc += u;
+    }
+    if (e < a.E && m == G - 1) sm.cnt[e] = inc;  // the expert's total
     __syncthreads();
     finish_experts(a, sm, tid, warp, lane);
-    __syncthreads();
-    for (int i = tid; i < nch * a.E; i += kDispatchThreads) a.chunk_hist[i] += sm.off[i % a.E];
+    if (e < a.E) {
+        int base = sm.off[e] + inc - sum;
+#pragma unroll
+        for (int j = 0; j < kMaxRun; ++j) {
+            if (j < run && cb + j < nch) {
+                a.chunk_hist[(cb + j) * a.E + e] = base;
+                base += v[j];
+            }
+        }
+    }
 }
 
 // 3: CTA c scatters its chunk from the chunk's per-expert bases.
